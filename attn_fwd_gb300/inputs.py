@@ -1,0 +1,110 @@
+"""Seeded synthetic inputs for exact attention.
+
+This module only draws random numbers and lays them out; it holds none of the
+attention arithmetic.  Both sides of every comparison (the CUDA path and the
+CPU oracle) take their inputs from here, so neither ever computes the other's
+inputs.
+
+Recipe (the plainest reading of the workloads the pages and their benchmark
+configurations describe):
+
+* A CPU ``torch.Generator`` is seeded with the workload's seed.
+* ``randn`` is drawn in fp32 in the order Q, K, V, dO, each of shape
+  [B, H, N, d]; a workload with an amplitude multiplies the fp32 draws by it
+  (peaked softmax rows); every tensor is then rounded to bf16.
+* The oracle up-casts the *same* bf16 values to fp64.
+* A block-sparse workload draws its mask from a fresh generator seeded with the
+  same seed: ``rand(nb, nb) < p`` per 128x128 block, then every diagonal block
+  is switched on.  One mask is shared by all (batch, head) pairs.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+
+import torch
+
+BLOCK = 128  # granularity of the block-sparse mask (one bit per 128x128 block)
+
+
+@dataclass(frozen=True)
+class Workload:
+    """One synthetic attention problem: sizes, mask kind and RNG recipe."""
+
+    name: str
+    B: int
+    H: int
+    N: int
+    d: int
+    seed: int
+    causal: bool = False
+    backward: bool = True
+    amplitude: float = 1.0
+    block_sparse_p: float | None = None  # keep-probability of an off-diagonal block
+    note: str = field(default="", compare=False)
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / (self.d ** 0.5)
+
+    @property
+    def mask_kind(self) -> str:
+        if self.block_sparse_p is not None:
+            return "block"
+        return "causal" if self.causal else "none"
+
+
+# The five benchmark workloads of this attention path.
+WORKLOADS = {
+    "fwd_b1h1n128d64": Workload(
+        "fwd_b1h1n128d64", 1, 1, 128, 64, seed=0, backward=False,
+        note="forward only, one 128x64 tile; latency case"),
+    "fwdbwd_b4h8n1024d64": Workload(
+        "fwdbwd_b4h8n1024d64", 4, 8, 1024, 64, seed=1,
+        note="forward + backward, non-causal"),
+    "fwdbwd_b2h16n4096d128_causal": Workload(
+        "fwdbwd_b2h16n4096d128_causal", 2, 16, 4096, 128, seed=2, causal=True,
+        note="forward + backward, causal, fully masked KV blocks skipped"),
+    "fwd_b1h32n16384d128_causal_x3": Workload(
+        "fwd_b1h32n16384d128_causal_x3", 1, 32, 16384, 128, seed=3, causal=True,
+        backward=False, amplitude=3.0,
+        note="forward only, causal, inputs x3 (peaked rows stress the rescale)"),
+    "fwdbwd_b1h16n8192d128_blocksparse": Workload(
+        "fwdbwd_b1h16n8192d128_blocksparse", 1, 16, 8192, 128, seed=4,
+        block_sparse_p=0.25,
+        note="forward + backward, 128x128 block mask, p=0.25 + diagonal"),
+}
+
+
+def make_qkvdo(B: int, H: int, N: int, d: int, seed: int, amplitude: float = 1.0,
+               with_dout: bool = True) -> dict[str, torch.Tensor]:
+    """Draw Q, K, V (and dO) as CPU bf16 tensors of shape [B, H, N, d]."""
+    g = torch.Generator(device="cpu").manual_seed(seed)
+    names = ["q", "k", "v"] + (["do"] if with_dout else [])
+    out = {}
+    for nm in names:
+        x = torch.randn((B, H, N, d), generator=g, dtype=torch.float32)
+        if amplitude != 1.0:
+            x = x * amplitude
+        out[nm] = x.to(torch.bfloat16)
+    return out
+
+
+def make_block_mask(N: int, seed: int, p: float, block: int = BLOCK) -> torch.Tensor:
+    """Block mask as uint8 [N/block, N/block]; diagonal blocks are always kept."""
+    if N % block:
+        raise ValueError("N must be a multiple of the block size")
+    nb = N // block
+    g = torch.Generator(device="cpu").manual_seed(seed)
+    keep = (torch.rand((nb, nb), generator=g) < p).to(torch.uint8)
+    keep.fill_diagonal_(1)
+    return keep
+
+
+def make_workload_inputs(w: Workload, heads: slice | None = None) -> dict[str, torch.Tensor]:
+    """All inputs of a workload (CPU).  ``heads`` optionally keeps a head slice."""
+    t = make_qkvdo(w.B, w.H, w.N, w.d, w.seed, w.amplitude, with_dout=w.backward)
+    if heads is not None:
+        t = {k: v[:, heads].contiguous() for k, v in t.items()}
+    if w.block_sparse_p is not None:
+        t["block_mask"] = make_block_mask(w.N, w.seed, w.block_sparse_p)
+    return t

@@ -1,0 +1,17 @@
+"""fp64 CPU oracle for exact attention -- test infrastructure only.
+
+Imported only by ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s
+CPU-baseline leg and reference arm.  It shares no code with the CUDA path.
+"""
+from .attention import (  # noqa: F401
+    NEG_INF,
+    backward,
+    backward_rows_dq,
+    flops,
+    forward,
+    forward_rows,
+    head_probs,
+    merge_stats,
+    tiled_forward,
+    visible,
+)

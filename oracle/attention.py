@@ -1,0 +1,258 @@
+"""Plain, slow, fp64 CPU oracle for exact attention -- TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py`` (its CPU-baseline
+leg and its reference arm) may import this package.  The CUDA library never
+reaches it, and it shares no code with the CUDA path.
+
+Pages cited below (by title and section):
+
+* [P1] "【多模态大模型】FlashAttention in NeurIPS 2022" (coreui.cn), section
+  "2.1 拆分": safe softmax with m(s), l(s), the m / l / o update rules and the
+  worked example softmax([1,2,3,10]) with V=[[1,2],[3,4],[5,6],[7,8]].
+* [P2] "FlashAttention" notes (maosong.website): "Standard Attention
+  Implementation" (S=QK^T, P=softmax(S), O=PV), "Tiling" (merge of m and l),
+  "Correctness" (Theorem 1), "Backward Pass of flashattention" (dV, dP, D_i,
+  dS, dq_i, dk_j), "Block-sparse Flashattention" (mask M, S restricted by M).
+* [P3] "Transformer 入门" (cansult.github.io), section "flash attention":
+  S = QK^T / sqrt(d), m = rowmax(S), l = rowsum(exp(S - m)), tiles T_r, T_c.
+* [P4] "Как работает FlashAttention математически" (aivaro.ru), sections 3
+  (online softmax), 4 (output correction), 6 (per-block pseudocode), and the
+  practice exercise (tiled vs standard within 1e-5).
+
+Readings where the pages are silent or disagree (each also listed in the design
+notes):
+
+* Scale: S = scale * Q K^T with scale = 1/sqrt(d) [P3]; [P1] drops the factor.
+  The backward carries it to dQ and dK by the chain rule.
+* Masked entries are -inf (they add nothing to m, l or O); [P2]'s block-sparse
+  text writes 0, which would not skip anything.
+* Causal: key j is visible to query i iff j <= i (equal query/key lengths).
+* Block-sparse: mask[i // block, j // block] keeps or drops a whole block.
+* A row with no visible key gets O = 0, LSE = -inf and zero gradients.
+* LSE = m + ln(l), natural log.
+
+Everything here works on float64 arrays laid out [B, H, N, d] (V may have its
+own last dimension).  Parity status: every public function is pinned by the
+CPU tests (worked example, closed forms, invariants, finite differences, and
+PyTorch's own fp64 attention routine).
+"""
+from __future__ import annotations
+
+import numpy as np
+
+NEG_INF = -np.inf
+
+
+# --------------------------------------------------------------------------- #
+# masks
+# --------------------------------------------------------------------------- #
+def visible(nq: int, nk: int, causal: bool = False, block_mask=None,
+            block: int = 128, rows=None) -> np.ndarray:
+    """Boolean [len(rows), nk]: True where query row i may attend to key j.
+
+    Causal: j <= i.  Block-sparse [P2 "Block-sparse Flashattention"]: the
+    N x N mask M is given at block granularity, M[i, j] = mask[i//block, j//block].
+    """
+    rows = np.arange(nq) if rows is None else np.asarray(rows)
+    cols = np.arange(nk)
+    vis = np.ones((rows.size, nk), dtype=bool)
+    if causal:
+        vis &= cols[None, :] <= rows[:, None]
+    if block_mask is not None:
+        bm = np.asarray(block_mask).astype(bool)
+        vis &= bm[rows[:, None] // block, cols[None, :] // block]
+    return vis
+
+
+# --------------------------------------------------------------------------- #
+# the definition: materialised S and P per (batch, head)
+# --------------------------------------------------------------------------- #
+def _scores(q: np.ndarray, k: np.ndarray, scale: float) -> np.ndarray:
+    """S = scale * q k^T for one head [P3 "flash attention" definitions]."""
+    return scale * (q @ k.T)
+
+
+def _apply_mask(s: np.ndarray, vis: np.ndarray) -> np.ndarray:
+    """Masked entries become -inf so they add nothing to m, l or O."""
+    return np.where(vis, s, NEG_INF)
+
+
+def _row_softmax(s: np.ndarray):
+    """Safe softmax per row [P1 2.1; P2 "Tiling"]: m = max, f = exp(s - m),
+    l = sum f, P = f / l.  Returns (P, m, l); an all -inf row gives P = 0."""
+    m = s.max(axis=1)
+    m_safe = np.where(np.isfinite(m), m, 0.0)
+    f = np.exp(s - m_safe[:, None])          # exp(-inf) = 0 on masked entries
+    l = f.sum(axis=1)
+    l_safe = np.where(l > 0, l, 1.0)
+    p = f / l_safe[:, None]
+    return p, m, l
+
+
+def _lse(m: np.ndarray, l: np.ndarray) -> np.ndarray:
+    """LSE = m + ln(l); -inf for a row without visible keys."""
+    with np.errstate(divide="ignore"):
+        return np.where(l > 0, m + np.log(np.where(l > 0, l, 1.0)), NEG_INF)
+
+
+def head_probs(q, k, scale, causal=False, block_mask=None, block=128, rows=None):
+    """P (rows x N) and LSE (rows) of one head, materialised."""
+    s = _scores(q if rows is None else q[np.asarray(rows)], k, scale)
+    s = _apply_mask(s, visible(q.shape[0], k.shape[0], causal, block_mask, block, rows))
+    p, m, l = _row_softmax(s)
+    return p, _lse(m, l)
+
+
+def forward(q, k, v, scale, causal=False, block_mask=None, block=128,
+            row_chunk: int | None = None):
+    """O = softmax(S) V and LSE for [B, H, N, d] fp64 inputs
+    [P2 "Standard Attention Implementation"; P3 definitions with the scale].
+
+    ``row_chunk`` splits the query rows of a head into chunks of full rows, so
+    a long sequence never holds all of S at once; each row's softmax is still
+    the plain definition over the whole row.
+    """
+    q, k, v = (np.asarray(x, dtype=np.float64) for x in (q, k, v))
+    B, H, N, _ = q.shape
+    o = np.zeros(q.shape[:3] + (v.shape[-1],))
+    lse = np.zeros((B, H, N))
+    step = N if row_chunk is None else row_chunk
+    for b in range(B):
+        for h in range(H):
+            for r0 in range(0, N, step):
+                rows = np.arange(r0, min(N, r0 + step))
+                p, lse_r = head_probs(q[b, h], k[b, h], scale, causal, block_mask,
+                                      block, rows if step != N else None)
+                o[b, h, rows] = p @ v[b, h]
+                lse[b, h, rows] = lse_r
+    return o, lse
+
+
+def forward_rows(q, k, v, scale, b, h, rows, causal=False, block_mask=None, block=128):
+    """O and LSE of selected query rows of head (b, h) only: for sampled checks
+    of workloads too large to materialise."""
+    q, k, v = (np.asarray(x, dtype=np.float64) for x in (q[b, h], k[b, h], v[b, h]))
+    p, lse = head_probs(q, k, scale, causal, block_mask, block, rows)
+    return p @ v, lse
+
+
+def _softmax_backward(p: np.ndarray, dp: np.ndarray, d_row: np.ndarray) -> np.ndarray:
+    """dS_ij = P_ij (dP_ij - D_i) [P2 "Backward Pass of flashattention"]."""
+    return p * (dp - d_row[:, None])
+
+
+def backward(q, k, v, do, scale, causal=False, block_mask=None, block=128):
+    """dQ, dK, dV and D for [B, H, N, d] fp64 inputs, using the oracle's own O and P.
+
+    Follows [P2 "Backward Pass of flashattention"] with the scale's chain rule:
+    dV = P^T dO;  dP = dO V^T;  D_i = sum_j P_ij dP_ij;  dS = P o (dP - D);
+    dQ = scale * dS K;  dK = scale * dS^T Q.
+    """
+    q, k, v, do = (np.asarray(x, dtype=np.float64) for x in (q, k, v, do))
+    B, H, N, _ = q.shape
+    dq, dk, dv = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
+    dvec = np.zeros((B, H, N))
+    for b in range(B):
+        for h in range(H):
+            p, _ = head_probs(q[b, h], k[b, h], scale, causal, block_mask, block)
+            dv[b, h] = p.T @ do[b, h]
+            dp = do[b, h] @ v[b, h].T
+            d_row = (p * dp).sum(axis=1)
+            ds = _softmax_backward(p, dp, d_row)
+            dq[b, h] = scale * (ds @ k[b, h])
+            dk[b, h] = scale * (ds.T @ q[b, h])
+            dvec[b, h] = d_row
+    return dq, dk, dv, dvec
+
+
+def backward_rows_dq(q, k, v, do, scale, b, h, rows, causal=False, block_mask=None,
+                     block=128):
+    """dQ of selected query rows of head (b, h) [P2: dq_i = sum_j P_ij (dP_ij - D_i) k_j],
+    with D_i taken as do_i . o_i of the oracle's own o_i."""
+    q, k, v, do = (np.asarray(x, dtype=np.float64) for x in (q[b, h], k[b, h], v[b, h], do[b, h]))
+    rows = np.asarray(rows)
+    p, _ = head_probs(q, k, scale, causal, block_mask, block, rows)
+    o = p @ v
+    dp = do[rows] @ v.T
+    d_row = (do[rows] * o).sum(axis=1)
+    return scale * (_softmax_backward(p, dp, d_row) @ k)
+
+
+# --------------------------------------------------------------------------- #
+# the tiled algorithm, step by step as the pages state it
+# --------------------------------------------------------------------------- #
+def tiled_forward(q, k, v, scale, Br: int, Bc: int, causal=False, block_mask=None,
+                  block=128, trace=False):
+    """Tiled forward with the online-softmax recurrence, one head at a time.
+
+    For each query tile Q_i (B_r rows) [P3 tiles T_r, T_c; V2 loop order]:
+    m = -inf, l = 0, O = 0; then for each key/value tile K_j, V_j (B_c rows)
+    [P4 section 6 pseudocode; P1 2.1 update rules]:
+        S_ij   = scale * Q_i K_j^T  (masked entries -inf)
+        m_new  = max(m, rowmax(S_ij))
+        l_new  = exp(m - m_new) l + rowsum(exp(S_ij - m_new))
+        O      = (l exp(m - m_new) O + exp(S_ij - m_new) V_j) / l_new
+        m, l   = m_new, l_new
+    and finally LSE = m + ln l.  Rows whose running max is still -inf skip the
+    update (nothing visible yet).  With ``trace`` it also returns, per head and
+    query tile, the (m, l, O) after every key tile.
+    """
+    q, k, v = (np.asarray(x, dtype=np.float64) for x in (q, k, v))
+    B, H, N, _ = q.shape
+    Nk = k.shape[2]
+    o_all = np.zeros(q.shape[:3] + (v.shape[-1],))
+    lse_all = np.zeros((B, H, N))
+    traces = []
+    for b in range(B):
+        for h in range(H):
+            for i0 in range(0, N, Br):
+                rows = np.arange(i0, min(N, i0 + Br))
+                m = np.full(rows.size, NEG_INF)
+                l = np.zeros(rows.size)
+                o = np.zeros((rows.size, v.shape[-1]))
+                tr = []
+                for j0 in range(0, Nk, Bc):
+                    cols = np.arange(j0, min(Nk, j0 + Bc))
+                    s = scale * (q[b, h, rows] @ k[b, h, cols].T)
+                    vis = visible(N, Nk, causal, block_mask, block, rows)[:, cols]
+                    s = np.where(vis, s, NEG_INF)
+                    m_new = np.maximum(m, s.max(axis=1))
+                    live = np.isfinite(m_new)
+                    mn = np.where(live, m_new, 0.0)
+                    alpha = np.where(live, np.exp(np.where(live, m, 0.0) - mn), 0.0)
+                    alpha = np.where(np.isfinite(m), alpha, 0.0)   # exp(-inf - m_new) = 0
+                    pt = np.exp(s - mn[:, None])
+                    l_new = alpha * l + pt.sum(axis=1)
+                    num = (l * alpha)[:, None] * o + pt @ v[b, h, cols]
+                    o = np.where(live[:, None], num / np.where(live, l_new, 1.0)[:, None], 0.0)
+                    m, l = np.where(live, m_new, NEG_INF), np.where(live, l_new, 0.0)
+                    if trace:
+                        tr.append((m.copy(), l.copy(), o.copy()))
+                o_all[b, h, rows] = o
+                lse_all[b, h, rows] = _lse(m, l)
+                if trace:
+                    traces.append(tr)
+    if trace:
+        return o_all, lse_all, traces
+    return o_all, lse_all
+
+
+def merge_stats(m1, l1, m2, l2):
+    """Merge (m, l) of two parts of a row [P2 "Tiling"]:
+    m = max(m1, m2);  l = exp(m1 - m) l1 + exp(m2 - m) l2."""
+    m = np.maximum(m1, m2)
+    return m, np.exp(m1 - m) * l1 + np.exp(m2 - m) * l2
+
+
+def flops(B, H, N, d, causal=False, backward=False, density=None) -> float:
+    """Algorithmic FLOP count: 4 B H N^2 d forward (two N x N x d products),
+    2.5x that backward (five products instead of two), halved when causal; a
+    block-sparse mask scales by the fraction of kept blocks."""
+    f = 4.0 * B * H * N * N * d
+    if backward:
+        f *= 2.5
+    if causal:
+        f *= 0.5
+    if density is not None:
+        f *= density
+    return f

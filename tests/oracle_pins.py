@@ -1,0 +1,257 @@
+"""Pins that tie the fp64 oracle to facts outside itself.
+
+Page shorthand: [P1] "【多模态大模型】FlashAttention in NeurIPS 2022" (coreui.cn);
+[P2] "FlashAttention" notes (maosong.website); [P3] "Transformer 入门"
+(cansult.github.io); [P4] "Как работает FlashAttention математически" (aivaro.ru).
+
+Each pin takes the oracle module and raises AssertionError when the oracle
+disagrees with: the pages' worked example, a closed form, an invariant the
+pages prove, central finite differences, or PyTorch's own fp64 attention
+routine with an independently built mask.  The mutation tests run the same
+pins against deliberately broken copies of the oracle and require a failure,
+so a plausible slip (dropped term, wrong sign or index, transposed operand)
+cannot pass unnoticed.
+"""
+from __future__ import annotations
+
+import json
+import math
+import os
+
+import numpy as np
+import torch
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _rng(seed):
+    return np.random.default_rng(seed)
+
+
+def _dense_mask_torch(N, causal=False, block_mask=None, block=128):
+    """Boolean [N, N] visibility built with torch ops, independently of the oracle."""
+    m = torch.ones(N, N, dtype=torch.bool)
+    if causal:
+        m = torch.tril(m)
+    if block_mask is not None:
+        bm = torch.as_tensor(np.asarray(block_mask)).bool()
+        m = m & bm.repeat_interleave(block, 0).repeat_interleave(block, 1)[:N, :N]
+    return m
+
+
+# --------------------------------------------------------------------------- #
+def pin_worked_example(orc):
+    """[P1 2.1] softmax([1,2,3,10]) in two blocks; V=[[1,2],[3,4],[5,6],[7,8]]."""
+    with open(os.path.join(GOLDEN, "worked_example.json")) as f:
+        g = json.load(f)
+    s = np.array(g["scores"])
+    V = np.array(g["V"])
+    # q . k_j = s_j with d = 1 and scale = 1 (the page applies no scale)
+    q = np.ones((1, 1, 1, 1))
+    k = s.reshape(1, 1, -1, 1)
+    v = V.reshape(1, 1, *V.shape)
+    o, lse = orc.forward(q, k, v, 1.0)
+    to, tlse, traces = orc.tiled_forward(q, k, v, 1.0, Br=1, Bc=g["block"], trace=True)
+
+    ex = [math.exp(e) for e in g["softmax_exponents"]]
+    p_expect = np.array(ex) / sum(ex)
+    p, lse_p = orc.head_probs(q[0, 0], k[0, 0], 1.0)
+    np.testing.assert_allclose(p[0], p_expect, rtol=1e-14, atol=0)
+    for step, st in zip(traces[0], g["after_block"]):
+        m_t, l_t, o_t = step
+        l_exp = sum(math.exp(e) for e in st["l_exponents"])
+        o_exp = sum(math.exp(e) * V[r] for r, e in zip(st["o_rows"], st["o_exponents"])) / l_exp
+        assert m_t[0] == st["m"]
+        np.testing.assert_allclose(l_t[0], l_exp, rtol=1e-14)
+        np.testing.assert_allclose(o_t[0], o_exp, rtol=1e-14)
+    final = g["after_block"][-1]
+    l_fin = sum(math.exp(e) for e in final["l_exponents"])
+    o_fin = sum(math.exp(e) * V[r] for r, e in zip(final["o_rows"], final["o_exponents"])) / l_fin
+    for oo in (o[0, 0, 0], to[0, 0, 0]):
+        np.testing.assert_allclose(oo, o_fin, rtol=1e-14)
+    for ll in (lse[0, 0, 0], tlse[0, 0, 0], lse_p[0]):
+        np.testing.assert_allclose(ll, final["m"] + math.log(l_fin), rtol=1e-14)
+
+
+# --------------------------------------------------------------------------- #
+def pin_closed_forms(orc):
+    r = _rng(1)
+    B, H, N, d = 1, 2, 37, 8
+    v = r.standard_normal((B, H, N, d))
+    k = r.standard_normal((B, H, N, d))
+    q0 = np.zeros((B, H, N, d))
+    scale = 0.3
+    # Q = 0: uniform weights -> O = mean of visible V rows, LSE = ln(#visible)
+    o, lse = orc.forward(q0, k, v, scale)
+    np.testing.assert_allclose(o, np.broadcast_to(v.mean(axis=2, keepdims=True), o.shape), atol=1e-13)
+    np.testing.assert_allclose(lse, np.full((B, H, N), math.log(N)), atol=1e-13)
+    o, lse = orc.forward(q0, k, v, scale, causal=True)
+    prefix = np.cumsum(v, axis=2) / np.arange(1, N + 1)[None, None, :, None]
+    np.testing.assert_allclose(o, prefix, atol=1e-13)
+    np.testing.assert_allclose(lse, np.broadcast_to(np.log(np.arange(1, N + 1)), lse.shape), atol=1e-13)
+    # block mask with block 4: row i sees the keys of its visible blocks
+    bm = (r.random((10, 10)) < 0.4).astype(np.uint8)
+    np.fill_diagonal(bm, 1)
+    o, lse = orc.forward(q0, k, v, scale, block_mask=bm, block=4)
+    for i in range(N):
+        keys = [j for j in range(N) if bm[i // 4, j // 4]]
+        np.testing.assert_allclose(o[:, :, i], v[:, :, keys].mean(axis=2), atol=1e-13)
+        np.testing.assert_allclose(lse[:, :, i], math.log(len(keys)), atol=1e-13)
+    # N = 1: O = V, LSE = scale * q . k
+    q1 = r.standard_normal((1, 1, 1, 5))
+    k1 = r.standard_normal((1, 1, 1, 5))
+    v1 = r.standard_normal((1, 1, 1, 3))
+    o, lse = orc.forward(q1, k1, v1, 0.7)
+    np.testing.assert_allclose(o, v1, rtol=1e-15)
+    np.testing.assert_allclose(lse[0, 0, 0], 0.7 * float(q1.ravel() @ k1.ravel()), rtol=1e-14)
+    # one key far above the rest: O equals that key's V row
+    qp = np.full((1, 1, 6, 4), 1e3)
+    kp = np.full((1, 1, 9, 4), -1.0)
+    kp[0, 0, 5] = 1.0                      # q . k_5 = 4e3, every other q . k_j = -4e3
+    vp = r.standard_normal((1, 1, 9, 3))
+    o, _ = orc.forward(qp, kp, vp, 1.0)
+    np.testing.assert_allclose(o[0, 0], np.broadcast_to(vp[0, 0, 5], (6, 3)), rtol=1e-12)
+
+
+# --------------------------------------------------------------------------- #
+def pin_invariants(orc):
+    r = _rng(2)
+    B, H, N, d = 2, 2, 45, 6
+    q, k, v = (r.standard_normal((B, H, N, d)) for _ in range(3))
+    scale = 1 / math.sqrt(d)
+    # rows of P sum to 1 [P1: softmax turns a row into a distribution]
+    for causal in (False, True):
+        p, lse = orc.head_probs(q[0, 1], k[0, 1], scale, causal=causal)
+        np.testing.assert_allclose(p.sum(axis=1), 1.0, atol=1e-14)
+        # LSE normalises exp(S): exp(S - LSE) reproduces P
+        s = scale * q[0, 1] @ k[0, 1].T
+        if causal:
+            s = np.where(np.tril(np.ones((N, N), bool)), s, -np.inf)
+        np.testing.assert_allclose(np.exp(s - lse[:, None]), p, atol=1e-14)
+    # shift invariance: add c_i to row i of S through an extra feature column
+    c = r.standard_normal(N) * 5
+    qa = np.concatenate([q, np.broadcast_to(c[None, None, :, None], (B, H, N, 1))], axis=-1)
+    ka = np.concatenate([k, np.full((B, H, N, 1), 1.0 / scale)], axis=-1)
+    o0, l0 = orc.forward(q, k, v, scale)
+    o1, l1 = orc.forward(qa, ka, v, scale)
+    np.testing.assert_allclose(o1, o0, atol=1e-12)
+    np.testing.assert_allclose(l1, l0 + c[None, None, :], atol=1e-12)
+    # tiled == materialised for any split point (Theorem 1), incl. 1 and non-divisors
+    bm = (r.random((12, 12)) < 0.5).astype(np.uint8)
+    np.fill_diagonal(bm, 1)
+    for causal, mask in ((False, None), (True, None), (False, bm)):
+        ref_o, ref_l = orc.forward(q, k, v, scale, causal=causal, block_mask=mask, block=4)
+        for Br, Bc in ((1, 1), (2, 3), (7, 16), (16, 7), (45, 45), (128, 128)):
+            to, tl = orc.tiled_forward(q, k, v, scale, Br, Bc, causal=causal,
+                                       block_mask=mask, block=4)
+            np.testing.assert_allclose(to, ref_o, atol=1e-12)
+            np.testing.assert_allclose(tl, ref_l, atol=1e-12)
+    # merge of (m, l) is exact for every split point [P2 "Tiling"]
+    x = r.standard_normal(40) * 4
+    for cut in range(1, 40):
+        a, b = x[:cut], x[cut:]
+        m, l = orc.merge_stats(a.max(), np.exp(a - a.max()).sum(), b.max(), np.exp(b - b.max()).sum())
+        assert m == x.max()
+        np.testing.assert_allclose(l, np.exp(x - x.max()).sum(), rtol=1e-14)
+    # causal row i == non-causal attention over keys 0..i
+    oc, lc = orc.forward(q, k, v, scale, causal=True)
+    for i in (0, 1, 17, N - 1):
+        op, lp = orc.forward(q[:, :, i:i + 1], k[:, :, :i + 1], v[:, :, :i + 1], scale)
+        np.testing.assert_allclose(oc[:, :, i], op[:, :, 0], atol=1e-13)
+        np.testing.assert_allclose(lc[:, :, i], lp[:, :, 0], atol=1e-13)
+    # block mask of all ones == dense; diagonal-only == independent blocks
+    Nb = 3 * 4
+    qb, kb, vb = q[:, :, :Nb], k[:, :, :Nb], v[:, :, :Nb]
+    od, ld = orc.forward(qb, kb, vb, scale)
+    o1, l1 = orc.forward(qb, kb, vb, scale, block_mask=np.ones((3, 3), np.uint8), block=4)
+    np.testing.assert_allclose(o1, od, atol=1e-14)
+    np.testing.assert_allclose(l1, ld, atol=1e-14)
+    o2, l2 = orc.forward(qb, kb, vb, scale, block_mask=np.eye(3, dtype=np.uint8), block=4)
+    for blk in range(3):
+        sl = slice(4 * blk, 4 * blk + 4)
+        ob, lb = orc.forward(qb[:, :, sl], kb[:, :, sl], vb[:, :, sl], scale)
+        np.testing.assert_allclose(o2[:, :, sl], ob, atol=1e-13)
+        np.testing.assert_allclose(l2[:, :, sl], lb, atol=1e-13)
+    # sampled-row helpers agree with the full computation
+    rows = [0, 3, 44]
+    orr, lrr = orc.forward_rows(q, k, v, scale, 1, 0, rows, causal=True)
+    np.testing.assert_allclose(orr, oc[1, 0, rows], atol=1e-14)
+    np.testing.assert_allclose(lrr, lc[1, 0, rows], atol=1e-14)
+
+
+# --------------------------------------------------------------------------- #
+def pin_backward_fd(orc):
+    """Central finite differences of phi = sum(dO o O) on tiny inputs."""
+    r = _rng(3)
+    cases = [(3, 2, False, None), (5, 4, True, None), (8, 2, False, "block"), (8, 4, True, "block")]
+    for N, d, causal, mk in cases:
+        q, k, v, do = (r.standard_normal((1, 1, N, d)) for _ in range(4))
+        scale = 1 / math.sqrt(d) * 1.3
+        bm = None
+        if mk:
+            bm = np.array([[1, 0, 1, 0], [1, 1, 0, 0], [0, 1, 1, 0], [1, 0, 1, 1]], np.uint8)
+
+        def phi(q_, k_, v_):
+            o, _ = orc.forward(q_, k_, v_, scale, causal=causal, block_mask=bm, block=2)
+            return float((o * do).sum())
+
+        dq, dk, dv, _ = orc.backward(q, k, v, do, scale, causal=causal, block_mask=bm, block=2)
+        h = 1e-6
+        for which, g in ((0, dq), (1, dk), (2, dv)):
+            fd = np.zeros_like(g)
+            for idx in np.ndindex(g.shape):
+                args_p = [q.copy(), k.copy(), v.copy()]
+                args_m = [q.copy(), k.copy(), v.copy()]
+                args_p[which][idx] += h
+                args_m[which][idx] -= h
+                fd[idx] = (phi(*args_p) - phi(*args_m)) / (2 * h)
+            err = np.linalg.norm(fd - g) / max(np.linalg.norm(fd), 1e-30)
+            assert err <= 1e-6, (N, d, causal, mk, which, err)
+
+
+def pin_dvec(orc):
+    """D_i = rowsum(P o dP) equals dO_i . O_i [P2 "Backward Pass of flashattention"]."""
+    r = _rng(4)
+    q, k, v, do = (r.standard_normal((1, 2, 33, 8)) for _ in range(4))
+    for causal in (False, True):
+        o, _ = orc.forward(q, k, v, 0.4, causal=causal)
+        _, _, _, dvec = orc.backward(q, k, v, do, 0.4, causal=causal)
+        np.testing.assert_allclose(dvec, (do * o).sum(axis=-1), atol=1e-12)
+
+
+def pin_backward_rows(orc):
+    r = _rng(6)
+    q, k, v, do = (r.standard_normal((1, 2, 29, 4)) for _ in range(4))
+    dq, _, _, _ = orc.backward(q, k, v, do, 0.5, causal=True)
+    rows = [0, 9, 28]
+    np.testing.assert_allclose(orc.backward_rows_dq(q, k, v, do, 0.5, 0, 1, rows, causal=True),
+                               dq[0, 1, rows], atol=1e-13)
+
+
+# --------------------------------------------------------------------------- #
+def pin_library(orc):
+    """PyTorch's fp64 scaled_dot_product_attention and autograd, with masks
+    built by torch ops, on shapes that span several blocks and a ragged tail."""
+    r = _rng(5)
+    B, H, N, d = 2, 3, 70, 16
+    q, k, v, do = (r.standard_normal((B, H, N, d)) for _ in range(4))
+    scale = 1 / math.sqrt(d)
+    bm = (r.random((5, 5)) < 0.4).astype(np.uint8)
+    np.fill_diagonal(bm, 1)
+    bm[0, 3] = 1
+    bm[3, 0] = 0                                           # make it asymmetric
+    for causal, mask in ((False, None), (True, None), (False, bm), (True, bm)):
+        tq, tk, tv = (torch.tensor(x, requires_grad=True) for x in (q, k, v))
+        am = _dense_mask_torch(N, causal, mask, block=16)
+        ref = torch.nn.functional.scaled_dot_product_attention(tq, tk, tv, attn_mask=am, scale=scale)
+        ref.backward(torch.tensor(do))
+        o, _ = orc.forward(q, k, v, scale, causal=causal, block_mask=mask, block=16)
+        dq, dk, dv, _ = orc.backward(q, k, v, do, scale, causal=causal, block_mask=mask, block=16)
+        np.testing.assert_allclose(o, ref.detach().numpy(), atol=1e-12)
+        np.testing.assert_allclose(dq, tq.grad.numpy(), atol=1e-11)
+        np.testing.assert_allclose(dk, tk.grad.numpy(), atol=1e-11)
+        np.testing.assert_allclose(dv, tv.grad.numpy(), atol=1e-11)
+
+
+ALL_PINS = [pin_worked_example, pin_closed_forms, pin_invariants, pin_backward_fd,
+            pin_dvec, pin_backward_rows, pin_library]

@@ -1,0 +1,144 @@
+"""Plant plausible mistakes in the oracle (on the CPU) and require that at least
+one pin fails for each: a dropped term, a wrong sign or index, a transposed
+operand.  This checks the pins, not the CUDA path."""
+import numpy as np
+import pytest
+
+import oracle.attention as orc
+from tests import oracle_pins as pins
+
+_real = {name: getattr(orc, name) for name in
+         ("_scores", "_apply_mask", "_row_softmax", "_softmax_backward", "visible",
+          "forward", "backward", "tiled_forward", "_lse")}
+
+
+def _m_no_scale(q, k, scale):
+    return q @ k.T
+
+
+def _m_transposed_scores(q, k, scale):
+    s = scale * (q @ k.T)
+    return s.T if s.shape[0] == s.shape[1] else s
+
+
+def _m_mask_zero(s, vis):            # masked entries set to 0 instead of -inf
+    return np.where(vis, s, 0.0)
+
+
+def _m_softmax_no_norm(s):
+    p, m, l = _real["_row_softmax"](s)
+    return p * l[:, None], m, l
+
+
+def _m_ds_sign(p, dp, d_row):
+    return p * (dp + d_row[:, None])
+
+
+def _m_ds_no_d(p, dp, d_row):
+    return p * dp
+
+
+def _m_causal_strict(nq, nk, causal=False, block_mask=None, block=128, rows=None):
+    vis = _real["visible"](nq, nk, False, block_mask, block, rows)
+    if causal:
+        r = np.arange(nq) if rows is None else np.asarray(rows)
+        vis &= np.arange(nk)[None, :] < np.maximum(r[:, None], 1)
+    return vis
+
+
+def _m_block_transposed(nq, nk, causal=False, block_mask=None, block=128, rows=None):
+    bm = None if block_mask is None else np.asarray(block_mask).T
+    return _real["visible"](nq, nk, causal, bm, block, rows)
+
+
+def _m_fwd_kv_swapped(q, k, v, scale, **kw):
+    if k.shape == v.shape:
+        return _real["forward"](q, v, k, scale, **kw)
+    return _real["forward"](q, k, v, scale, **kw)
+
+
+def _m_bwd_dk_unscaled(q, k, v, do, scale, **kw):
+    dq, dk, dv, dvec = _real["backward"](q, k, v, do, scale, **kw)
+    return dq, dk / scale, dv, dvec
+
+
+def _m_bwd_dq_transposed(q, k, v, do, scale, causal=False, block_mask=None, block=128):
+    dq, dk, dv, dvec = _real["backward"](q, k, v, do, scale, causal=causal,
+                                         block_mask=block_mask, block=block)
+    q64, k64, v64, do64 = (np.asarray(x, np.float64) for x in (q, k, v, do))
+    for b in range(q64.shape[0]):
+        for h in range(q64.shape[1]):
+            p, _ = orc.head_probs(q64[b, h], k64[b, h], scale, causal, block_mask, block)
+            dp = do64[b, h] @ v64[b, h].T
+            ds = p * (dp - (p * dp).sum(1)[:, None])
+            dq[b, h] = scale * (ds.T @ k64[b, h])
+    return dq, dk, dv, dvec
+
+
+def _m_tiled_l_no_alpha(q, k, v, scale, Br, Bc, causal=False, block_mask=None, block=128,
+                        trace=False):
+    """The tiled recurrence with the exp(m - m_new) factor dropped from the l update."""
+    q, k, v = (np.asarray(x, np.float64) for x in (q, k, v))
+    B, H, N, _ = q.shape
+    o_all = np.zeros(q.shape[:3] + (v.shape[-1],))
+    lse_all = np.zeros((B, H, N))
+    traces = []
+    for b in range(B):
+        for h in range(H):
+            for i0 in range(0, N, Br):
+                rows = np.arange(i0, min(N, i0 + Br))
+                m = np.full(rows.size, -np.inf)
+                l = np.zeros(rows.size)
+                o = np.zeros((rows.size, v.shape[-1]))
+                tr = []
+                for j0 in range(0, k.shape[2], Bc):
+                    cols = np.arange(j0, min(k.shape[2], j0 + Bc))
+                    s = scale * (q[b, h, rows] @ k[b, h, cols].T)
+                    vis = orc.visible(N, k.shape[2], causal, block_mask, block, rows)[:, cols]
+                    s = np.where(vis, s, -np.inf)
+                    m_new = np.maximum(m, s.max(axis=1))
+                    mn = np.where(np.isfinite(m_new), m_new, 0.0)
+                    alpha = np.exp(np.where(np.isfinite(m), m, -np.inf) - mn)
+                    pt = np.exp(s - mn[:, None])
+                    l_new = l + pt.sum(axis=1)                       # planted mistake
+                    o = ((l * alpha)[:, None] * o + pt @ v[b, h, cols]) / np.where(l_new > 0, l_new, 1)[:, None]
+                    m, l = m_new, l_new
+                    tr.append((m.copy(), l.copy(), o.copy()))
+                o_all[b, h, rows] = o
+                lse_all[b, h, rows] = np.where(l > 0, m + np.log(np.where(l > 0, l, 1)), -np.inf)
+                traces.append(tr)
+    return (o_all, lse_all, traces) if trace else (o_all, lse_all)
+
+
+def _m_lse_log2(m, l):
+    return np.where(l > 0, m + np.log2(np.where(l > 0, l, 1.0)), -np.inf)
+
+
+MUTANTS = {
+    "scale_dropped": ("_scores", _m_no_scale),
+    "scores_transposed": ("_scores", _m_transposed_scores),
+    "mask_as_zero": ("_apply_mask", _m_mask_zero),
+    "softmax_unnormalised": ("_row_softmax", _m_softmax_no_norm),
+    "dS_sign_flipped": ("_softmax_backward", _m_ds_sign),
+    "dS_missing_D": ("_softmax_backward", _m_ds_no_d),
+    "causal_off_by_one": ("visible", _m_causal_strict),
+    "block_mask_transposed": ("visible", _m_block_transposed),
+    "forward_kv_swapped": ("forward", _m_fwd_kv_swapped),
+    "dK_scale_dropped": ("backward", _m_bwd_dk_unscaled),
+    "dQ_dS_transposed": ("backward", _m_bwd_dq_transposed),
+    "tiled_l_rescale_dropped": ("tiled_forward", _m_tiled_l_no_alpha),
+    "lse_wrong_base": ("_lse", _m_lse_log2),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_mutant_is_caught(name, monkeypatch):
+    attr, fn = MUTANTS[name]
+    monkeypatch.setattr(orc, attr, fn)
+    failures = []
+    for pin in pins.ALL_PINS:
+        try:
+            pin(orc)
+        except (AssertionError, ValueError, IndexError):
+            failures.append(pin.__name__)
+    assert failures, f"mutant {name} passed every pin"
