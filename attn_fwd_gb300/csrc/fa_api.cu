@@ -1,0 +1,372 @@
+// fa_api.cu -- the C ABI of libfa.so (declared in include/fa.h): argument
+// validation, device checks, TMA tensor-map encoding, the device status word
+// and the launches of the attention kernels.
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include "../../include/fa.h"
+#include "fa_common.cuh"
+#include "fa_ptx.cuh"
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr int kVersion = 100;  // 0.1.0
+
+// One status word per device; kernels record FA_ERR_TIMEOUT here.
+__device__ int g_fa_status;
+
+std::atomic<uint64_t> g_timeout_ns{2000000000ull};
+
+struct DeviceState {
+  std::once_flag once;
+  int arch_ok = 0;      // 1 when compute capability is 10.3
+  int* status = nullptr;
+  cudaError_t err = cudaSuccess;
+};
+DeviceState g_dev[kMaxDevices];
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+bool log_enabled() {
+  static const bool on = [] {
+    const char* e = std::getenv("FA_LOG");
+    return e && e[0] == '1';
+  }();
+  return on;
+}
+
+// Current device, checked once per device: compute capability 10.3 and the
+// device address of its status word.
+int device_ready(int** status_out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FA_ERR_CUDA;
+  DeviceState& st = g_dev[dev];
+  std::call_once(st.once, [&] {
+    int major = 0, minor = 0;
+    st.err = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    if (st.err == cudaSuccess) st.err = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    st.arch_ok = (major == 10 && minor == 3) ? 1 : 0;
+    if (st.err == cudaSuccess && st.arch_ok) {
+      void* a = nullptr;
+      st.err = cudaGetSymbolAddress(&a, g_fa_status);
+      st.status = static_cast<int*>(a);
+    }
+  });
+  if (st.err != cudaSuccess) return FA_ERR_CUDA;
+  if (!st.arch_ok) return FA_ERR_ARCH;
+  *status_out = st.status;
+  return FA_OK;
+}
+
+int encoder_ready() {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  return g_encode ? FA_OK : FA_ERR_CUDA;
+}
+
+// 3-D map over a bf16 array [BH][N][d]: box {64, box_rows, 1}, 128-byte
+// swizzle, zero fill outside the array.
+int make_map_bf16(CUtensorMap* m, const void* ptr, int BH, int N, int d, int box_rows) {
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(BH)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(N) * d * 2};
+  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_rows), 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Shape and scalar checks shared by every compute entry point.
+int check_shape(int B, int H, int N, int d) {
+  if (B < 1 || H < 1 || N < 1 || d < 1) return FA_ERR_INVALID;
+  const long long elems = static_cast<long long>(B) * H * N * d;
+  if (elems >= (1ll << 31)) return FA_ERR_INVALID;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  if (N % fa::TILE != 0) return FA_ERR_UNSUPPORTED;
+  return FA_OK;
+}
+
+int check_scale(float scale) { return (std::isfinite(scale) && scale > 0.f) ? FA_OK : FA_ERR_INVALID; }
+
+int check_ptrs(std::initializer_list<const void*> ps) {
+  for (const void* p : ps)
+    if (p == nullptr || !aligned16(p)) return FA_ERR_INVALID;
+  return FA_OK;
+}
+
+struct Workspace {
+  float* dq_acc;
+  float* dvec;
+};
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+Workspace carve(void* ws, int B, int H, int N, int d) {
+  const size_t rows = static_cast<size_t>(B) * H * N;
+  char* base = static_cast<char*>(ws);
+  Workspace w;
+  w.dq_acc = reinterpret_cast<float*>(base);
+  w.dvec = reinterpret_cast<float*>(base + align256(rows * d * sizeof(float)));
+  return w;
+}
+
+int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, const uint8_t* block_mask,
+             int B, int H, int N, int d, float scale, int mask_kind, fa_stream_t stream) {
+  int rc;
+  if ((rc = check_ptrs({q, k, v, o, lse})) != FA_OK) return rc;
+  if (mask_kind == fa::MASK_BLOCK && block_mask == nullptr) return FA_ERR_INVALID;
+  if ((rc = check_shape(B, H, N, d)) != FA_OK) return rc;
+  if ((rc = check_scale(scale)) != FA_OK) return rc;
+  int* status = nullptr;
+  if ((rc = device_ready(&status)) != FA_OK) return rc;
+  if ((rc = encoder_ready()) != FA_OK) return rc;
+
+  fa::FwdParams p;
+  std::memset(&p, 0, sizeof(p));
+  const int BH = B * H;
+  if (make_map_bf16(&p.tm_q, q, BH, N, d, fa::TILE) != FA_OK || make_map_bf16(&p.tm_k, k, BH, N, d, fa::TILE) != FA_OK ||
+      make_map_bf16(&p.tm_v, v, BH, N, d, fa::TILE) != FA_OK)
+    return FA_ERR_CUDA;
+  p.o = static_cast<__nv_bfloat16*>(o);
+  p.lse = lse;
+  p.block_mask = block_mask;
+  p.status = status;
+  p.timeout_ns = g_timeout_ns.load(std::memory_order_relaxed);
+  p.N = N;
+  p.BH = BH;
+  p.n_qt = N / fa::TILE;
+  p.n_pairs = (p.n_qt + 1) / 2;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.mask_kind = mask_kind;
+  if (log_enabled())
+    std::fprintf(stderr, "[fa] fwd B=%d H=%d N=%d d=%d mask=%d grid=%d\n", B, H, N, d, mask_kind, p.n_pairs * BH);
+  return fa::launch_fwd(p, d, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int bwd_main_impl(const void* q, const void* k, const void* v, const void* dout, const float* lse,
+                  const uint8_t* block_mask, void* dk, void* dv, void* workspace, int B, int H, int N, int d,
+                  float scale, int mask_kind, fa_stream_t stream) {
+  int rc;
+  if ((rc = check_ptrs({q, k, v, dout, lse, dk, dv, workspace})) != FA_OK) return rc;
+  if (mask_kind < 0 || mask_kind > 2) return FA_ERR_INVALID;
+  if (mask_kind == fa::MASK_BLOCK && block_mask == nullptr) return FA_ERR_INVALID;
+  if ((rc = check_shape(B, H, N, d)) != FA_OK) return rc;
+  if ((rc = check_scale(scale)) != FA_OK) return rc;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return FA_ERR_INVALID;
+  int* status = nullptr;
+  if ((rc = device_ready(&status)) != FA_OK) return rc;
+  if ((rc = encoder_ready()) != FA_OK) return rc;
+
+  const int BH = B * H;
+  const int bq = (d == 128) ? 64 : 128;  // query rows per backward step
+  fa::BwdParams p;
+  std::memset(&p, 0, sizeof(p));
+  if (make_map_bf16(&p.tm_q, q, BH, N, d, bq) != FA_OK || make_map_bf16(&p.tm_do, dout, BH, N, d, bq) != FA_OK ||
+      make_map_bf16(&p.tm_k, k, BH, N, d, fa::TILE) != FA_OK || make_map_bf16(&p.tm_v, v, BH, N, d, fa::TILE) != FA_OK)
+    return FA_ERR_CUDA;
+  Workspace w = carve(workspace, B, H, N, d);
+  p.lse = lse;
+  p.dvec = w.dvec;
+  p.dq_acc = w.dq_acc;
+  p.dk = static_cast<__nv_bfloat16*>(dk);
+  p.dv = static_cast<__nv_bfloat16*>(dv);
+  p.block_mask = block_mask;
+  p.status = status;
+  p.timeout_ns = g_timeout_ns.load(std::memory_order_relaxed);
+  p.N = N;
+  p.BH = BH;
+  p.n_kt = N / fa::TILE;
+  p.scale = scale;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.mask_kind = mask_kind;
+  if (log_enabled())
+    std::fprintf(stderr, "[fa] bwd B=%d H=%d N=%d d=%d mask=%d bq=%d\n", B, H, N, d, mask_kind, bq);
+  return fa::launch_bwd_main(p, d, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int preprocess_impl(const void* o, const void* dout, void* workspace, int B, int H, int N, int d,
+                    fa_stream_t stream) {
+  int rc;
+  if ((rc = check_ptrs({o, dout, workspace})) != FA_OK) return rc;
+  if ((rc = check_shape(B, H, N, d)) != FA_OK) return rc;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return FA_ERR_INVALID;
+  int* status = nullptr;
+  if ((rc = device_ready(&status)) != FA_OK) return rc;
+  Workspace w = carve(workspace, B, H, N, d);
+  return fa::launch_bwd_preprocess(static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dout),
+                                   w.dvec, w.dq_acc, B * H * N, d, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int convert_impl(const void* workspace, void* dq, int B, int H, int N, int d, float scale, fa_stream_t stream) {
+  int rc;
+  if ((rc = check_ptrs({workspace, dq})) != FA_OK) return rc;
+  if ((rc = check_shape(B, H, N, d)) != FA_OK) return rc;
+  if ((rc = check_scale(scale)) != FA_OK) return rc;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return FA_ERR_INVALID;
+  int* status = nullptr;
+  if ((rc = device_ready(&status)) != FA_OK) return rc;
+  Workspace w = carve(const_cast<void*>(workspace), B, H, N, d);
+  return fa::launch_bwd_dq_convert(w.dq_acc, static_cast<__nv_bfloat16*>(dq),
+                                   static_cast<long long>(B) * H * N * d, scale,
+                                   reinterpret_cast<cudaStream_t>(stream));
+}
+
+int bwd_impl(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
+             const uint8_t* block_mask, void* dq, void* dk, void* dv, void* workspace, int B, int H, int N, int d,
+             float scale, int mask_kind, fa_stream_t stream) {
+  int rc;
+  // validate everything first so that nothing is enqueued on a bad call
+  if ((rc = check_ptrs({q, k, v, o, dout, lse, dq, dk, dv, workspace})) != FA_OK) return rc;
+  if (mask_kind == fa::MASK_BLOCK && block_mask == nullptr) return FA_ERR_INVALID;
+  if ((rc = check_shape(B, H, N, d)) != FA_OK) return rc;
+  if ((rc = check_scale(scale)) != FA_OK) return rc;
+  if ((rc = preprocess_impl(o, dout, workspace, B, H, N, d, stream)) != FA_OK) return rc;
+  if ((rc = bwd_main_impl(q, k, v, dout, lse, block_mask, dk, dv, workspace, B, H, N, d, scale, mask_kind,
+                          stream)) != FA_OK)
+    return rc;
+  return convert_impl(workspace, dq, B, H, N, d, scale, stream);
+}
+
+}  // namespace
+
+// --------------------------------------------------------------------------
+// the timeout self-test kernel: waits on a barrier that nothing completes
+// --------------------------------------------------------------------------
+namespace fa {
+__global__ void wait_timeout_probe_kernel(int* status, uint64_t timeout_ns) {
+  __shared__ __align__(8) uint64_t b;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&b), 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  const WaitCtx wc{&abort_flag, status, timeout_ns};
+  if (threadIdx.x < 32) (void)mbar_wait_warp(smem_u32(&b), 0, wc);
+  __syncthreads();
+}
+
+int launch_wait_timeout_probe(int* status, uint64_t timeout_ns, cudaStream_t stream) {
+  wait_timeout_probe_kernel<<<1, 64, 0, stream>>>(status, timeout_ns);
+  return cudaGetLastError() == cudaSuccess ? 0 : -4;
+}
+}  // namespace fa
+
+// --------------------------------------------------------------------------
+// exported C ABI
+// --------------------------------------------------------------------------
+extern "C" {
+
+int fa_version(void) { return kVersion; }
+
+const char* fa_status_string(int status) {
+  switch (status) {
+    case FA_OK: return "FA_OK";
+    case FA_ERR_INVALID: return "FA_ERR_INVALID: invalid argument";
+    case FA_ERR_UNSUPPORTED: return "FA_ERR_UNSUPPORTED: head dim must be 64 or 128 and N a multiple of 128";
+    case FA_ERR_ARCH: return "FA_ERR_ARCH: device is not compute capability 10.3";
+    case FA_ERR_LAUNCH: return "FA_ERR_LAUNCH: kernel launch failed";
+    case FA_ERR_TIMEOUT: return "FA_ERR_TIMEOUT: a kernel wait exceeded the wait timeout";
+    case FA_ERR_CUDA: return "FA_ERR_CUDA: CUDA runtime error";
+    default: return "unknown fa_status";
+  }
+}
+
+int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
+           float scale, int causal, fa_stream_t stream) {
+  return fwd_impl(q, k, v, o, lse, nullptr, B, H, N, d, scale, causal ? fa::MASK_CAUSAL : fa::MASK_NONE, stream);
+}
+
+int fa_fwd_blocksparse(const void* q, const void* k, const void* v, void* o, float* lse, const uint8_t* block_mask,
+                       int B, int H, int N, int d, float scale, fa_stream_t stream) {
+  return fwd_impl(q, k, v, o, lse, block_mask, B, H, N, d, scale, fa::MASK_BLOCK, stream);
+}
+
+size_t fa_bwd_workspace_bytes(int B, int H, int N, int d) {
+  if (B < 1 || H < 1 || N < 1 || d < 1) return 0;
+  if (static_cast<long long>(B) * H * N * d >= (1ll << 31)) return 0;
+  const size_t rows = static_cast<size_t>(B) * H * N;
+  return align256(rows * d * sizeof(float)) + align256(rows * sizeof(float));
+}
+
+int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse, void* dq,
+           void* dk, void* dv, void* workspace, int B, int H, int N, int d, float scale, int causal,
+           fa_stream_t stream) {
+  return bwd_impl(q, k, v, o, dout, lse, nullptr, dq, dk, dv, workspace, B, H, N, d, scale,
+                  causal ? fa::MASK_CAUSAL : fa::MASK_NONE, stream);
+}
+
+int fa_bwd_blocksparse(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                       const float* lse, const uint8_t* block_mask, void* dq, void* dk, void* dv, void* workspace,
+                       int B, int H, int N, int d, float scale, fa_stream_t stream) {
+  return bwd_impl(q, k, v, o, dout, lse, block_mask, dq, dk, dv, workspace, B, H, N, d, scale, fa::MASK_BLOCK,
+                  stream);
+}
+
+int fa_bwd_preprocess(const void* o, const void* dout, void* workspace, int B, int H, int N, int d,
+                      fa_stream_t stream) {
+  return preprocess_impl(o, dout, workspace, B, H, N, d, stream);
+}
+
+int fa_bwd_main(const void* q, const void* k, const void* v, const void* dout, const float* lse,
+                const uint8_t* block_mask, void* dk, void* dv, void* workspace, int B, int H, int N, int d,
+                float scale, int mask_kind, fa_stream_t stream) {
+  return bwd_main_impl(q, k, v, dout, lse, block_mask, dk, dv, workspace, B, H, N, d, scale, mask_kind, stream);
+}
+
+int fa_bwd_dq_convert(const void* workspace, void* dq, int B, int H, int N, int d, float scale, fa_stream_t stream) {
+  return convert_impl(workspace, dq, B, H, N, d, scale, stream);
+}
+
+int fa_get_device_error(fa_stream_t stream) {
+  int* status = nullptr;
+  int rc = device_ready(&status);
+  if (rc != FA_OK) return rc;
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return FA_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_fa_status, sizeof(int)) != cudaSuccess) return FA_ERR_CUDA;
+  if (v != 0) {
+    const int zero = 0;
+    if (cudaMemcpyToSymbol(g_fa_status, &zero, sizeof(int)) != cudaSuccess) return FA_ERR_CUDA;
+  }
+  return v;
+}
+
+int fa_set_wait_timeout_ns(uint64_t ns) {
+  if (ns == 0) return FA_ERR_INVALID;
+  g_timeout_ns.store(ns, std::memory_order_relaxed);
+  return FA_OK;
+}
+
+int fa_debug_wait_timeout(uint64_t timeout_ns, fa_stream_t stream) {
+  if (timeout_ns == 0 || timeout_ns > 1000000000ull) return FA_ERR_INVALID;
+  int* status = nullptr;
+  int rc = device_ready(&status);
+  if (rc != FA_OK) return rc;
+  if (fa::launch_wait_timeout_probe(status, timeout_ns, reinterpret_cast<cudaStream_t>(stream)) != 0)
+    return FA_ERR_LAUNCH;
+  return fa_get_device_error(stream);
+}
+
+}  // extern "C"

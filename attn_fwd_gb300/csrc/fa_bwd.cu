@@ -1,0 +1,456 @@
+// fa_bwd.cu -- backward main kernel for sm_103a: recompute P from Q, K and
+// the saved LSE, then accumulate dK, dV and the fp32 dQ accumulator.
+//
+// What one CTA computes ("FlashAttention" notes, "Backward Pass of
+// flashattention"): for one 128-row key tile K_j, V_j of one (batch, head)
+// and every visible query tile Q_i (BQ rows), with the scale's chain rule:
+//   S_ij  = scale * Q_i K_j^T,  P_ij = exp(S_ij - LSE_i)      (recompute)
+//   dV_j += P_ij^T dO_i
+//   dP_ij = dO_i V_j^T,  dS_ij = P_ij o (dP_ij - D_i)           (D_i = dO_i . O_i)
+//   dK_j += scale * dS_ij^T Q_i
+//   dQ_i += dS_ij K_j   (fp32 reductions into the accumulator; scaled later)
+// Masks are regenerated from (i, j) or the block mask, never stored.  K_j and
+// V_j stay in shared memory for the whole loop (the key/value-stationary loop
+// order of "Transformer 入门", V1), so dK_j and dV_j are written once.
+//
+// The five products run on the tensor cores (tcgen05, fp32 accumulators in
+// tensor memory), computed transposed so that the key index is the
+// tensor-memory lane, i.e. one softmax thread per key:
+//   S^T  = K_j Q_i^T          (M=128 keys, N=BQ, K=d)   A,B K-major
+//   dP^T = V_j dO_i^T         (M=128, N=BQ, K=d)        A,B K-major
+//   dV  += P^T dO_i           (M=128, N=d, K=BQ)        A = P^T (smem), B MN-major
+//   dK  += dS^T Q_i           (M=128, N=d, K=BQ)        A = dS^T (smem), B MN-major
+//   d=128: dQ^T = K_j^T dS^T  (M=d=128, N=BQ=64, K=128) A,B MN-major
+//   d=64:  dQ   = dS K_j      (M=BQ=128, N=d, K=128)    A,B MN-major
+// The d=128 form keeps the head-dim index on the lanes, so each warp's fp32
+// reduction covers 32 consecutive floats of one dQ row (128-byte coalesced).
+//
+// Warp roles (10 warps): 0-3 recompute P and dS (thread = key row), write
+// P^T and dS^T (bf16, 128-byte swizzle) to shared memory; 4-7 drain dQ from
+// tensor memory into the fp32 accumulator; 8 issues MMAs; 9 loads K_j, V_j
+// once and Q_i, dO_i, LSE_i, D_i per step into a two-stage ring.
+#include "fa_common.cuh"
+#include "fa_ptx.cuh"
+
+namespace fa {
+
+template <int D>
+struct BwdLayout {
+  static constexpr int BQ = (D == 128) ? 64 : 128;          // query rows per step
+  static constexpr bool DQ_T = (D == 128);                  // dQ computed transposed
+  static constexpr int NCH = D / 64;
+  static constexpr int KV_CHUNK = TILE * 128;               // [128 rows][128 B]
+  static constexpr int KV_BYTES = NCH * KV_CHUNK;           // 128 x D bf16
+  static constexpr int Q_CHUNK = BQ * 128;                  // [BQ rows][128 B]
+  static constexpr int Q_BYTES = NCH * Q_CHUNK;             // BQ x D bf16
+  static constexpr int STAGES = 2;
+  static constexpr int ST_Q = 0;
+  static constexpr int ST_DO = Q_BYTES;
+  static constexpr int ST_LSE = 2 * Q_BYTES;
+  static constexpr int ST_DV = 2 * Q_BYTES + BQ * 4;
+  static constexpr int STAGE_BYTES = ((2 * Q_BYTES + 2 * BQ * 4) + 1023) / 1024 * 1024;
+  static constexpr int PT_CHUNK = TILE * 128;               // [128 key rows][64 queries]
+  static constexpr int PT_BYTES = (BQ / 64) * PT_CHUNK;     // 128 x BQ bf16
+  static constexpr int PBUFS = (D == 128) ? 2 : 1;          // P^T / dS^T buffers
+  static constexpr int K_OFF = 0;
+  static constexpr int V_OFF = KV_BYTES;
+  static constexpr int RING_OFF = 2 * KV_BYTES;
+  static constexpr int PT_OFF = RING_OFF + STAGES * STAGE_BYTES;   // buffer b: P^T at +2b*PT, dS^T at +(2b+1)*PT
+  static constexpr int BAR_OFF = PT_OFF + PBUFS * 2 * PT_BYTES;
+  // barriers
+  static constexpr int B_KV = 0;
+  static constexpr int B_FULL = 1;                       // STAGES
+  static constexpr int B_EMPTY = B_FULL + STAGES;        // STAGES
+  static constexpr int B_SDP = B_EMPTY + STAGES;         // S^T and dP^T of a step in tensor memory
+  static constexpr int B_SDP_FREE = B_SDP + 1;           // ... and read out (128 arrivals)
+  static constexpr int B_DS = B_SDP_FREE + 1;            // PBUFS: P^T, dS^T written (128 arrivals)
+  static constexpr int B_PFREE = B_DS + PBUFS;           // PBUFS: MMAs done reading a buffer
+  static constexpr int B_DQ = B_PFREE + PBUFS;           // dQ of a step in tensor memory
+  static constexpr int B_DQ_FREE = B_DQ + 1;             // ... and read out (128 arrivals)
+  static constexpr int B_DONE = B_DQ_FREE + 1;
+  static constexpr int NBARS = B_DONE + 1;
+  static constexpr int SMEM_BYTES = BAR_OFF + NBARS * 8 + 16 + 1024;
+  static constexpr uint32_t TMEM_COLS = 512;
+  static constexpr uint32_t COL_S = 0;
+  static constexpr uint32_t COL_DP = BQ;
+  static constexpr uint32_t COL_DQ = 2 * BQ;
+  static constexpr uint32_t COL_DV = (D == 128) ? 256 : 320;
+  static constexpr uint32_t COL_DK = 384;
+  static constexpr int THREADS = 320;
+};
+
+__device__ __forceinline__ bool bwd_visible(const BwdParams& p, int qi, int bq, int kt) {
+  if (p.mask_kind == MASK_CAUSAL) return qi * bq + bq - 1 >= kt * TILE;
+  if (p.mask_kind == MASK_BLOCK)
+    return __ldg(p.block_mask + static_cast<size_t>(qi * bq / TILE) * p.n_kt + kt) != 0;
+  return true;
+}
+
+__device__ __forceinline__ void mbar_drain_b(uint32_t bar, uint32_t parity, uint64_t ns) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_test(bar, parity)) {
+    if (globaltimer_ns() - t0 > ns) return;
+  }
+}
+
+template <int D>
+__global__ void __launch_bounds__(320, 1) fa_bwd_kernel(const __grid_constant__ BwdParams p) {
+  using L = BwdLayout<D>;
+  constexpr int BQ = L::BQ;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::BAR_OFF);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + L::NBARS);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  auto bar = [&](int i) { return smem_u32(bars + i); };
+
+  const uint32_t warp = warp_id();
+  const uint32_t lane = lane_id();
+  const int bh = blockIdx.x % p.BH;
+  const int kt = blockIdx.x / p.BH;        // causal: small key tiles have the most query tiles, start them first
+  const int n_qi = p.N / BQ;
+  const int qi_begin = (p.mask_kind == MASK_CAUSAL) ? (kt * TILE) / BQ : 0;
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar(L::B_KV), 1);
+    for (int s = 0; s < L::STAGES; ++s) {
+      mbar_init(bar(L::B_FULL + s), 1);
+      mbar_init(bar(L::B_EMPTY + s), 1);
+    }
+    mbar_init(bar(L::B_SDP), 1);
+    mbar_init(bar(L::B_SDP_FREE), 128);
+    for (int b = 0; b < L::PBUFS; ++b) {
+      mbar_init(bar(L::B_DS + b), 128);
+      mbar_init(bar(L::B_PFREE + b), 1);
+    }
+    mbar_init(bar(L::B_DQ), 1);
+    mbar_init(bar(L::B_DQ_FREE), 128);
+    mbar_init(bar(L::B_DONE), 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 8) {
+    tmem_alloc(smem_u32(tmem_slot), L::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const WaitCtx wc{abort_flag, p.status, p.timeout_ns};
+
+  int n_steps = 0;
+  for (int qi = qi_begin; qi < n_qi; ++qi) n_steps += bwd_visible(p, qi, BQ, kt);
+
+  if (warp == 9) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      prefetch_tmap(&p.tm_q);
+      prefetch_tmap(&p.tm_do);
+      prefetch_tmap(&p.tm_k);
+      prefetch_tmap(&p.tm_v);
+      const uint64_t pol_first = l2_policy_evict_first();
+      const uint64_t pol_last = l2_policy_evict_last();
+      uint32_t issued[L::STAGES] = {};
+      bool ok = true;
+      bool kv_issued = false;
+      if (n_steps > 0) {
+        mbar_arrive_expect_tx(bar(L::B_KV), 2 * L::KV_BYTES);
+        for (int c = 0; c < L::NCH; ++c) {
+          tma_load_3d(sbase + L::K_OFF + c * L::KV_CHUNK, &p.tm_k, bar(L::B_KV), c * 64, kt * TILE, bh, pol_first);
+          tma_load_3d(sbase + L::V_OFF + c * L::KV_CHUNK, &p.tm_v, bar(L::B_KV), c * 64, kt * TILE, bh, pol_first);
+        }
+        kv_issued = true;
+      }
+      int step = 0;
+      for (int qi = qi_begin; qi < n_qi && ok; ++qi) {
+        if (!bwd_visible(p, qi, BQ, kt)) continue;
+        const int st = step % L::STAGES;
+        if (!mbar_wait(bar(L::B_EMPTY + st), ((step / L::STAGES) & 1) ^ 1, wc)) { ok = false; break; }
+        const uint32_t fb = bar(L::B_FULL + st);
+        const uint32_t sb = sbase + L::RING_OFF + st * L::STAGE_BYTES;
+        mbar_arrive_expect_tx(fb, 2 * L::Q_BYTES + 2 * BQ * 4);
+        for (int c = 0; c < L::NCH; ++c) {
+          tma_load_3d(sb + L::ST_Q + c * L::Q_CHUNK, &p.tm_q, fb, c * 64, qi * BQ, bh, pol_last);
+          tma_load_3d(sb + L::ST_DO + c * L::Q_CHUNK, &p.tm_do, fb, c * 64, qi * BQ, bh, pol_last);
+        }
+        const size_t row0 = static_cast<size_t>(bh) * p.N + static_cast<size_t>(qi) * BQ;
+        bulk_load(sb + L::ST_LSE, p.lse + row0, BQ * 4, fb);
+        bulk_load(sb + L::ST_DV, p.dvec + row0, BQ * 4, fb);
+        ++issued[st];
+        ++step;
+      }
+      if (!ok) {
+        if (kv_issued) mbar_drain_b(bar(L::B_KV), 0, 100000000ull);
+        for (int s = 0; s < L::STAGES; ++s)
+          if (issued[s]) mbar_drain_b(bar(L::B_FULL + s), (issued[s] - 1) & 1u, 100000000ull);
+      }
+    }
+  } else if (warp == 8) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0 && n_steps > 0) {
+      constexpr uint32_t ID_S = idesc_bf16(128, BQ, false, false);     // S^T, dP^T
+      constexpr uint32_t ID_G = idesc_bf16(128, D, false, true);       // dV, dK
+      constexpr uint32_t ID_Q = L::DQ_T ? idesc_bf16(128, BQ, true, true) : idesc_bf16(128, D, true, true);
+      const uint32_t kA = sbase + L::K_OFF, vA = sbase + L::V_OFF;
+      bool ok = mbar_wait(bar(L::B_KV), 0, wc);
+
+      // S^T = K Q_i^T and dP^T = V dO_i^T for the step held in ring stage st
+      auto issue_sdp = [&](int st) {
+        const uint32_t sb = sbase + L::RING_OFF + st * L::STAGE_BYTES;
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {
+          const uint32_t ao = (k >> 2) * L::KV_CHUNK + (k & 3) * 32;
+          const uint32_t bo = (k >> 2) * L::Q_CHUNK + (k & 3) * 32;
+          mma_ss(tmem + L::COL_S, sdesc_sw128(kA + ao, 16, 1024), sdesc_sw128(sb + L::ST_Q + bo, 16, 1024), ID_S,
+                 k > 0 ? 1u : 0u);
+        }
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {
+          const uint32_t ao = (k >> 2) * L::KV_CHUNK + (k & 3) * 32;
+          const uint32_t bo = (k >> 2) * L::Q_CHUNK + (k & 3) * 32;
+          mma_ss(tmem + L::COL_DP, sdesc_sw128(vA + ao, 16, 1024), sdesc_sw128(sb + L::ST_DO + bo, 16, 1024), ID_S,
+                 k > 0 ? 1u : 0u);
+        }
+        mma_commit(bar(L::B_SDP));
+      };
+
+      if (ok) {
+        ok = mbar_wait(bar(L::B_FULL + 0), 0, wc);
+        if (ok) {
+          tc_fence_after();
+          issue_sdp(0);
+        }
+      }
+      for (int i = 0; i < n_steps && ok; ++i) {
+        const int st = i % L::STAGES;
+        const int b = i % L::PBUFS;
+        if (i + 1 < n_steps) {
+          // the next S^T, dP^T may overwrite tensor memory once step i's are read out
+          const int st1 = (i + 1) % L::STAGES;
+          if (!(ok = mbar_wait(bar(L::B_SDP_FREE), i & 1, wc))) break;
+          if (!(ok = mbar_wait(bar(L::B_FULL + st1), ((i + 1) / L::STAGES) & 1, wc))) break;
+          tc_fence_after();
+          issue_sdp(st1);
+        }
+        if (!(ok = mbar_wait(bar(L::B_DS + b), (i / L::PBUFS) & 1, wc))) break;
+        tc_fence_after();
+        const uint32_t sb = sbase + L::RING_OFF + st * L::STAGE_BYTES;
+        const uint32_t pt = sbase + L::PT_OFF + (2 * b) * L::PT_BYTES;
+        const uint32_t dst = pt + L::PT_BYTES;
+        // dV += P^T dO_i ; dK += dS^T Q_i   (K = BQ queries, 16 per step)
+#pragma unroll
+        for (int k = 0; k < BQ / 16; ++k) {
+          const uint32_t ao = (k >> 2) * L::PT_CHUNK + (k & 3) * 32;
+          mma_ss(tmem + L::COL_DV, sdesc_sw128(pt + ao, 16, 1024),
+                 sdesc_sw128(sb + L::ST_DO + k * 2048, L::Q_CHUNK, 1024), ID_G, (i > 0 || k > 0) ? 1u : 0u);
+        }
+#pragma unroll
+        for (int k = 0; k < BQ / 16; ++k) {
+          const uint32_t ao = (k >> 2) * L::PT_CHUNK + (k & 3) * 32;
+          mma_ss(tmem + L::COL_DK, sdesc_sw128(dst + ao, 16, 1024),
+                 sdesc_sw128(sb + L::ST_Q + k * 2048, L::Q_CHUNK, 1024), ID_G, (i > 0 || k > 0) ? 1u : 0u);
+        }
+        // dQ for this step, once the drain warps have read the previous one
+        if (i > 0) {
+          if (!(ok = mbar_wait(bar(L::B_DQ_FREE), (i - 1) & 1, wc))) break;
+          tc_fence_after();
+        }
+#pragma unroll
+        for (int k = 0; k < TILE / 16; ++k) {
+          if constexpr (L::DQ_T) {
+            // A = K^T: MN-major over d (two 64-wide blocks 16 KB apart), 16 keys per step
+            // B = dS^T seen as [queries][keys]: MN-major over the 64 queries
+            mma_ss(tmem + L::COL_DQ, sdesc_sw128(kA + k * 2048, L::KV_CHUNK, 1024),
+                   sdesc_sw128(dst + k * 2048, L::PT_CHUNK, 1024), ID_Q, k > 0 ? 1u : 0u);
+          } else {
+            // A = dS: MN-major over queries (two 64-wide blocks 16 KB apart)
+            // B = K: MN-major over d (one 64-wide block)
+            mma_ss(tmem + L::COL_DQ, sdesc_sw128(dst + k * 2048, L::PT_CHUNK, 1024),
+                   sdesc_sw128(kA + k * 2048, L::KV_CHUNK, 1024), ID_Q, k > 0 ? 1u : 0u);
+          }
+        }
+        mma_commit(bar(L::B_DQ));
+        mma_commit(bar(L::B_EMPTY + st));
+        mma_commit(bar(L::B_PFREE + b));
+      }
+      mma_commit(bar(L::B_DONE));
+      mbar_drain_b(bar(L::B_DONE), 0, 1000000000ull);
+    }
+    __syncwarp();
+  } else if (warp < 4) {
+    // ------------------------------------------------- recompute P and dS
+    const uint32_t quarter = warp;
+    const int r = static_cast<int>(quarter * 32 + lane);    // key row in the tile == lane
+    const int key = kt * TILE + r;
+    const uint32_t lane_base = quarter * 32;
+    const float sl2 = p.scale_log2;
+    bool ok = true;
+    int i = 0;
+    for (int qi = qi_begin; qi < n_qi && ok; ++qi) {
+      if (!bwd_visible(p, qi, BQ, kt)) continue;
+      const int st = i % L::STAGES;
+      const int b = i % L::PBUFS;
+      if (!(ok = mbar_wait_warp(bar(L::B_SDP), i & 1, wc))) break;
+      tc_fence_after();
+      if (i >= L::PBUFS) {
+        if (!(ok = mbar_wait_warp(bar(L::B_PFREE + b), ((i / L::PBUFS) - 1) & 1, wc))) break;
+      }
+      const uint8_t* stage = smem + L::RING_OFF + st * L::STAGE_BYTES;
+      const float* lse = reinterpret_cast<const float*>(stage + L::ST_LSE);
+      const float* dv = reinterpret_cast<const float*>(stage + L::ST_DV);
+      uint8_t* pt = smem + L::PT_OFF + (2 * b) * L::PT_BYTES;
+      uint8_t* dsT = pt + L::PT_BYTES;
+      const bool diag = (p.mask_kind == MASK_CAUSAL) && (qi * BQ < kt * TILE + TILE);
+#pragma unroll 1
+      for (int h = 0; h < BQ / 64; ++h) {
+        uint32_t sr[64], dr[64];
+        tmem_ld_x64(tmem_addr(tmem, lane_base, L::COL_S + h * 64), sr);
+        tmem_ld_x64(tmem_addr(tmem, lane_base, L::COL_DP + h * 64), dr);
+        if (h == BQ / 64 - 1) {
+          tc_fence_before();
+          mbar_arrive(bar(L::B_SDP_FREE));
+        }
+        uint8_t* prow = pt + h * L::PT_CHUNK + r * 128;
+        uint8_t* drow = dsT + h * L::PT_CHUNK + r * 128;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {            // 8 queries per 16-byte chunk
+          uint32_t pp[4], dd[4];
+#pragma unroll
+          for (int e = 0; e < 8; e += 2) {
+            const int c = h * 64 + j * 8 + e;
+            const float4 l4 = *reinterpret_cast<const float4*>(lse + (c & ~3));
+            const float4 d4 = *reinterpret_cast<const float4*>(dv + (c & ~3));
+            const float la = (c & 3) == 0 ? l4.x : l4.z;
+            const float lb = (c & 3) == 0 ? l4.y : l4.w;
+            const float da = (c & 3) == 0 ? d4.x : d4.z;
+            const float db = (c & 3) == 0 ? d4.y : d4.w;
+            float p0 = ex2_approx(fmaf(__uint_as_float(sr[j * 8 + e]), sl2, -la * 1.4426950408889634f));
+            float p1 = ex2_approx(fmaf(__uint_as_float(sr[j * 8 + e + 1]), sl2, -lb * 1.4426950408889634f));
+            if (diag) {
+              const int q0 = qi * BQ + c;
+              if (q0 < key) p0 = 0.f;
+              if (q0 + 1 < key) p1 = 0.f;
+            }
+            const float ds0 = p0 * (__uint_as_float(dr[j * 8 + e]) - da);
+            const float ds1 = p1 * (__uint_as_float(dr[j * 8 + e + 1]) - db);
+            pp[e / 2] = pack_bf16x2(p0, p1);
+            dd[e / 2] = pack_bf16x2(ds0, ds1);
+          }
+          const int sw = (j ^ (r & 7)) << 4;       // 128-byte swizzle of the 16-byte chunk
+          *reinterpret_cast<uint4*>(prow + sw) = make_uint4(pp[0], pp[1], pp[2], pp[3]);
+          *reinterpret_cast<uint4*>(drow + sw) = make_uint4(dd[0], dd[1], dd[2], dd[3]);
+        }
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(bar(L::B_DS + b));
+      ++i;
+    }
+    // ------------------------------------------------- epilogue: dV rows
+    if (ok) {
+      __nv_bfloat16* out = p.dv + (static_cast<size_t>(bh) * p.N + static_cast<size_t>(kt) * TILE + r) * D;
+      if (n_steps > 0 && mbar_wait_warp(bar(L::B_DONE), 0, wc)) {
+        tc_fence_after();
+#pragma unroll 1
+        for (int c = 0; c < D; c += 32) {
+          uint32_t v[32];
+          tmem_ld_x32(tmem_addr(tmem, lane_base, L::COL_DV + c), v);
+          uint4 o4[4];
+          uint32_t* ow = reinterpret_cast<uint32_t*>(o4);
+#pragma unroll
+          for (int e = 0; e < 16; ++e) ow[e] = pack_bf16x2(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1]));
+          uint4* dst = reinterpret_cast<uint4*>(out + c);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) dst[e] = o4[e];
+        }
+      } else if (n_steps == 0) {
+        uint4* dst = reinterpret_cast<uint4*>(out);
+#pragma unroll
+        for (int e = 0; e < D / 8; ++e) dst[e] = make_uint4(0, 0, 0, 0);
+      }
+    }
+  } else {
+    // ------------------------------------------------- drain dQ; dK epilogue
+    const uint32_t quarter = warp & 3u;
+    const uint32_t lane_base = quarter * 32;
+    const int t = static_cast<int>(quarter * 32 + lane);
+    bool ok = true;
+    int i = 0;
+    for (int qi = qi_begin; qi < n_qi && ok; ++qi) {
+      if (!bwd_visible(p, qi, BQ, kt)) continue;
+      if (!(ok = mbar_wait_warp(bar(L::B_DQ), i & 1, wc))) break;
+      tc_fence_after();
+      uint32_t v[64];
+      tmem_ld_x64(tmem_addr(tmem, lane_base, L::COL_DQ), v);
+      tc_fence_before();
+      mbar_arrive(bar(L::B_DQ_FREE));
+      const size_t row0 = static_cast<size_t>(bh) * p.N + static_cast<size_t>(qi) * BQ;
+      if constexpr (L::DQ_T) {
+        // lane t holds head-dim column t of dQ for the BQ = 64 queries of the step
+        float* dst = p.dq_acc + row0 * D + t;
+#pragma unroll
+        for (int c = 0; c < 64; ++c) atomicAdd(dst + static_cast<size_t>(c) * D, __uint_as_float(v[c]));
+      } else {
+        // lane t holds query row t of the step, 64 head-dim columns
+        float4* dst = reinterpret_cast<float4*>(p.dq_acc + (row0 + t) * D);
+#pragma unroll
+        for (int c = 0; c < 16; ++c)
+          atomicAdd(dst + c, make_float4(__uint_as_float(v[4 * c]), __uint_as_float(v[4 * c + 1]),
+                                         __uint_as_float(v[4 * c + 2]), __uint_as_float(v[4 * c + 3])));
+      }
+      ++i;
+    }
+    // dK rows (lane = key row), scaled by the chain-rule factor
+    if (ok) {
+      __nv_bfloat16* out = p.dk + (static_cast<size_t>(bh) * p.N + static_cast<size_t>(kt) * TILE + t) * D;
+      if (n_steps > 0 && mbar_wait_warp(bar(L::B_DONE), 0, wc)) {
+        tc_fence_after();
+#pragma unroll 1
+        for (int c = 0; c < D; c += 32) {
+          uint32_t v[32];
+          tmem_ld_x32(tmem_addr(tmem, lane_base, L::COL_DK + c), v);
+          uint4 o4[4];
+          uint32_t* ow = reinterpret_cast<uint32_t*>(o4);
+#pragma unroll
+          for (int e = 0; e < 16; ++e)
+            ow[e] = pack_bf16x2(__uint_as_float(v[2 * e]) * p.scale, __uint_as_float(v[2 * e + 1]) * p.scale);
+          uint4* dst = reinterpret_cast<uint4*>(out + c);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) dst[e] = o4[e];
+        }
+      } else if (n_steps == 0) {
+        uint4* dst = reinterpret_cast<uint4*>(out);
+#pragma unroll
+        for (int e = 0; e < D / 8; ++e) dst[e] = make_uint4(0, 0, 0, 0);
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 8) {
+    tc_fence_after();
+    tmem_dealloc(tmem, L::TMEM_COLS);
+  }
+}
+
+template <int D>
+static int launch_bwd_t(const BwdParams& p, cudaStream_t stream) {
+  using L = BwdLayout<D>;
+  static_assert(L::SMEM_BYTES <= 232448, "shared memory budget");
+  if (cudaFuncSetAttribute(fa_bwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM_BYTES) !=
+      cudaSuccess)
+    return -4;
+  const unsigned grid = static_cast<unsigned>(p.n_kt) * static_cast<unsigned>(p.BH);
+  fa_bwd_kernel<D><<<grid, L::THREADS, L::SMEM_BYTES, stream>>>(p);
+  return cudaGetLastError() == cudaSuccess ? 0 : -4;
+}
+
+int launch_bwd_main(const BwdParams& p, int d, cudaStream_t stream) {
+  if (d == 128) return launch_bwd_t<128>(p, stream);
+  if (d == 64) return launch_bwd_t<64>(p, stream);
+  return -2;
+}
+
+}  // namespace fa

@@ -1,0 +1,68 @@
+// fa_common.cuh -- launch parameters shared by the host launchers and the
+// kernels of libfa.so.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+namespace fa {
+
+enum MaskKind : int { MASK_NONE = 0, MASK_CAUSAL = 1, MASK_BLOCK = 2 };
+
+// Tile sizes along the sequence: B_r = B_c = 128 (one tensor-memory lane per
+// query row, one 128-byte swizzle span per 64 head-dim columns).
+constexpr int TILE = 128;
+
+// Forward launch parameters.  Tensor maps describe Q, K, V as 3-D bf16
+// arrays [B*H][N][d] with a {64, 128, 1} box and 128-byte swizzle.
+struct FwdParams {
+  CUtensorMap tm_q;
+  CUtensorMap tm_k;
+  CUtensorMap tm_v;
+  __nv_bfloat16* o;          // [B*H][N][d]
+  float* lse;                // [B*H][N]
+  const uint8_t* block_mask; // [N/128][N/128] or null
+  int* status;               // device status word
+  uint64_t timeout_ns;
+  int N;
+  int BH;
+  int n_qt;                  // N / 128
+  int n_pairs;               // ceil(n_qt / 2): each CTA owns two query tiles
+  float scale_log2;          // scale * log2(e)
+  int mask_kind;
+};
+
+// Backward main-kernel parameters.  Q and dO use a {64, BQ, 1} box, K and V a
+// {64, 128, 1} box.
+struct BwdParams {
+  CUtensorMap tm_q;
+  CUtensorMap tm_k;
+  CUtensorMap tm_v;
+  CUtensorMap tm_do;
+  const float* lse;          // [B*H][N]
+  const float* dvec;         // [B*H][N], D_i = dO_i . O_i
+  float* dq_acc;             // [B*H][N][d] fp32 accumulator
+  __nv_bfloat16* dk;         // [B*H][N][d]
+  __nv_bfloat16* dv;         // [B*H][N][d]
+  const uint8_t* block_mask; // [N/128][N/128] or null
+  int* status;
+  uint64_t timeout_ns;
+  int N;
+  int BH;
+  int n_kt;                  // N / 128 key tiles
+  float scale;
+  float scale_log2;
+  int mask_kind;
+};
+
+int launch_fwd(const FwdParams& p, int d, cudaStream_t stream);
+int launch_bwd_preprocess(const __nv_bfloat16* o, const __nv_bfloat16* dout, float* dvec,
+                          float* dq_acc, int rows, int d, cudaStream_t stream);
+int launch_bwd_main(const BwdParams& p, int d, cudaStream_t stream);
+int launch_bwd_dq_convert(const float* dq_acc, __nv_bfloat16* dq, long long n, float scale,
+                          cudaStream_t stream);
+int launch_wait_timeout_probe(int* status, uint64_t timeout_ns, cudaStream_t stream);
+
+}  // namespace fa

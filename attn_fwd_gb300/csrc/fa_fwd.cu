@@ -1,0 +1,424 @@
+// fa_fwd.cu -- fused attention forward for sm_103a.
+//
+// What one CTA computes: two 128-row query tiles Q_i (i = 2t, 2t+1) of one
+// (batch, head), each against every visible 128-row key/value tile K_j, V_j,
+// with the online-softmax recurrence ("FlashAttention" notes, "Tiling" and
+// Theorem 1; "Как работает FlashAttention математически", sections 3, 4, 6):
+//   S_ij = scale * Q_i K_j^T;  m_new = max(m, rowmax S_ij);
+//   P~_ij = exp(S_ij - m_new); l = exp(m - m_new) l + rowsum P~_ij;
+//   O_i = exp(m - m_new) O_i + P~_ij V_j;  finally O_i /= l, LSE = m + ln l.
+// O is kept un-normalised and divided once at the end (the same page's
+// section 4 notes that implementations do this).  S and P live only in
+// tensor memory.  The loop runs query-tile outer, key-tile inner (the V2
+// order of "Transformer 入门"), so O is written once per tile.
+//
+// GB300 mapping (warp specialisation, 10 warps):
+//   warp 9      TMA producer: Q tiles once, then K_j and V_j into a ring of
+//               shared-memory slots (128-byte swizzle), L2 evict-last for K/V.
+//   warp 8      MMA issuer (one thread): S_w = Q_w K_j^T (SS form) and
+//               O_w += P_w V_j (A operand P_w read from tensor memory).
+//   warps 0-3   softmax for query tile 0, warps 4-7 for tile 1: one thread
+//               per query row reads its S row from tensor memory, computes the
+//               masked row max, exp2, row sum, writes P (bf16) back over S,
+//               and rescales its O row in tensor memory when needed.
+// The MMA order S0(j) S1(j) | PV0(j) S0(j+1) PV1(j) S1(j+1) | ... lets the
+// softmax of one tile overlap the tensor-core work of the other.
+//
+// Rescaling is lazy: the reference max m only moves when the tile max
+// exceeds it by more than 2^8 in exp2 units.  exp(S - m) then stays <= 256,
+// and because O and l always share the same m the result is unchanged
+// (every term carries the same factor exp(-m)).
+//
+// Tensor memory (512 columns x 128 lanes): S0 [0,128) S1 [128,256)
+// O0 [256,256+d) O1 [256+d,256+2d); P_w (bf16 pairs) overwrites the first 64
+// columns of S_w.  tcgen05 MMAs issued by one thread execute in order, so the
+// next S_w(j+1) never overwrites P_w(j) before O_w += P_w(j) V_j has read it.
+#include "fa_common.cuh"
+#include "fa_ptx.cuh"
+
+namespace fa {
+
+template <int D>
+struct FwdLayout {
+  static constexpr int NCH = D / 64;                      // 64-column (128-byte) chunks
+  static constexpr int CHUNK_BYTES = TILE * 128;          // 128 rows x 128 bytes
+  static constexpr int TILE_BYTES = NCH * CHUNK_BYTES;    // one 128 x D bf16 tile
+  static constexpr int STAGES = (D == 128) ? 4 : 6;       // K/V ring slots
+  static constexpr int Q_OFF = 0;
+  static constexpr int RING_OFF = 2 * TILE_BYTES;
+  static constexpr int BAR_OFF = RING_OFF + STAGES * TILE_BYTES;
+  // barrier indices
+  static constexpr int B_Q = 0;                  // 2
+  static constexpr int B_FULL = 2;               // STAGES
+  static constexpr int B_EMPTY = 2 + STAGES;     // STAGES
+  static constexpr int B_S = 2 + 2 * STAGES;     // 2
+  static constexpr int B_P = B_S + 2;            // 2
+  static constexpr int B_O = B_P + 2;            // 2
+  static constexpr int B_DONE = B_O + 2;         // 1
+  static constexpr int NBARS = B_DONE + 1;
+  static constexpr int SMEM_BYTES = BAR_OFF + NBARS * 8 + 16 + 1024;  // + 1 KB alignment slack
+  static constexpr uint32_t TMEM_COLS = 512;
+  static constexpr uint32_t S_COL0 = 0, S_COL1 = 128;
+  static constexpr uint32_t O_COL0 = 256, O_COL1 = 256 + D;
+  static constexpr int THREADS = 320;
+};
+
+// Reference-max threshold for lazy rescaling, in exp2 units (factor 256).
+constexpr float RESCALE_THRESHOLD = 8.0f;
+
+__device__ __forceinline__ bool fwd_visible(const FwdParams& p, int qt, int kt) {
+  if (qt >= p.n_qt) return false;
+  if (p.mask_kind == MASK_CAUSAL) return kt <= qt;
+  if (p.mask_kind == MASK_BLOCK) return __ldg(p.block_mask + static_cast<size_t>(qt) * p.n_qt + kt) != 0;
+  return true;
+}
+
+// Bounded wait used only while tearing down after a failure: ignores the
+// abort flag, gives up after `ns`.
+__device__ __forceinline__ void mbar_drain(uint32_t bar, uint32_t parity, uint64_t ns) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_test(bar, parity)) {
+    if (globaltimer_ns() - t0 > ns) return;
+  }
+}
+
+template <int D>
+__global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ FwdParams p) {
+  using L = FwdLayout<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::BAR_OFF);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + L::NBARS);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  auto bar = [&](int i) { return smem_u32(bars + i); };
+
+  const uint32_t warp = warp_id();
+  const uint32_t lane = lane_id();
+  const int bh = blockIdx.x % p.BH;
+  int pair = blockIdx.x / p.BH;
+  if (p.mask_kind == MASK_CAUSAL) pair = p.n_pairs - 1 - pair;  // longest rows first
+  const int qt0 = 2 * pair;
+  const int qt1 = 2 * pair + 1;
+  const int kt_end = (p.mask_kind == MASK_CAUSAL) ? min(qt1, p.n_qt - 1) + 1 : p.n_qt;
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar(L::B_Q + 0), 1);
+    mbar_init(bar(L::B_Q + 1), 1);
+    for (int s = 0; s < L::STAGES; ++s) {
+      mbar_init(bar(L::B_FULL + s), 1);
+      mbar_init(bar(L::B_EMPTY + s), 1);
+    }
+    for (int w = 0; w < 2; ++w) {
+      mbar_init(bar(L::B_S + w), 1);
+      mbar_init(bar(L::B_P + w), 128);
+      mbar_init(bar(L::B_O + w), 1);
+    }
+    mbar_init(bar(L::B_DONE), 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 8) {
+    tmem_alloc(smem_u32(tmem_slot), L::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const WaitCtx wc{abort_flag, p.status, p.timeout_ns};
+
+  if (warp == 9) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      prefetch_tmap(&p.tm_q);
+      prefetch_tmap(&p.tm_k);
+      prefetch_tmap(&p.tm_v);
+      const uint64_t pol_q = l2_policy_evict_first();
+      const uint64_t pol_kv = l2_policy_evict_last();
+      for (int w = 0; w < 2; ++w) {
+        const int qt = qt0 + w;
+        if (qt >= p.n_qt) continue;
+        mbar_arrive_expect_tx(bar(L::B_Q + w), L::TILE_BYTES);
+        for (int c = 0; c < L::NCH; ++c)
+          tma_load_3d(sbase + L::Q_OFF + w * L::TILE_BYTES + c * L::CHUNK_BYTES, &p.tm_q,
+                      bar(L::B_Q + w), c * 64, qt * TILE, bh, pol_q);
+      }
+      int slot = 0;
+      uint32_t phase = 0;
+      uint32_t issued[L::STAGES];
+      for (int s = 0; s < L::STAGES; ++s) issued[s] = 0;
+      bool ok = true;
+      for (int kt = 0; kt < kt_end && ok; ++kt) {
+        if (!(fwd_visible(p, qt0, kt) || fwd_visible(p, qt1, kt))) continue;
+        for (int which = 0; which < 2; ++which) {  // K_j, then V_j
+          if (!mbar_wait(bar(L::B_EMPTY + slot), phase ^ 1u, wc)) { ok = false; break; }
+          const uint32_t fb = bar(L::B_FULL + slot);
+          mbar_arrive_expect_tx(fb, L::TILE_BYTES);
+          const CUtensorMap* m = which ? &p.tm_v : &p.tm_k;
+          for (int c = 0; c < L::NCH; ++c)
+            tma_load_3d(sbase + L::RING_OFF + slot * L::TILE_BYTES + c * L::CHUNK_BYTES, m, fb,
+                        c * 64, kt * TILE, bh, pol_kv);
+          ++issued[slot];
+          if (++slot == L::STAGES) { slot = 0; phase ^= 1u; }
+        }
+      }
+      if (!ok) {  // let copies already in flight land before the CTA exits
+        for (int s = 0; s < L::STAGES; ++s)
+          if (issued[s]) mbar_drain(bar(L::B_FULL + s), (issued[s] - 1) & 1u, 100000000ull);
+      }
+    }
+  } else if (warp == 8) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t IDESC_S = idesc_bf16(128, 128, false, false);
+      constexpr uint32_t IDESC_O = idesc_bf16(128, D, false, true);
+      const uint32_t s_col[2] = {L::S_COL0, L::S_COL1};
+      const uint32_t o_col[2] = {L::O_COL0, L::O_COL1};
+      int n_vis[2] = {0, 0};
+      for (int kt = 0; kt < kt_end; ++kt) {
+        n_vis[0] += fwd_visible(p, qt0, kt);
+        n_vis[1] += fwd_visible(p, qt1, kt);
+      }
+      bool ok = true;
+      for (int w = 0; w < 2 && ok; ++w)
+        if (n_vis[w] > 0) ok = mbar_wait(bar(L::B_Q + w), 0, wc);
+
+      // S_w(entry) = Q_w K^T over D/16 k-steps of 16 (32 bytes inside a
+      // 128-byte swizzle row; a new 16 KB chunk every 64 columns).
+      auto issue_s = [&](int w, int kslot) {
+        const uint32_t qa = sbase + L::Q_OFF + w * L::TILE_BYTES;
+        const uint32_t ka = sbase + L::RING_OFF + kslot * L::TILE_BYTES;
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {
+          const uint32_t off = (k >> 2) * L::CHUNK_BYTES + (k & 3) * 32;
+          mma_ss(tmem + s_col[w], sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024),
+                 IDESC_S, k > 0 ? 1u : 0u);
+        }
+      };
+      // O_w += P_w V over 128/16 k-steps: P from tensor memory (8 columns
+      // of bf16 pairs per step), V as an MN-major operand (16 key rows of 128
+      // bytes per step; the second 64-column half of d sits 16 KB further).
+      bool o_started[2] = {false, false};
+      auto issue_pv = [&](int w, int vslot) {
+        const uint32_t va = sbase + L::RING_OFF + vslot * L::TILE_BYTES;
+#pragma unroll
+        for (int k = 0; k < TILE / 16; ++k) {
+          mma_ts(tmem + o_col[w], tmem + s_col[w] + 8 * k, sdesc_sw128(va + k * 2048, L::CHUNK_BYTES, 1024),
+                 IDESC_O, (o_started[w] || k > 0) ? 1u : 0u);
+        }
+        o_started[w] = true;
+      };
+
+      struct Ent { int kslot, vslot; uint32_t vphase; bool f[2]; };
+      Ent prev{0, 0, 0u, {false, false}};
+      bool has_prev = false;
+      int slot = 0;
+      uint32_t phase = 0;
+      uint32_t pphase[2] = {0u, 0u};
+      int pv_done[2] = {0, 0};
+
+      // O_w += P_w(prev) V(prev), after softmax w has published P_w(prev).
+      auto do_pv = [&](int w, const Ent& e, bool& v_ready) -> bool {
+        if (!v_ready) {
+          if (!mbar_wait(bar(L::B_FULL + e.vslot), e.vphase, wc)) return false;
+          v_ready = true;
+        }
+        if (!mbar_wait(bar(L::B_P + w), pphase[w], wc)) return false;
+        pphase[w] ^= 1u;
+        tc_fence_after();
+        issue_pv(w, e.vslot);
+        if (++pv_done[w] == n_vis[w]) mma_commit(bar(L::B_O + w));
+        return true;
+      };
+
+      for (int kt = 0; kt < kt_end && ok; ++kt) {
+        Ent e;
+        e.f[0] = fwd_visible(p, qt0, kt);
+        e.f[1] = fwd_visible(p, qt1, kt);
+        if (!(e.f[0] || e.f[1])) continue;
+        e.kslot = slot;
+        const uint32_t kphase = phase;
+        if (++slot == L::STAGES) { slot = 0; phase ^= 1u; }
+        e.vslot = slot;
+        e.vphase = phase;
+        if (++slot == L::STAGES) { slot = 0; phase ^= 1u; }
+
+        if (!mbar_wait(bar(L::B_FULL + e.kslot), kphase, wc)) { ok = false; break; }
+        tc_fence_after();
+        bool v_ready = false;
+        for (int w = 0; w < 2 && ok; ++w) {
+          if (has_prev && prev.f[w]) ok = do_pv(w, prev, v_ready);
+          if (!ok) break;
+          if (e.f[w]) {
+            issue_s(w, e.kslot);
+            mma_commit(bar(L::B_S + w));
+          }
+        }
+        if (!ok) break;
+        mma_commit(bar(L::B_EMPTY + e.kslot));
+        if (has_prev) mma_commit(bar(L::B_EMPTY + prev.vslot));
+        prev = e;
+        has_prev = true;
+      }
+      if (ok && has_prev) {
+        bool v_ready = false;
+        for (int w = 0; w < 2 && ok; ++w)
+          if (prev.f[w]) ok = do_pv(w, prev, v_ready);
+        if (ok) mma_commit(bar(L::B_EMPTY + prev.vslot));
+      }
+      // nothing may be in flight when tensor memory is released
+      mma_commit(bar(L::B_DONE));
+      mbar_drain(bar(L::B_DONE), 0, 1000000000ull);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ softmax
+    const int w = static_cast<int>(warp >> 2);
+    const uint32_t quarter = warp & 3u;
+    const int qt = qt0 + w;
+    if (qt < p.n_qt) {
+      const int row = static_cast<int>(quarter * 32 + lane);      // row in tile == TMEM lane
+      const uint32_t s_addr = tmem_addr(tmem, quarter * 32, w ? L::S_COL1 : L::S_COL0);
+      const uint32_t o_addr = tmem_addr(tmem, quarter * 32, w ? L::O_COL1 : L::O_COL0);
+      const float sl2 = p.scale_log2;
+      float m = -INFINITY;  // reference max, in exp2 units of scaled scores
+      float l = 0.f;
+      bool has_o = false;
+      bool ok = true;
+      uint32_t sphase = 0;
+      int n_vis = 0;
+      for (int kt = 0; kt < kt_end; ++kt) {
+        if (!fwd_visible(p, qt, kt)) continue;
+        ++n_vis;
+        if (!mbar_wait_warp(bar(L::B_S + w), sphase, wc)) { ok = false; break; }
+        sphase ^= 1u;
+        tc_fence_after();
+        uint32_t r[128];
+        tmem_ld_x128(s_addr, r);
+        float* s = reinterpret_cast<float*>(r);
+        if (p.mask_kind == MASK_CAUSAL && kt == qt) {
+#pragma unroll
+          for (int c = 0; c < 128; ++c)
+            if (c > row) s[c] = -INFINITY;
+        }
+        float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
+#pragma unroll
+        for (int c = 4; c < 128; c += 4) {
+          mx0 = fmaxf(mx0, s[c]);
+          mx1 = fmaxf(mx1, s[c + 1]);
+          mx2 = fmaxf(mx2, s[c + 2]);
+          mx3 = fmaxf(mx3, s[c + 3]);
+        }
+        const float m_tile = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
+        const bool need = m_tile > m + RESCALE_THRESHOLD;   // always true on the first tile
+        float alpha = 1.f;
+        if (need) {
+          alpha = ex2_approx(m - m_tile);                  // 0 when m = -inf
+          m = m_tile;
+        }
+        float sum0 = 0.f, sum1 = 0.f, sum2 = 0.f, sum3 = 0.f;
+        uint32_t pk[64];
+#pragma unroll
+        for (int c = 0; c < 64; c += 2) {
+          const float p0 = ex2_approx(fmaf(s[2 * c + 0], sl2, -m));
+          const float p1 = ex2_approx(fmaf(s[2 * c + 1], sl2, -m));
+          const float p2 = ex2_approx(fmaf(s[2 * c + 2], sl2, -m));
+          const float p3 = ex2_approx(fmaf(s[2 * c + 3], sl2, -m));
+          pk[c] = pack_bf16x2(p0, p1);
+          pk[c + 1] = pack_bf16x2(p2, p3);
+          // l sums the bf16 values that P V multiplies, so O = sum_j w_j v_j
+          // with weights that sum to exactly one.
+          sum0 += __uint_as_float(pk[c] << 16);
+          sum1 += __uint_as_float(pk[c] & 0xffff0000u);
+          sum2 += __uint_as_float(pk[c + 1] << 16);
+          sum3 += __uint_as_float(pk[c + 1] & 0xffff0000u);
+        }
+        l = l * alpha + ((sum0 + sum1) + (sum2 + sum3));
+        if (has_o && __any_sync(0xffffffffu, need)) {
+          // O may be read here: S(j) completing implies the previous PV is done.
+#pragma unroll 1
+          for (int c = 0; c < D; c += 32) {
+            uint32_t ov[32];
+            tmem_ld_x32(o_addr + c, ov);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
+            tmem_st_x32(o_addr + c, ov);
+          }
+        }
+        {
+          uint32_t h0[32], h1[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            h0[i] = pk[i];
+            h1[i] = pk[32 + i];
+          }
+          tmem_st_x32(s_addr, h0);
+          tmem_st_x32(s_addr + 32, h1);
+        }
+        tc_fence_before();
+        mbar_arrive(bar(L::B_P + w));
+        has_o = true;
+      }
+      // ---------------------------------------------------------- epilogue
+      if (ok) {
+        const size_t grow = static_cast<size_t>(bh) * p.N + static_cast<size_t>(qt) * TILE + row;
+        __nv_bfloat16* orow = p.o + grow * D;
+        if (n_vis > 0) {
+          ok = mbar_wait_warp(bar(L::B_O + w), 0, wc);
+          if (ok) {
+            tc_fence_after();
+            const float inv_l = 1.f / l;
+#pragma unroll 1
+            for (int c = 0; c < D; c += 32) {
+              uint32_t ov[32];
+              tmem_ld_x32(o_addr + c, ov);
+              uint4 pkd[4];
+              uint32_t* pw = reinterpret_cast<uint32_t*>(pkd);
+#pragma unroll
+              for (int i = 0; i < 16; ++i)
+                pw[i] = pack_bf16x2(__uint_as_float(ov[2 * i]) * inv_l, __uint_as_float(ov[2 * i + 1]) * inv_l);
+              uint4* dst = reinterpret_cast<uint4*>(orow + c);
+#pragma unroll
+              for (int i = 0; i < 4; ++i) dst[i] = pkd[i];
+            }
+            p.lse[grow] = (m + __log2f(l)) * 0.69314718055994530942f;
+          }
+        } else {
+          // no visible key: O = 0, LSE = -inf
+          uint4* dst = reinterpret_cast<uint4*>(orow);
+#pragma unroll
+          for (int i = 0; i < D / 8; ++i) dst[i] = make_uint4(0, 0, 0, 0);
+          p.lse[grow] = -INFINITY;
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 8) {
+    tc_fence_after();
+    tmem_dealloc(tmem, L::TMEM_COLS);
+  }
+}
+
+template <int D>
+static int launch_fwd_t(const FwdParams& p, cudaStream_t stream) {
+  using L = FwdLayout<D>;
+  static_assert(L::SMEM_BYTES <= 232448, "shared memory budget");
+  cudaError_t e = cudaFuncSetAttribute(fa_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       L::SMEM_BYTES);
+  if (e != cudaSuccess) return -4;
+  const unsigned grid = static_cast<unsigned>(p.n_pairs) * static_cast<unsigned>(p.BH);
+  fa_fwd_kernel<D><<<grid, L::THREADS, L::SMEM_BYTES, stream>>>(p);
+  return cudaGetLastError() == cudaSuccess ? 0 : -4;
+}
+
+int launch_fwd(const FwdParams& p, int d, cudaStream_t stream) {
+  if (d == 128) return launch_fwd_t<128>(p, stream);
+  if (d == 64) return launch_fwd_t<64>(p, stream);
+  return -2;
+}
+
+}  // namespace fa

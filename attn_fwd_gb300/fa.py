@@ -1,0 +1,234 @@
+"""Thin Python binding of libfa.so (the C ABI in include/fa.h).
+
+Functions named like the C entry points take PyTorch CUDA tensors and
+marshal pointers, sizes and the current stream; every step of the attention
+path runs in the library's kernels.  ``forward`` and ``backward`` are small
+conveniences that allocate the outputs and the workspace.  If the library is
+missing or fails to load, every call raises: there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import build as _build
+
+FA_OK = 0
+FA_ERR_INVALID = -1
+FA_ERR_UNSUPPORTED = -2
+FA_ERR_ARCH = -3
+FA_ERR_LAUNCH = -4
+FA_ERR_TIMEOUT = -5
+FA_ERR_CUDA = -6
+
+MASK_NONE, MASK_CAUSAL, MASK_BLOCK = 0, 1, 2
+
+_lib = None
+_lock = threading.Lock()
+
+_vp, _i, _f, _sz, _u64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t, ctypes.c_uint64
+_SIGS = {
+    "fa_version": (_i, []),
+    "fa_status_string": (ctypes.c_char_p, [_i]),
+    "fa_fwd": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp]),
+    "fa_fwd_blocksparse": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _vp]),
+    "fa_bwd_workspace_bytes": (_sz, [_i, _i, _i, _i]),
+    "fa_bwd": (_i, [_vp] * 10 + [_i, _i, _i, _i, _f, _i, _vp]),
+    "fa_bwd_blocksparse": (_i, [_vp] * 11 + [_i, _i, _i, _i, _f, _vp]),
+    "fa_bwd_preprocess": (_i, [_vp, _vp, _vp, _i, _i, _i, _i, _vp]),
+    "fa_bwd_main": (_i, [_vp] * 9 + [_i, _i, _i, _i, _f, _i, _vp]),
+    "fa_bwd_dq_convert": (_i, [_vp, _vp, _i, _i, _i, _i, _f, _vp]),
+    "fa_get_device_error": (_i, [_vp]),
+    "fa_set_wait_timeout_ns": (_i, [_u64]),
+    "fa_debug_wait_timeout": (_i, [_u64, _vp]),
+}
+
+
+class FAError(RuntimeError):
+    def __init__(self, fn, code):
+        self.code = code
+        super().__init__(f"{fn} returned {code}: {status_string(code) if _lib else code}")
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load(path: str | None = None) -> ctypes.CDLL:
+    """Load libfa.so (once).  Raises if it is absent: build it with
+    ``__graft_entry__.build()``."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            p = path or _build.LIB
+            if not os.path.exists(p):
+                raise RuntimeError(f"libfa.so not found at {p}; run __graft_entry__.build() first")
+            lib = ctypes.CDLL(p)
+            for name, (res, args) in _SIGS.items():
+                fn = getattr(lib, name)
+                fn.restype = res
+                fn.argtypes = args
+            _lib = lib
+    return _lib
+
+
+def status_string(code: int) -> str:
+    return load().fa_status_string(code).decode()
+
+
+def _check(fn: str, rc: int):
+    if rc != FA_OK:
+        raise FAError(fn, rc)
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _bf16(t: torch.Tensor, name: str):
+    if not (t.is_cuda and t.dtype == torch.bfloat16 and t.is_contiguous() and t.dim() == 4):
+        raise ValueError(f"{name} must be a contiguous bf16 CUDA tensor [B, H, N, d]")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _f32(t: torch.Tensor, name: str):
+    if not (t.is_cuda and t.dtype == torch.float32 and t.is_contiguous()):
+        raise ValueError(f"{name} must be a contiguous fp32 CUDA tensor")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _mask_ptr(block_mask):
+    if block_mask is None:
+        return ctypes.c_void_p(0)
+    if not (block_mask.is_cuda and block_mask.dtype == torch.uint8 and block_mask.is_contiguous()):
+        raise ValueError("block_mask must be a contiguous uint8 CUDA tensor [N/128, N/128]")
+    return ctypes.c_void_p(block_mask.data_ptr())
+
+
+def _ptr_or_null(t):
+    return ctypes.c_void_p(0 if t is None else t.data_ptr())
+
+
+# --------------------------------------------------------------------------- #
+# C entry points (same names)
+# --------------------------------------------------------------------------- #
+def fa_version() -> int:
+    return load().fa_version()
+
+
+def fa_fwd(q, k, v, o, lse, scale, causal=False, stream=None):
+    B, H, N, d = q.shape
+    rc = load().fa_fwd(_bf16(q, "q"), _bf16(k, "k"), _bf16(v, "v"), _bf16(o, "o"), _f32(lse, "lse"),
+                       B, H, N, d, float(scale), int(bool(causal)), _stream(stream))
+    _check("fa_fwd", rc)
+
+
+def fa_fwd_blocksparse(q, k, v, o, lse, block_mask, scale, stream=None):
+    B, H, N, d = q.shape
+    rc = load().fa_fwd_blocksparse(_bf16(q, "q"), _bf16(k, "k"), _bf16(v, "v"), _bf16(o, "o"),
+                                   _f32(lse, "lse"), _mask_ptr(block_mask), B, H, N, d, float(scale),
+                                   _stream(stream))
+    _check("fa_fwd_blocksparse", rc)
+
+
+def fa_bwd_workspace_bytes(B, H, N, d) -> int:
+    return load().fa_bwd_workspace_bytes(B, H, N, d)
+
+
+def fa_bwd(q, k, v, o, do, lse, dq, dk, dv, workspace, scale, causal=False, stream=None):
+    B, H, N, d = q.shape
+    rc = load().fa_bwd(_bf16(q, "q"), _bf16(k, "k"), _bf16(v, "v"), _bf16(o, "o"), _bf16(do, "do"),
+                       _f32(lse, "lse"), _bf16(dq, "dq"), _bf16(dk, "dk"), _bf16(dv, "dv"),
+                       ctypes.c_void_p(workspace.data_ptr()), B, H, N, d, float(scale),
+                       int(bool(causal)), _stream(stream))
+    _check("fa_bwd", rc)
+
+
+def fa_bwd_blocksparse(q, k, v, o, do, lse, block_mask, dq, dk, dv, workspace, scale, stream=None):
+    B, H, N, d = q.shape
+    rc = load().fa_bwd_blocksparse(_bf16(q, "q"), _bf16(k, "k"), _bf16(v, "v"), _bf16(o, "o"),
+                                   _bf16(do, "do"), _f32(lse, "lse"), _mask_ptr(block_mask),
+                                   _bf16(dq, "dq"), _bf16(dk, "dk"), _bf16(dv, "dv"),
+                                   ctypes.c_void_p(workspace.data_ptr()), B, H, N, d, float(scale),
+                                   _stream(stream))
+    _check("fa_bwd_blocksparse", rc)
+
+
+def fa_bwd_preprocess(o, do, workspace, stream=None):
+    B, H, N, d = o.shape
+    rc = load().fa_bwd_preprocess(_bf16(o, "o"), _bf16(do, "do"), ctypes.c_void_p(workspace.data_ptr()),
+                                  B, H, N, d, _stream(stream))
+    _check("fa_bwd_preprocess", rc)
+
+
+def fa_bwd_main(q, k, v, do, lse, block_mask, dk, dv, workspace, scale, mask_kind, stream=None):
+    B, H, N, d = q.shape
+    rc = load().fa_bwd_main(_bf16(q, "q"), _bf16(k, "k"), _bf16(v, "v"), _bf16(do, "do"), _f32(lse, "lse"),
+                            _mask_ptr(block_mask), _bf16(dk, "dk"), _bf16(dv, "dv"),
+                            ctypes.c_void_p(workspace.data_ptr()), B, H, N, d, float(scale), int(mask_kind),
+                            _stream(stream))
+    _check("fa_bwd_main", rc)
+
+
+def fa_bwd_dq_convert(workspace, dq, scale, stream=None):
+    B, H, N, d = dq.shape
+    rc = load().fa_bwd_dq_convert(ctypes.c_void_p(workspace.data_ptr()), _bf16(dq, "dq"), B, H, N, d,
+                                  float(scale), _stream(stream))
+    _check("fa_bwd_dq_convert", rc)
+
+
+def fa_get_device_error(stream=None) -> int:
+    return load().fa_get_device_error(_stream(stream))
+
+
+def fa_set_wait_timeout_ns(ns: int):
+    _check("fa_set_wait_timeout_ns", load().fa_set_wait_timeout_ns(int(ns)))
+
+
+def fa_debug_wait_timeout(ns: int, stream=None) -> int:
+    return load().fa_debug_wait_timeout(int(ns), _stream(stream))
+
+
+# --------------------------------------------------------------------------- #
+# conveniences that allocate outputs
+# --------------------------------------------------------------------------- #
+def forward(q, k, v, causal=False, scale=None, block_mask=None, stream=None):
+    """Returns (O bf16 [B,H,N,d], LSE fp32 [B,H,N])."""
+    B, H, N, d = q.shape
+    scale = (1.0 / d ** 0.5) if scale is None else scale
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    if block_mask is not None:
+        fa_fwd_blocksparse(q, k, v, o, lse, block_mask, scale, stream)
+    else:
+        fa_fwd(q, k, v, o, lse, scale, causal, stream)
+    return o, lse
+
+
+def workspace(B, H, N, d, device) -> torch.Tensor:
+    n = fa_bwd_workspace_bytes(B, H, N, d)
+    if n == 0:
+        raise ValueError("invalid sizes for the backward workspace")
+    return torch.empty(n, dtype=torch.uint8, device=device)
+
+
+def backward(q, k, v, o, lse, do, causal=False, scale=None, block_mask=None, ws=None, stream=None):
+    """Returns (dQ, dK, dV), bf16 [B,H,N,d]."""
+    B, H, N, d = q.shape
+    scale = (1.0 / d ** 0.5) if scale is None else scale
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws = workspace(B, H, N, d, q.device) if ws is None else ws
+    if block_mask is not None:
+        fa_bwd_blocksparse(q, k, v, o, do, lse, block_mask, dq, dk, dv, ws, scale, stream)
+    else:
+        fa_bwd(q, k, v, o, do, lse, dq, dk, dv, ws, scale, causal, stream)
+    return dq, dk, dv
+
+
+def fa_status_string(code: int) -> str:
+    return status_string(code)

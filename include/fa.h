@@ -1,0 +1,176 @@
+/*
+ * fa.h -- C ABI of libfa.so: exact scaled dot-product attention on one GB300
+ * (sm_103a), forward with the online-softmax recurrence and a recompute
+ * backward.
+ *
+ * What is computed (per batch b and head h, rows of N x d matrices):
+ *   S = scale * Q K^T, masked entries -inf   ("Transformer 入门", section
+ *       "flash attention": S = QK^T/sqrt(d), m = rowmax(S), l = rowsum(exp(S-m)))
+ *   P = softmax(S) row by row, O = P V        ("FlashAttention" notes,
+ *       "Standard Attention Implementation")
+ *   LSE_i = m_i + ln(l_i), natural log, stored instead of S and P
+ *       ("FlashAttention" notes, "Tiling": keep (m, l) instead of S, P)
+ *   dV = P^T dO, dP = dO V^T, D_i = dO_i . O_i, dS = P o (dP - D),
+ *   dQ = scale * dS K, dK = scale * dS^T Q   ("FlashAttention" notes,
+ *       "Backward Pass of flashattention", with the scale's chain rule)
+ * The forward never writes S or P to memory; the backward recomputes P from
+ * Q, K and the saved LSE.
+ *
+ * Layout and types (every tensor argument):
+ *   q, k, v, o, dout, dq, dk, dv : bf16, contiguous [B, H, N, d], device memory
+ *   lse                          : fp32, contiguous [B, H, N], device memory
+ *   block_mask                   : uint8, contiguous [N/128, N/128], device
+ *                                  memory, shared by every (b, h); nonzero keeps
+ *                                  the 128 x 128 block (query block, key block)
+ *   workspace                    : device memory of at least
+ *                                  fa_bwd_workspace_bytes(B, H, N, d) bytes,
+ *                                  256-byte aligned; its contents on entry do
+ *                                  not matter.
+ * Supported: d in {64, 128}; N a positive multiple of 128; B, H >= 1;
+ * B * H * N * d < 2^31; scale finite and > 0; pointers 16-byte aligned;
+ * a device of compute capability 10.3.
+ *
+ * Masks: causal keeps key j for query i iff j <= i (equal query and key
+ * lengths); key tiles that a mask removes entirely are skipped, never loaded.
+ * A query row with no visible key (possible only with a block mask whose
+ * diagonal block is off) gets O = 0, LSE = -inf and zero gradients.
+ *
+ * Ownership: the caller allocates and frees every buffer and keeps it alive
+ * until the enqueued work has finished.  The library holds no pointer after
+ * a call returns; its only state is one status word per device (read through
+ * fa_get_device_error()) and the wait timeout.
+ *
+ * Asynchrony and errors: every compute call validates its arguments on the
+ * host, enqueues its kernels on `stream` and returns without waiting.  A
+ * negative return value (an fa_status) means nothing was enqueued, except
+ * FA_ERR_LAUNCH, which reports a launch failure from the CUDA runtime.  A
+ * kernel whose internal wait exceeds the wait timeout (see
+ * fa_set_wait_timeout_ns) records FA_ERR_TIMEOUT in the status word and
+ * returns early; its outputs are then undefined.
+ */
+#ifndef FA_H_
+#define FA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Symbols of the C ABI are exported from libfa.so; everything else is hidden. */
+#if defined(__GNUC__)
+#define FA_API __attribute__((visibility("default")))
+#else
+#define FA_API
+#endif
+
+/* Same type as cudaStream_t; NULL is the legacy default stream. */
+typedef struct CUstream_st *fa_stream_t;
+
+typedef enum fa_status {
+  FA_OK = 0,
+  FA_ERR_INVALID = -1,     /* bad argument: null pointer, size, alignment, scale */
+  FA_ERR_UNSUPPORTED = -2, /* valid but not built: head dim other than 64/128, N % 128 != 0 */
+  FA_ERR_ARCH = -3,        /* current device is not compute capability 10.3 */
+  FA_ERR_LAUNCH = -4,      /* the CUDA runtime refused a launch or attribute call */
+  FA_ERR_TIMEOUT = -5,     /* a kernel wait ran past the wait timeout (device status) */
+  FA_ERR_CUDA = -6         /* another CUDA runtime error (device query, descriptor) */
+} fa_status;
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+FA_API int fa_version(void);
+
+/* Human-readable name of an fa_status value; never NULL. */
+FA_API const char *fa_status_string(int status);
+
+/*
+ * Forward: O and LSE from Q, K, V.  causal != 0 applies the lower-triangular
+ * mask.  Cited: "FlashAttention" notes, "Tiling" and "Correctness"
+ * (Theorem 1: the tiled recurrence yields softmax(S) V exactly);
+ * "Как работает FlashAttention математически", sections 3-4 (online softmax
+ * and output correction).
+ */
+FA_API int fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
+           int B, int H, int N, int d, float scale, int causal, fa_stream_t stream);
+
+/*
+ * Forward with a 128 x 128 block mask (block-sparse attention, "FlashAttention"
+ * notes, "Block-sparse Flashattention"): blocks whose mask byte is 0 are
+ * skipped and add nothing to m, l or O.
+ */
+FA_API int fa_fwd_blocksparse(const void *q, const void *k, const void *v, void *o, float *lse,
+                       const uint8_t *block_mask, int B, int H, int N, int d, float scale,
+                       fa_stream_t stream);
+
+/*
+ * Bytes of device workspace that fa_bwd needs: an fp32 dQ accumulator
+ * [B, H, N, d] and the fp32 vector D [B, H, N], each 256-byte aligned.
+ * Returns 0 when the sizes are invalid.
+ */
+FA_API size_t fa_bwd_workspace_bytes(int B, int H, int N, int d);
+
+/*
+ * Backward: dQ, dK, dV from Q, K, V, the forward's O and LSE, and dO.
+ * Runs the three stages below in order on `stream`.  Cited: "FlashAttention"
+ * notes, "Backward Pass of flashattention" (recompute P from the saved
+ * statistics; D_i = do_i . o_i; masks are regenerated, not stored).
+ */
+FA_API int fa_bwd(const void *q, const void *k, const void *v, const void *o, const void *dout,
+           const float *lse, void *dq, void *dk, void *dv, void *workspace,
+           int B, int H, int N, int d, float scale, int causal, fa_stream_t stream);
+
+/* Backward with the block mask of fa_fwd_blocksparse. */
+FA_API int fa_bwd_blocksparse(const void *q, const void *k, const void *v, const void *o,
+                       const void *dout, const float *lse, const uint8_t *block_mask,
+                       void *dq, void *dk, void *dv, void *workspace,
+                       int B, int H, int N, int d, float scale, fa_stream_t stream);
+
+/*
+ * Backward stage 1 of 3: D_i = sum_c dO[i,c] O[i,c] in fp32 into the
+ * workspace, and the workspace's dQ accumulator set to zero.
+ */
+FA_API int fa_bwd_preprocess(const void *o, const void *dout, void *workspace,
+                      int B, int H, int N, int d, fa_stream_t stream);
+
+/*
+ * Backward stage 2 of 3: per 128-key tile, recompute P and accumulate dK, dV
+ * (written as bf16) and add dS K into the workspace's dQ accumulator.
+ * mask_kind: 0 none, 1 causal, 2 block (block_mask required).
+ */
+FA_API int fa_bwd_main(const void *q, const void *k, const void *v, const void *dout,
+                const float *lse, const uint8_t *block_mask, void *dk, void *dv,
+                void *workspace, int B, int H, int N, int d, float scale, int mask_kind,
+                fa_stream_t stream);
+
+/* Backward stage 3 of 3: dQ = bf16(scale * accumulator). */
+FA_API int fa_bwd_dq_convert(const void *workspace, void *dq, int B, int H, int N, int d,
+                      float scale, fa_stream_t stream);
+
+/*
+ * Synchronises `stream`, then returns and clears the current device's status
+ * word: FA_OK, or FA_ERR_TIMEOUT when a kernel wait gave up.  Returns
+ * FA_ERR_CUDA when the synchronisation itself fails.
+ */
+FA_API int fa_get_device_error(fa_stream_t stream);
+
+/*
+ * Sets the limit, in nanoseconds, after which a kernel's wait on an on-chip
+ * barrier gives up (default 2e9).  Applies to launches made after the call,
+ * from any thread.  Returns FA_ERR_INVALID for 0.
+ */
+FA_API int fa_set_wait_timeout_ns(uint64_t ns);
+
+/*
+ * Self-test of the timeout path: launches one small kernel whose barrier wait
+ * can never complete, with the given limit (nanoseconds, at most 1e9), waits
+ * for it and returns what fa_get_device_error() then reports (FA_ERR_TIMEOUT
+ * when the bounded wait works).  Faults nothing; the context stays usable.
+ */
+FA_API int fa_debug_wait_timeout(uint64_t timeout_ns, fa_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_H_ */

@@ -1,0 +1,114 @@
+"""The C ABI without a GPU: the library builds, loads, exports every symbol the
+header declares, and rejects bad arguments on the host before any CUDA call."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from attn_fwd_gb300 import build
+    import attn_fwd_gb300.fa as fa
+    build.build()
+    return fa.load()
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "fa.h")).read()
+    return sorted(set(re.findall(r"FA_API\s+[^;(]*?\b(fa_\w+)\s*\(", src)))
+
+
+def test_header_declares_the_abi():
+    names = _declared()
+    for must in ("fa_fwd", "fa_bwd", "fa_fwd_blocksparse", "fa_bwd_blocksparse",
+                 "fa_bwd_workspace_bytes", "fa_get_device_error", "fa_status_string"):
+        assert must in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in _declared():
+        assert hasattr(lib, name), name
+    # and nothing else of ours leaks out of the shared object
+    import subprocess
+    out = subprocess.run(["nm", "-D", "--defined-only", lib._name], capture_output=True, text=True).stdout
+    exported = sorted(set(re.findall(r"\bT (fa_\w+)", out)))
+    assert exported == _declared()
+
+
+def test_python_binding_covers_every_entry_point(lib):
+    import attn_fwd_gb300.fa as fa
+    for name in _declared():
+        assert callable(getattr(fa, name)), name
+
+
+def test_status_strings(lib):
+    import attn_fwd_gb300.fa as fa
+    for code in range(0, -7, -1):
+        assert fa.status_string(code).startswith("FA_")
+    assert fa.status_string(12345) == "unknown fa_status"
+    assert fa.fa_version() >= 100
+
+
+def test_workspace_bytes(lib):
+    import attn_fwd_gb300.fa as fa
+    B, H, N, d = 2, 16, 4096, 128
+    n = fa.fa_bwd_workspace_bytes(B, H, N, d)
+    assert n >= B * H * N * d * 4 + B * H * N * 4
+    assert n % 256 == 0
+    assert fa.fa_bwd_workspace_bytes(0, 1, 128, 64) == 0
+    assert fa.fa_bwd_workspace_bytes(1 << 20, 1 << 10, 128, 128) == 0   # 2^31 elements or more
+
+
+P = ctypes.c_void_p(4096)   # 16-byte aligned dummy pointers; never dereferenced on these paths
+NULL = ctypes.c_void_p(0)
+ODD = ctypes.c_void_p(4096 + 8)
+
+
+@pytest.mark.parametrize("args,expect", [
+    ((NULL, P, P, P, P, 1, 1, 128, 64, 0.125, 0), -1),          # null q
+    ((P, P, P, P, ODD, 1, 1, 128, 64, 0.125, 0), -1),           # misaligned lse
+    ((P, P, P, P, P, 0, 1, 128, 64, 0.125, 0), -1),             # B = 0
+    ((P, P, P, P, P, 1, 1, 128, 96, 0.125, 0), -2),             # d not built
+    ((P, P, P, P, P, 1, 1, 200, 64, 0.125, 0), -2),             # N % 128 != 0
+    ((P, P, P, P, P, 1, 1, 128, 64, float("nan"), 0), -1),      # scale not finite
+    ((P, P, P, P, P, 1, 1, 128, 64, -1.0, 0), -1),              # scale <= 0
+    ((P, P, P, P, P, 65536, 256, 1024, 128, 0.1, 0), -1),       # 2^31 elements or more
+])
+def test_fwd_rejects_bad_arguments(lib, args, expect):
+    assert lib.fa_fwd(*args, NULL) == expect
+
+
+def test_blocksparse_requires_mask(lib):
+    assert lib.fa_fwd_blocksparse(P, P, P, P, P, NULL, 1, 1, 128, 64, 0.125, NULL) == -1
+    assert lib.fa_bwd_blocksparse(P, P, P, P, P, P, NULL, P, P, P, P, 1, 1, 128, 64, 0.125, NULL) == -1
+
+
+def test_bwd_rejects_bad_arguments(lib):
+    ws = ctypes.c_void_p(4096 + 16)       # 16- but not 256-byte aligned
+    assert lib.fa_bwd(P, P, P, P, P, P, P, P, P, NULL, 1, 1, 128, 64, 0.125, 0, NULL) == -1
+    assert lib.fa_bwd_main(P, P, P, P, P, NULL, P, P, ws, 1, 1, 128, 64, 0.125, 0, NULL) == -1
+    assert lib.fa_bwd_main(P, P, P, P, P, NULL, P, P, P, 1, 1, 128, 64, 0.125, 7, NULL) == -1
+    assert lib.fa_bwd_main(P, P, P, P, P, NULL, P, P, P, 1, 1, 128, 64, 0.125, 2, NULL) == -1
+    assert lib.fa_bwd_preprocess(P, P, P, 1, 1, 100, 64, NULL) == -2
+    assert lib.fa_bwd_dq_convert(P, P, 1, 1, 128, 64, 0.0, NULL) == -1
+
+
+def test_timeout_setter(lib):
+    assert lib.fa_set_wait_timeout_ns(0) == -1
+    assert lib.fa_set_wait_timeout_ns(2_000_000_000) == 0
+    assert lib.fa_debug_wait_timeout(0, NULL) == -1
+    assert lib.fa_debug_wait_timeout(5_000_000_000, NULL) == -1
+
+
+def test_valid_call_without_gpu_fails_loudly(lib):
+    """With no usable CUDA device a valid call reports an error code; it never
+    computes anything on the host."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    rc = lib.fa_fwd(P, P, P, P, P, 1, 1, 128, 64, 0.125, 0, NULL)
+    assert rc in (-6, -3)

@@ -1,0 +1,345 @@
+"""CUDA path vs the fp64 oracle, element by element, on the same seeded inputs.
+
+Tolerances (bf16 inputs, fp32 accumulation): forward O max-abs error <= 1e-2
+beyond the rounding of O to bf16 itself (|O - O_ref| <= 1e-2 + 2^-8 |O_ref|:
+2^-8 |x| is half a bf16 ulp, which alone exceeds 1e-2 once |O| > 2.56, as in
+the x3-amplitude workload); LSE relative error <= 1e-3, relative to
+max(|LSE|, 1); dQ, dK, dV relative L2 error <= 2e-2.
+Workloads the oracle cannot finish in seconds are checked on sampled heads
+(whole heads through the oracle) or on sampled query rows.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from attn_fwd_gb300.inputs import WORKLOADS, make_block_mask, make_qkvdo, make_workload_inputs
+import oracle
+
+pytestmark = pytest.mark.gpu
+
+O_ATOL = 1e-2
+BF16_HALF_ULP_REL = 2.0 ** -8
+LSE_RTOL = 1e-3
+GRAD_RTOL = 2e-2
+
+
+@pytest.fixture(scope="module")
+def fa():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import __graft_entry__
+    __graft_entry__.build()
+    import attn_fwd_gb300.fa as fa
+    fa.load()
+    fa.fa_set_wait_timeout_ns(500_000_000)   # a broken pipeline fails fast instead of waiting 2 s per CTA
+    return fa
+
+
+def _dev(t):
+    return t.to("cuda")
+
+
+def _np64(t):
+    return t.double().numpy()
+
+
+def _check_fwd(o_gpu, lse_gpu, o_ref, lse_ref, what=""):
+    o_gpu = o_gpu.float().cpu().numpy()
+    lse_gpu = lse_gpu.float().cpu().numpy()
+    assert np.isfinite(o_gpu).all(), what
+    err_o = np.abs(o_gpu - o_ref).max()
+    excess = (np.abs(o_gpu - o_ref) - (O_ATOL + BF16_HALF_ULP_REL * np.abs(o_ref))).max()
+    fin = np.isfinite(lse_ref)
+    assert np.array_equal(np.isfinite(lse_gpu), fin), what
+    err_l = (np.abs(lse_gpu[fin] - lse_ref[fin]) / np.maximum(np.abs(lse_ref[fin]), 1.0)).max() if fin.any() else 0.0
+    assert excess <= 0, f"{what}: O error {err_o} exceeds 1e-2 + 2^-8|O| by {excess}"
+    assert err_l <= LSE_RTOL, f"{what}: LSE rel error {err_l}"
+    return err_o, err_l
+
+
+def _rel_l2(g, r):
+    g = g.float().cpu().numpy()
+    return np.linalg.norm(g - r) / max(np.linalg.norm(r), 1e-30)
+
+
+def _check_device_status(fa):
+    torch.cuda.synchronize()
+    rc = fa.fa_get_device_error()
+    assert rc == 0, fa.status_string(rc)
+
+
+# --------------------------------------------------------------------------- #
+# forward, oracle on every element
+# --------------------------------------------------------------------------- #
+SMALL = [
+    # B, H, N, d, causal, mask_p
+    (1, 1, 128, 64, False, None),
+    (1, 1, 128, 128, True, None),
+    (2, 3, 256, 64, True, None),
+    (1, 2, 384, 128, False, None),       # odd tile count: the last CTA has one query tile
+    (1, 2, 384, 64, True, None),
+    (2, 1, 640, 128, True, None),
+    (1, 2, 512, 64, False, 0.3),
+    (1, 2, 768, 128, False, 0.25),
+]
+
+
+@pytest.mark.parametrize("B,H,N,d,causal,p", SMALL)
+def test_forward_small(fa, B, H, N, d, causal, p):
+    t = make_qkvdo(B, H, N, d, seed=10 + N + d, with_dout=False)
+    scale = 1 / math.sqrt(d)
+    bm = make_block_mask(N, seed=N, p=p) if p is not None else None
+    o, lse = fa.forward(_dev(t["q"]), _dev(t["k"]), _dev(t["v"]), causal=causal, scale=scale,
+                        block_mask=None if bm is None else _dev(bm))
+    _check_device_status(fa)
+    ro, rl = oracle.forward(_np64(t["q"]), _np64(t["k"]), _np64(t["v"]), scale, causal=causal,
+                            block_mask=None if bm is None else bm.numpy())
+    _check_fwd(o, lse, ro, rl, f"B{B} H{H} N{N} d{d} causal={causal} p={p}")
+
+
+def test_forward_workload_small_tile(fa):
+    """The single-tile latency workload: B1 H1 N128 d64, seed 0."""
+    w = WORKLOADS["fwd_b1h1n128d64"]
+    t = make_workload_inputs(w)
+    o, lse = fa.forward(_dev(t["q"]), _dev(t["k"]), _dev(t["v"]), causal=w.causal, scale=w.scale)
+    _check_device_status(fa)
+    ro, rl = oracle.forward(_np64(t["q"]), _np64(t["k"]), _np64(t["v"]), w.scale)
+    _check_fwd(o, lse, ro, rl, w.name)
+
+
+def test_forward_workload_n1024(fa):
+    w = WORKLOADS["fwdbwd_b4h8n1024d64"]
+    t = make_workload_inputs(w)
+    o, lse = fa.forward(_dev(t["q"]), _dev(t["k"]), _dev(t["v"]), causal=w.causal, scale=w.scale)
+    _check_device_status(fa)
+    ro, rl = oracle.forward(_np64(t["q"]), _np64(t["k"]), _np64(t["v"]), w.scale)
+    _check_fwd(o, lse, ro, rl, w.name)
+
+
+def test_forward_fully_masked_rows(fa):
+    """Query blocks whose every block-mask byte is 0 get O = 0 and LSE = -inf."""
+    B, H, N, d = 1, 2, 512, 64
+    t = make_qkvdo(B, H, N, d, seed=77, with_dout=False)
+    bm = torch.ones(4, 4, dtype=torch.uint8)
+    bm[1, :] = 0
+    bm[3, 1:] = 0
+    o, lse = fa.forward(_dev(t["q"]), _dev(t["k"]), _dev(t["v"]), block_mask=_dev(bm))
+    _check_device_status(fa)
+    ro, rl = oracle.forward(_np64(t["q"]), _np64(t["k"]), _np64(t["v"]), 1 / 8, block_mask=bm.numpy())
+    _check_fwd(o, lse, ro, rl, "fully masked rows")
+    assert torch.all(o[:, :, 128:256] == 0)
+
+
+def test_forward_guard_bands(fa):
+    """Outputs written through views of larger buffers leave the padding untouched."""
+    B, H, N, d = 1, 2, 256, 128
+    t = make_qkvdo(B, H, N, d, seed=5, with_dout=False)
+    n = B * H * N * d
+    pad = 4096
+    obuf = torch.full((n + 2 * pad,), 7.0, dtype=torch.bfloat16, device="cuda")
+    lbuf = torch.full((B * H * N + 2 * pad,), 7.0, dtype=torch.float32, device="cuda")
+    o = obuf[pad:pad + n].view(B, H, N, d)
+    lse = lbuf[pad:pad + B * H * N].view(B, H, N)
+    fa.fa_fwd(_dev(t["q"]), _dev(t["k"]), _dev(t["v"]), o, lse, 1 / math.sqrt(d), causal=True)
+    _check_device_status(fa)
+    assert torch.all(obuf[:pad] == 7.0) and torch.all(obuf[pad + n:] == 7.0)
+    assert torch.all(lbuf[:pad] == 7.0) and torch.all(lbuf[pad + B * H * N:] == 7.0)
+
+
+def test_forward_deterministic(fa):
+    t = make_qkvdo(1, 4, 1024, 128, seed=6, with_dout=False)
+    q, k, v = (_dev(t[n]) for n in ("q", "k", "v"))
+    o1, l1 = fa.forward(q, k, v, causal=True)
+    o2, l2 = fa.forward(q, k, v, causal=True)
+    _check_device_status(fa)
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_forward_on_side_stream(fa):
+    t = make_qkvdo(1, 2, 256, 64, seed=8, with_dout=False)
+    q, k, v = (_dev(t[n]) for n in ("q", "k", "v"))
+    ref_o, ref_l = fa.forward(q, k, v)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        o, lse = fa.forward(q, k, v)
+    s.synchronize()
+    assert torch.equal(o, ref_o) and torch.equal(lse, ref_l)
+
+
+# --------------------------------------------------------------------------- #
+# forward at full workload sizes, sampled
+# --------------------------------------------------------------------------- #
+def _sampled_heads(BH, k, seed):
+    r = np.random.default_rng(seed)
+    return sorted(r.choice(BH, size=min(k, BH), replace=False).tolist())
+
+
+@pytest.mark.parametrize("name", ["fwdbwd_b2h16n4096d128_causal", "fwdbwd_b1h16n8192d128_blocksparse"])
+def test_forward_workload_sampled_heads(fa, name):
+    w = WORKLOADS[name]
+    t = make_workload_inputs(w)
+    bm = t.get("block_mask")
+    o, lse = fa.forward(_dev(t["q"]), _dev(t["k"]), _dev(t["v"]), causal=w.causal, scale=w.scale,
+                        block_mask=None if bm is None else _dev(bm))
+    _check_device_status(fa)
+    assert torch.isfinite(o).all() and torch.isfinite(lse).all()
+    for hh in _sampled_heads(w.B * w.H, 3, seed=w.seed):
+        b, h = divmod(hh, w.H)
+        sl = (slice(b, b + 1), slice(h, h + 1))
+        ro, rl = oracle.forward(_np64(t["q"][sl]), _np64(t["k"][sl]), _np64(t["v"][sl]), w.scale,
+                                causal=w.causal, block_mask=None if bm is None else bm.numpy())
+        _check_fwd(o[sl], lse[sl], ro, rl, f"{name} head {hh}")
+
+
+def test_forward_workload_long_causal_sampled_rows(fa):
+    """N=16384 causal with x3 inputs: S would be 16 GiB; check sampled rows of
+    sampled heads, including the first and last rows of the sequence."""
+    w = WORKLOADS["fwd_b1h32n16384d128_causal_x3"]
+    t = make_workload_inputs(w)
+    o, lse = fa.forward(_dev(t["q"]), _dev(t["k"]), _dev(t["v"]), causal=True, scale=w.scale)
+    _check_device_status(fa)
+    assert torch.isfinite(o).all() and torch.isfinite(lse).all()
+    r = np.random.default_rng(3)
+    rows = sorted(set([0, 1, 127, 128, w.N - 1] + r.choice(w.N, 59, replace=False).tolist()))
+    for h in _sampled_heads(w.H, 4, seed=33):
+        sl = (slice(0, 1), slice(h, h + 1))
+        ro, rl = oracle.forward_rows(_np64(t["q"][sl]), _np64(t["k"][sl]), _np64(t["v"][sl]), w.scale,
+                                     0, 0, rows, causal=True)
+        _check_fwd(o[0, h, rows], lse[0, h, rows], ro, rl, f"N=16384 head {h}")
+
+
+# --------------------------------------------------------------------------- #
+# failure detection without a fault
+# --------------------------------------------------------------------------- #
+def test_bounded_wait_reports_timeout(fa):
+    """A kernel waits on a barrier that nothing completes; the bounded wait gives
+    up after 1 ms, the status word says FA_ERR_TIMEOUT, and the context stays
+    usable for the next call."""
+    assert fa.fa_debug_wait_timeout(1_000_000) == fa.FA_ERR_TIMEOUT
+    assert fa.fa_get_device_error() == 0        # the read cleared it
+    t = make_qkvdo(1, 1, 128, 64, seed=0, with_dout=False)
+    o, lse = fa.forward(_dev(t["q"]), _dev(t["k"]), _dev(t["v"]))
+    _check_device_status(fa)
+    ro, rl = oracle.forward(_np64(t["q"]), _np64(t["k"]), _np64(t["v"]), 1 / 8)
+    _check_fwd(o, lse, ro, rl, "after timeout")
+
+
+# --------------------------------------------------------------------------- #
+# backward
+# --------------------------------------------------------------------------- #
+def _run_fwd_bwd(fa, t, causal, scale, bm=None):
+    q, k, v, do = (_dev(t[n]) for n in ("q", "k", "v", "do"))
+    bmd = None if bm is None else _dev(bm)
+    o, lse = fa.forward(q, k, v, causal=causal, scale=scale, block_mask=bmd)
+    dq, dk, dv = fa.backward(q, k, v, o, lse, do, causal=causal, scale=scale, block_mask=bmd)
+    _check_device_status(fa)
+    return dq, dk, dv
+
+
+def _check_bwd(g, ref, what):
+    for name, a, r in zip(("dQ", "dK", "dV"), g, ref):
+        assert torch.isfinite(a).all(), f"{what}: {name} not finite"
+        rel = _rel_l2(a, r)
+        assert rel <= GRAD_RTOL, f"{what}: {name} rel-L2 error {rel}"
+
+
+BWD_SMALL = [
+    (1, 1, 128, 64, False, None),
+    (1, 1, 128, 128, True, None),
+    (2, 2, 256, 64, True, None),
+    (1, 2, 384, 128, True, None),
+    (1, 2, 384, 64, False, None),
+    (2, 1, 512, 128, False, None),
+    (1, 2, 512, 64, False, 0.3),
+    (1, 2, 768, 128, False, 0.25),
+]
+
+
+@pytest.mark.parametrize("B,H,N,d,causal,p", BWD_SMALL)
+def test_backward_small(fa, B, H, N, d, causal, p):
+    t = make_qkvdo(B, H, N, d, seed=20 + N + d)
+    scale = 1 / math.sqrt(d)
+    bm = make_block_mask(N, seed=N + 1, p=p) if p is not None else None
+    g = _run_fwd_bwd(fa, t, causal, scale, bm)
+    f64 = {n: _np64(t[n]) for n in ("q", "k", "v", "do")}
+    rdq, rdk, rdv, _ = oracle.backward(f64["q"], f64["k"], f64["v"], f64["do"], scale, causal=causal,
+                                       block_mask=None if bm is None else bm.numpy())
+    _check_bwd(g, (rdq, rdk, rdv), f"B{B} H{H} N{N} d{d} causal={causal} p={p}")
+
+
+def test_backward_workload_n1024(fa):
+    w = WORKLOADS["fwdbwd_b4h8n1024d64"]
+    t = make_workload_inputs(w)
+    g = _run_fwd_bwd(fa, t, w.causal, w.scale)
+    f64 = {n: _np64(t[n]) for n in ("q", "k", "v", "do")}
+    rdq, rdk, rdv, _ = oracle.backward(f64["q"], f64["k"], f64["v"], f64["do"], w.scale)
+    _check_bwd(g, (rdq, rdk, rdv), w.name)
+
+
+@pytest.mark.parametrize("name", ["fwdbwd_b2h16n4096d128_causal", "fwdbwd_b1h16n8192d128_blocksparse"])
+def test_backward_workload_sampled_heads(fa, name):
+    w = WORKLOADS[name]
+    t = make_workload_inputs(w)
+    bm = t.get("block_mask")
+    g = _run_fwd_bwd(fa, t, w.causal, w.scale, bm)
+    for hh in _sampled_heads(w.B * w.H, 2, seed=w.seed + 100):
+        b, h = divmod(hh, w.H)
+        sl = (slice(b, b + 1), slice(h, h + 1))
+        f64 = {n: _np64(t[n][sl]) for n in ("q", "k", "v", "do")}
+        rdq, rdk, rdv, _ = oracle.backward(f64["q"], f64["k"], f64["v"], f64["do"], w.scale, causal=w.causal,
+                                           block_mask=None if bm is None else bm.numpy())
+        _check_bwd(tuple(x[sl] for x in g), (rdq, rdk, rdv), f"{name} head {hh}")
+
+
+def test_backward_fully_masked_blocks(fa):
+    """A query block that sees nothing gets dQ = 0; a key block that no query
+    sees gets dK = dV = 0."""
+    B, H, N, d = 1, 2, 512, 128
+    t = make_qkvdo(B, H, N, d, seed=78)
+    bm = torch.ones(4, 4, dtype=torch.uint8)
+    bm[1, :] = 0          # query block 1 sees nothing
+    bm[:, 2] = 0          # key block 2 is seen by nobody
+    g = _run_fwd_bwd(fa, t, False, 1 / math.sqrt(d), bm)
+    f64 = {n: _np64(t[n]) for n in ("q", "k", "v", "do")}
+    ref = oracle.backward(f64["q"], f64["k"], f64["v"], f64["do"], 1 / math.sqrt(d), block_mask=bm.numpy())[:3]
+    _check_bwd(g, ref, "fully masked blocks")
+    dq, dk, dv = g
+    assert torch.all(dq[:, :, 128:256] == 0)
+    assert torch.all(dk[:, :, 256:384] == 0) and torch.all(dv[:, :, 256:384] == 0)
+
+
+def test_backward_stages_match_fused_call(fa):
+    """fa_bwd equals its three stages called one by one."""
+    B, H, N, d = 1, 2, 512, 128
+    t = make_qkvdo(B, H, N, d, seed=9)
+    q, k, v, do = (_dev(t[n]) for n in ("q", "k", "v", "do"))
+    scale = 1 / math.sqrt(d)
+    o, lse = fa.forward(q, k, v, causal=True, scale=scale)
+    dq, dk, dv = fa.backward(q, k, v, o, lse, do, causal=True, scale=scale)
+    ws = fa.workspace(B, H, N, d, q.device)
+    dq2, dk2, dv2 = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    fa.fa_bwd_preprocess(o, do, ws)
+    fa.fa_bwd_main(q, k, v, do, lse, None, dk2, dv2, ws, scale, fa.MASK_CAUSAL)
+    fa.fa_bwd_dq_convert(ws, dq2, scale)
+    _check_device_status(fa)
+    assert torch.equal(dk, dk2) and torch.equal(dv, dv2)
+    # dQ sums fp32 atomics in arrival order, so it is equal up to rounding only
+    assert (dq.float() - dq2.float()).abs().max().item() <= 1e-2 * dq.float().abs().max().item()
+
+
+def test_backward_guard_bands(fa):
+    B, H, N, d = 1, 1, 256, 64
+    t = make_qkvdo(B, H, N, d, seed=11)
+    q, k, v, do = (_dev(t[n]) for n in ("q", "k", "v", "do"))
+    o, lse = fa.forward(q, k, v, causal=True)
+    n, pad = B * H * N * d, 2048
+    bufs = [torch.full((n + 2 * pad,), 5.0, dtype=torch.bfloat16, device="cuda") for _ in range(3)]
+    outs = [b[pad:pad + n].view(B, H, N, d) for b in bufs]
+    ws = fa.workspace(B, H, N, d, q.device)
+    fa.fa_bwd(q, k, v, o, do, lse, *outs, ws, 1 / 8, causal=True)
+    _check_device_status(fa)
+    for b in bufs:
+        assert torch.all(b[:pad] == 5.0) and torch.all(b[pad + n:] == 5.0)
