@@ -283,7 +283,8 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
       const uint32_t o_addr = tmem_addr(tmem, quarter * 32, w ? L::O_COL1 : L::O_COL0);
       const float sl2 = p.scale_log2;
       float m = -INFINITY;  // reference max, in exp2 units of scaled scores
-      float l = 0.f;
+      float l = 0.f;    // row sum of exp2(S - m), fp32
+      float lr = 0.f;   // the same sum over the bf16-rounded values used in P V
       bool has_o = false;
       bool ok = true;
       uint32_t sphase = 0;
@@ -327,14 +328,15 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
           const float p3 = ex2_approx(fmaf(s[2 * c + 3], sl2, -m));
           pk[c] = pack_bf16x2(p0, p1);
           pk[c + 1] = pack_bf16x2(p2, p3);
-          // l sums the bf16 values that P V multiplies, so O = sum_j w_j v_j
-          // with weights that sum to exactly one.
-          sum0 += __uint_as_float(pk[c] << 16);
-          sum1 += __uint_as_float(pk[c] & 0xffff0000u);
-          sum2 += __uint_as_float(pk[c + 1] << 16);
-          sum3 += __uint_as_float(pk[c + 1] & 0xffff0000u);
+          // lr sums the bf16 values that P V multiplies, so O / lr weighs the
+          // V rows with weights summing to exactly one; l (unrounded) gives LSE.
+          sum0 += p0 + p1;
+          sum1 += p2 + p3;
+          sum2 += __uint_as_float(pk[c] << 16) + __uint_as_float(pk[c] & 0xffff0000u);
+          sum3 += __uint_as_float(pk[c + 1] << 16) + __uint_as_float(pk[c + 1] & 0xffff0000u);
         }
-        l = l * alpha + ((sum0 + sum1) + (sum2 + sum3));
+        l = l * alpha + (sum0 + sum1);
+        lr = lr * alpha + (sum2 + sum3);
         if (has_o && __any_sync(0xffffffffu, need)) {
           // O may be read here: S(j) completing implies the previous PV is done.
 #pragma unroll 1
@@ -368,7 +370,7 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
           ok = mbar_wait_warp(bar(L::B_O + w), 0, wc);
           if (ok) {
             tc_fence_after();
-            const float inv_l = 1.f / l;
+            const float inv_l = 1.f / lr;
 #pragma unroll 1
             for (int c = 0; c < D; c += 32) {
               uint32_t ov[32];

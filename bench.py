@@ -1,0 +1,433 @@
+"""Benchmark of the exact-attention hot path (forward + backward) on one GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+
+One step = fa_fwd then fa_bwd (its three stages) over one batch of the
+workload, inputs resident in HBM.  `value` is algorithmic TFLOPS (forward
+4 B H N^2 d, backward 2.5x that, halved for causal; block-sparse counts the
+kept blocks), summed over ranks under torchrun (each rank runs the whole
+workload on its own GPU: weak scaling, no collective on the data path).
+L2 is flushed (a 256 MiB write) between timed steps, outside the timed events.
+`e2e` is the same metric through the public binding with pinned host inputs
+copied in and every output copied back inside the timed region.
+`--impl reference` times the fp64 CPU oracle on a bounded sample instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+# BLAS threads for the CPU oracle: every core this process may run on.
+_CORES = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
+for _v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_v, str(_CORES))
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "attention fwd/bwd TFLOPS (bf16, 1×GB300) and % of dense tensor-core peak"
+UNIT = "TFLOPS"
+DEFAULT_WORKLOAD = "fwdbwd_b2h16n4096d128_causal"
+PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f), "measured"
+    except OSError:
+        return PEAKS_FALLBACK, "fallback"
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def _flops(w, density):
+    import oracle
+    f_fwd = oracle.flops(w.B, w.H, w.N, w.d, causal=w.causal, density=density)
+    f_bwd = oracle.flops(w.B, w.H, w.N, w.d, causal=w.causal, backward=True, density=density) if w.backward else 0.0
+    return f_fwd, f_bwd
+
+
+def _density(t):
+    bm = t.get("block_mask")
+    return None if bm is None else float(bm.float().mean())
+
+
+def _config(w, density, extra=None):
+    c = {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": w.causal,
+         "mask": w.mask_kind, "backward": w.backward, "inputs": f"N(0,1)x{w.amplitude:g} seed {w.seed}",
+         "l2": "flushed (256 MiB write) between timed steps", "parallelism": "replica per GPU"}
+    if density is not None:
+        c["block_density"] = round(density, 4)
+    if extra:
+        c.update(extra)
+    return c
+
+
+# --------------------------------------------------------------------------- #
+# clocks during the timed region
+# --------------------------------------------------------------------------- #
+class ClockSampler:
+    FIELDS = ("index,uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid=None):
+        self.uuid = uuid
+        self.proc = None
+        self.file = None
+
+    def start(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-lms", "100"], stdout=self.file, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.file.flush()
+        rows = []
+        with open(self.file.name) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 10:
+                    continue
+                if self.uuid and self.uuid not in parts[1]:
+                    continue
+                try:
+                    rows.append({"sm": float(parts[2]), "max": float(parts[3]), "power": float(parts[4]),
+                                 "hw": parts[6], "hw_thermal": parts[7], "sw_thermal": parts[8], "power_cap": parts[9]})
+                except ValueError:
+                    continue
+        os.unlink(self.file.name)
+        if not rows:
+            return None
+        loaded = [r for r in rows if r["power"] > 200.0] or rows
+        reasons = set()
+        for r in loaded:
+            for key, name in (("hw", "hw_slowdown"), ("hw_thermal", "hw_thermal_slowdown"),
+                              ("sw_thermal", "sw_thermal_slowdown"), ("power_cap", "sw_power_cap")):
+                if r[key].lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r["sm"] for r in loaded), "sm_max_mhz": max(r["max"] for r in rows),
+                "reasons": sorted(reasons), "samples": len(rows), "samples_under_load": len(loaded),
+                "power_w_max": max(r["power"] for r in rows)}
+
+
+# --------------------------------------------------------------------------- #
+# the CPU oracle on a bounded sample
+# --------------------------------------------------------------------------- #
+def _oracle_sample(w, t, budget_s=15.0, max_heads=None):
+    """Time the fp64 oracle (forward + backward) head by head until `budget_s`
+    has passed.  Returns (TFLOPS, seconds, heads)."""
+    import oracle
+    bm = t.get("block_mask")
+    bmn = None if bm is None else bm.numpy()
+    heads = 0
+    flops = 0.0
+    t0 = time.perf_counter()
+    for hh in range(w.B * w.H):
+        b, h = divmod(hh, w.H)
+        sl = (slice(b, b + 1), slice(h, h + 1))
+        q, k, v = (t[n][sl].double().numpy() for n in ("q", "k", "v"))
+        oracle.forward(q, k, v, w.scale, causal=w.causal, block_mask=bmn, row_chunk=2048 if w.N > 8192 else None)
+        if w.backward:
+            oracle.backward(q, k, v, t["do"][sl].double().numpy(), w.scale, causal=w.causal, block_mask=bmn)
+        heads += 1
+        dens = None if bm is None else float(bm.float().mean())
+        ff, fb = _flops(type(w)(**{**w.__dict__, "B": 1, "H": 1}), dens)
+        flops += ff + fb
+        el = time.perf_counter() - t0
+        if el >= budget_s or (max_heads and heads >= max_heads):
+            break
+    el = time.perf_counter() - t0
+    return flops / el / 1e12, el, heads
+
+
+def run_reference(args):
+    ws, rank, _ = _dist()
+    if rank != 0:
+        return 0
+    from attn_fwd_gb300.inputs import WORKLOADS, make_workload_inputs
+    w = WORKLOADS[args.workload]
+    t = make_workload_inputs(w, heads=slice(0, 1)) if w.B * w.H > 1 else make_workload_inputs(w)
+    w1 = type(w)(**{**w.__dict__, "B": 1, "H": 1})
+    for _ in range(args.warmup):
+        _oracle_sample(w1, t, budget_s=0.0, max_heads=1)
+    times = []
+    tf = []
+    for _ in range(args.steps):
+        v, el, _h = _oracle_sample(w1, t, budget_s=0.0, max_heads=1)
+        times.append(el)
+        tf.append(v)
+    total = sum(times)
+    f_fwd, f_bwd = _flops(w1, _density(t))
+    value = (f_fwd + f_bwd) * args.steps / total / 1e12
+    sample = f"one (batch, head) of {w.B * w.H}: head (0, 0), forward + backward, fp64, materialised S and P"
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": total / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
+            "config": _config(w, _density(t), {"sample": sample}),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": _CORES, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# --------------------------------------------------------------------------- #
+# the CUDA path
+# --------------------------------------------------------------------------- #
+def _profile_traffic(kernel_tag, workload):
+    """DRAM traffic per launch from a committed ncu summary, if it was taken on
+    the current source of the kernel (matching source hash); else None."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", f"{kernel_tag}_{workload}.md")
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    h = re.search(r"source_sha256:\s*([0-9a-f]{64})", text)
+    src = re.search(r"source_files:\s*(.+)", text)
+    if not (m and h and src):
+        return None
+    cur = source_sha256(src.group(1).split())
+    return float(m.group(1)) if cur == h.group(1) else None
+
+
+def source_sha256(files):
+    """sha256 over the concatenated bytes of the given repo-relative files."""
+    import hashlib
+    hh = hashlib.sha256()
+    for f in files:
+        try:
+            hh.update(open(os.path.join(ROOT, f), "rb").read())
+        except OSError:
+            return None
+    return hh.hexdigest()
+
+
+def run_cuda(args):
+    import torch
+    import torch.distributed as dist
+
+    ws, rank, local = _dist()
+    if ws > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    import __graft_entry__
+    __graft_entry__.build()
+    import attn_fwd_gb300.fa as fa
+    from attn_fwd_gb300.inputs import WORKLOADS, make_workload_inputs
+
+    w = WORKLOADS[args.workload]
+    t = make_workload_inputs(w)
+    density = _density(t)
+    f_fwd, f_bwd = _flops(w, density)
+    q, k, v = (t[n].to(dev) for n in ("q", "k", "v"))
+    do = t["do"].to(dev) if w.backward else None
+    bm = t["block_mask"].to(dev) if "block_mask" in t else None
+    mask_kind = fa.MASK_BLOCK if bm is not None else (fa.MASK_CAUSAL if w.causal else fa.MASK_NONE)
+    o = torch.empty_like(q)
+    lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev)
+    if w.backward:
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        wsp = fa.workspace(w.B, w.H, w.N, w.d, dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    def fwd():
+        if bm is not None:
+            fa.fa_fwd_blocksparse(q, k, v, o, lse, bm, w.scale)
+        else:
+            fa.fa_fwd(q, k, v, o, lse, w.scale, causal=w.causal)
+
+    def step(ev=None):
+        if ev:
+            ev[0].record()
+        fwd()
+        if ev:
+            ev[1].record()
+        if w.backward:
+            fa.fa_bwd_preprocess(o, do, wsp)
+            if ev:
+                ev[2].record()
+            fa.fa_bwd_main(q, k, v, do, lse, bm, dk, dv, wsp, w.scale, mask_kind)
+            if ev:
+                ev[3].record()
+            fa.fa_bwd_dq_convert(wsp, dq, w.scale)
+            if ev:
+                ev[4].record()
+
+    launches_per_step = 4 if w.backward else 1
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    rc = fa.fa_get_device_error()
+    if rc != 0:
+        raise RuntimeError(f"device status after warm-up: {fa.status_string(rc)}")
+
+    uuid = None
+    try:
+        uuid = str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        pass
+    sampler = ClockSampler(uuid) if rank == 0 else None
+    if sampler:
+        sampler.start()
+    nev = 5 if w.backward else 2
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(nev)] for _ in range(args.steps)]
+    if ws > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    for i in range(args.steps):
+        flush.zero_()
+        step(events[i])
+    torch.cuda.synchronize()
+    if ws > 1:
+        dist.barrier()
+    clocks = sampler.stop() if sampler else None
+    rc = fa.fa_get_device_error()
+    if rc != 0:
+        raise RuntimeError(f"device status after timing: {fa.status_string(rc)}")
+
+    per = {"fwd": [], "bwd_preprocess": [], "bwd_main": [], "bwd_dq_convert": []}
+    step_ms = []
+    for ev in events:
+        step_ms.append(ev[0].elapsed_time(ev[-1]))
+        per["fwd"].append(ev[0].elapsed_time(ev[1]))
+        if w.backward:
+            per["bwd_preprocess"].append(ev[1].elapsed_time(ev[2]))
+            per["bwd_main"].append(ev[2].elapsed_time(ev[3]))
+            per["bwd_dq_convert"].append(ev[3].elapsed_time(ev[4]))
+    total_ms = sum(step_ms)
+    if ws > 1:
+        tt = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        total_ms = float(tt.item())
+    ms_per_step = total_ms / args.steps
+    value = ws * (f_fwd + f_bwd) / (ms_per_step * 1e-3) / 1e12
+
+    # ---- end to end through the public binding, host buffers ------------- #
+    host_in = {n: t[n].pin_memory() for n in (("q", "k", "v", "do") if w.backward else ("q", "k", "v"))}
+    host_out = {"o": torch.empty(q.shape, dtype=q.dtype).pin_memory(),
+                "lse": torch.empty(lse.shape, dtype=lse.dtype).pin_memory()}
+    if w.backward:
+        for n in ("dq", "dk", "dv"):
+            host_out[n] = torch.empty(q.shape, dtype=q.dtype).pin_memory()
+    h2d = sum(x.numel() * x.element_size() for x in host_in.values())
+    d2h = sum(x.numel() * x.element_size() for x in host_out.values())
+    dev_in = {"q": q, "k": k, "v": v}
+    if w.backward:
+        dev_in["do"] = do
+    dev_out = {"o": o, "lse": lse}
+    if w.backward:
+        dev_out.update({"dq": dq, "dk": dk, "dv": dv})
+    e2e_steps = max(3, min(args.steps, 20))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if ws > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    e0.record()
+    for _ in range(e2e_steps):
+        for n, x in host_in.items():
+            dev_in[n].copy_(x, non_blocking=True)
+        step()
+        for n, x in dev_out.items():
+            host_out[n].copy_(x, non_blocking=True)
+    e1.record()
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    if ws > 1:
+        tt = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        e2e_ms = float(tt.item())
+    e2e_value = ws * (f_fwd + f_bwd) / (e2e_ms * 1e-3) / 1e12
+
+    # ---- roofline of the dominant kernel -------------------------------- #
+    peaks, peak_src = _peaks()
+    avg = {kname: (sum(x) / len(x) if x else 0.0) for kname, x in per.items()}
+    algo = {"fwd": f_fwd, "bwd_main": f_bwd}
+    dom = max(("fwd", "bwd_main") if w.backward else ("fwd",), key=lambda n: avg[n])
+    achieved = algo[dom] / (avg[dom] * 1e-3) / 1e12
+    peak = float(peaks["bf16_tflops"])
+    tag = {"fwd": "fa_fwd_kernel", "bwd_main": "fa_bwd_kernel"}[dom]
+    roofline = {"bound": "tensor", "kernel": tag, "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "peak_source": f"{peak_src} bf16 dense (burst)",
+                "traffic": _profile_traffic(tag, w.name),
+                "algorithmic_flops_per_launch": algo[dom]}
+    kernels = {kname: {"ms": avg[kname], "share": avg[kname] / ms_per_step if ms_per_step else 0.0}
+               for kname in avg if per[kname]}
+    kernels["fwd"]["tflops"] = f_fwd / (avg["fwd"] * 1e-3) / 1e12
+    kernels["fwd"]["frac_of_peak"] = kernels["fwd"]["tflops"] / peak
+    if w.backward:
+        kernels["bwd_main"]["tflops"] = f_bwd / (avg["bwd_main"] * 1e-3) / 1e12
+        kernels["bwd_main"]["frac_of_peak"] = kernels["bwd_main"]["tflops"] / peak
+        bwd_ms = avg["bwd_preprocess"] + avg["bwd_main"] + avg["bwd_dq_convert"]
+        kernels["bwd_total"] = {"ms": bwd_ms, "tflops": f_bwd / (bwd_ms * 1e-3) / 1e12,
+                                "frac_of_peak": f_bwd / (bwd_ms * 1e-3) / 1e12 / peak}
+
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": _config(w, density),
+            "frac_of_peak": value / ws / peak,
+            "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "ms_per_step": e2e_ms},
+            "gpu_launches": launches_per_step * args.steps, "roofline": roofline, "kernels": kernels,
+            "clocks": clocks}
+
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        tf, el, heads = _oracle_sample(w, t, budget_s=args.cpu_budget)
+        line["cpu_baseline"] = {"value": tf, "unit": UNIT, "cores": _CORES, "kind": "oracle",
+                                "sample": f"{heads} of {w.B * w.H} (batch, head) pairs, forward"
+                                          f"{' + backward' if w.backward else ''}, fp64, {el:.1f} s"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--impl", choices=("cuda", "reference"), default="cuda")
+    ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle time for cpu_baseline")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_cuda(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())
