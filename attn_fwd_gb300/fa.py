@@ -23,6 +23,7 @@ FA_ERR_ARCH = -3
 FA_ERR_LAUNCH = -4
 FA_ERR_TIMEOUT = -5
 FA_ERR_CUDA = -6
+FA_ERR_SCRATCH = -7
 
 MASK_NONE, MASK_CAUSAL, MASK_BLOCK = 0, 1, 2
 
@@ -41,6 +42,7 @@ _SIGS = {
     "fa_bwd_preprocess": (_i, [_vp, _vp, _vp, _i, _i, _i, _i, _vp]),
     "fa_bwd_main": (_i, [_vp] * 9 + [_i, _i, _i, _i, _f, _i, _vp]),
     "fa_bwd_dq_convert": (_i, [_vp, _vp, _i, _i, _i, _i, _f, _vp]),
+    "fa_bwd_noalloc": (_i, [_vp] * 9 + [_i, _i, _i, _i, _f, _i, _vp]),
     "fa_get_device_error": (_i, [_vp]),
     "fa_set_wait_timeout_ns": (_i, [_u64]),
     "fa_debug_wait_timeout": (_i, [_u64, _vp]),
@@ -180,6 +182,16 @@ def fa_bwd_dq_convert(workspace, dq, scale, stream=None):
     rc = load().fa_bwd_dq_convert(ctypes.c_void_p(workspace.data_ptr()), _bf16(dq, "dq"), B, H, N, d,
                                   float(scale), _stream(stream))
     _check("fa_bwd_dq_convert", rc)
+
+
+def fa_bwd_noalloc(q, k, v, o, do, lse, dq, dk, dv, scale, causal=False, stream=None):
+    """fa_bwd without a workspace argument: the library uses its own static
+    device scratch (see include/fa.h), so this call allocates nothing."""
+    B, H, N, d = q.shape
+    rc = load().fa_bwd_noalloc(_bf16(q, "q"), _bf16(k, "k"), _bf16(v, "v"), _bf16(o, "o"), _bf16(do, "do"),
+                               _f32(lse, "lse"), _bf16(dq, "dq"), _bf16(dk, "dk"), _bf16(dv, "dv"),
+                               B, H, N, d, float(scale), int(bool(causal)), _stream(stream))
+    _check("fa_bwd_noalloc", rc)
 
 
 def fa_get_device_error(stream=None) -> int:

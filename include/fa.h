@@ -75,7 +75,8 @@ typedef enum fa_status {
   FA_ERR_ARCH = -3,        /* current device is not compute capability 10.3 */
   FA_ERR_LAUNCH = -4,      /* the CUDA runtime refused a launch or attribute call */
   FA_ERR_TIMEOUT = -5,     /* a kernel wait ran past the wait timeout (device status) */
-  FA_ERR_CUDA = -6         /* another CUDA runtime error (device query, descriptor) */
+  FA_ERR_CUDA = -6,        /* another CUDA runtime error (device query, descriptor) */
+  FA_ERR_SCRATCH = -7      /* fa_bwd_noalloc: the problem needs more than its static scratch */
 } fa_status;
 
 /* Library version, major * 10000 + minor * 100 + patch. */
@@ -146,6 +147,43 @@ FA_API int fa_bwd_main(const void *q, const void *k, const void *v, const void *
 /* Backward stage 3 of 3: dQ = bf16(scale * accumulator). */
 FA_API int fa_bwd_dq_convert(const void *workspace, void *dq, int B, int H, int N, int d,
                       float scale, fa_stream_t stream);
+
+/*
+ * Size of the device scratch array behind fa_bwd_noalloc: 64 MiB per device.
+ * fa_bwd_noalloc accepts a problem when fa_bwd_workspace_bytes(B, H, N, d) is
+ * at most this, e.g. B * H * N * d up to about 16.6 million elements.
+ */
+#define FA_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
+
+/*
+ * Backward that allocates nothing: the same computation and arguments as
+ * fa_bwd, minus `workspace`.  (The attention pages have no counterpart to
+ * this entry point; it exists for callers, not for the method.)
+ *
+ * Who needs it: callers that cannot call cudaMalloc on the compute path,
+ * for example a serving process whose memory pool has reserved the device
+ * up front, or a plugin inside a host framework that owns the allocator and
+ * forbids side allocations.  They still pass every input and output buffer;
+ * only the fp32 dQ accumulator and the D vector move into a file-scope
+ * device array of FA_NOALLOC_SCRATCH_BYTES inside libfa.so, which every GPU
+ * that loads the library holds until the process exits.
+ *
+ * Behaviour:
+ *   - Returns FA_ERR_SCRATCH, without enqueuing anything, when
+ *     fa_bwd_workspace_bytes(B, H, N, d) exceeds FA_NOALLOC_SCRATCH_BYTES;
+ *     the other argument checks are those of fa_bwd.
+ *   - The first call on each device looks up the device address of the
+ *     array (cudaGetSymbolAddress, with that device current).  Make that
+ *     first call before any stream capture on that device.
+ *   - Calls no cudaMalloc, cudaFree or other allocating routine.
+ *   - Every call on a device shares the one array and leaves its last
+ *     contents there; the first stage zeroes the dQ accumulator on every
+ *     call.  Calls whose work overlaps on the GPU (other streams, other
+ *     threads) race on the array: serialise them.
+ */
+FA_API int fa_bwd_noalloc(const void *q, const void *k, const void *v, const void *o,
+                          const void *dout, const float *lse, void *dq, void *dk, void *dv,
+                          int B, int H, int N, int d, float scale, int causal, fa_stream_t stream);
 
 /*
  * Synchronises `stream`, then returns and clears the current device's status
