@@ -53,6 +53,23 @@ def _dist():
     return ws, rank, local
 
 
+def max_over_ranks(x: float, device) -> float:
+    """The largest value of x over all ranks (the job's time is its slowest rank's)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tflops(world_size: int, flops_per_rank_step: float, ms_per_step: float) -> float:
+    """Weak scaling: every rank runs the whole workload, so the job does
+    world_size times the work of one rank in the slowest rank's time."""
+    return world_size * flops_per_rank_step / (ms_per_step * 1e-3) / 1e12
+
+
 def _flops(w, density):
     import oracle
     f_fwd = oracle.flops(w.B, w.H, w.N, w.d, causal=w.causal, density=density)
@@ -324,13 +341,9 @@ def run_cuda(args):
             per["bwd_preprocess"].append(ev[1].elapsed_time(ev[2]))
             per["bwd_main"].append(ev[2].elapsed_time(ev[3]))
             per["bwd_dq_convert"].append(ev[3].elapsed_time(ev[4]))
-    total_ms = sum(step_ms)
-    if ws > 1:
-        tt = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        total_ms = float(tt.item())
+    total_ms = max_over_ranks(sum(step_ms), dev)
     ms_per_step = total_ms / args.steps
-    value = ws * (f_fwd + f_bwd) / (ms_per_step * 1e-3) / 1e12
+    value = whole_job_tflops(ws, f_fwd + f_bwd, ms_per_step)
 
     # ---- end to end through the public binding, host buffers ------------- #
     host_in = {n: t[n].pin_memory() for n in (("q", "k", "v", "do") if w.backward else ("q", "k", "v"))}
@@ -361,12 +374,8 @@ def run_cuda(args):
             host_out[n].copy_(x, non_blocking=True)
     e1.record()
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / e2e_steps
-    if ws > 1:
-        tt = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        e2e_ms = float(tt.item())
-    e2e_value = ws * (f_fwd + f_bwd) / (e2e_ms * 1e-3) / 1e12
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, dev)
+    e2e_value = whole_job_tflops(ws, f_fwd + f_bwd, e2e_ms)
 
     # ---- roofline of the dominant kernel -------------------------------- #
     peaks, peak_src = _peaks()
