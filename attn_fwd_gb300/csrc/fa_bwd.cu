@@ -25,9 +25,11 @@
 // The d=128 form keeps the head-dim index on the lanes, so each warp's fp32
 // reduction covers 32 consecutive floats of one dQ row (128-byte coalesced).
 //
-// Warp roles (10 warps): 0-3 recompute P and dS (thread = key row), write
-// P^T and dS^T (bf16, 128-byte swizzle) to shared memory; 4-7 drain dQ from
-// tensor memory into the fp32 accumulator; 8 issues MMAs; 9 loads K_j, V_j
+// Warp roles (14 warps): 0-7 recompute P and dS (thread = key row; warps
+// 0-3 take the first half of the step's query columns, 4-7 the second half,
+// so two warps per SM sub-partition share the CUDA-core work) and write P^T
+// and dS^T (bf16, 128-byte swizzle) to shared memory; 8-11 drain dQ from
+// tensor memory into the fp32 accumulator; 12 issues MMAs; 13 loads K_j, V_j
 // once and Q_i, dO_i, LSE_i, D_i per step into a two-stage ring.
 #include "fa_common.cuh"
 #include "fa_ptx.cuh"
@@ -43,7 +45,7 @@ struct BwdLayout {
   static constexpr int KV_BYTES = NCH * KV_CHUNK;           // 128 x D bf16
   static constexpr int Q_CHUNK = BQ * 128;                  // [BQ rows][128 B]
   static constexpr int Q_BYTES = NCH * Q_CHUNK;             // BQ x D bf16
-  static constexpr int STAGES = 2;
+  static constexpr int STAGES = 3;                          // Q_i/dO_i ring: loads run two steps ahead
   static constexpr int ST_Q = 0;
   static constexpr int ST_DO = Q_BYTES;
   static constexpr int ST_LSE = 2 * Q_BYTES;
@@ -51,7 +53,7 @@ struct BwdLayout {
   static constexpr int STAGE_BYTES = ((2 * Q_BYTES + 2 * BQ * 4) + 1023) / 1024 * 1024;
   static constexpr int PT_CHUNK = TILE * 128;               // [128 key rows][64 queries]
   static constexpr int PT_BYTES = (BQ / 64) * PT_CHUNK;     // 128 x BQ bf16
-  static constexpr int PBUFS = (D == 128) ? 2 : 1;          // P^T / dS^T buffers
+  static constexpr int PBUFS = 1;                           // P^T / dS^T buffers
   static constexpr int K_OFF = 0;
   static constexpr int V_OFF = KV_BYTES;
   static constexpr int RING_OFF = 2 * KV_BYTES;
@@ -62,11 +64,11 @@ struct BwdLayout {
   static constexpr int B_FULL = 1;                       // STAGES
   static constexpr int B_EMPTY = B_FULL + STAGES;        // STAGES
   static constexpr int B_SDP = B_EMPTY + STAGES;         // S^T and dP^T of a step in tensor memory
-  static constexpr int B_SDP_FREE = B_SDP + 1;           // ... and read out (128 arrivals)
-  static constexpr int B_DS = B_SDP_FREE + 1;            // PBUFS: P^T, dS^T written (128 arrivals)
+  static constexpr int B_SDP_FREE = B_SDP + 1;           // ... and read out (one arrival per warp)
+  static constexpr int B_DS = B_SDP_FREE + 1;            // PBUFS: P^T, dS^T written (one arrival per warp)
   static constexpr int B_PFREE = B_DS + PBUFS;           // PBUFS: MMAs done reading a buffer
   static constexpr int B_DQ = B_PFREE + PBUFS;           // dQ of a step in tensor memory
-  static constexpr int B_DQ_FREE = B_DQ + 1;             // ... and read out (128 arrivals)
+  static constexpr int B_DQ_FREE = B_DQ + 1;             // ... and read out (one arrival per warp)
   static constexpr int B_DONE = B_DQ_FREE + 1;
   static constexpr int NBARS = B_DONE + 1;
   static constexpr int SMEM_BYTES = BAR_OFF + NBARS * 8 + 16 + 1024;
@@ -76,7 +78,11 @@ struct BwdLayout {
   static constexpr uint32_t COL_DQ = 2 * BQ;
   static constexpr uint32_t COL_DV = (D == 128) ? 256 : 320;
   static constexpr uint32_t COL_DK = 384;
-  static constexpr int THREADS = 320;
+  static constexpr int THREADS = 448;
+  static constexpr int W_DRAIN = 8;      // first drain warp
+  static constexpr int W_MMA = 12;
+  static constexpr int W_TMA = 13;
+  static constexpr int RECOMPUTE_WARPS = 8;
 };
 
 __device__ __forceinline__ bool bwd_visible(const BwdParams& p, int qi, int bq, int kt) {
@@ -94,7 +100,7 @@ __device__ __forceinline__ void mbar_drain_b(uint32_t bar, uint32_t parity, uint
 }
 
 template <int D>
-__global__ void __launch_bounds__(320, 1) fa_bwd_kernel(const __grid_constant__ BwdParams p) {
+__global__ void __launch_bounds__(448, 1) fa_bwd_kernel(const __grid_constant__ BwdParams p) {
   using L = BwdLayout<D>;
   constexpr int BQ = L::BQ;
   extern __shared__ uint8_t smem_raw[];
@@ -107,8 +113,15 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_kernel(const __grid_constant__ 
 
   const uint32_t warp = warp_id();
   const uint32_t lane = lane_id();
-  const int bh = blockIdx.x % p.BH;
-  const int kt = blockIdx.x / p.BH;        // causal: small key tiles have the most query tiles, start them first
+  // CTA order: bands of up to 8 heads; within a band key tile outer, head
+  // inner.  A band's Q, dO and dQ accumulator stay L2-resident while its key
+  // tiles run, and causal key tiles with the most query tiles start first.
+  const int band_heads = p.BH < 8 ? p.BH : 8;
+  const int band = blockIdx.x / (band_heads * p.n_kt);
+  const int in_band = blockIdx.x % (band_heads * p.n_kt);
+  const int heads_here = min(band_heads, p.BH - band * band_heads);
+  const int kt = in_band / heads_here;
+  const int bh = band * band_heads + in_band % heads_here;
   const int n_qi = p.N / BQ;
   const int qi_begin = (p.mask_kind == MASK_CAUSAL) ? (kt * TILE) / BQ : 0;
 
@@ -119,18 +132,18 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_kernel(const __grid_constant__ 
       mbar_init(bar(L::B_EMPTY + s), 1);
     }
     mbar_init(bar(L::B_SDP), 1);
-    mbar_init(bar(L::B_SDP_FREE), 128);
+    mbar_init(bar(L::B_SDP_FREE), L::RECOMPUTE_WARPS);   // one arrival per warp
     for (int b = 0; b < L::PBUFS; ++b) {
-      mbar_init(bar(L::B_DS + b), 128);
+      mbar_init(bar(L::B_DS + b), L::RECOMPUTE_WARPS);
       mbar_init(bar(L::B_PFREE + b), 1);
     }
     mbar_init(bar(L::B_DQ), 1);
-    mbar_init(bar(L::B_DQ_FREE), 128);
+    mbar_init(bar(L::B_DQ_FREE), 4);
     mbar_init(bar(L::B_DONE), 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 8) {
+  if (warp == L::W_MMA) {
     tmem_alloc(smem_u32(tmem_slot), L::TMEM_COLS);
     tmem_relinquish();
   }
@@ -143,7 +156,7 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_kernel(const __grid_constant__ 
   int n_steps = 0;
   for (int qi = qi_begin; qi < n_qi; ++qi) n_steps += bwd_visible(p, qi, BQ, kt);
 
-  if (warp == 9) {
+  if (warp == L::W_TMA) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       prefetch_tmap(&p.tm_q);
@@ -187,7 +200,7 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_kernel(const __grid_constant__ 
           if (issued[s]) mbar_drain_b(bar(L::B_FULL + s), (issued[s] - 1) & 1u, 100000000ull);
       }
     }
-  } else if (warp == 8) {
+  } else if (warp == L::W_MMA) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0 && n_steps > 0) {
       constexpr uint32_t ID_S = idesc_bf16(128, BQ, false, false);     // S^T, dP^T
@@ -252,6 +265,7 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_kernel(const __grid_constant__ 
           mma_ss(tmem + L::COL_DK, sdesc_sw128(dst + ao, 16, 1024),
                  sdesc_sw128(sb + L::ST_Q + k * 2048, L::Q_CHUNK, 1024), ID_G, (i > 0 || k > 0) ? 1u : 0u);
         }
+        mma_commit(bar(L::B_EMPTY + st));     // Q_i, dO_i are no longer needed after dV, dK
         // dQ for this step, once the drain warps have read the previous one
         if (i > 0) {
           if (!(ok = mbar_wait(bar(L::B_DQ_FREE), (i - 1) & 1, wc))) break;
@@ -272,20 +286,21 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_kernel(const __grid_constant__ 
           }
         }
         mma_commit(bar(L::B_DQ));
-        mma_commit(bar(L::B_EMPTY + st));
         mma_commit(bar(L::B_PFREE + b));
       }
       mma_commit(bar(L::B_DONE));
       mbar_drain_b(bar(L::B_DONE), 0, 1000000000ull);
     }
     __syncwarp();
-  } else if (warp < 4) {
+  } else if (warp < L::W_DRAIN) {
     // ------------------------------------------------- recompute P and dS
-    const uint32_t quarter = warp;
+    const uint32_t quarter = warp & 3u;
+    const int half = static_cast<int>(warp >> 2);           // which half of the query columns
     const int r = static_cast<int>(quarter * 32 + lane);    // key row in the tile == lane
     const int key = kt * TILE + r;
     const uint32_t lane_base = quarter * 32;
-    const float sl2 = p.scale_log2;
+    const float2 sl2v = make_float2(p.scale_log2, p.scale_log2);
+    constexpr float LOG2E = 1.4426950408889634f;
     bool ok = true;
     int i = 0;
     for (int qi = qi_begin; qi < n_qi && ok; ++qi) {
@@ -294,68 +309,77 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_kernel(const __grid_constant__ 
       const int b = i % L::PBUFS;
       if (!(ok = mbar_wait_warp(bar(L::B_SDP), i & 1, wc))) break;
       tc_fence_after();
-      if (i >= L::PBUFS) {
-        if (!(ok = mbar_wait_warp(bar(L::B_PFREE + b), ((i / L::PBUFS) - 1) & 1, wc))) break;
-      }
       const uint8_t* stage = smem + L::RING_OFF + st * L::STAGE_BYTES;
       const float* lse = reinterpret_cast<const float*>(stage + L::ST_LSE);
-      const float* dv = reinterpret_cast<const float*>(stage + L::ST_DV);
+      const float* dvec = reinterpret_cast<const float*>(stage + L::ST_DV);
       uint8_t* pt = smem + L::PT_OFF + (2 * b) * L::PT_BYTES;
       uint8_t* dsT = pt + L::PT_BYTES;
       const bool diag = (p.mask_kind == MASK_CAUSAL) && (qi * BQ < kt * TILE + TILE);
+      constexpr int COLS = BQ / 2;                           // query columns of this warp
 #pragma unroll 1
-      for (int h = 0; h < BQ / 64; ++h) {
-        uint32_t sr[64], dr[64];
-        tmem_ld_x64(tmem_addr(tmem, lane_base, L::COL_S + h * 64), sr);
-        tmem_ld_x64(tmem_addr(tmem, lane_base, L::COL_DP + h * 64), dr);
-        if (h == BQ / 64 - 1) {
+      for (int c0 = half * COLS; c0 < (half + 1) * COLS; c0 += 32) {
+        uint32_t sr[32], dr[32];
+        tmem_ld_x32(tmem_addr(tmem, lane_base, L::COL_S + c0), sr);
+        tmem_ld_x32(tmem_addr(tmem, lane_base, L::COL_DP + c0), dr);
+        if (c0 + 32 == (half + 1) * COLS) {                  // this warp's last read of S^T, dP^T
           tc_fence_before();
-          mbar_arrive(bar(L::B_SDP_FREE));
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(L::B_SDP_FREE));
         }
-        uint8_t* prow = pt + h * L::PT_CHUNK + r * 128;
-        uint8_t* drow = dsT + h * L::PT_CHUNK + r * 128;
+        if (c0 == half * COLS && i >= L::PBUFS) {
+          // the MMAs of the step that last used this P^T / dS^T buffer must be done
+          if (!(ok = mbar_wait_warp(bar(L::B_PFREE + b), ((i / L::PBUFS) - 1) & 1, wc))) break;
+        }
+        uint8_t* prow = pt + (c0 >> 6) * L::PT_CHUNK + r * 128;
+        uint8_t* drow = dsT + (c0 >> 6) * L::PT_CHUNK + r * 128;
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {            // 8 queries per 16-byte chunk
+        for (int j = 0; j < 4; ++j) {                        // 8 queries per 16-byte chunk
+          const int cq = c0 + 8 * j;                         // first query column of the chunk
+          const float4 l0 = *reinterpret_cast<const float4*>(lse + cq);
+          const float4 l1 = *reinterpret_cast<const float4*>(lse + cq + 4);
+          const float4 d0 = *reinterpret_cast<const float4*>(dvec + cq);
+          const float4 d1 = *reinterpret_cast<const float4*>(dvec + cq + 4);
+          const float2 nl[4] = {make_float2(-l0.x * LOG2E, -l0.y * LOG2E), make_float2(-l0.z * LOG2E, -l0.w * LOG2E),
+                                make_float2(-l1.x * LOG2E, -l1.y * LOG2E), make_float2(-l1.z * LOG2E, -l1.w * LOG2E)};
+          const float2 nd[4] = {make_float2(-d0.x, -d0.y), make_float2(-d0.z, -d0.w), make_float2(-d1.x, -d1.y),
+                                make_float2(-d1.z, -d1.w)};
           uint32_t pp[4], dd[4];
 #pragma unroll
-          for (int e = 0; e < 8; e += 2) {
-            const int c = h * 64 + j * 8 + e;
-            const float4 l4 = *reinterpret_cast<const float4*>(lse + (c & ~3));
-            const float4 d4 = *reinterpret_cast<const float4*>(dv + (c & ~3));
-            const float la = (c & 3) == 0 ? l4.x : l4.z;
-            const float lb = (c & 3) == 0 ? l4.y : l4.w;
-            const float da = (c & 3) == 0 ? d4.x : d4.z;
-            const float db = (c & 3) == 0 ? d4.y : d4.w;
-            float p0 = ex2_approx(fmaf(__uint_as_float(sr[j * 8 + e]), sl2, -la * 1.4426950408889634f));
-            float p1 = ex2_approx(fmaf(__uint_as_float(sr[j * 8 + e + 1]), sl2, -lb * 1.4426950408889634f));
+          for (int e = 0; e < 4; ++e) {
+            const int k = 8 * j + 2 * e;                     // register index within the 32 columns
+            const float2 x = ffma2(make_float2(__uint_as_float(sr[k]), __uint_as_float(sr[k + 1])), sl2v, nl[e]);
+            float2 pv = make_float2(ex2_approx(x.x), ex2_approx(x.y));
             if (diag) {
-              const int q0 = qi * BQ + c;
-              if (q0 < key) p0 = 0.f;
-              if (q0 + 1 < key) p1 = 0.f;
+              const int q0 = qi * BQ + cq + 2 * e;
+              if (q0 < key) pv.x = 0.f;
+              if (q0 + 1 < key) pv.y = 0.f;
             }
-            const float ds0 = p0 * (__uint_as_float(dr[j * 8 + e]) - da);
-            const float ds1 = p1 * (__uint_as_float(dr[j * 8 + e + 1]) - db);
-            pp[e / 2] = pack_bf16x2(p0, p1);
-            dd[e / 2] = pack_bf16x2(ds0, ds1);
+            const float2 ds =
+                fmul2(pv, fadd2(make_float2(__uint_as_float(dr[k]), __uint_as_float(dr[k + 1])), nd[e]));
+            pp[e] = pack_bf16x2(pv.x, pv.y);
+            dd[e] = pack_bf16x2(ds.x, ds.y);
           }
-          const int sw = (j ^ (r & 7)) << 4;       // 128-byte swizzle of the 16-byte chunk
+          const int sw = ((((c0 & 63) >> 3) + j) ^ (r & 7)) << 4;   // 128-byte swizzle of the 16-byte chunk
           *reinterpret_cast<uint4*>(prow + sw) = make_uint4(pp[0], pp[1], pp[2], pp[3]);
           *reinterpret_cast<uint4*>(drow + sw) = make_uint4(dd[0], dd[1], dd[2], dd[3]);
         }
       }
+      if (!ok) break;
       fence_proxy_async_smem();
-      mbar_arrive(bar(L::B_DS + b));
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(L::B_DS + b));
       ++i;
     }
-    // ------------------------------------------------- epilogue: dV rows
+    // ------------------------------------------------- epilogue: dV rows, half the columns each
     if (ok) {
-      __nv_bfloat16* out = p.dv + (static_cast<size_t>(bh) * p.N + static_cast<size_t>(kt) * TILE + r) * D;
+      constexpr int DC = D / 2;
+      __nv_bfloat16* out = p.dv + (static_cast<size_t>(bh) * p.N + static_cast<size_t>(kt) * TILE + r) * D + half * DC;
       if (n_steps > 0 && mbar_wait_warp(bar(L::B_DONE), 0, wc)) {
         tc_fence_after();
 #pragma unroll 1
-        for (int c = 0; c < D; c += 32) {
+        for (int c = 0; c < DC; c += 32) {
           uint32_t v[32];
-          tmem_ld_x32(tmem_addr(tmem, lane_base, L::COL_DV + c), v);
+          tmem_ld_x32(tmem_addr(tmem, lane_base, L::COL_DV + half * DC + c), v);
           uint4 o4[4];
           uint32_t* ow = reinterpret_cast<uint32_t*>(o4);
 #pragma unroll
@@ -367,7 +391,7 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_kernel(const __grid_constant__ 
       } else if (n_steps == 0) {
         uint4* dst = reinterpret_cast<uint4*>(out);
 #pragma unroll
-        for (int e = 0; e < D / 8; ++e) dst[e] = make_uint4(0, 0, 0, 0);
+        for (int e = 0; e < DC / 8; ++e) dst[e] = make_uint4(0, 0, 0, 0);
       }
     }
   } else {
@@ -384,7 +408,8 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_kernel(const __grid_constant__ 
       uint32_t v[64];
       tmem_ld_x64(tmem_addr(tmem, lane_base, L::COL_DQ), v);
       tc_fence_before();
-      mbar_arrive(bar(L::B_DQ_FREE));
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(L::B_DQ_FREE));
       const size_t row0 = static_cast<size_t>(bh) * p.N + static_cast<size_t>(qi) * BQ;
       if constexpr (L::DQ_T) {
         // lane t holds head-dim column t of dQ for the BQ = 64 queries of the step
@@ -429,7 +454,7 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_kernel(const __grid_constant__ 
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 8) {
+  if (warp == L::W_MMA) {
     tc_fence_after();
     tmem_dealloc(tmem, L::TMEM_COLS);
   }

@@ -111,7 +111,7 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
     }
     for (int w = 0; w < 2; ++w) {
       mbar_init(bar(L::B_S + w), 1);
-      mbar_init(bar(L::B_P + w), 128);
+      mbar_init(bar(L::B_P + w), 4);      // the four warps of softmax group w
       mbar_init(bar(L::B_O + w), 1);
     }
     mbar_init(bar(L::B_DONE), 1);
@@ -303,40 +303,52 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
           for (int c = 0; c < 128; ++c)
             if (c > row) s[c] = -INFINITY;
         }
+        // row max: 3-input max over four independent chains
         float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
 #pragma unroll
-        for (int c = 4; c < 128; c += 4) {
-          mx0 = fmaxf(mx0, s[c]);
-          mx1 = fmaxf(mx1, s[c + 1]);
-          mx2 = fmaxf(mx2, s[c + 2]);
-          mx3 = fmaxf(mx3, s[c + 3]);
+        for (int c = 4; c < 124; c += 8) {
+          mx0 = fmax3(mx0, s[c], s[c + 1]);
+          mx1 = fmax3(mx1, s[c + 2], s[c + 3]);
+          mx2 = fmax3(mx2, s[c + 4], s[c + 5]);
+          mx3 = fmax3(mx3, s[c + 6], s[c + 7]);
         }
-        const float m_tile = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
+        mx0 = fmax3(mx0, s[124], s[125]);
+        mx1 = fmax3(mx1, s[126], s[127]);
+        const float m_tile = fmax3(mx0, mx1, fmaxf(mx2, mx3)) * sl2;
         const bool need = m_tile > m + RESCALE_THRESHOLD;   // always true on the first tile
         float alpha = 1.f;
         if (need) {
           alpha = ex2_approx(m - m_tile);                  // 0 when m = -inf
           m = m_tile;
         }
-        float sum0 = 0.f, sum1 = 0.f, sum2 = 0.f, sum3 = 0.f;
-        uint32_t pk[64];
+        // P = exp2(S * scale * log2e - m), two columns per packed FMA; the
+        // bf16 pairs go to tensor memory 32 columns at a time while the next
+        // 32 are computed.  l sums the fp32 values (for LSE); lr sums the
+        // bf16-rounded values that P V multiplies, so O / lr weighs the V rows
+        // with weights summing to exactly one.
+        const float2 sl2v = make_float2(sl2, sl2);
+        const float2 negm = make_float2(-m, -m);
+        float2 la = make_float2(0.f, 0.f), lb = la, ra = la, rb = la;
 #pragma unroll
-        for (int c = 0; c < 64; c += 2) {
-          const float p0 = ex2_approx(fmaf(s[2 * c + 0], sl2, -m));
-          const float p1 = ex2_approx(fmaf(s[2 * c + 1], sl2, -m));
-          const float p2 = ex2_approx(fmaf(s[2 * c + 2], sl2, -m));
-          const float p3 = ex2_approx(fmaf(s[2 * c + 3], sl2, -m));
-          pk[c] = pack_bf16x2(p0, p1);
-          pk[c + 1] = pack_bf16x2(p2, p3);
-          // lr sums the bf16 values that P V multiplies, so O / lr weighs the
-          // V rows with weights summing to exactly one; l (unrounded) gives LSE.
-          sum0 += p0 + p1;
-          sum1 += p2 + p3;
-          sum2 += __uint_as_float(pk[c] << 16) + __uint_as_float(pk[c] & 0xffff0000u);
-          sum3 += __uint_as_float(pk[c + 1] << 16) + __uint_as_float(pk[c + 1] & 0xffff0000u);
+        for (int q = 0; q < 4; ++q) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const float2 x = ffma2(make_float2(s[32 * q + 2 * e], s[32 * q + 2 * e + 1]), sl2v, negm);
+            const float2 pv = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+            pk[e] = pack_bf16x2(pv.x, pv.y);
+            if (e & 1) {
+              lb = fadd2(lb, pv);
+              add_bf16x2_to_f32(rb, pk[e]);
+            } else {
+              la = fadd2(la, pv);
+              add_bf16x2_to_f32(ra, pk[e]);
+            }
+          }
+          tmem_st_x16_async(s_addr + 16 * q, pk);
         }
-        l = l * alpha + (sum0 + sum1);
-        lr = lr * alpha + (sum2 + sum3);
+        l = l * alpha + ((la.x + la.y) + (lb.x + lb.y));
+        lr = lr * alpha + ((ra.x + ra.y) + (rb.x + rb.y));
         if (has_o && __any_sync(0xffffffffu, need)) {
           // O may be read here: S(j) completing implies the previous PV is done.
 #pragma unroll 1
@@ -348,18 +360,10 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
             tmem_st_x32(o_addr + c, ov);
           }
         }
-        {
-          uint32_t h0[32], h1[32];
-#pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            h0[i] = pk[i];
-            h1[i] = pk[32 + i];
-          }
-          tmem_st_x32(s_addr, h0);
-          tmem_st_x32(s_addr + 32, h1);
-        }
+        tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(bar(L::B_P + w));
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(L::B_P + w));   // one arrival per warp
         has_o = true;
       }
       // ---------------------------------------------------------- epilogue
