@@ -18,8 +18,9 @@
 // tensor-memory lane, i.e. one softmax thread per key:
 //   S^T  = K_j Q_i^T          (M=128 keys, N=BQ, K=d)   A,B K-major
 //   dP^T = V_j dO_i^T         (M=128, N=BQ, K=d)        A,B K-major
-//   dV  += P^T dO_i           (M=128, N=d, K=BQ)        A = P^T (smem), B MN-major
-//   dK  += dS^T Q_i           (M=128, N=d, K=BQ)        A = dS^T (smem), B MN-major
+//   dV  += P^T dO_i           (M=128, N=d, K=BQ)        A = P^T, B MN-major
+//   dK  += dS^T Q_i           (M=128, N=d, K=BQ)        A = dS^T, B MN-major
+// (A of dV and dK from tensor memory at d=128, from shared memory at d=64)
 //   d=128: dQ^T = K_j^T dS^T  (M=d=128, N=BQ=64, K=128) A,B MN-major
 //   d=64:  dQ   = dS K_j      (M=BQ=128, N=d, K=128)    A,B MN-major
 // The d=128 form keeps the head-dim index on the lanes, so each warp's fp32
@@ -77,7 +78,15 @@ struct BwdLayout {
   static constexpr uint32_t COL_DP = BQ;
   static constexpr uint32_t COL_DQ = 2 * BQ;
   static constexpr uint32_t COL_DV = (D == 128) ? 256 : 320;
-  static constexpr uint32_t COL_DK = 384;
+  static constexpr uint32_t COL_DK = 384;     // dK [384, 384 + d)
+  // d=128: P^T and dS^T (bf16 pairs, 32 columns each) also go to tensor
+  // memory, so dV and dK read their A operand from there (TS form) instead of
+  // shared memory.  Map at d=128: S^T [0,64) dP^T [64,128) dQ^T [128,192)
+  // P^T [192,224) dS^T [224,256) dV [256,384) dK [384,512).  d=64 has no room
+  // left (S^T and dP^T take 128 columns each).
+  static constexpr bool P_TMEM = (D == 128);
+  static constexpr uint32_t COL_PT = 192;     // free columns between dQ^T [128,192) and dV [256,384)
+  static constexpr uint32_t COL_DST = 224;
   static constexpr int THREADS = 448;
   static constexpr int W_DRAIN = 8;      // first drain warp
   static constexpr int W_MMA = 12;
@@ -133,10 +142,8 @@ __global__ void __launch_bounds__(448, 1) fa_bwd_kernel(const __grid_constant__ 
     }
     mbar_init(bar(L::B_SDP), 1);
     mbar_init(bar(L::B_SDP_FREE), L::RECOMPUTE_WARPS);   // one arrival per warp
-    for (int b = 0; b < L::PBUFS; ++b) {
-      mbar_init(bar(L::B_DS + b), L::RECOMPUTE_WARPS);
-      mbar_init(bar(L::B_PFREE + b), 1);
-    }
+    mbar_init(bar(L::B_DS), L::RECOMPUTE_WARPS);
+    mbar_init(bar(L::B_PFREE), 1);
     mbar_init(bar(L::B_DQ), 1);
     mbar_init(bar(L::B_DQ_FREE), 4);
     mbar_init(bar(L::B_DONE), 1);
@@ -202,35 +209,47 @@ __global__ void __launch_bounds__(448, 1) fa_bwd_kernel(const __grid_constant__ 
     }
   } else if (warp == L::W_MMA) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0 && n_steps > 0) {
+    // Warp-uniform schedule; one elected lane issues each tcgen05 instruction.
+    // Descriptors are a base plus a compile-time offset (16-byte units).
+    if (n_steps > 0) {
       constexpr uint32_t ID_S = idesc_bf16(128, BQ, false, false);     // S^T, dP^T
       constexpr uint32_t ID_G = idesc_bf16(128, D, false, true);       // dV, dK
       constexpr uint32_t ID_Q = L::DQ_T ? idesc_bf16(128, BQ, true, true) : idesc_bf16(128, D, true, true);
-      const uint32_t kA = sbase + L::K_OFF, vA = sbase + L::V_OFF;
-      bool ok = mbar_wait(bar(L::B_KV), 0, wc);
+      constexpr uint32_t STAGE16 = L::STAGE_BYTES >> 4;
+      const uint64_t dK_kmaj = sdesc_sw128(sbase + L::K_OFF, 16, 1024);             // K as A of S^T
+      const uint64_t dV_kmaj = sdesc_sw128(sbase + L::V_OFF, 16, 1024);             // V as A of dP^T
+      const uint64_t dK_mn = sdesc_sw128(sbase + L::K_OFF, L::KV_CHUNK, 1024);      // K^T (d=128) / K (d=64), MN-major
+      const uint64_t dQ_kmaj = sdesc_sw128(sbase + L::RING_OFF + L::ST_Q, 16, 1024);    // stage 0 Q, K-major
+      const uint64_t dO_kmaj = sdesc_sw128(sbase + L::RING_OFF + L::ST_DO, 16, 1024);   // stage 0 dO, K-major
+      const uint64_t dQ_mn = sdesc_sw128(sbase + L::RING_OFF + L::ST_Q, L::Q_CHUNK, 1024);   // stage 0 Q, MN-major
+      const uint64_t dO_mn = sdesc_sw128(sbase + L::RING_OFF + L::ST_DO, L::Q_CHUNK, 1024);  // stage 0 dO, MN-major
+      const uint32_t pt = sbase + L::PT_OFF;                                         // single P^T / dS^T buffer
+      const uint64_t dPT_kmaj = sdesc_sw128(pt, 16, 1024);
+      const uint64_t dDS_kmaj = sdesc_sw128(pt + L::PT_BYTES, 16, 1024);
+      const uint64_t dDS_mn = sdesc_sw128(pt + L::PT_BYTES, L::PT_CHUNK, 1024);
+      static_assert(L::PBUFS == 1, "one P^T / dS^T buffer");
+      bool ok = mbar_wait_warp(bar(L::B_KV), 0, wc);
 
       // S^T = K Q_i^T and dP^T = V dO_i^T for the step held in ring stage st
       auto issue_sdp = [&](int st) {
-        const uint32_t sb = sbase + L::RING_OFF + st * L::STAGE_BYTES;
+        const uint64_t so = static_cast<uint64_t>(st) * STAGE16;
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
-          const uint32_t ao = (k >> 2) * L::KV_CHUNK + (k & 3) * 32;
-          const uint32_t bo = (k >> 2) * L::Q_CHUNK + (k & 3) * 32;
-          mma_ss(tmem + L::COL_S, sdesc_sw128(kA + ao, 16, 1024), sdesc_sw128(sb + L::ST_Q + bo, 16, 1024), ID_S,
-                 k > 0 ? 1u : 0u);
+          const uint32_t ao = ((k >> 2) * L::KV_CHUNK + (k & 3) * 32) >> 4;
+          const uint32_t bo = ((k >> 2) * L::Q_CHUNK + (k & 3) * 32) >> 4;
+          mma_ss_elect(tmem + L::COL_S, dK_kmaj + ao, dQ_kmaj + so + bo, ID_S, k > 0 ? 1u : 0u);
         }
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
-          const uint32_t ao = (k >> 2) * L::KV_CHUNK + (k & 3) * 32;
-          const uint32_t bo = (k >> 2) * L::Q_CHUNK + (k & 3) * 32;
-          mma_ss(tmem + L::COL_DP, sdesc_sw128(vA + ao, 16, 1024), sdesc_sw128(sb + L::ST_DO + bo, 16, 1024), ID_S,
-                 k > 0 ? 1u : 0u);
+          const uint32_t ao = ((k >> 2) * L::KV_CHUNK + (k & 3) * 32) >> 4;
+          const uint32_t bo = ((k >> 2) * L::Q_CHUNK + (k & 3) * 32) >> 4;
+          mma_ss_elect(tmem + L::COL_DP, dV_kmaj + ao, dO_kmaj + so + bo, ID_S, k > 0 ? 1u : 0u);
         }
-        mma_commit(bar(L::B_SDP));
+        mma_commit_elect(bar(L::B_SDP));
       };
 
       if (ok) {
-        ok = mbar_wait(bar(L::B_FULL + 0), 0, wc);
+        ok = mbar_wait_warp(bar(L::B_FULL + 0), 0, wc);
         if (ok) {
           tc_fence_after();
           issue_sdp(0);
@@ -238,58 +257,60 @@ __global__ void __launch_bounds__(448, 1) fa_bwd_kernel(const __grid_constant__ 
       }
       for (int i = 0; i < n_steps && ok; ++i) {
         const int st = i % L::STAGES;
-        const int b = i % L::PBUFS;
         if (i + 1 < n_steps) {
           // the next S^T, dP^T may overwrite tensor memory once step i's are read out
           const int st1 = (i + 1) % L::STAGES;
-          if (!(ok = mbar_wait(bar(L::B_SDP_FREE), i & 1, wc))) break;
-          if (!(ok = mbar_wait(bar(L::B_FULL + st1), ((i + 1) / L::STAGES) & 1, wc))) break;
+          if (!(ok = mbar_wait_warp(bar(L::B_SDP_FREE), i & 1, wc))) break;
+          if (!(ok = mbar_wait_warp(bar(L::B_FULL + st1), ((i + 1) / L::STAGES) & 1, wc))) break;
           tc_fence_after();
           issue_sdp(st1);
         }
-        if (!(ok = mbar_wait(bar(L::B_DS + b), (i / L::PBUFS) & 1, wc))) break;
+        if (!(ok = mbar_wait_warp(bar(L::B_DS), i & 1, wc))) break;
         tc_fence_after();
-        const uint32_t sb = sbase + L::RING_OFF + st * L::STAGE_BYTES;
-        const uint32_t pt = sbase + L::PT_OFF + (2 * b) * L::PT_BYTES;
-        const uint32_t dst = pt + L::PT_BYTES;
+        const uint64_t so = static_cast<uint64_t>(st) * STAGE16;
         // dV += P^T dO_i ; dK += dS^T Q_i   (K = BQ queries, 16 per step)
 #pragma unroll
         for (int k = 0; k < BQ / 16; ++k) {
-          const uint32_t ao = (k >> 2) * L::PT_CHUNK + (k & 3) * 32;
-          mma_ss(tmem + L::COL_DV, sdesc_sw128(pt + ao, 16, 1024),
-                 sdesc_sw128(sb + L::ST_DO + k * 2048, L::Q_CHUNK, 1024), ID_G, (i > 0 || k > 0) ? 1u : 0u);
+          const uint32_t ao = ((k >> 2) * L::PT_CHUNK + (k & 3) * 32) >> 4;
+          const uint64_t bd = dO_mn + so + ((k * 2048) >> 4);
+          if constexpr (L::P_TMEM)
+            mma_ts_elect(tmem + L::COL_DV, tmem + L::COL_PT + 8 * k, bd, ID_G, (i > 0 || k > 0) ? 1u : 0u);
+          else
+            mma_ss_elect(tmem + L::COL_DV, dPT_kmaj + ao, bd, ID_G, (i > 0 || k > 0) ? 1u : 0u);
         }
 #pragma unroll
         for (int k = 0; k < BQ / 16; ++k) {
-          const uint32_t ao = (k >> 2) * L::PT_CHUNK + (k & 3) * 32;
-          mma_ss(tmem + L::COL_DK, sdesc_sw128(dst + ao, 16, 1024),
-                 sdesc_sw128(sb + L::ST_Q + k * 2048, L::Q_CHUNK, 1024), ID_G, (i > 0 || k > 0) ? 1u : 0u);
+          const uint32_t ao = ((k >> 2) * L::PT_CHUNK + (k & 3) * 32) >> 4;
+          const uint64_t bd = dQ_mn + so + ((k * 2048) >> 4);
+          if constexpr (L::P_TMEM)
+            mma_ts_elect(tmem + L::COL_DK, tmem + L::COL_DST + 8 * k, bd, ID_G, (i > 0 || k > 0) ? 1u : 0u);
+          else
+            mma_ss_elect(tmem + L::COL_DK, dDS_kmaj + ao, bd, ID_G, (i > 0 || k > 0) ? 1u : 0u);
         }
-        mma_commit(bar(L::B_EMPTY + st));     // Q_i, dO_i are no longer needed after dV, dK
+        mma_commit_elect(bar(L::B_EMPTY + st));     // Q_i, dO_i are no longer needed after dV, dK
         // dQ for this step, once the drain warps have read the previous one
         if (i > 0) {
-          if (!(ok = mbar_wait(bar(L::B_DQ_FREE), (i - 1) & 1, wc))) break;
+          if (!(ok = mbar_wait_warp(bar(L::B_DQ_FREE), (i - 1) & 1, wc))) break;
           tc_fence_after();
         }
 #pragma unroll
         for (int k = 0; k < TILE / 16; ++k) {
+          const uint32_t o = (k * 2048) >> 4;
           if constexpr (L::DQ_T) {
             // A = K^T: MN-major over d (two 64-wide blocks 16 KB apart), 16 keys per step
             // B = dS^T seen as [queries][keys]: MN-major over the 64 queries
-            mma_ss(tmem + L::COL_DQ, sdesc_sw128(kA + k * 2048, L::KV_CHUNK, 1024),
-                   sdesc_sw128(dst + k * 2048, L::PT_CHUNK, 1024), ID_Q, k > 0 ? 1u : 0u);
+            mma_ss_elect(tmem + L::COL_DQ, dK_mn + o, dDS_mn + o, ID_Q, k > 0 ? 1u : 0u);
           } else {
             // A = dS: MN-major over queries (two 64-wide blocks 16 KB apart)
             // B = K: MN-major over d (one 64-wide block)
-            mma_ss(tmem + L::COL_DQ, sdesc_sw128(dst + k * 2048, L::PT_CHUNK, 1024),
-                   sdesc_sw128(kA + k * 2048, L::KV_CHUNK, 1024), ID_Q, k > 0 ? 1u : 0u);
+            mma_ss_elect(tmem + L::COL_DQ, dDS_mn + o, dK_mn + o, ID_Q, k > 0 ? 1u : 0u);
           }
         }
-        mma_commit(bar(L::B_DQ));
-        mma_commit(bar(L::B_PFREE + b));
+        mma_commit_elect(bar(L::B_DQ));
+        mma_commit_elect(bar(L::B_PFREE));
       }
-      mma_commit(bar(L::B_DONE));
-      mbar_drain_b(bar(L::B_DONE), 0, 1000000000ull);
+      mma_commit_elect(bar(L::B_DONE));
+      if (lane == 0) mbar_drain_b(bar(L::B_DONE), 0, 1000000000ull);
     }
     __syncwarp();
   } else if (warp < L::W_DRAIN) {
@@ -332,6 +353,7 @@ __global__ void __launch_bounds__(448, 1) fa_bwd_kernel(const __grid_constant__ 
         }
         uint8_t* prow = pt + (c0 >> 6) * L::PT_CHUNK + r * 128;
         uint8_t* drow = dsT + (c0 >> 6) * L::PT_CHUNK + r * 128;
+        uint32_t pt_pk[16], ds_pk[16];                       // this chunk's bf16 pairs for tensor memory
 #pragma unroll
         for (int j = 0; j < 4; ++j) {                        // 8 queries per 16-byte chunk
           const int cq = c0 + 8 * j;                         // first query column of the chunk
@@ -360,11 +382,25 @@ __global__ void __launch_bounds__(448, 1) fa_bwd_kernel(const __grid_constant__ 
             dd[e] = pack_bf16x2(ds.x, ds.y);
           }
           const int sw = ((((c0 & 63) >> 3) + j) ^ (r & 7)) << 4;   // 128-byte swizzle of the 16-byte chunk
-          *reinterpret_cast<uint4*>(prow + sw) = make_uint4(pp[0], pp[1], pp[2], pp[3]);
+          if constexpr (!L::P_TMEM) *reinterpret_cast<uint4*>(prow + sw) = make_uint4(pp[0], pp[1], pp[2], pp[3]);
           *reinterpret_cast<uint4*>(drow + sw) = make_uint4(dd[0], dd[1], dd[2], dd[3]);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            pt_pk[4 * j + e] = pp[e];
+            ds_pk[4 * j + e] = dd[e];
+          }
+        }
+        if constexpr (L::P_TMEM) {
+          // 32 query columns = 16 bf16-pair columns of P^T and of dS^T
+          tmem_st_x16_async(tmem_addr(tmem, lane_base, L::COL_PT + c0 / 2), pt_pk);
+          tmem_st_x16_async(tmem_addr(tmem, lane_base, L::COL_DST + c0 / 2), ds_pk);
         }
       }
       if (!ok) break;
+      if constexpr (L::P_TMEM) {
+        tmem_wait_st();
+        tc_fence_before();
+      }
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(L::B_DS + b));

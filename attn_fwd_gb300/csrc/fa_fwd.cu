@@ -15,7 +15,8 @@
 // GB300 mapping (warp specialisation, 10 warps):
 //   warp 9      TMA producer: Q tiles once, then K_j and V_j into a ring of
 //               shared-memory slots (128-byte swizzle), L2 evict-last for K/V.
-//   warp 8      MMA issuer (one thread): S_w = Q_w K_j^T (SS form) and
+//   warp 8      MMA issuer (warp-uniform, one elected lane issues):
+//               S_w = Q_w K_j^T (SS form) and
 //               O_w += P_w V_j (A operand P_w read from tensor memory).
 //   warps 0-3   softmax for query tile 0, warps 4-7 for tile 1: one thread
 //               per query row reads its S row from tensor memory, computes the
@@ -170,107 +171,123 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
     }
   } else if (warp == 8) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t IDESC_S = idesc_bf16(128, 128, false, false);
-      constexpr uint32_t IDESC_O = idesc_bf16(128, D, false, true);
-      const uint32_t s_col[2] = {L::S_COL0, L::S_COL1};
-      const uint32_t o_col[2] = {L::O_COL0, L::O_COL1};
-      int n_vis[2] = {0, 0};
-      for (int kt = 0; kt < kt_end; ++kt) {
-        n_vis[0] += fwd_visible(p, qt0, kt);
-        n_vis[1] += fwd_visible(p, qt1, kt);
-      }
-      bool ok = true;
-      for (int w = 0; w < 2 && ok; ++w)
-        if (n_vis[w] > 0) ok = mbar_wait(bar(L::B_Q + w), 0, wc);
-
-      // S_w(entry) = Q_w K^T over D/16 k-steps of 16 (32 bytes inside a
-      // 128-byte swizzle row; a new 16 KB chunk every 64 columns).
-      auto issue_s = [&](int w, int kslot) {
-        const uint32_t qa = sbase + L::Q_OFF + w * L::TILE_BYTES;
-        const uint32_t ka = sbase + L::RING_OFF + kslot * L::TILE_BYTES;
-#pragma unroll
-        for (int k = 0; k < D / 16; ++k) {
-          const uint32_t off = (k >> 2) * L::CHUNK_BYTES + (k & 3) * 32;
-          mma_ss(tmem + s_col[w], sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024),
-                 IDESC_S, k > 0 ? 1u : 0u);
-        }
-      };
-      // O_w += P_w V over 128/16 k-steps: P from tensor memory (8 columns
-      // of bf16 pairs per step), V as an MN-major operand (16 key rows of 128
-      // bytes per step; the second 64-column half of d sits 16 KB further).
-      bool o_started[2] = {false, false};
-      auto issue_pv = [&](int w, int vslot) {
-        const uint32_t va = sbase + L::RING_OFF + vslot * L::TILE_BYTES;
-#pragma unroll
-        for (int k = 0; k < TILE / 16; ++k) {
-          mma_ts(tmem + o_col[w], tmem + s_col[w] + 8 * k, sdesc_sw128(va + k * 2048, L::CHUNK_BYTES, 1024),
-                 IDESC_O, (o_started[w] || k > 0) ? 1u : 0u);
-        }
-        o_started[w] = true;
-      };
-
-      struct Ent { int kslot, vslot; uint32_t vphase; bool f[2]; };
-      Ent prev{0, 0, 0u, {false, false}};
-      bool has_prev = false;
-      int slot = 0;
-      uint32_t phase = 0;
-      uint32_t pphase[2] = {0u, 0u};
-      int pv_done[2] = {0, 0};
-
-      // O_w += P_w(prev) V(prev), after softmax w has published P_w(prev).
-      auto do_pv = [&](int w, const Ent& e, bool& v_ready) -> bool {
-        if (!v_ready) {
-          if (!mbar_wait(bar(L::B_FULL + e.vslot), e.vphase, wc)) return false;
-          v_ready = true;
-        }
-        if (!mbar_wait(bar(L::B_P + w), pphase[w], wc)) return false;
-        pphase[w] ^= 1u;
-        tc_fence_after();
-        issue_pv(w, e.vslot);
-        if (++pv_done[w] == n_vis[w]) mma_commit(bar(L::B_O + w));
-        return true;
-      };
-
-      for (int kt = 0; kt < kt_end && ok; ++kt) {
-        Ent e;
-        e.f[0] = fwd_visible(p, qt0, kt);
-        e.f[1] = fwd_visible(p, qt1, kt);
-        if (!(e.f[0] || e.f[1])) continue;
-        e.kslot = slot;
-        const uint32_t kphase = phase;
-        if (++slot == L::STAGES) { slot = 0; phase ^= 1u; }
-        e.vslot = slot;
-        e.vphase = phase;
-        if (++slot == L::STAGES) { slot = 0; phase ^= 1u; }
-
-        if (!mbar_wait(bar(L::B_FULL + e.kslot), kphase, wc)) { ok = false; break; }
-        tc_fence_after();
-        bool v_ready = false;
-        for (int w = 0; w < 2 && ok; ++w) {
-          if (has_prev && prev.f[w]) ok = do_pv(w, prev, v_ready);
-          if (!ok) break;
-          if (e.f[w]) {
-            issue_s(w, e.kslot);
-            mma_commit(bar(L::B_S + w));
-          }
-        }
-        if (!ok) break;
-        mma_commit(bar(L::B_EMPTY + e.kslot));
-        if (has_prev) mma_commit(bar(L::B_EMPTY + prev.vslot));
-        prev = e;
-        has_prev = true;
-      }
-      if (ok && has_prev) {
-        bool v_ready = false;
-        for (int w = 0; w < 2 && ok; ++w)
-          if (prev.f[w]) ok = do_pv(w, prev, v_ready);
-        if (ok) mma_commit(bar(L::B_EMPTY + prev.vslot));
-      }
-      // nothing may be in flight when tensor memory is released
-      mma_commit(bar(L::B_DONE));
-      mbar_drain(bar(L::B_DONE), 0, 1000000000ull);
+    // The whole warp runs this schedule (warp-uniform); one elected lane
+    // issues each tcgen05 instruction.  Descriptors are a base plus a
+    // compile-time offset (start-address field, in 16-byte units).
+    constexpr uint32_t IDESC_S = idesc_bf16(128, 128, false, false);
+    constexpr uint32_t IDESC_O = idesc_bf16(128, D, false, true);
+    int nv0 = 0, nv1 = 0;
+    for (int kt = 0; kt < kt_end; ++kt) {
+      nv0 += fwd_visible(p, qt0, kt);
+      nv1 += fwd_visible(p, qt1, kt);
     }
+    bool ok = true;
+    if (nv0 > 0) ok = mbar_wait_warp(bar(L::B_Q + 0), 0, wc);
+    if (ok && nv1 > 0) ok = mbar_wait_warp(bar(L::B_Q + 1), 0, wc);
+    const uint64_t dq0 = sdesc_sw128(sbase + L::Q_OFF, 16, 1024);                 // Q tile 0, K-major
+    const uint64_t dq1 = sdesc_sw128(sbase + L::Q_OFF + L::TILE_BYTES, 16, 1024);  // Q tile 1
+    const uint64_t dk_ring = sdesc_sw128(sbase + L::RING_OFF, 16, 1024);           // ring slot 0 as K (K-major)
+    const uint64_t dv_ring = sdesc_sw128(sbase + L::RING_OFF, L::CHUNK_BYTES, 1024);  // ring slot 0 as V (MN-major)
+    constexpr uint32_t SLOT16 = L::TILE_BYTES >> 4;
+
+    // S_w = Q_w K^T: D/16 k-steps of 16 (32 bytes inside a 128-byte swizzle
+    // row; a new 16 KB chunk every 64 columns).
+    auto issue_s = [&](uint64_t dq, uint32_t scol, int kslot) {
+      const uint64_t dk = dk_ring + static_cast<uint64_t>(kslot) * SLOT16;
+#pragma unroll
+      for (int k = 0; k < D / 16; ++k) {
+        const uint32_t off = ((k >> 2) * L::CHUNK_BYTES + (k & 3) * 32) >> 4;
+        mma_ss_elect(tmem + scol, dq + off, dk + off, IDESC_S, k > 0 ? 1u : 0u);
+      }
+    };
+    // O_w += P_w V: 128/16 k-steps; P from tensor memory (8 columns of bf16
+    // pairs per step), V MN-major (16 key rows of 128 bytes per step; the
+    // second 64-column half of d sits 16 KB further).
+    auto issue_pv = [&](uint32_t ocol, uint32_t scol, int vslot, bool started) {
+      const uint64_t dv = dv_ring + static_cast<uint64_t>(vslot) * SLOT16;
+#pragma unroll
+      for (int k = 0; k < TILE / 16; ++k)
+        mma_ts_elect(tmem + ocol, tmem + scol + 8 * k, dv + ((k * 2048) >> 4), IDESC_O, (started || k > 0) ? 1u : 0u);
+    };
+
+    int slot = 0;
+    uint32_t phase = 0;
+    uint32_t pph0 = 0, pph1 = 0;       // phases of the P barriers
+    int done0 = 0, done1 = 0;          // PV products issued per tile
+    bool has_prev = false, pf0 = false, pf1 = false;
+    int pvslot = 0;
+    uint32_t pvphase = 0;
+    for (int kt = 0; kt < kt_end && ok; ++kt) {
+      const bool f0 = fwd_visible(p, qt0, kt);
+      const bool f1 = fwd_visible(p, qt1, kt);
+      if (!(f0 || f1)) continue;
+      const int kslot = slot;
+      const uint32_t kphase = phase;
+      if (++slot == L::STAGES) { slot = 0; phase ^= 1u; }
+      const int vslot = slot;
+      const uint32_t vphase = phase;
+      if (++slot == L::STAGES) { slot = 0; phase ^= 1u; }
+
+      if (!(ok = mbar_wait_warp(bar(L::B_FULL + kslot), kphase, wc))) break;
+      tc_fence_after();
+      if (has_prev) {
+        if (!(ok = mbar_wait_warp(bar(L::B_FULL + pvslot), pvphase, wc))) break;
+      }
+      // tile 0: PV(prev), then S(this)
+      if (has_prev && pf0) {
+        if (!(ok = mbar_wait_warp(bar(L::B_P + 0), pph0, wc))) break;
+        pph0 ^= 1u;
+        tc_fence_after();
+        issue_pv(L::O_COL0, L::S_COL0, pvslot, done0 > 0);
+        if (++done0 == nv0) mma_commit_elect(bar(L::B_O + 0));
+      }
+      if (f0) {
+        issue_s(dq0, L::S_COL0, kslot);
+        mma_commit_elect(bar(L::B_S + 0));
+      }
+      // tile 1
+      if (has_prev && pf1) {
+        if (!(ok = mbar_wait_warp(bar(L::B_P + 1), pph1, wc))) break;
+        pph1 ^= 1u;
+        tc_fence_after();
+        issue_pv(L::O_COL1, L::S_COL1, pvslot, done1 > 0);
+        if (++done1 == nv1) mma_commit_elect(bar(L::B_O + 1));
+      }
+      if (f1) {
+        issue_s(dq1, L::S_COL1, kslot);
+        mma_commit_elect(bar(L::B_S + 1));
+      }
+      mma_commit_elect(bar(L::B_EMPTY + kslot));
+      if (has_prev) mma_commit_elect(bar(L::B_EMPTY + pvslot));
+      has_prev = true;
+      pf0 = f0;
+      pf1 = f1;
+      pvslot = vslot;
+      pvphase = vphase;
+    }
+    if (ok && has_prev) {
+      ok = mbar_wait_warp(bar(L::B_FULL + pvslot), pvphase, wc);
+      if (ok && pf0) {
+        ok = mbar_wait_warp(bar(L::B_P + 0), pph0, wc);
+        if (ok) {
+          tc_fence_after();
+          issue_pv(L::O_COL0, L::S_COL0, pvslot, done0 > 0);
+          mma_commit_elect(bar(L::B_O + 0));
+        }
+      }
+      if (ok && pf1) {
+        ok = mbar_wait_warp(bar(L::B_P + 1), pph1, wc);
+        if (ok) {
+          tc_fence_after();
+          issue_pv(L::O_COL1, L::S_COL1, pvslot, done1 > 0);
+          mma_commit_elect(bar(L::B_O + 1));
+        }
+      }
+      if (ok) mma_commit_elect(bar(L::B_EMPTY + pvslot));
+    }
+    // nothing may be in flight when tensor memory is released
+    mma_commit_elect(bar(L::B_DONE));
+    if (lane == 0) mbar_drain(bar(L::B_DONE), 0, 1000000000ull);
     __syncwarp();
   } else {
     // ------------------------------------------------------------ softmax

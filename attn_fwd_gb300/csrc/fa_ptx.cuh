@@ -123,6 +123,23 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Like mbar_test, but a thread whose phase is not complete yet is parked by
+// the hardware for up to `ns` nanoseconds (woken early when the phase
+// completes) instead of returning at once, so waiting warps do not take issue
+// slots from the warps that compute.
+__device__ __forceinline__ bool mbar_test_suspend(uint32_t bar, uint32_t parity, uint32_t ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(ns)
+      : "memory");
+  return ok != 0;
+}
+constexpr uint32_t WAIT_SUSPEND_NS = 20000;
+
 // Per-CTA wait context.  Every wait is bounded: after `timeout_ns` of
 // polling, or once another role of the CTA has given up (`abort` flag in
 // shared memory), the wait records FA_DEV_TIMEOUT in the device status word
@@ -145,7 +162,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const W
   if (mbar_test(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 1;; ++it) {
-    if (mbar_test(bar, parity)) return true;
+    if (mbar_test_suspend(bar, parity, WAIT_SUSPEND_NS)) return true;
     if ((it & 63u) == 0) {
       if (*w.abort || globaltimer_ns() - t0 > w.timeout_ns) {
         wait_fail(w);
@@ -162,7 +179,7 @@ __device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, co
   uint64_t t0 = 0;
   if (lane_id() == 0) t0 = globaltimer_ns();
   for (uint32_t it = 1;; ++it) {
-    if (__all_sync(0xffffffffu, mbar_test(bar, parity))) return true;
+    if (__all_sync(0xffffffffu, mbar_test_suspend(bar, parity, WAIT_SUSPEND_NS))) return true;
     if ((it & 63u) == 0) {
       int give_up = 0;
       if (lane_id() == 0) give_up = (*w.abort || globaltimer_ns() - t0 > w.timeout_ns) ? 1 : 0;
@@ -262,6 +279,37 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
       "setp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
       "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Warp-wide forms: every lane of the warp executes the call with the same
+// arguments and one lane, chosen by elect.sync, issues the instruction.  The
+// issuing warp then runs its schedule warp-uniformly.
+__device__ __forceinline__ void mma_ss_elect(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                             uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void mma_ts_elect(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                             uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void mma_commit_elect(uint32_t bar) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(bar)
       : "memory");
 }
 
