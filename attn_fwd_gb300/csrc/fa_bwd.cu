@@ -54,7 +54,10 @@ struct BwdLayout {
   static constexpr int STAGE_BYTES = ((2 * Q_BYTES + 2 * BQ * 4) + 1023) / 1024 * 1024;
   static constexpr int PT_CHUNK = TILE * 128;               // [128 key rows][64 queries]
   static constexpr int PT_BYTES = (BQ / 64) * PT_CHUNK;     // 128 x BQ bf16
-  static constexpr int PBUFS = 1;                           // P^T / dS^T buffers
+  // Shared P^T / dS^T area (2 x PT_BYTES): d=64 keeps P^T and dS^T there
+  // (one buffer each); d=128 keeps P^T in tensor memory and double-buffers
+  // dS^T there, so step i+1 can write while dQ(i) still reads step i's.
+  static constexpr int PBUFS = 1;
   static constexpr int K_OFF = 0;
   static constexpr int V_OFF = KV_BYTES;
   static constexpr int RING_OFF = 2 * KV_BYTES;
@@ -66,9 +69,10 @@ struct BwdLayout {
   static constexpr int B_EMPTY = B_FULL + STAGES;        // STAGES
   static constexpr int B_SDP = B_EMPTY + STAGES;         // S^T and dP^T of a step in tensor memory
   static constexpr int B_SDP_FREE = B_SDP + 1;           // ... and read out (one arrival per warp)
-  static constexpr int B_DS = B_SDP_FREE + 1;            // PBUFS: P^T, dS^T written (one arrival per warp)
-  static constexpr int B_PFREE = B_DS + PBUFS;           // PBUFS: MMAs done reading a buffer
-  static constexpr int B_DQ = B_PFREE + PBUFS;           // dQ of a step in tensor memory
+  static constexpr int B_DS = B_SDP_FREE + 1;            // P^T, dS^T of a step written (one arrival per warp)
+  static constexpr int B_PFREE = B_DS + 1;               // dV, dK done reading them (d=64: dQ too)
+  static constexpr int B_DSF = B_PFREE + 1;              // 2: d=128 dS^T smem buffer b consumed by dQ
+  static constexpr int B_DQ = B_DSF + 2;                 // dQ of a step in tensor memory
   static constexpr int B_DQ_FREE = B_DQ + 1;             // ... and read out (one arrival per warp)
   static constexpr int B_DONE = B_DQ_FREE + 1;
   static constexpr int NBARS = B_DONE + 1;
@@ -144,6 +148,8 @@ __global__ void __launch_bounds__(448, 1) fa_bwd_kernel(const __grid_constant__ 
     mbar_init(bar(L::B_SDP_FREE), L::RECOMPUTE_WARPS);   // one arrival per warp
     mbar_init(bar(L::B_DS), L::RECOMPUTE_WARPS);
     mbar_init(bar(L::B_PFREE), 1);
+    mbar_init(bar(L::B_DSF + 0), 1);
+    mbar_init(bar(L::B_DSF + 1), 1);
     mbar_init(bar(L::B_DQ), 1);
     mbar_init(bar(L::B_DQ_FREE), 4);
     mbar_init(bar(L::B_DONE), 1);
@@ -226,8 +232,10 @@ __global__ void __launch_bounds__(448, 1) fa_bwd_kernel(const __grid_constant__ 
       const uint32_t pt = sbase + L::PT_OFF;                                         // single P^T / dS^T buffer
       const uint64_t dPT_kmaj = sdesc_sw128(pt, 16, 1024);
       const uint64_t dDS_kmaj = sdesc_sw128(pt + L::PT_BYTES, 16, 1024);
-      const uint64_t dDS_mn = sdesc_sw128(pt + L::PT_BYTES, L::PT_CHUNK, 1024);
-      static_assert(L::PBUFS == 1, "one P^T / dS^T buffer");
+      // dS^T as the B (d=128) or A (d=64) operand of the dQ product; at d=128
+      // step i uses buffer i % 2 of the area, at d=64 the second half.
+      const uint64_t dDS_mn0 = sdesc_sw128(L::P_TMEM ? pt : pt + L::PT_BYTES, L::PT_CHUNK, 1024);
+      constexpr uint32_t PT16 = L::PT_BYTES >> 4;
       bool ok = mbar_wait_warp(bar(L::B_KV), 0, wc);
 
       // S^T = K Q_i^T and dP^T = V dO_i^T for the step held in ring stage st
@@ -288,11 +296,13 @@ __global__ void __launch_bounds__(448, 1) fa_bwd_kernel(const __grid_constant__ 
             mma_ss_elect(tmem + L::COL_DK, dDS_kmaj + ao, bd, ID_G, (i > 0 || k > 0) ? 1u : 0u);
         }
         mma_commit_elect(bar(L::B_EMPTY + st));     // Q_i, dO_i are no longer needed after dV, dK
+        if constexpr (L::P_TMEM) mma_commit_elect(bar(L::B_PFREE));   // P^T, dS^T in TMEM consumed
         // dQ for this step, once the drain warps have read the previous one
         if (i > 0) {
           if (!(ok = mbar_wait_warp(bar(L::B_DQ_FREE), (i - 1) & 1, wc))) break;
           tc_fence_after();
         }
+        const uint64_t dDS_mn = dDS_mn0 + (L::P_TMEM ? static_cast<uint64_t>(i & 1) * PT16 : 0);
 #pragma unroll
         for (int k = 0; k < TILE / 16; ++k) {
           const uint32_t o = (k * 2048) >> 4;
@@ -307,7 +317,10 @@ __global__ void __launch_bounds__(448, 1) fa_bwd_kernel(const __grid_constant__ 
           }
         }
         mma_commit_elect(bar(L::B_DQ));
-        mma_commit_elect(bar(L::B_PFREE));
+        if constexpr (L::P_TMEM)
+          mma_commit_elect(bar(L::B_DSF + (i & 1)));   // dS^T buffer i % 2 consumed
+        else
+          mma_commit_elect(bar(L::B_PFREE));           // P^T, dS^T buffer consumed
       }
       mma_commit_elect(bar(L::B_DONE));
       if (lane == 0) mbar_drain_b(bar(L::B_DONE), 0, 1000000000ull);
@@ -327,14 +340,15 @@ __global__ void __launch_bounds__(448, 1) fa_bwd_kernel(const __grid_constant__ 
     for (int qi = qi_begin; qi < n_qi && ok; ++qi) {
       if (!bwd_visible(p, qi, BQ, kt)) continue;
       const int st = i % L::STAGES;
-      const int b = i % L::PBUFS;
       if (!(ok = mbar_wait_warp(bar(L::B_SDP), i & 1, wc))) break;
       tc_fence_after();
       const uint8_t* stage = smem + L::RING_OFF + st * L::STAGE_BYTES;
       const float* lse = reinterpret_cast<const float*>(stage + L::ST_LSE);
       const float* dvec = reinterpret_cast<const float*>(stage + L::ST_DV);
-      uint8_t* pt = smem + L::PT_OFF + (2 * b) * L::PT_BYTES;
-      uint8_t* dsT = pt + L::PT_BYTES;
+      uint8_t* const area = smem + L::PT_OFF;
+      // d=128: dS^T into buffer i % 2; d=64: P^T in the first half, dS^T in the second
+      uint8_t* const pt = area;
+      uint8_t* const dsT = L::P_TMEM ? area + (i & 1) * L::PT_BYTES : area + L::PT_BYTES;
       const bool diag = (p.mask_kind == MASK_CAUSAL) && (qi * BQ < kt * TILE + TILE);
       constexpr int COLS = BQ / 2;                           // query columns of this warp
 #pragma unroll 1
@@ -347,16 +361,12 @@ __global__ void __launch_bounds__(448, 1) fa_bwd_kernel(const __grid_constant__ 
           __syncwarp();
           if (lane == 0) mbar_arrive(bar(L::B_SDP_FREE));
         }
-        if (c0 == half * COLS && i >= L::PBUFS) {
-          // the MMAs of the step that last used this P^T / dS^T buffer must be done
-          if (!(ok = mbar_wait_warp(bar(L::B_PFREE + b), ((i / L::PBUFS) - 1) & 1, wc))) break;
-        }
-        uint8_t* prow = pt + (c0 >> 6) * L::PT_CHUNK + r * 128;
-        uint8_t* drow = dsT + (c0 >> 6) * L::PT_CHUNK + r * 128;
-        uint32_t pt_pk[16], ds_pk[16];                       // this chunk's bf16 pairs for tensor memory
+        // pass 1: P and dS for these 32 query columns, in registers only (no
+        // shared-memory stores in between, so the LSE/D loads can be hoisted)
+        uint32_t pt_pk[16], ds_pk[16];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {                        // 8 queries per 16-byte chunk
-          const int cq = c0 + 8 * j;                         // first query column of the chunk
+        for (int j = 0; j < 4; ++j) {                        // 8 queries per group
+          const int cq = c0 + 8 * j;
           const float4 l0 = *reinterpret_cast<const float4*>(lse + cq);
           const float4 l1 = *reinterpret_cast<const float4*>(lse + cq + 4);
           const float4 d0 = *reinterpret_cast<const float4*>(dvec + cq);
@@ -365,7 +375,6 @@ __global__ void __launch_bounds__(448, 1) fa_bwd_kernel(const __grid_constant__ 
                                 make_float2(-l1.x * LOG2E, -l1.y * LOG2E), make_float2(-l1.z * LOG2E, -l1.w * LOG2E)};
           const float2 nd[4] = {make_float2(-d0.x, -d0.y), make_float2(-d0.z, -d0.w), make_float2(-d1.x, -d1.y),
                                 make_float2(-d1.z, -d1.w)};
-          uint32_t pp[4], dd[4];
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const int k = 8 * j + 2 * e;                     // register index within the 32 columns
@@ -378,19 +387,30 @@ __global__ void __launch_bounds__(448, 1) fa_bwd_kernel(const __grid_constant__ 
             }
             const float2 ds =
                 fmul2(pv, fadd2(make_float2(__uint_as_float(dr[k]), __uint_as_float(dr[k + 1])), nd[e]));
-            pp[e] = pack_bf16x2(pv.x, pv.y);
-            dd[e] = pack_bf16x2(ds.x, ds.y);
-          }
-          const int sw = ((((c0 & 63) >> 3) + j) ^ (r & 7)) << 4;   // 128-byte swizzle of the 16-byte chunk
-          if constexpr (!L::P_TMEM) *reinterpret_cast<uint4*>(prow + sw) = make_uint4(pp[0], pp[1], pp[2], pp[3]);
-          *reinterpret_cast<uint4*>(drow + sw) = make_uint4(dd[0], dd[1], dd[2], dd[3]);
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            pt_pk[4 * j + e] = pp[e];
-            ds_pk[4 * j + e] = dd[e];
+            pt_pk[4 * j + e] = pack_bf16x2(pv.x, pv.y);
+            ds_pk[4 * j + e] = pack_bf16x2(ds.x, ds.y);
           }
         }
+        // pass 2: stores, once the buffers they overwrite have been consumed
+        if (c0 == half * COLS) {
+          if constexpr (L::P_TMEM) {
+            if (i >= 2 && !(ok = mbar_wait_warp(bar(L::B_DSF + (i & 1)), ((i >> 1) - 1) & 1, wc))) break;
+          } else {
+            if (i >= 1 && !(ok = mbar_wait_warp(bar(L::B_PFREE), (i - 1) & 1, wc))) break;
+          }
+        }
+        uint8_t* prow = pt + (c0 >> 6) * L::PT_CHUNK + r * 128;
+        uint8_t* drow = dsT + (c0 >> 6) * L::PT_CHUNK + r * 128;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int sw = ((((c0 & 63) >> 3) + j) ^ (r & 7)) << 4;   // 128-byte swizzle of the 16-byte chunk
+          if constexpr (!L::P_TMEM)
+            *reinterpret_cast<uint4*>(prow + sw) = make_uint4(pt_pk[4 * j], pt_pk[4 * j + 1], pt_pk[4 * j + 2], pt_pk[4 * j + 3]);
+          *reinterpret_cast<uint4*>(drow + sw) = make_uint4(ds_pk[4 * j], ds_pk[4 * j + 1], ds_pk[4 * j + 2], ds_pk[4 * j + 3]);
+        }
         if constexpr (L::P_TMEM) {
+          // P^T, dS^T in tensor memory are free once dV(i-1), dK(i-1) are done
+          if (i >= 1 && !(ok = mbar_wait_warp(bar(L::B_PFREE), (i - 1) & 1, wc))) break;
           // 32 query columns = 16 bf16-pair columns of P^T and of dS^T
           tmem_st_x16_async(tmem_addr(tmem, lane_base, L::COL_PT + c0 / 2), pt_pk);
           tmem_st_x16_async(tmem_addr(tmem, lane_base, L::COL_DST + c0 / 2), ds_pk);
@@ -403,7 +423,7 @@ __global__ void __launch_bounds__(448, 1) fa_bwd_kernel(const __grid_constant__ 
       }
       fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(L::B_DS + b));
+      if (lane == 0) mbar_arrive(bar(L::B_DS));
       ++i;
     }
     // ------------------------------------------------- epilogue: dV rows, half the columns each
