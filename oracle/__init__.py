@@ -6,6 +6,7 @@ CPU-baseline leg and reference arm.  It shares no code with the CUDA path.
 from .attention import (  # noqa: F401
     NEG_INF,
     backward,
+    backward_rows,
     backward_rows_dq,
     flops,
     forward,

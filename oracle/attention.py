@@ -178,6 +178,22 @@ def backward_rows_dq(q, k, v, do, scale, b, h, rows, causal=False, block_mask=No
     return scale * (_softmax_backward(p, dp, d_row) @ k)
 
 
+def backward_rows(q, k, v, do, scale, b, h, rows, causal=False, block_mask=None, block=128):
+    """The backward restricted to selected query rows of head (b, h): dQ of
+    those rows and their contributions to dK and dV [P2 "Backward Pass of
+    flashattention": dv_j = sum_i P_ij do_i, dk_j = sum_i dS_ij q_i, both sums
+    over query rows i, so a partition of the rows splits them exactly].
+    Returns (dq_rows, dk_part, dv_part, o_rows, lse_rows)."""
+    q, k, v, do = (np.asarray(x, dtype=np.float64) for x in (q[b, h], k[b, h], v[b, h], do[b, h]))
+    rows = np.asarray(rows)
+    p, lse = head_probs(q, k, scale, causal, block_mask, block, rows)
+    o = p @ v
+    dp = do[rows] @ v.T
+    d_row = (p * dp).sum(axis=1)
+    ds = _softmax_backward(p, dp, d_row)
+    return scale * (ds @ k), scale * (ds.T @ q[rows]), p.T @ do[rows], o, lse
+
+
 # --------------------------------------------------------------------------- #
 # the tiled algorithm, step by step as the pages state it
 # --------------------------------------------------------------------------- #

@@ -222,10 +222,22 @@ def pin_dvec(orc):
 def pin_backward_rows(orc):
     r = _rng(6)
     q, k, v, do = (r.standard_normal((1, 2, 29, 4)) for _ in range(4))
-    dq, _, _, _ = orc.backward(q, k, v, do, 0.5, causal=True)
+    dq, dk, dv, _ = orc.backward(q, k, v, do, 0.5, causal=True)
+    o, lse = orc.forward(q, k, v, 0.5, causal=True)
     rows = [0, 9, 28]
     np.testing.assert_allclose(orc.backward_rows_dq(q, k, v, do, 0.5, 0, 1, rows, causal=True),
                                dq[0, 1, rows], atol=1e-13)
+    # row blocks partition the rows: their dK, dV contributions sum to the whole
+    sdk, sdv = np.zeros_like(dk[0, 1]), np.zeros_like(dv[0, 1])
+    for blk in (range(0, 10), range(10, 11), range(11, 29)):
+        dqr, dkp, dvp, orr, lr = orc.backward_rows(q, k, v, do, 0.5, 0, 1, list(blk), causal=True)
+        np.testing.assert_allclose(dqr, dq[0, 1, list(blk)], atol=1e-13)
+        np.testing.assert_allclose(orr, o[0, 1, list(blk)], atol=1e-13)
+        np.testing.assert_allclose(lr, lse[0, 1, list(blk)], atol=1e-13)
+        sdk += dkp
+        sdv += dvp
+    np.testing.assert_allclose(sdk, dk[0, 1], atol=1e-12)
+    np.testing.assert_allclose(sdv, dv[0, 1], atol=1e-12)
 
 
 # --------------------------------------------------------------------------- #
