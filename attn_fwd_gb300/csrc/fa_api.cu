@@ -137,6 +137,7 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, c
   if (mask_kind == fa::MASK_BLOCK && block_mask == nullptr) return FA_ERR_INVALID;
   if ((rc = check_shape(B, H, N, d)) != FA_OK) return rc;
   if ((rc = check_scale(scale)) != FA_OK) return rc;
+  if (mask_kind == fa::MASK_BLOCK && N / fa::TILE > fa::MAX_SPARSE_TILES) return FA_ERR_UNSUPPORTED;
   int* status = nullptr;
   if ((rc = device_ready(&status)) != FA_OK) return rc;
   if ((rc = encoder_ready()) != FA_OK) return rc;

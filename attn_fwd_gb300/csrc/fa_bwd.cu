@@ -76,7 +76,10 @@ struct BwdLayout {
   static constexpr int B_DQ_FREE = B_DQ + 1;             // ... and read out (one arrival per warp)
   static constexpr int B_DONE = B_DQ_FREE + 1;
   static constexpr int NBARS = B_DONE + 1;
-  static constexpr int SMEM_BYTES = BAR_OFF + NBARS * 8 + 16 + 1024;
+  // block masks: list of the visible 128-row query blocks of this key tile
+  static constexpr int LIST_OFF = BAR_OFF + NBARS * 8 + 16;
+  static constexpr int LIST_BYTES = MAX_SPARSE_TILES * 2 + 16;
+  static constexpr int SMEM_BYTES = LIST_OFF + LIST_BYTES + 1024;
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t COL_S = 0;
   static constexpr uint32_t COL_DP = BQ;
@@ -98,11 +101,35 @@ struct BwdLayout {
   static constexpr int RECOMPUTE_WARPS = 8;
 };
 
-__device__ __forceinline__ bool bwd_visible(const BwdParams& p, int qi, int bq, int kt) {
-  if (p.mask_kind == MASK_CAUSAL) return qi * bq + bq - 1 >= kt * TILE;
-  if (p.mask_kind == MASK_BLOCK)
-    return __ldg(p.block_mask + static_cast<size_t>(qi * bq / TILE) * p.n_kt + kt) != 0;
-  return true;
+// The query tiles (BQ rows) a key tile visits, in increasing order, as steps
+// 0..count-1.  No mask: all; causal: from the first tile that reaches the
+// key tile's diagonal; block mask: the 128-row query blocks whose mask byte
+// for this key tile is nonzero (compacted once per CTA by one warp into a
+// shared-memory list), each split into 128 / BQ steps.
+template <int BQ>
+struct StepSched {
+  static constexpr int SUB = TILE / BQ;
+  const uint16_t* list;
+  int mask_kind;
+  int first;      // causal: the first visible query tile
+  int count;
+
+  __device__ __forceinline__ int qi(int i) const {
+    if (mask_kind == MASK_BLOCK) return static_cast<int>(list[i / SUB]) * SUB + i % SUB;
+    return first + i;
+  }
+};
+
+__device__ __forceinline__ int build_sparse_column(const BwdParams& p, int kt, uint16_t* list, uint32_t lane) {
+  int n = 0;
+  for (int base = 0; base < p.n_kt; base += 32) {
+    const int qb = base + static_cast<int>(lane);
+    const bool v = qb < p.n_kt && __ldg(p.block_mask + static_cast<size_t>(qb) * p.n_kt + kt) != 0;
+    const uint32_t m = __ballot_sync(0xffffffffu, v);
+    if (v) list[n + __popc(m & ((1u << lane) - 1u))] = static_cast<uint16_t>(qb);
+    n += __popc(m);
+  }
+  return n;
 }
 
 __device__ __forceinline__ void mbar_drain_b(uint32_t bar, uint32_t parity, uint64_t ns) {
@@ -137,6 +164,12 @@ __global__ void __launch_bounds__(448, 1) fa_bwd_kernel(const __grid_constant__ 
   const int bh = band * band_heads + in_band % heads_here;
   const int n_qi = p.N / BQ;
   const int qi_begin = (p.mask_kind == MASK_CAUSAL) ? (kt * TILE) / BQ : 0;
+  uint16_t* list = reinterpret_cast<uint16_t*>(smem + L::LIST_OFF);
+  int* list_count = reinterpret_cast<int*>(smem + L::LIST_OFF + MAX_SPARSE_TILES * 2);
+  if (p.mask_kind == MASK_BLOCK && warp == 0) {
+    const int n = build_sparse_column(p, kt, list, lane);
+    if (lane == 0) *list_count = n;
+  }
 
   if (threadIdx.x == 0) {
     mbar_init(bar(L::B_KV), 1);
@@ -166,8 +199,8 @@ __global__ void __launch_bounds__(448, 1) fa_bwd_kernel(const __grid_constant__ 
   const uint32_t tmem = *tmem_slot;
   const WaitCtx wc{abort_flag, p.status, p.timeout_ns};
 
-  int n_steps = 0;
-  for (int qi = qi_begin; qi < n_qi; ++qi) n_steps += bwd_visible(p, qi, BQ, kt);
+  const int n_steps = p.mask_kind == MASK_BLOCK ? *list_count * StepSched<BQ>::SUB : n_qi - qi_begin;
+  const StepSched<BQ> sched{list, p.mask_kind, qi_begin, n_steps};
 
   if (warp == L::W_TMA) {
     // ------------------------------------------------------------ producer
@@ -189,9 +222,8 @@ __global__ void __launch_bounds__(448, 1) fa_bwd_kernel(const __grid_constant__ 
         }
         kv_issued = true;
       }
-      int step = 0;
-      for (int qi = qi_begin; qi < n_qi && ok; ++qi) {
-        if (!bwd_visible(p, qi, BQ, kt)) continue;
+      for (int step = 0; step < n_steps && ok; ++step) {
+        const int qi = sched.qi(step);
         const int st = step % L::STAGES;
         if (!mbar_wait(bar(L::B_EMPTY + st), ((step / L::STAGES) & 1) ^ 1, wc)) { ok = false; break; }
         const uint32_t fb = bar(L::B_FULL + st);
@@ -205,7 +237,6 @@ __global__ void __launch_bounds__(448, 1) fa_bwd_kernel(const __grid_constant__ 
         bulk_load(sb + L::ST_LSE, p.lse + row0, BQ * 4, fb);
         bulk_load(sb + L::ST_DV, p.dvec + row0, BQ * 4, fb);
         ++issued[st];
-        ++step;
       }
       if (!ok) {
         if (kv_issued) mbar_drain_b(bar(L::B_KV), 0, 100000000ull);
@@ -336,9 +367,8 @@ __global__ void __launch_bounds__(448, 1) fa_bwd_kernel(const __grid_constant__ 
     const float2 sl2v = make_float2(p.scale_log2, p.scale_log2);
     constexpr float LOG2E = 1.4426950408889634f;
     bool ok = true;
-    int i = 0;
-    for (int qi = qi_begin; qi < n_qi && ok; ++qi) {
-      if (!bwd_visible(p, qi, BQ, kt)) continue;
+    for (int i = 0; i < n_steps && ok; ++i) {
+      const int qi = sched.qi(i);
       const int st = i % L::STAGES;
       if (!(ok = mbar_wait_warp(bar(L::B_SDP), i & 1, wc))) break;
       tc_fence_after();
@@ -424,7 +454,6 @@ __global__ void __launch_bounds__(448, 1) fa_bwd_kernel(const __grid_constant__ 
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(L::B_DS));
-      ++i;
     }
     // ------------------------------------------------- epilogue: dV rows, half the columns each
     if (ok) {
@@ -456,9 +485,8 @@ __global__ void __launch_bounds__(448, 1) fa_bwd_kernel(const __grid_constant__ 
     const uint32_t lane_base = quarter * 32;
     const int t = static_cast<int>(quarter * 32 + lane);
     bool ok = true;
-    int i = 0;
-    for (int qi = qi_begin; qi < n_qi && ok; ++qi) {
-      if (!bwd_visible(p, qi, BQ, kt)) continue;
+    for (int i = 0; i < n_steps && ok; ++i) {
+      const int qi = sched.qi(i);
       if (!(ok = mbar_wait_warp(bar(L::B_DQ), i & 1, wc))) break;
       tc_fence_after();
       uint32_t v[64];
@@ -480,7 +508,6 @@ __global__ void __launch_bounds__(448, 1) fa_bwd_kernel(const __grid_constant__ 
           atomicAdd(dst + c, make_float4(__uint_as_float(v[4 * c]), __uint_as_float(v[4 * c + 1]),
                                          __uint_as_float(v[4 * c + 2]), __uint_as_float(v[4 * c + 3])));
       }
-      ++i;
     }
     // dK rows (lane = key row), scaled by the chain-rule factor
     if (ok) {

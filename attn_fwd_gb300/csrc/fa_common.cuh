@@ -15,6 +15,11 @@ enum MaskKind : int { MASK_NONE = 0, MASK_CAUSAL = 1, MASK_BLOCK = 2 };
 // query row, one 128-byte swizzle span per 64 head-dim columns).
 constexpr int TILE = 128;
 
+// Block-sparse masks: each CTA keeps the mask bits of its tiles in shared
+// memory, one bit per 128-row tile, for at most this many tiles per row
+// (N <= 131072).
+constexpr int MAX_SPARSE_TILES = 1024;
+
 // Forward launch parameters.  Tensor maps describe Q, K, V as 3-D bf16
 // arrays [B*H][N][d] with a {64, 128, 1} box and 128-byte swizzle.
 struct FwdParams {

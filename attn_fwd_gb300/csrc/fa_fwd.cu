@@ -39,12 +39,14 @@
 
 namespace fa {
 
-template <int D>
+template <int D, bool SPARSE>
 struct FwdLayout {
   static constexpr int NCH = D / 64;                      // 64-column (128-byte) chunks
   static constexpr int CHUNK_BYTES = TILE * 128;          // 128 rows x 128 bytes
   static constexpr int TILE_BYTES = NCH * CHUNK_BYTES;    // one 128 x D bf16 tile
-  static constexpr int STAGES = (D == 128) ? 4 : 6;       // K/V ring slots
+  // K/V ring slots.  A block-sparse round can need two K and two V tiles,
+  // so it gets a fifth slot at d=128 to keep one load in flight ahead.
+  static constexpr int STAGES = (D == 128) ? (SPARSE ? 5 : 4) : 6;
   static constexpr int Q_OFF = 0;
   static constexpr int RING_OFF = 2 * TILE_BYTES;
   static constexpr int BAR_OFF = RING_OFF + STAGES * TILE_BYTES;
@@ -57,7 +59,12 @@ struct FwdLayout {
   static constexpr int B_O = B_P + 2;            // 2
   static constexpr int B_DONE = B_O + 2;         // 1
   static constexpr int NBARS = B_DONE + 1;
-  static constexpr int SMEM_BYTES = BAR_OFF + NBARS * 8 + 16 + 1024;  // + 1 KB alignment slack
+  // block-sparse: one bit per key tile for each of the two query tiles, and
+  // the two counts
+  static constexpr int BITS_OFF = BAR_OFF + NBARS * 8 + 16;
+  static constexpr int BITS_WORDS = MAX_SPARSE_TILES / 32;
+  static constexpr int BITS_BYTES = SPARSE ? 2 * BITS_WORDS * 4 + 16 : 0;
+  static constexpr int SMEM_BYTES = BITS_OFF + BITS_BYTES + 1024;      // + 1 KB alignment slack
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t S_COL0 = 0, S_COL1 = 128;
   static constexpr uint32_t O_COL0 = 256, O_COL1 = 256 + D;
@@ -67,11 +74,41 @@ struct FwdLayout {
 // Reference-max threshold for lazy rescaling, in exp2 units (factor 256).
 constexpr float RESCALE_THRESHOLD = 8.0f;
 
-__device__ __forceinline__ bool fwd_visible(const FwdParams& p, int qt, int kt) {
+// Block-sparse masks: which key tiles a query tile visits, as one bit per key
+// tile, copied once per CTA from the mask row into shared memory by one warp
+// (a ballot per 32 tiles).  Roles walk the set bits in increasing order.
+__device__ __forceinline__ void build_sparse_bits(const FwdParams& p, int qt, uint32_t* bits, int* count,
+                                                  uint32_t lane) {
+  int n = 0;
+  const int nw = (p.n_qt + 31) / 32;
+  for (int wd = 0; wd < nw; ++wd) {
+    const int kt = wd * 32 + static_cast<int>(lane);
+    const bool v = qt < p.n_qt && kt < p.n_qt && __ldg(p.block_mask + static_cast<size_t>(qt) * p.n_qt + kt) != 0;
+    const uint32_t m = __ballot_sync(0xffffffffu, v);
+    if (lane == 0) bits[wd] = m;
+    n += __popc(m);
+  }
+  if (lane == 0) *count = n;
+}
+
+// The first visible key tile at or after `from`, or -1.
+__device__ __forceinline__ int next_visible(const uint32_t* bits, int from, int n_kt) {
+  if (from >= n_kt) return -1;
+  int wd = from >> 5;
+  uint32_t m = bits[wd] & (0xffffffffu << (from & 31));
+  const int nw = (n_kt + 31) >> 5;
+  while (m == 0) {
+    if (++wd >= nw) return -1;
+    m = bits[wd];
+  }
+  return wd * 32 + __ffs(m) - 1;
+}
+
+// No mask or causal: the two query tiles of a CTA share one key-tile
+// sequence 0..kt_end-1 (causal: a tile skips the tiles above its diagonal).
+__device__ __forceinline__ bool dense_visible(const FwdParams& p, int qt, int kt) {
   if (qt >= p.n_qt) return false;
-  if (p.mask_kind == MASK_CAUSAL) return kt <= qt;
-  if (p.mask_kind == MASK_BLOCK) return __ldg(p.block_mask + static_cast<size_t>(qt) * p.n_qt + kt) != 0;
-  return true;
+  return p.mask_kind != MASK_CAUSAL || kt <= qt;
 }
 
 // Bounded wait used only while tearing down after a failure: ignores the
@@ -83,9 +120,9 @@ __device__ __forceinline__ void mbar_drain(uint32_t bar, uint32_t parity, uint64
   }
 }
 
-template <int D>
+template <int D, bool SPARSE>
 __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ FwdParams p) {
-  using L = FwdLayout<D>;
+  using L = FwdLayout<D, SPARSE>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
@@ -102,6 +139,11 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
   const int qt0 = 2 * pair;
   const int qt1 = 2 * pair + 1;
   const int kt_end = (p.mask_kind == MASK_CAUSAL) ? min(qt1, p.n_qt - 1) + 1 : p.n_qt;
+  uint32_t* bits = reinterpret_cast<uint32_t*>(smem + L::BITS_OFF);   // [2][BITS_WORDS], then 2 counts
+  int* bit_counts = reinterpret_cast<int*>(bits + 2 * L::BITS_WORDS);
+  if constexpr (SPARSE) {
+    if (warp < 2) build_sparse_bits(p, warp == 0 ? qt0 : qt1, bits + warp * L::BITS_WORDS, bit_counts + warp, lane);
+  }
 
   if (threadIdx.x == 0) {
     mbar_init(bar(L::B_Q + 0), 1);
@@ -128,6 +170,22 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const WaitCtx wc{abort_flag, p.status, p.timeout_ns};
+  // key tiles visited by each query tile
+  int nv0, nv1;
+  if constexpr (SPARSE) {
+    nv0 = bit_counts[0];
+    nv1 = bit_counts[1];
+  } else {
+    nv0 = qt0 < p.n_qt ? (p.mask_kind == MASK_CAUSAL ? qt0 + 1 : p.n_qt) : 0;
+    nv1 = qt1 < p.n_qt ? (p.mask_kind == MASK_CAUSAL ? qt1 + 1 : p.n_qt) : 0;
+  }
+  const uint32_t* bits0 = bits;
+  const uint32_t* bits1 = bits + L::BITS_WORDS;
+  const int rounds = nv0 > nv1 ? nv0 : nv1;
+  // Round r pairs tile 0's r-th key tile a_r with tile 1's r-th key tile b_r
+  // (-1 when a tile has no more).  The producer loads, per round, K(a) K(b)
+  // V(a) V(b) into consecutive ring slots, once when a_r == b_r; the MMA
+  // issuer walks the same sequence.
 
   if (warp == 9) {
     // ------------------------------------------------------------ producer
@@ -150,8 +208,9 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
       uint32_t issued[L::STAGES];
       for (int s = 0; s < L::STAGES; ++s) issued[s] = 0;
       bool ok = true;
+      if constexpr (!SPARSE) {
       for (int kt = 0; kt < kt_end && ok; ++kt) {
-        if (!(fwd_visible(p, qt0, kt) || fwd_visible(p, qt1, kt))) continue;
+        if (!(dense_visible(p, qt0, kt) || dense_visible(p, qt1, kt))) continue;
         for (int which = 0; which < 2; ++which) {  // K_j, then V_j
           if (!mbar_wait(bar(L::B_EMPTY + slot), phase ^ 1u, wc)) { ok = false; break; }
           const uint32_t fb = bar(L::B_FULL + slot);
@@ -163,6 +222,30 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
           ++issued[slot];
           if (++slot == L::STAGES) { slot = 0; phase ^= 1u; }
         }
+      }
+      } else {
+      auto load = [&](const CUtensorMap* m, int kt) {
+        if (!mbar_wait(bar(L::B_EMPTY + slot), phase ^ 1u, wc)) return false;
+        const uint32_t fb = bar(L::B_FULL + slot);
+        mbar_arrive_expect_tx(fb, L::TILE_BYTES);
+        for (int c = 0; c < L::NCH; ++c)
+          tma_load_3d(sbase + L::RING_OFF + slot * L::TILE_BYTES + c * L::CHUNK_BYTES, m, fb, c * 64, kt * TILE,
+                      bh, pol_kv);
+        ++issued[slot];
+        if (++slot == L::STAGES) { slot = 0; phase ^= 1u; }
+        return true;
+      };
+      int cur0 = next_visible(bits0, 0, p.n_qt), cur1 = next_visible(bits1, 0, p.n_qt);
+      for (int r = 0; r < rounds && ok; ++r) {
+        const int a = cur0, b = cur1;
+        if (a >= 0) cur0 = next_visible(bits0, a + 1, p.n_qt);
+        if (b >= 0) cur1 = next_visible(bits1, b + 1, p.n_qt);
+        const bool two = b >= 0 && b != a;
+        if (a >= 0) ok = load(&p.tm_k, a);
+        if (ok && two) ok = load(&p.tm_k, b);
+        if (ok && a >= 0) ok = load(&p.tm_v, a);
+        if (ok && two) ok = load(&p.tm_v, b);
+      }
       }
       if (!ok) {  // let copies already in flight land before the CTA exits
         for (int s = 0; s < L::STAGES; ++s)
@@ -176,11 +259,6 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
     // compile-time offset (start-address field, in 16-byte units).
     constexpr uint32_t IDESC_S = idesc_bf16(128, 128, false, false);
     constexpr uint32_t IDESC_O = idesc_bf16(128, D, false, true);
-    int nv0 = 0, nv1 = 0;
-    for (int kt = 0; kt < kt_end; ++kt) {
-      nv0 += fwd_visible(p, qt0, kt);
-      nv1 += fwd_visible(p, qt1, kt);
-    }
     bool ok = true;
     if (nv0 > 0) ok = mbar_wait_warp(bar(L::B_Q + 0), 0, wc);
     if (ok && nv1 > 0) ok = mbar_wait_warp(bar(L::B_Q + 1), 0, wc);
@@ -210,6 +288,7 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
         mma_ts_elect(tmem + ocol, tmem + scol + 8 * k, dv + ((k * 2048) >> 4), IDESC_O, (started || k > 0) ? 1u : 0u);
     };
 
+    if constexpr (!SPARSE) {
     int slot = 0;
     uint32_t phase = 0;
     uint32_t pph0 = 0, pph1 = 0;       // phases of the P barriers
@@ -218,8 +297,8 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
     int pvslot = 0;
     uint32_t pvphase = 0;
     for (int kt = 0; kt < kt_end && ok; ++kt) {
-      const bool f0 = fwd_visible(p, qt0, kt);
-      const bool f1 = fwd_visible(p, qt1, kt);
+      const bool f0 = dense_visible(p, qt0, kt);
+      const bool f1 = dense_visible(p, qt1, kt);
       if (!(f0 || f1)) continue;
       const int kslot = slot;
       const uint32_t kphase = phase;
@@ -285,6 +364,96 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
       }
       if (ok) mma_commit_elect(bar(L::B_EMPTY + pvslot));
     }
+    } else {
+    // Ring slots in load order (the producer's sequence): the n-th tile
+    // loaded sits in slot n % STAGES, and its fill barrier completes for the
+    // (n / STAGES)-th time.
+    auto slot_of = [](int n) { return n % L::STAGES; };
+    auto phase_of = [](int n) { return static_cast<uint32_t>((n / L::STAGES) & 1); };
+    int cnt = 0;                       // tiles taken so far
+    uint32_t pph0 = 0, pph1 = 0;       // phases of the P barriers
+    int done0 = 0, done1 = 0;          // PV products issued per tile
+    // previous round: which tiles had a key tile, and where its V tiles sit
+    bool pa = false, pb = false, ptwo = false;
+    int pv = 0;                        // load index of the previous round's first V tile
+    int cur0 = next_visible(bits0, 0, p.n_qt), cur1 = next_visible(bits1, 0, p.n_qt);
+    for (int r = 0; r < rounds && ok; ++r) {
+      const int a = cur0, b = cur1;
+      if (a >= 0) cur0 = next_visible(bits0, a + 1, p.n_qt);
+      if (b >= 0) cur1 = next_visible(bits1, b + 1, p.n_qt);
+      const bool two = b >= 0 && b != a;
+      const int nk = (a >= 0 ? 1 : 0) + (two ? 1 : 0);   // K tiles this round (as many V tiles)
+      const int k0 = cnt;                                  // first K tile of this round
+      const int kb_n = two ? k0 + nk - 1 : k0;             // the K tile tile 1 uses
+      if (!(ok = mbar_wait_warp(bar(L::B_FULL + slot_of(k0)), phase_of(k0), wc))) break;
+      if (two && a >= 0 && !(ok = mbar_wait_warp(bar(L::B_FULL + slot_of(k0 + 1)), phase_of(k0 + 1), wc))) break;
+      if (pa || pb) {
+        if (!(ok = mbar_wait_warp(bar(L::B_FULL + slot_of(pv)), phase_of(pv), wc))) break;
+        if (pa && pb && ptwo && !(ok = mbar_wait_warp(bar(L::B_FULL + slot_of(pv + 1)), phase_of(pv + 1), wc))) break;
+      }
+      tc_fence_after();
+      // tile 0: PV of the previous round, then S of this round
+      if (pa) {
+        if (!(ok = mbar_wait_warp(bar(L::B_P + 0), pph0, wc))) break;
+        pph0 ^= 1u;
+        tc_fence_after();
+        issue_pv(L::O_COL0, L::S_COL0, slot_of(pv), done0 > 0);
+        if (++done0 == nv0) mma_commit_elect(bar(L::B_O + 0));
+      }
+      if (a >= 0) {
+        issue_s(dq0, L::S_COL0, slot_of(k0));
+        mma_commit_elect(bar(L::B_S + 0));
+      }
+      // tile 1 (its V tile of the previous round is the last V tile loaded then)
+      if (pb) {
+        if (!(ok = mbar_wait_warp(bar(L::B_P + 1), pph1, wc))) break;
+        pph1 ^= 1u;
+        tc_fence_after();
+        issue_pv(L::O_COL1, L::S_COL1, slot_of(pv + ((pa && ptwo) ? 1 : 0)), done1 > 0);
+        if (++done1 == nv1) mma_commit_elect(bar(L::B_O + 1));
+      }
+      if (b >= 0) {
+        issue_s(dq1, L::S_COL1, slot_of(kb_n));
+        mma_commit_elect(bar(L::B_S + 1));
+      }
+      // release this round's K slots and the previous round's V slots
+      for (int j = 0; j < nk; ++j) mma_commit_elect(bar(L::B_EMPTY + slot_of(k0 + j)));
+      if (pa || pb) {
+        mma_commit_elect(bar(L::B_EMPTY + slot_of(pv)));
+        if (pa && pb && ptwo) mma_commit_elect(bar(L::B_EMPTY + slot_of(pv + 1)));
+      }
+      pa = a >= 0;
+      pb = b >= 0;
+      ptwo = two;
+      pv = k0 + nk;
+      cnt = k0 + 2 * nk;
+    }
+    // the last round's PV products
+    if (ok && (pa || pb)) {
+      ok = mbar_wait_warp(bar(L::B_FULL + slot_of(pv)), phase_of(pv), wc);
+      if (ok && pa && pb && ptwo) ok = mbar_wait_warp(bar(L::B_FULL + slot_of(pv + 1)), phase_of(pv + 1), wc);
+      if (ok && pa) {
+        ok = mbar_wait_warp(bar(L::B_P + 0), pph0, wc);
+        if (ok) {
+          tc_fence_after();
+          issue_pv(L::O_COL0, L::S_COL0, slot_of(pv), done0 > 0);
+          mma_commit_elect(bar(L::B_O + 0));
+        }
+      }
+      if (ok && pb) {
+        ok = mbar_wait_warp(bar(L::B_P + 1), pph1, wc);
+        if (ok) {
+          tc_fence_after();
+          issue_pv(L::O_COL1, L::S_COL1, slot_of(pv + ((pa && ptwo) ? 1 : 0)), done1 > 0);
+          mma_commit_elect(bar(L::B_O + 1));
+        }
+      }
+      if (ok) {
+        mma_commit_elect(bar(L::B_EMPTY + slot_of(pv)));
+        if (pa && pb && ptwo) mma_commit_elect(bar(L::B_EMPTY + slot_of(pv + 1)));
+      }
+    }
+    }
     // nothing may be in flight when tensor memory is released
     mma_commit_elect(bar(L::B_DONE));
     if (lane == 0) mbar_drain(bar(L::B_DONE), 0, 1000000000ull);
@@ -305,10 +474,10 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
       bool has_o = false;
       bool ok = true;
       uint32_t sphase = 0;
-      int n_vis = 0;
-      for (int kt = 0; kt < kt_end; ++kt) {
-        if (!fwd_visible(p, qt, kt)) continue;
-        ++n_vis;
+      const int n_vis = w ? nv1 : nv0;
+      const uint32_t* my_bits = w ? bits1 : bits0;
+      int kt = SPARSE ? next_visible(my_bits, 0, p.n_qt) : 0;
+      for (int rr = 0; rr < n_vis; ++rr, kt = SPARSE ? next_visible(my_bits, kt + 1, p.n_qt) : kt + 1) {
         if (!mbar_wait_warp(bar(L::B_S + w), sphase, wc)) { ok = false; break; }
         sphase ^= 1u;
         tc_fence_after();
@@ -426,21 +595,22 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
   }
 }
 
-template <int D>
+template <int D, bool SPARSE>
 static int launch_fwd_t(const FwdParams& p, cudaStream_t stream) {
-  using L = FwdLayout<D>;
+  using L = FwdLayout<D, SPARSE>;
   static_assert(L::SMEM_BYTES <= 232448, "shared memory budget");
-  cudaError_t e = cudaFuncSetAttribute(fa_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaError_t e = cudaFuncSetAttribute(fa_fwd_kernel<D, SPARSE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        L::SMEM_BYTES);
   if (e != cudaSuccess) return -4;
   const unsigned grid = static_cast<unsigned>(p.n_pairs) * static_cast<unsigned>(p.BH);
-  fa_fwd_kernel<D><<<grid, L::THREADS, L::SMEM_BYTES, stream>>>(p);
+  fa_fwd_kernel<D, SPARSE><<<grid, L::THREADS, L::SMEM_BYTES, stream>>>(p);
   return cudaGetLastError() == cudaSuccess ? 0 : -4;
 }
 
 int launch_fwd(const FwdParams& p, int d, cudaStream_t stream) {
-  if (d == 128) return launch_fwd_t<128>(p, stream);
-  if (d == 64) return launch_fwd_t<64>(p, stream);
+  const bool sparse = p.mask_kind == MASK_BLOCK;
+  if (d == 128) return sparse ? launch_fwd_t<128, true>(p, stream) : launch_fwd_t<128, false>(p, stream);
+  if (d == 64) return sparse ? launch_fwd_t<64, true>(p, stream) : launch_fwd_t<64, false>(p, stream);
   return -2;
 }
 
