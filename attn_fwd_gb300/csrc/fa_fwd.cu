@@ -235,16 +235,22 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
         if (++slot == L::STAGES) { slot = 0; phase ^= 1u; }
         return true;
       };
+      // Loads go in the order the MMAs consume them, so a FIFO ring of
+      // STAGES slots keeps STAGES - 1 tiles in flight ahead: per round r,
+      // V(a_{r-1}), K(a_r), V(b_{r-1}), K(b_r) -- a tile both query tiles
+      // use is loaded once -- and after the last round the last V tiles.
       int cur0 = next_visible(bits0, 0, p.n_qt), cur1 = next_visible(bits1, 0, p.n_qt);
-      for (int r = 0; r < rounds && ok; ++r) {
-        const int a = cur0, b = cur1;
+      int pa = -1, pb = -1;                 // previous round's key tiles
+      for (int r = 0; r <= rounds && ok; ++r) {
+        const int a = r < rounds ? cur0 : -1, b = r < rounds ? cur1 : -1;
         if (a >= 0) cur0 = next_visible(bits0, a + 1, p.n_qt);
         if (b >= 0) cur1 = next_visible(bits1, b + 1, p.n_qt);
-        const bool two = b >= 0 && b != a;
-        if (a >= 0) ok = load(&p.tm_k, a);
-        if (ok && two) ok = load(&p.tm_k, b);
-        if (ok && a >= 0) ok = load(&p.tm_v, a);
-        if (ok && two) ok = load(&p.tm_v, b);
+        if (pa >= 0) ok = load(&p.tm_v, pa);
+        if (ok && a >= 0) ok = load(&p.tm_k, a);
+        if (ok && pb >= 0 && pb != pa) ok = load(&p.tm_v, pb);
+        if (ok && b >= 0 && b != a) ok = load(&p.tm_k, b);
+        pa = a;
+        pb = b;
       }
       }
       if (!ok) {  // let copies already in flight land before the CTA exits
@@ -367,91 +373,62 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
     } else {
     // Ring slots in load order (the producer's sequence): the n-th tile
     // loaded sits in slot n % STAGES, and its fill barrier completes for the
-    // (n / STAGES)-th time.
+    // (n / STAGES)-th time.  Each slot is released right after the MMAs that
+    // read it.
     auto slot_of = [](int n) { return n % L::STAGES; };
     auto phase_of = [](int n) { return static_cast<uint32_t>((n / L::STAGES) & 1); };
-    int cnt = 0;                       // tiles taken so far
+    auto ready = [&](int n) { return mbar_wait_warp(bar(L::B_FULL + slot_of(n)), phase_of(n), wc); };
+    int cnt = 0;                       // tiles taken so far, in load order
     uint32_t pph0 = 0, pph1 = 0;       // phases of the P barriers
     int done0 = 0, done1 = 0;          // PV products issued per tile
-    // previous round: which tiles had a key tile, and where its V tiles sit
-    bool pa = false, pb = false, ptwo = false;
-    int pv = 0;                        // load index of the previous round's first V tile
     int cur0 = next_visible(bits0, 0, p.n_qt), cur1 = next_visible(bits1, 0, p.n_qt);
-    for (int r = 0; r < rounds && ok; ++r) {
-      const int a = cur0, b = cur1;
+    int pa = -1, pb = -1;              // previous round's key tiles
+    for (int r = 0; r <= rounds && ok; ++r) {
+      const int a = r < rounds ? cur0 : -1, b = r < rounds ? cur1 : -1;
       if (a >= 0) cur0 = next_visible(bits0, a + 1, p.n_qt);
       if (b >= 0) cur1 = next_visible(bits1, b + 1, p.n_qt);
-      const bool two = b >= 0 && b != a;
-      const int nk = (a >= 0 ? 1 : 0) + (two ? 1 : 0);   // K tiles this round (as many V tiles)
-      const int k0 = cnt;                                  // first K tile of this round
-      const int kb_n = two ? k0 + nk - 1 : k0;             // the K tile tile 1 uses
-      if (!(ok = mbar_wait_warp(bar(L::B_FULL + slot_of(k0)), phase_of(k0), wc))) break;
-      if (two && a >= 0 && !(ok = mbar_wait_warp(bar(L::B_FULL + slot_of(k0 + 1)), phase_of(k0 + 1), wc))) break;
-      if (pa || pb) {
-        if (!(ok = mbar_wait_warp(bar(L::B_FULL + slot_of(pv)), phase_of(pv), wc))) break;
-        if (pa && pb && ptwo && !(ok = mbar_wait_warp(bar(L::B_FULL + slot_of(pv + 1)), phase_of(pv + 1), wc))) break;
-      }
-      tc_fence_after();
+      const bool vshared = pb >= 0 && pb == pa;   // tile 1 reuses tile 0's V of the previous round
+      const bool kshared = b >= 0 && b == a;      // and its K of this round
+      const int nva = pa >= 0 ? cnt++ : -1;
+      const int nka = a >= 0 ? cnt++ : -1;
+      const int nvb = pb >= 0 ? (vshared ? nva : cnt++) : -1;
+      const int nkb = b >= 0 ? (kshared ? nka : cnt++) : -1;
       // tile 0: PV of the previous round, then S of this round
-      if (pa) {
+      if (pa >= 0) {
+        if (!(ok = ready(nva))) break;
         if (!(ok = mbar_wait_warp(bar(L::B_P + 0), pph0, wc))) break;
         pph0 ^= 1u;
         tc_fence_after();
-        issue_pv(L::O_COL0, L::S_COL0, slot_of(pv), done0 > 0);
+        issue_pv(L::O_COL0, L::S_COL0, slot_of(nva), done0 > 0);
         if (++done0 == nv0) mma_commit_elect(bar(L::B_O + 0));
+        if (!vshared) mma_commit_elect(bar(L::B_EMPTY + slot_of(nva)));
       }
       if (a >= 0) {
-        issue_s(dq0, L::S_COL0, slot_of(k0));
+        if (!(ok = ready(nka))) break;
+        tc_fence_after();
+        issue_s(dq0, L::S_COL0, slot_of(nka));
         mma_commit_elect(bar(L::B_S + 0));
+        if (!kshared) mma_commit_elect(bar(L::B_EMPTY + slot_of(nka)));
       }
-      // tile 1 (its V tile of the previous round is the last V tile loaded then)
-      if (pb) {
+      // tile 1
+      if (pb >= 0) {
+        if (!vshared && !(ok = ready(nvb))) break;
         if (!(ok = mbar_wait_warp(bar(L::B_P + 1), pph1, wc))) break;
         pph1 ^= 1u;
         tc_fence_after();
-        issue_pv(L::O_COL1, L::S_COL1, slot_of(pv + ((pa && ptwo) ? 1 : 0)), done1 > 0);
+        issue_pv(L::O_COL1, L::S_COL1, slot_of(nvb), done1 > 0);
         if (++done1 == nv1) mma_commit_elect(bar(L::B_O + 1));
+        mma_commit_elect(bar(L::B_EMPTY + slot_of(nvb)));
       }
       if (b >= 0) {
-        issue_s(dq1, L::S_COL1, slot_of(kb_n));
+        if (!kshared && !(ok = ready(nkb))) break;
+        tc_fence_after();
+        issue_s(dq1, L::S_COL1, slot_of(nkb));
         mma_commit_elect(bar(L::B_S + 1));
+        mma_commit_elect(bar(L::B_EMPTY + slot_of(nkb)));
       }
-      // release this round's K slots and the previous round's V slots
-      for (int j = 0; j < nk; ++j) mma_commit_elect(bar(L::B_EMPTY + slot_of(k0 + j)));
-      if (pa || pb) {
-        mma_commit_elect(bar(L::B_EMPTY + slot_of(pv)));
-        if (pa && pb && ptwo) mma_commit_elect(bar(L::B_EMPTY + slot_of(pv + 1)));
-      }
-      pa = a >= 0;
-      pb = b >= 0;
-      ptwo = two;
-      pv = k0 + nk;
-      cnt = k0 + 2 * nk;
-    }
-    // the last round's PV products
-    if (ok && (pa || pb)) {
-      ok = mbar_wait_warp(bar(L::B_FULL + slot_of(pv)), phase_of(pv), wc);
-      if (ok && pa && pb && ptwo) ok = mbar_wait_warp(bar(L::B_FULL + slot_of(pv + 1)), phase_of(pv + 1), wc);
-      if (ok && pa) {
-        ok = mbar_wait_warp(bar(L::B_P + 0), pph0, wc);
-        if (ok) {
-          tc_fence_after();
-          issue_pv(L::O_COL0, L::S_COL0, slot_of(pv), done0 > 0);
-          mma_commit_elect(bar(L::B_O + 0));
-        }
-      }
-      if (ok && pb) {
-        ok = mbar_wait_warp(bar(L::B_P + 1), pph1, wc);
-        if (ok) {
-          tc_fence_after();
-          issue_pv(L::O_COL1, L::S_COL1, slot_of(pv + ((pa && ptwo) ? 1 : 0)), done1 > 0);
-          mma_commit_elect(bar(L::B_O + 1));
-        }
-      }
-      if (ok) {
-        mma_commit_elect(bar(L::B_EMPTY + slot_of(pv)));
-        if (pa && pb && ptwo) mma_commit_elect(bar(L::B_EMPTY + slot_of(pv + 1)));
-      }
+      pa = a;
+      pb = b;
     }
     }
     // nothing may be in flight when tensor memory is released
