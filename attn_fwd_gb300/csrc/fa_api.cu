@@ -94,6 +94,9 @@ int make_map_bf16(CUtensorMap* m, const void* ptr, int BH, int N, int d, int box
   return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
 }
 
+// 128-row tiles covering N rows (the last one may be ragged).
+int tiles(int N) { return (N + fa::TILE - 1) / fa::TILE; }
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // Shape and scalar checks shared by every compute entry point.
@@ -102,7 +105,6 @@ int check_shape(int B, int H, int N, int d) {
   const long long elems = static_cast<long long>(B) * H * N * d;
   if (elems >= (1ll << 31)) return FA_ERR_INVALID;
   if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
-  if (N % fa::TILE != 0) return FA_ERR_UNSUPPORTED;
   return FA_OK;
 }
 
@@ -114,19 +116,37 @@ int check_ptrs(std::initializer_list<const void*> ps) {
   return FA_OK;
 }
 
+// Backward workspace: the fp32 dQ accumulator [B*H][N][d], then -D and
+// -LSE * log2(e), each [B*H][npad] with every head's row padded to a multiple
+// of 128 (zeros past N), each region 256-byte aligned.
 struct Workspace {
   float* dq_acc;
-  float* dvec;
+  float* nd;
+  float* nlse;
+  int npad;
 };
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
+int padded(int N) { return tiles(N) * fa::TILE; }
+
+size_t workspace_bytes(int B, int H, int N, int d) {
+  const size_t rows = static_cast<size_t>(B) * H * N;
+  const size_t prows = static_cast<size_t>(B) * H * padded(N);
+  return align256(rows * d * sizeof(float)) + 2 * align256(prows * sizeof(float));
+}
+
 Workspace carve(void* ws, int B, int H, int N, int d) {
   const size_t rows = static_cast<size_t>(B) * H * N;
+  const size_t prows = static_cast<size_t>(B) * H * padded(N);
   char* base = static_cast<char*>(ws);
   Workspace w;
+  w.npad = padded(N);
   w.dq_acc = reinterpret_cast<float*>(base);
-  w.dvec = reinterpret_cast<float*>(base + align256(rows * d * sizeof(float)));
+  base += align256(rows * d * sizeof(float));
+  w.nd = reinterpret_cast<float*>(base);
+  base += align256(prows * sizeof(float));
+  w.nlse = reinterpret_cast<float*>(base);
   return w;
 }
 
@@ -137,7 +157,7 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, c
   if (mask_kind == fa::MASK_BLOCK && block_mask == nullptr) return FA_ERR_INVALID;
   if ((rc = check_shape(B, H, N, d)) != FA_OK) return rc;
   if ((rc = check_scale(scale)) != FA_OK) return rc;
-  if (mask_kind == fa::MASK_BLOCK && N / fa::TILE > fa::MAX_SPARSE_TILES) return FA_ERR_UNSUPPORTED;
+  if (mask_kind == fa::MASK_BLOCK && tiles(N) > fa::MAX_SPARSE_TILES) return FA_ERR_UNSUPPORTED;
   int* status = nullptr;
   if ((rc = device_ready(&status)) != FA_OK) return rc;
   if ((rc = encoder_ready()) != FA_OK) return rc;
@@ -155,7 +175,7 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, c
   p.timeout_ns = g_timeout_ns.load(std::memory_order_relaxed);
   p.N = N;
   p.BH = BH;
-  p.n_qt = N / fa::TILE;
+  p.n_qt = tiles(N);
   p.n_pairs = (p.n_qt + 1) / 2;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.mask_kind = mask_kind;
@@ -164,16 +184,17 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, c
   return fa::launch_fwd(p, d, reinterpret_cast<cudaStream_t>(stream));
 }
 
-int bwd_main_impl(const void* q, const void* k, const void* v, const void* dout, const float* lse,
-                  const uint8_t* block_mask, void* dk, void* dv, void* workspace, int B, int H, int N, int d,
-                  float scale, int mask_kind, fa_stream_t stream) {
+int bwd_main_impl(const void* q, const void* k, const void* v, const void* dout, const uint8_t* block_mask,
+                  void* dk, void* dv, void* workspace, int B, int H, int N, int d, float scale, int mask_kind,
+                  fa_stream_t stream) {
   int rc;
-  if ((rc = check_ptrs({q, k, v, dout, lse, dk, dv, workspace})) != FA_OK) return rc;
+  if ((rc = check_ptrs({q, k, v, dout, dk, dv, workspace})) != FA_OK) return rc;
   if (mask_kind < 0 || mask_kind > 2) return FA_ERR_INVALID;
   if (mask_kind == fa::MASK_BLOCK && block_mask == nullptr) return FA_ERR_INVALID;
   if ((rc = check_shape(B, H, N, d)) != FA_OK) return rc;
   if ((rc = check_scale(scale)) != FA_OK) return rc;
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return FA_ERR_INVALID;
+  if (mask_kind == fa::MASK_BLOCK && tiles(N) > fa::MAX_SPARSE_TILES) return FA_ERR_UNSUPPORTED;
   int* status = nullptr;
   if ((rc = device_ready(&status)) != FA_OK) return rc;
   if ((rc = encoder_ready()) != FA_OK) return rc;
@@ -186,8 +207,8 @@ int bwd_main_impl(const void* q, const void* k, const void* v, const void* dout,
       make_map_bf16(&p.tm_k, k, BH, N, d, fa::TILE) != FA_OK || make_map_bf16(&p.tm_v, v, BH, N, d, fa::TILE) != FA_OK)
     return FA_ERR_CUDA;
   Workspace w = carve(workspace, B, H, N, d);
-  p.lse = lse;
-  p.dvec = w.dvec;
+  p.nlse = w.nlse;
+  p.nd = w.nd;
   p.dq_acc = w.dq_acc;
   p.dk = static_cast<__nv_bfloat16*>(dk);
   p.dv = static_cast<__nv_bfloat16*>(dv);
@@ -195,8 +216,9 @@ int bwd_main_impl(const void* q, const void* k, const void* v, const void* dout,
   p.status = status;
   p.timeout_ns = g_timeout_ns.load(std::memory_order_relaxed);
   p.N = N;
+  p.npad = w.npad;
   p.BH = BH;
-  p.n_kt = N / fa::TILE;
+  p.n_kt = tiles(N);
   p.scale = scale;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.mask_kind = mask_kind;
@@ -205,17 +227,18 @@ int bwd_main_impl(const void* q, const void* k, const void* v, const void* dout,
   return fa::launch_bwd_main(p, d, reinterpret_cast<cudaStream_t>(stream));
 }
 
-int preprocess_impl(const void* o, const void* dout, void* workspace, int B, int H, int N, int d,
+int preprocess_impl(const void* o, const void* dout, const float* lse, void* workspace, int B, int H, int N, int d,
                     fa_stream_t stream) {
   int rc;
-  if ((rc = check_ptrs({o, dout, workspace})) != FA_OK) return rc;
+  if ((rc = check_ptrs({o, dout, lse, workspace})) != FA_OK) return rc;
   if ((rc = check_shape(B, H, N, d)) != FA_OK) return rc;
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return FA_ERR_INVALID;
   int* status = nullptr;
   if ((rc = device_ready(&status)) != FA_OK) return rc;
   Workspace w = carve(workspace, B, H, N, d);
   return fa::launch_bwd_preprocess(static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dout),
-                                   w.dvec, w.dq_acc, B * H * N, d, reinterpret_cast<cudaStream_t>(stream));
+                                   lse, w.nd, w.nlse, w.dq_acc, B * H, N, w.npad, d,
+                                   reinterpret_cast<cudaStream_t>(stream));
 }
 
 int convert_impl(const void* workspace, void* dq, int B, int H, int N, int d, float scale, fa_stream_t stream) {
@@ -241,8 +264,9 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* o, const v
   if (mask_kind == fa::MASK_BLOCK && block_mask == nullptr) return FA_ERR_INVALID;
   if ((rc = check_shape(B, H, N, d)) != FA_OK) return rc;
   if ((rc = check_scale(scale)) != FA_OK) return rc;
-  if ((rc = preprocess_impl(o, dout, workspace, B, H, N, d, stream)) != FA_OK) return rc;
-  if ((rc = bwd_main_impl(q, k, v, dout, lse, block_mask, dk, dv, workspace, B, H, N, d, scale, mask_kind,
+  if (mask_kind == fa::MASK_BLOCK && tiles(N) > fa::MAX_SPARSE_TILES) return FA_ERR_UNSUPPORTED;
+  if ((rc = preprocess_impl(o, dout, lse, workspace, B, H, N, d, stream)) != FA_OK) return rc;
+  if ((rc = bwd_main_impl(q, k, v, dout, block_mask, dk, dv, workspace, B, H, N, d, scale, mask_kind,
                           stream)) != FA_OK)
     return rc;
   return convert_impl(workspace, dq, B, H, N, d, scale, stream);
@@ -285,7 +309,7 @@ const char* fa_status_string(int status) {
   switch (status) {
     case FA_OK: return "FA_OK";
     case FA_ERR_INVALID: return "FA_ERR_INVALID: invalid argument";
-    case FA_ERR_UNSUPPORTED: return "FA_ERR_UNSUPPORTED: head dim must be 64 or 128 and N a multiple of 128";
+    case FA_ERR_UNSUPPORTED: return "FA_ERR_UNSUPPORTED: head dim must be 64 or 128 (block masks: N <= 131072)";
     case FA_ERR_ARCH: return "FA_ERR_ARCH: device is not compute capability 10.3";
     case FA_ERR_LAUNCH: return "FA_ERR_LAUNCH: kernel launch failed";
     case FA_ERR_TIMEOUT: return "FA_ERR_TIMEOUT: a kernel wait exceeded the wait timeout";
@@ -308,8 +332,7 @@ int fa_fwd_blocksparse(const void* q, const void* k, const void* v, void* o, flo
 size_t fa_bwd_workspace_bytes(int B, int H, int N, int d) {
   if (B < 1 || H < 1 || N < 1 || d < 1) return 0;
   if (static_cast<long long>(B) * H * N * d >= (1ll << 31)) return 0;
-  const size_t rows = static_cast<size_t>(B) * H * N;
-  return align256(rows * d * sizeof(float)) + align256(rows * sizeof(float));
+  return workspace_bytes(B, H, N, d);
 }
 
 int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse, void* dq,
@@ -326,15 +349,15 @@ int fa_bwd_blocksparse(const void* q, const void* k, const void* v, const void* 
                   stream);
 }
 
-int fa_bwd_preprocess(const void* o, const void* dout, void* workspace, int B, int H, int N, int d,
+int fa_bwd_preprocess(const void* o, const void* dout, const float* lse, void* workspace, int B, int H, int N, int d,
                       fa_stream_t stream) {
-  return preprocess_impl(o, dout, workspace, B, H, N, d, stream);
+  return preprocess_impl(o, dout, lse, workspace, B, H, N, d, stream);
 }
 
-int fa_bwd_main(const void* q, const void* k, const void* v, const void* dout, const float* lse,
-                const uint8_t* block_mask, void* dk, void* dv, void* workspace, int B, int H, int N, int d,
-                float scale, int mask_kind, fa_stream_t stream) {
-  return bwd_main_impl(q, k, v, dout, lse, block_mask, dk, dv, workspace, B, H, N, d, scale, mask_kind, stream);
+int fa_bwd_main(const void* q, const void* k, const void* v, const void* dout, const uint8_t* block_mask, void* dk,
+                void* dv, void* workspace, int B, int H, int N, int d, float scale, int mask_kind,
+                fa_stream_t stream) {
+  return bwd_main_impl(q, k, v, dout, block_mask, dk, dv, workspace, B, H, N, d, scale, mask_kind, stream);
 }
 
 int fa_bwd_dq_convert(const void* workspace, void* dq, int B, int H, int N, int d, float scale, fa_stream_t stream) {

@@ -139,6 +139,43 @@ __device__ __forceinline__ void mbar_drain_b(uint32_t bar, uint32_t parity, uint
   }
 }
 
+// P^T and dS^T of one key row over 32 query columns c0 .. c0+31 of a step:
+// P = exp2(S^T * scale * log2 e - LSE * log2 e), dS = P (dP - D), packed as
+// bf16 pairs.  nlse and nd hold -LSE * log2 e and -D per query column.
+// MASKED: P = 0 where the query q (q_base + column) is at or past q_end, or,
+// causal, where q < key.
+template <bool MASKED>
+__device__ __forceinline__ void recompute32(const uint32_t (&sr)[32], const uint32_t (&dr)[32], const float* nlse,
+                                            const float* nd, int c0, float2 sl2v, int q_base, int q_end, int key,
+                                            bool causal, uint32_t (&pt_pk)[16], uint32_t (&ds_pk)[16]) {
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {                        // 8 queries per group
+    const int cq = c0 + 8 * j;
+    const float4 l0 = *reinterpret_cast<const float4*>(nlse + cq);
+    const float4 l1 = *reinterpret_cast<const float4*>(nlse + cq + 4);
+    const float4 d0 = *reinterpret_cast<const float4*>(nd + cq);
+    const float4 d1 = *reinterpret_cast<const float4*>(nd + cq + 4);
+    const float2 nl[4] = {make_float2(l0.x, l0.y), make_float2(l0.z, l0.w), make_float2(l1.x, l1.y),
+                          make_float2(l1.z, l1.w)};
+    const float2 ndv[4] = {make_float2(d0.x, d0.y), make_float2(d0.z, d0.w), make_float2(d1.x, d1.y),
+                           make_float2(d1.z, d1.w)};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int k = 8 * j + 2 * e;                     // register index within the 32 columns
+      const float2 x = ffma2(make_float2(__uint_as_float(sr[k]), __uint_as_float(sr[k + 1])), sl2v, nl[e]);
+      float2 pv = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+      if constexpr (MASKED) {
+        const int q0 = q_base + cq + 2 * e;
+        if (!(q0 < q_end && (!causal || q0 >= key))) pv.x = 0.f;
+        if (!(q0 + 1 < q_end && (!causal || q0 + 1 >= key))) pv.y = 0.f;
+      }
+      const float2 ds = fmul2(pv, fadd2(make_float2(__uint_as_float(dr[k]), __uint_as_float(dr[k + 1])), ndv[e]));
+      pt_pk[4 * j + e] = pack_bf16x2(pv.x, pv.y);
+      ds_pk[4 * j + e] = pack_bf16x2(ds.x, ds.y);
+    }
+  }
+}
+
 template <int D>
 __global__ void __launch_bounds__(448, 1) fa_bwd_kernel(const __grid_constant__ BwdParams p) {
   using L = BwdLayout<D>;
@@ -162,7 +199,7 @@ __global__ void __launch_bounds__(448, 1) fa_bwd_kernel(const __grid_constant__ 
   const int heads_here = min(band_heads, p.BH - band * band_heads);
   const int kt = in_band / heads_here;
   const int bh = band * band_heads + in_band % heads_here;
-  const int n_qi = p.N / BQ;
+  const int n_qi = (p.N + BQ - 1) / BQ;
   const int qi_begin = (p.mask_kind == MASK_CAUSAL) ? (kt * TILE) / BQ : 0;
   uint16_t* list = reinterpret_cast<uint16_t*>(smem + L::LIST_OFF);
   int* list_count = reinterpret_cast<int*>(smem + L::LIST_OFF + MAX_SPARSE_TILES * 2);
@@ -233,9 +270,12 @@ __global__ void __launch_bounds__(448, 1) fa_bwd_kernel(const __grid_constant__ 
           tma_load_3d(sb + L::ST_Q + c * L::Q_CHUNK, &p.tm_q, fb, c * 64, qi * BQ, bh, pol_last);
           tma_load_3d(sb + L::ST_DO + c * L::Q_CHUNK, &p.tm_do, fb, c * 64, qi * BQ, bh, pol_last);
         }
-        const size_t row0 = static_cast<size_t>(bh) * p.N + static_cast<size_t>(qi) * BQ;
-        bulk_load(sb + L::ST_LSE, p.lse + row0, BQ * 4, fb);
-        bulk_load(sb + L::ST_DV, p.dvec + row0, BQ * 4, fb);
+        // -LSE * log2 e and -D of the step's query rows (rows past N are zero;
+        // each head's row is padded to a multiple of 128, so the copy stays in
+        // bounds and 16-byte aligned)
+        const size_t row0 = static_cast<size_t>(bh) * p.npad + static_cast<size_t>(qi) * BQ;
+        bulk_load(sb + L::ST_LSE, p.nlse + row0, BQ * 4, fb);
+        bulk_load(sb + L::ST_DV, p.nd + row0, BQ * 4, fb);
         ++issued[st];
       }
       if (!ok) {
@@ -365,7 +405,6 @@ __global__ void __launch_bounds__(448, 1) fa_bwd_kernel(const __grid_constant__ 
     const int key = kt * TILE + r;
     const uint32_t lane_base = quarter * 32;
     const float2 sl2v = make_float2(p.scale_log2, p.scale_log2);
-    constexpr float LOG2E = 1.4426950408889634f;
     bool ok = true;
     for (int i = 0; i < n_steps && ok; ++i) {
       const int qi = sched.qi(i);
@@ -379,7 +418,9 @@ __global__ void __launch_bounds__(448, 1) fa_bwd_kernel(const __grid_constant__ 
       // d=128: dS^T into buffer i % 2; d=64: P^T in the first half, dS^T in the second
       uint8_t* const pt = area;
       uint8_t* const dsT = L::P_TMEM ? area + (i & 1) * L::PT_BYTES : area + L::PT_BYTES;
-      const bool diag = (p.mask_kind == MASK_CAUSAL) && (qi * BQ < kt * TILE + TILE);
+      const bool causal = p.mask_kind == MASK_CAUSAL;
+      const bool key_ok = key < p.N;
+      const bool need_mask = (causal && qi * BQ < kt * TILE + TILE) || !key_ok || qi * BQ + BQ > p.N;
       constexpr int COLS = BQ / 2;                           // query columns of this warp
 #pragma unroll 1
       for (int c0 = half * COLS; c0 < (half + 1) * COLS; c0 += 32) {
@@ -392,35 +433,13 @@ __global__ void __launch_bounds__(448, 1) fa_bwd_kernel(const __grid_constant__ 
           if (lane == 0) mbar_arrive(bar(L::B_SDP_FREE));
         }
         // pass 1: P and dS for these 32 query columns, in registers only (no
-        // shared-memory stores in between, so the LSE/D loads can be hoisted)
+        // shared-memory stores in between, so the LSE/D loads can be hoisted);
+        // the masked form only for steps that need it (causal diagonal, past N)
         uint32_t pt_pk[16], ds_pk[16];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {                        // 8 queries per group
-          const int cq = c0 + 8 * j;
-          const float4 l0 = *reinterpret_cast<const float4*>(lse + cq);
-          const float4 l1 = *reinterpret_cast<const float4*>(lse + cq + 4);
-          const float4 d0 = *reinterpret_cast<const float4*>(dvec + cq);
-          const float4 d1 = *reinterpret_cast<const float4*>(dvec + cq + 4);
-          const float2 nl[4] = {make_float2(-l0.x * LOG2E, -l0.y * LOG2E), make_float2(-l0.z * LOG2E, -l0.w * LOG2E),
-                                make_float2(-l1.x * LOG2E, -l1.y * LOG2E), make_float2(-l1.z * LOG2E, -l1.w * LOG2E)};
-          const float2 nd[4] = {make_float2(-d0.x, -d0.y), make_float2(-d0.z, -d0.w), make_float2(-d1.x, -d1.y),
-                                make_float2(-d1.z, -d1.w)};
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int k = 8 * j + 2 * e;                     // register index within the 32 columns
-            const float2 x = ffma2(make_float2(__uint_as_float(sr[k]), __uint_as_float(sr[k + 1])), sl2v, nl[e]);
-            float2 pv = make_float2(ex2_approx(x.x), ex2_approx(x.y));
-            if (diag) {
-              const int q0 = qi * BQ + cq + 2 * e;
-              if (q0 < key) pv.x = 0.f;
-              if (q0 + 1 < key) pv.y = 0.f;
-            }
-            const float2 ds =
-                fmul2(pv, fadd2(make_float2(__uint_as_float(dr[k]), __uint_as_float(dr[k + 1])), nd[e]));
-            pt_pk[4 * j + e] = pack_bf16x2(pv.x, pv.y);
-            ds_pk[4 * j + e] = pack_bf16x2(ds.x, ds.y);
-          }
-        }
+        if (need_mask)
+          recompute32<true>(sr, dr, lse, dvec, c0, sl2v, qi * BQ, key_ok ? p.N : -1, key, causal, pt_pk, ds_pk);
+        else
+          recompute32<false>(sr, dr, lse, dvec, c0, sl2v, 0, 0, 0, false, pt_pk, ds_pk);
         // pass 2: stores, once the buffers they overwrite have been consumed
         if (c0 == half * COLS) {
           if constexpr (L::P_TMEM) {
@@ -456,6 +475,7 @@ __global__ void __launch_bounds__(448, 1) fa_bwd_kernel(const __grid_constant__ 
       if (lane == 0) mbar_arrive(bar(L::B_DS));
     }
     // ------------------------------------------------- epilogue: dV rows, half the columns each
+    const bool key_ok = key < p.N;                 // rows past N are not stored
     if (ok) {
       constexpr int DC = D / 2;
       __nv_bfloat16* out = p.dv + (static_cast<size_t>(bh) * p.N + static_cast<size_t>(kt) * TILE + r) * D + half * DC;
@@ -470,10 +490,11 @@ __global__ void __launch_bounds__(448, 1) fa_bwd_kernel(const __grid_constant__ 
 #pragma unroll
           for (int e = 0; e < 16; ++e) ow[e] = pack_bf16x2(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1]));
           uint4* dst = reinterpret_cast<uint4*>(out + c);
+          if (key_ok)
 #pragma unroll
-          for (int e = 0; e < 4; ++e) dst[e] = o4[e];
+            for (int e = 0; e < 4; ++e) dst[e] = o4[e];
         }
-      } else if (n_steps == 0) {
+      } else if (n_steps == 0 && key_ok) {
         uint4* dst = reinterpret_cast<uint4*>(out);
 #pragma unroll
         for (int e = 0; e < DC / 8; ++e) dst[e] = make_uint4(0, 0, 0, 0);
@@ -498,11 +519,19 @@ __global__ void __launch_bounds__(448, 1) fa_bwd_kernel(const __grid_constant__ 
       if constexpr (L::DQ_T) {
         // lane t holds head-dim column t of dQ for the BQ = 64 queries of the step
         float* dst = p.dq_acc + row0 * D + t;
+        const int c_lim = p.N - qi * BQ;          // query rows of the step inside N
+        if (c_lim >= 64) {
 #pragma unroll
-        for (int c = 0; c < 64; ++c) atomicAdd(dst + static_cast<size_t>(c) * D, __uint_as_float(v[c]));
+          for (int c = 0; c < 64; ++c) atomicAdd(dst + static_cast<size_t>(c) * D, __uint_as_float(v[c]));
+        } else {
+#pragma unroll
+          for (int c = 0; c < 64; ++c)
+            if (c < c_lim) atomicAdd(dst + static_cast<size_t>(c) * D, __uint_as_float(v[c]));
+        }
       } else {
         // lane t holds query row t of the step, 64 head-dim columns
         float4* dst = reinterpret_cast<float4*>(p.dq_acc + (row0 + t) * D);
+        if (qi * BQ + t < p.N)
 #pragma unroll
         for (int c = 0; c < 16; ++c)
           atomicAdd(dst + c, make_float4(__uint_as_float(v[4 * c]), __uint_as_float(v[4 * c + 1]),
@@ -510,6 +539,7 @@ __global__ void __launch_bounds__(448, 1) fa_bwd_kernel(const __grid_constant__ 
       }
     }
     // dK rows (lane = key row), scaled by the chain-rule factor
+    const bool key_ok = kt * TILE + t < p.N;        // rows past N are not stored
     if (ok) {
       __nv_bfloat16* out = p.dk + (static_cast<size_t>(bh) * p.N + static_cast<size_t>(kt) * TILE + t) * D;
       if (n_steps > 0 && mbar_wait_warp(bar(L::B_DONE), 0, wc)) {
@@ -524,10 +554,11 @@ __global__ void __launch_bounds__(448, 1) fa_bwd_kernel(const __grid_constant__ 
           for (int e = 0; e < 16; ++e)
             ow[e] = pack_bf16x2(__uint_as_float(v[2 * e]) * p.scale, __uint_as_float(v[2 * e + 1]) * p.scale);
           uint4* dst = reinterpret_cast<uint4*>(out + c);
+          if (key_ok)
 #pragma unroll
-          for (int e = 0; e < 4; ++e) dst[e] = o4[e];
+            for (int e = 0; e < 4; ++e) dst[e] = o4[e];
         }
-      } else if (n_steps == 0) {
+      } else if (n_steps == 0 && key_ok) {
         uint4* dst = reinterpret_cast<uint4*>(out);
 #pragma unroll
         for (int e = 0; e < D / 8; ++e) dst[e] = make_uint4(0, 0, 0, 0);

@@ -46,8 +46,8 @@ struct BwdParams {
   CUtensorMap tm_k;
   CUtensorMap tm_v;
   CUtensorMap tm_do;
-  const float* lse;          // [B*H][N]
-  const float* dvec;         // [B*H][N], D_i = dO_i . O_i
+  const float* nlse;         // [B*H][npad]: -LSE_i * log2(e), zero past N
+  const float* nd;           // [B*H][npad]: -D_i = -dO_i . O_i, zero past N
   float* dq_acc;             // [B*H][N][d] fp32 accumulator
   __nv_bfloat16* dk;         // [B*H][N][d]
   __nv_bfloat16* dv;         // [B*H][N][d]
@@ -55,16 +55,17 @@ struct BwdParams {
   int* status;
   uint64_t timeout_ns;
   int N;
+  int npad;                  // N rounded up to a multiple of 128
   int BH;
-  int n_kt;                  // N / 128 key tiles
+  int n_kt;                  // ceil(N / 128) key tiles
   float scale;
   float scale_log2;
   int mask_kind;
 };
 
 int launch_fwd(const FwdParams& p, int d, cudaStream_t stream);
-int launch_bwd_preprocess(const __nv_bfloat16* o, const __nv_bfloat16* dout, float* dvec,
-                          float* dq_acc, int rows, int d, cudaStream_t stream);
+int launch_bwd_preprocess(const __nv_bfloat16* o, const __nv_bfloat16* dout, const float* lse, float* nd,
+                          float* nlse, float* dq_acc, int BH, int N, int npad, int d, cudaStream_t stream);
 int launch_bwd_main(const BwdParams& p, int d, cudaStream_t stream);
 int launch_bwd_dq_convert(const float* dq_acc, __nv_bfloat16* dq, long long n, float scale,
                           cudaStream_t stream);

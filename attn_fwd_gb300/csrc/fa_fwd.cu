@@ -461,10 +461,15 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
         uint32_t r[128];
         tmem_ld_x128(s_addr, r);
         float* s = reinterpret_cast<float*>(r);
-        if (p.mask_kind == MASK_CAUSAL && kt == qt) {
+        // keys beyond N (ragged last tile) and, on the causal diagonal, keys
+        // after the query are masked to -inf
+        const bool diag = !SPARSE && p.mask_kind == MASK_CAUSAL && kt == qt;
+        if (diag || (kt + 1) * TILE > p.N) {
+          const int kv_lim = p.N - kt * TILE;
+          const int col_lim = diag ? min(row + 1, kv_lim) : kv_lim;
 #pragma unroll
           for (int c = 0; c < 128; ++c)
-            if (c > row) s[c] = -INFINITY;
+            if (c >= col_lim) s[c] = -INFINITY;
         }
         // row max: 3-input max over four independent chains
         float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
@@ -531,6 +536,8 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
       }
       // ---------------------------------------------------------- epilogue
       if (ok) {
+        // rows beyond N (ragged last query tile) are computed but not stored
+        const bool row_ok = qt * TILE + row < p.N;
         const size_t grow = static_cast<size_t>(bh) * p.N + static_cast<size_t>(qt) * TILE + row;
         __nv_bfloat16* orow = p.o + grow * D;
         if (n_vis > 0) {
@@ -547,13 +554,15 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
 #pragma unroll
               for (int i = 0; i < 16; ++i)
                 pw[i] = pack_bf16x2(__uint_as_float(ov[2 * i]) * inv_l, __uint_as_float(ov[2 * i + 1]) * inv_l);
-              uint4* dst = reinterpret_cast<uint4*>(orow + c);
+              if (row_ok) {
+                uint4* dst = reinterpret_cast<uint4*>(orow + c);
 #pragma unroll
-              for (int i = 0; i < 4; ++i) dst[i] = pkd[i];
+                for (int i = 0; i < 4; ++i) dst[i] = pkd[i];
+              }
             }
-            p.lse[grow] = (m + __log2f(l)) * 0.69314718055994530942f;
+            if (row_ok) p.lse[grow] = (m + __log2f(l)) * 0.69314718055994530942f;
           }
-        } else {
+        } else if (row_ok) {
           // no visible key: O = 0, LSE = -inf
           uint4* dst = reinterpret_cast<uint4*>(orow);
 #pragma unroll

@@ -39,8 +39,8 @@ _SIGS = {
     "fa_bwd_workspace_bytes": (_sz, [_i, _i, _i, _i]),
     "fa_bwd": (_i, [_vp] * 10 + [_i, _i, _i, _i, _f, _i, _vp]),
     "fa_bwd_blocksparse": (_i, [_vp] * 11 + [_i, _i, _i, _i, _f, _vp]),
-    "fa_bwd_preprocess": (_i, [_vp, _vp, _vp, _i, _i, _i, _i, _vp]),
-    "fa_bwd_main": (_i, [_vp] * 9 + [_i, _i, _i, _i, _f, _i, _vp]),
+    "fa_bwd_preprocess": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp]),
+    "fa_bwd_main": (_i, [_vp] * 8 + [_i, _i, _i, _i, _f, _i, _vp]),
     "fa_bwd_dq_convert": (_i, [_vp, _vp, _i, _i, _i, _i, _f, _vp]),
     "fa_bwd_noalloc": (_i, [_vp] * 9 + [_i, _i, _i, _i, _f, _i, _vp]),
     "fa_get_device_error": (_i, [_vp]),
@@ -161,16 +161,16 @@ def fa_bwd_blocksparse(q, k, v, o, do, lse, block_mask, dq, dk, dv, workspace, s
     _check("fa_bwd_blocksparse", rc)
 
 
-def fa_bwd_preprocess(o, do, workspace, stream=None):
+def fa_bwd_preprocess(o, do, lse, workspace, stream=None):
     B, H, N, d = o.shape
-    rc = load().fa_bwd_preprocess(_bf16(o, "o"), _bf16(do, "do"), ctypes.c_void_p(workspace.data_ptr()),
-                                  B, H, N, d, _stream(stream))
+    rc = load().fa_bwd_preprocess(_bf16(o, "o"), _bf16(do, "do"), _f32(lse, "lse"),
+                                  ctypes.c_void_p(workspace.data_ptr()), B, H, N, d, _stream(stream))
     _check("fa_bwd_preprocess", rc)
 
 
-def fa_bwd_main(q, k, v, do, lse, block_mask, dk, dv, workspace, scale, mask_kind, stream=None):
+def fa_bwd_main(q, k, v, do, block_mask, dk, dv, workspace, scale, mask_kind, stream=None):
     B, H, N, d = q.shape
-    rc = load().fa_bwd_main(_bf16(q, "q"), _bf16(k, "k"), _bf16(v, "v"), _bf16(do, "do"), _f32(lse, "lse"),
+    rc = load().fa_bwd_main(_bf16(q, "q"), _bf16(k, "k"), _bf16(v, "v"), _bf16(do, "do"),
                             _mask_ptr(block_mask), _bf16(dk, "dk"), _bf16(dv, "dv"),
                             ctypes.c_void_p(workspace.data_ptr()), B, H, N, d, float(scale), int(mask_kind),
                             _stream(stream))

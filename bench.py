@@ -312,10 +312,10 @@ def run_cuda(args):
         if ev:
             ev[1].record()
         if w.backward:
-            fa.fa_bwd_preprocess(o, do, wsp)
+            fa.fa_bwd_preprocess(o, do, lse, wsp)
             if ev:
                 ev[2].record()
-            fa.fa_bwd_main(q, k, v, do, lse, bm, dk, dv, wsp, w.scale, mask_kind)
+            fa.fa_bwd_main(q, k, v, do, bm, dk, dv, wsp, w.scale, mask_kind)
             if ev:
                 ev[3].record()
             fa.fa_bwd_dq_convert(wsp, dq, w.scale)

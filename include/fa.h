@@ -19,16 +19,17 @@
  * Layout and types (every tensor argument):
  *   q, k, v, o, dout, dq, dk, dv : bf16, contiguous [B, H, N, d], device memory
  *   lse                          : fp32, contiguous [B, H, N], device memory
- *   block_mask                   : uint8, contiguous [N/128, N/128], device
+ *   block_mask                   : uint8, contiguous [nb, nb] with nb = ceil(N/128), device
  *                                  memory, shared by every (b, h); nonzero keeps
  *                                  the 128 x 128 block (query block, key block)
  *   workspace                    : device memory of at least
  *                                  fa_bwd_workspace_bytes(B, H, N, d) bytes,
  *                                  256-byte aligned; its contents on entry do
  *                                  not matter.
- * Supported: d in {64, 128}; N a positive multiple of 128; B, H >= 1;
- * B * H * N * d < 2^31; scale finite and > 0; pointers 16-byte aligned;
- * a device of compute capability 10.3.
+ * Supported: d in {64, 128}; any N >= 1 (the last 128-row tile may be
+ * partial); B, H >= 1; B * H * N * d < 2^31; scale finite and > 0; pointers
+ * 16-byte aligned; a device of compute capability 10.3.  Block masks: N at
+ * most 131072 (1024 tiles per row).
  *
  * Masks: causal keeps key j for query i iff j <= i (equal query and key
  * lengths); key tiles that a mask removes entirely are skipped, never loaded.
@@ -71,7 +72,7 @@ typedef struct CUstream_st *fa_stream_t;
 typedef enum fa_status {
   FA_OK = 0,
   FA_ERR_INVALID = -1,     /* bad argument: null pointer, size, alignment, scale */
-  FA_ERR_UNSUPPORTED = -2, /* valid but not built: head dim other than 64/128, N % 128 != 0 */
+  FA_ERR_UNSUPPORTED = -2, /* valid but not built: head dim other than 64/128, or a block mask longer than 1024 tiles */
   FA_ERR_ARCH = -3,        /* current device is not compute capability 10.3 */
   FA_ERR_LAUNCH = -4,      /* the CUDA runtime refused a launch or attribute call */
   FA_ERR_TIMEOUT = -5,     /* a kernel wait ran past the wait timeout (device status) */
@@ -106,8 +107,9 @@ FA_API int fa_fwd_blocksparse(const void *q, const void *k, const void *v, void 
 
 /*
  * Bytes of device workspace that fa_bwd needs: an fp32 dQ accumulator
- * [B, H, N, d] and the fp32 vector D [B, H, N], each 256-byte aligned.
- * Returns 0 when the sizes are invalid.
+ * [B, H, N, d], then two fp32 vectors [B, H, npad] (npad = N rounded up to a
+ * multiple of 128) holding -D and -LSE * log2(e), each region 256-byte
+ * aligned.  Returns 0 when the sizes are invalid.
  */
 FA_API size_t fa_bwd_workspace_bytes(int B, int H, int N, int d);
 
@@ -128,19 +130,22 @@ FA_API int fa_bwd_blocksparse(const void *q, const void *k, const void *v, const
                        int B, int H, int N, int d, float scale, fa_stream_t stream);
 
 /*
- * Backward stage 1 of 3: D_i = sum_c dO[i,c] O[i,c] in fp32 into the
- * workspace, and the workspace's dQ accumulator set to zero.
+ * Backward stage 1 of 3: D_i = sum_c dO[i,c] O[i,c] in fp32, stored as -D_i
+ * next to -LSE_i * log2(e) (the form stage 2 consumes; zeros for the padding
+ * rows past N), and the workspace's dQ accumulator set to zero.  lse is the
+ * forward's output, read only here.
  */
-FA_API int fa_bwd_preprocess(const void *o, const void *dout, void *workspace,
+FA_API int fa_bwd_preprocess(const void *o, const void *dout, const float *lse, void *workspace,
                       int B, int H, int N, int d, fa_stream_t stream);
 
 /*
- * Backward stage 2 of 3: per 128-key tile, recompute P and accumulate dK, dV
- * (written as bf16) and add dS K into the workspace's dQ accumulator.
+ * Backward stage 2 of 3: per 128-key tile, recompute P from Q, K and the
+ * workspace's LSE, accumulate dK, dV (written as bf16) and add dS K into the
+ * workspace's dQ accumulator.  Needs the workspace as stage 1 left it.
  * mask_kind: 0 none, 1 causal, 2 block (block_mask required).
  */
 FA_API int fa_bwd_main(const void *q, const void *k, const void *v, const void *dout,
-                const float *lse, const uint8_t *block_mask, void *dk, void *dv,
+                const uint8_t *block_mask, void *dk, void *dv,
                 void *workspace, int B, int H, int N, int d, float scale, int mask_kind,
                 fa_stream_t stream);
 
@@ -151,7 +156,8 @@ FA_API int fa_bwd_dq_convert(const void *workspace, void *dq, int B, int H, int 
 /*
  * Size of the device scratch array behind fa_bwd_noalloc: 64 MiB per device.
  * fa_bwd_noalloc accepts a problem when fa_bwd_workspace_bytes(B, H, N, d) is
- * at most this, e.g. B * H * N * d up to about 16.6 million elements.
+ * at most this: B * H * N * d up to about 16.5 million elements at d = 128
+ * and 16.2 million at d = 64 (N a multiple of 128).
  */
 #define FA_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
 

@@ -57,8 +57,11 @@ def test_workspace_bytes(lib):
     import attn_fwd_gb300.fa as fa
     B, H, N, d = 2, 16, 4096, 128
     n = fa.fa_bwd_workspace_bytes(B, H, N, d)
-    assert n >= B * H * N * d * 4 + B * H * N * 4
+    assert n == B * H * N * d * 4 + 2 * B * H * N * 4
     assert n % 256 == 0
+    # -D and -LSE rows are padded to a multiple of 128 per head
+    assert fa.fa_bwd_workspace_bytes(1, 3, 200, 64) == 1 * 3 * 200 * 64 * 4 + 2 * 3072
+    assert fa.fa_bwd_workspace_bytes(1, 1, 1, 64) == 256 + 2 * 512
     assert fa.fa_bwd_workspace_bytes(0, 1, 128, 64) == 0
     assert fa.fa_bwd_workspace_bytes(1 << 20, 1 << 10, 128, 128) == 0   # 2^31 elements or more
 
@@ -73,7 +76,6 @@ ODD = ctypes.c_void_p(4096 + 8)
     ((P, P, P, P, ODD, 1, 1, 128, 64, 0.125, 0), -1),           # misaligned lse
     ((P, P, P, P, P, 0, 1, 128, 64, 0.125, 0), -1),             # B = 0
     ((P, P, P, P, P, 1, 1, 128, 96, 0.125, 0), -2),             # d not built
-    ((P, P, P, P, P, 1, 1, 200, 64, 0.125, 0), -2),             # N % 128 != 0
     ((P, P, P, P, P, 1, 1, 128, 64, float("nan"), 0), -1),      # scale not finite
     ((P, P, P, P, P, 1, 1, 128, 64, -1.0, 0), -1),              # scale <= 0
     ((P, P, P, P, P, 65536, 256, 1024, 128, 0.1, 0), -1),       # 2^31 elements or more
@@ -90,10 +92,13 @@ def test_blocksparse_requires_mask(lib):
 def test_bwd_rejects_bad_arguments(lib):
     ws = ctypes.c_void_p(4096 + 16)       # 16- but not 256-byte aligned
     assert lib.fa_bwd(P, P, P, P, P, P, P, P, P, NULL, 1, 1, 128, 64, 0.125, 0, NULL) == -1
-    assert lib.fa_bwd_main(P, P, P, P, P, NULL, P, P, ws, 1, 1, 128, 64, 0.125, 0, NULL) == -1
-    assert lib.fa_bwd_main(P, P, P, P, P, NULL, P, P, P, 1, 1, 128, 64, 0.125, 7, NULL) == -1
-    assert lib.fa_bwd_main(P, P, P, P, P, NULL, P, P, P, 1, 1, 128, 64, 0.125, 2, NULL) == -1
-    assert lib.fa_bwd_preprocess(P, P, P, 1, 1, 100, 64, NULL) == -2
+    assert lib.fa_bwd_main(P, P, P, P, NULL, P, P, ws, 1, 1, 128, 64, 0.125, 0, NULL) == -1
+    assert lib.fa_bwd_main(P, P, P, P, NULL, P, P, P, 1, 1, 128, 64, 0.125, 7, NULL) == -1
+    assert lib.fa_bwd_main(P, P, P, P, NULL, P, P, P, 1, 1, 128, 64, 0.125, 2, NULL) == -1
+    assert lib.fa_bwd_preprocess(P, P, P, P, 1, 1, 100, 96, NULL) == -2
+    assert lib.fa_bwd_preprocess(P, P, NULL, P, 1, 1, 100, 64, NULL) == -1    # lse required here
+    # block masks are limited to 1024 tiles per row
+    assert lib.fa_fwd_blocksparse(P, P, P, P, P, P, 1, 1, 1024 * 128 + 1, 64, 0.125, NULL) == -2
     assert lib.fa_bwd_dq_convert(P, P, 1, 1, 128, 64, 0.0, NULL) == -1
 
 
