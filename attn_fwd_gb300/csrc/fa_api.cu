@@ -154,10 +154,10 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, c
              int B, int H, int N, int d, float scale, int mask_kind, fa_stream_t stream) {
   int rc;
   if ((rc = check_ptrs({q, k, v, o, lse})) != FA_OK) return rc;
-  if (mask_kind == fa::MASK_BLOCK && block_mask == nullptr) return FA_ERR_INVALID;
+  if ((mask_kind & fa::MASK_BLOCK) && block_mask == nullptr) return FA_ERR_INVALID;
   if ((rc = check_shape(B, H, N, d)) != FA_OK) return rc;
   if ((rc = check_scale(scale)) != FA_OK) return rc;
-  if (mask_kind == fa::MASK_BLOCK && tiles(N) > fa::MAX_SPARSE_TILES) return FA_ERR_UNSUPPORTED;
+  if ((mask_kind & fa::MASK_BLOCK) && tiles(N) > fa::MAX_SPARSE_TILES) return FA_ERR_UNSUPPORTED;
   int* status = nullptr;
   if ((rc = device_ready(&status)) != FA_OK) return rc;
   if ((rc = encoder_ready()) != FA_OK) return rc;
@@ -189,12 +189,12 @@ int bwd_main_impl(const void* q, const void* k, const void* v, const void* dout,
                   fa_stream_t stream) {
   int rc;
   if ((rc = check_ptrs({q, k, v, dout, dk, dv, workspace})) != FA_OK) return rc;
-  if (mask_kind < 0 || mask_kind > 2) return FA_ERR_INVALID;
-  if (mask_kind == fa::MASK_BLOCK && block_mask == nullptr) return FA_ERR_INVALID;
+  if (mask_kind < 0 || mask_kind > 3) return FA_ERR_INVALID;
+  if ((mask_kind & fa::MASK_BLOCK) && block_mask == nullptr) return FA_ERR_INVALID;
   if ((rc = check_shape(B, H, N, d)) != FA_OK) return rc;
   if ((rc = check_scale(scale)) != FA_OK) return rc;
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return FA_ERR_INVALID;
-  if (mask_kind == fa::MASK_BLOCK && tiles(N) > fa::MAX_SPARSE_TILES) return FA_ERR_UNSUPPORTED;
+  if ((mask_kind & fa::MASK_BLOCK) && tiles(N) > fa::MAX_SPARSE_TILES) return FA_ERR_UNSUPPORTED;
   int* status = nullptr;
   if ((rc = device_ready(&status)) != FA_OK) return rc;
   if ((rc = encoder_ready()) != FA_OK) return rc;
@@ -261,10 +261,10 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* o, const v
   int rc;
   // validate everything first so that nothing is enqueued on a bad call
   if ((rc = check_ptrs({q, k, v, o, dout, lse, dq, dk, dv, workspace})) != FA_OK) return rc;
-  if (mask_kind == fa::MASK_BLOCK && block_mask == nullptr) return FA_ERR_INVALID;
+  if ((mask_kind & fa::MASK_BLOCK) && block_mask == nullptr) return FA_ERR_INVALID;
   if ((rc = check_shape(B, H, N, d)) != FA_OK) return rc;
   if ((rc = check_scale(scale)) != FA_OK) return rc;
-  if (mask_kind == fa::MASK_BLOCK && tiles(N) > fa::MAX_SPARSE_TILES) return FA_ERR_UNSUPPORTED;
+  if ((mask_kind & fa::MASK_BLOCK) && tiles(N) > fa::MAX_SPARSE_TILES) return FA_ERR_UNSUPPORTED;
   if ((rc = preprocess_impl(o, dout, lse, workspace, B, H, N, d, stream)) != FA_OK) return rc;
   if ((rc = bwd_main_impl(q, k, v, dout, block_mask, dk, dv, workspace, B, H, N, d, scale, mask_kind,
                           stream)) != FA_OK)
@@ -325,8 +325,9 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
 }
 
 int fa_fwd_blocksparse(const void* q, const void* k, const void* v, void* o, float* lse, const uint8_t* block_mask,
-                       int B, int H, int N, int d, float scale, fa_stream_t stream) {
-  return fwd_impl(q, k, v, o, lse, block_mask, B, H, N, d, scale, fa::MASK_BLOCK, stream);
+                       int B, int H, int N, int d, float scale, int causal, fa_stream_t stream) {
+  return fwd_impl(q, k, v, o, lse, block_mask, B, H, N, d, scale, causal ? fa::MASK_BLOCK_CAUSAL : fa::MASK_BLOCK,
+                  stream);
 }
 
 size_t fa_bwd_workspace_bytes(int B, int H, int N, int d) {
@@ -344,9 +345,9 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
 
 int fa_bwd_blocksparse(const void* q, const void* k, const void* v, const void* o, const void* dout,
                        const float* lse, const uint8_t* block_mask, void* dq, void* dk, void* dv, void* workspace,
-                       int B, int H, int N, int d, float scale, fa_stream_t stream) {
-  return bwd_impl(q, k, v, o, dout, lse, block_mask, dq, dk, dv, workspace, B, H, N, d, scale, fa::MASK_BLOCK,
-                  stream);
+                       int B, int H, int N, int d, float scale, int causal, fa_stream_t stream) {
+  return bwd_impl(q, k, v, o, dout, lse, block_mask, dq, dk, dv, workspace, B, H, N, d, scale,
+                  causal ? fa::MASK_BLOCK_CAUSAL : fa::MASK_BLOCK, stream);
 }
 
 int fa_bwd_preprocess(const void* o, const void* dout, const float* lse, void* workspace, int B, int H, int N, int d,
@@ -362,6 +363,29 @@ int fa_bwd_main(const void* q, const void* k, const void* v, const void* dout, c
 
 int fa_bwd_dq_convert(const void* workspace, void* dq, int B, int H, int N, int d, float scale, fa_stream_t stream) {
   return convert_impl(workspace, dq, B, H, N, d, scale, stream);
+}
+
+int fa_block_mask_window(uint8_t* mask, int N, int left, int right) {
+  if (mask == nullptr || N < 1 || left < 0 || right < 0) return FA_ERR_INVALID;
+  const int nb = tiles(N);
+  if (nb > fa::MAX_SPARSE_TILES) return FA_ERR_UNSUPPORTED;
+  for (int i = 0; i < nb; ++i)
+    for (int j = 0; j < nb; ++j) mask[static_cast<size_t>(i) * nb + j] = (j - i <= right && i - j <= left) ? 1 : 0;
+  return FA_OK;
+}
+
+int fa_block_mask_dilated(uint8_t* mask, int N, int window, int dilation, int causal) {
+  if (mask == nullptr || N < 1 || window < 0 || dilation < 1) return FA_ERR_INVALID;
+  const int nb = tiles(N);
+  if (nb > fa::MAX_SPARSE_TILES) return FA_ERR_UNSUPPORTED;
+  const long long reach = static_cast<long long>(window) * dilation;
+  for (int i = 0; i < nb; ++i)
+    for (int j = 0; j < nb; ++j) {
+      const int delta = i - j;  // query block minus key block
+      const bool keep = delta % dilation == 0 && (delta < 0 ? -delta : delta) <= reach && (!causal || delta >= 0);
+      mask[static_cast<size_t>(i) * nb + j] = keep ? 1 : 0;
+    }
+  return FA_OK;
 }
 
 int fa_get_device_error(fa_stream_t stream) {

@@ -104,8 +104,9 @@ struct BwdLayout {
 // The query tiles (BQ rows) a key tile visits, in increasing order, as steps
 // 0..count-1.  No mask: all; causal: from the first tile that reaches the
 // key tile's diagonal; block mask: the 128-row query blocks whose mask byte
-// for this key tile is nonzero (compacted once per CTA by one warp into a
-// shared-memory list), each split into 128 / BQ steps.
+// for this key tile is nonzero (with the causal flag, only blocks at or below
+// the diagonal), compacted once per CTA by one warp into a shared-memory list,
+// each split into 128 / BQ steps.
 template <int BQ>
 struct StepSched {
   static constexpr int SUB = TILE / BQ;
@@ -115,7 +116,7 @@ struct StepSched {
   int count;
 
   __device__ __forceinline__ int qi(int i) const {
-    if (mask_kind == MASK_BLOCK) return static_cast<int>(list[i / SUB]) * SUB + i % SUB;
+    if (mask_kind & MASK_BLOCK) return static_cast<int>(list[i / SUB]) * SUB + i % SUB;
     return first + i;
   }
 };
@@ -124,7 +125,8 @@ __device__ __forceinline__ int build_sparse_column(const BwdParams& p, int kt, u
   int n = 0;
   for (int base = 0; base < p.n_kt; base += 32) {
     const int qb = base + static_cast<int>(lane);
-    const bool v = qb < p.n_kt && __ldg(p.block_mask + static_cast<size_t>(qb) * p.n_kt + kt) != 0;
+    const bool v = qb < p.n_kt && (!(p.mask_kind & MASK_CAUSAL) || qb >= kt) &&
+                   __ldg(p.block_mask + static_cast<size_t>(qb) * p.n_kt + kt) != 0;
     const uint32_t m = __ballot_sync(0xffffffffu, v);
     if (v) list[n + __popc(m & ((1u << lane) - 1u))] = static_cast<uint16_t>(qb);
     n += __popc(m);
@@ -203,7 +205,7 @@ __global__ void __launch_bounds__(448, 1) fa_bwd_kernel(const __grid_constant__ 
   const int qi_begin = (p.mask_kind == MASK_CAUSAL) ? (kt * TILE) / BQ : 0;
   uint16_t* list = reinterpret_cast<uint16_t*>(smem + L::LIST_OFF);
   int* list_count = reinterpret_cast<int*>(smem + L::LIST_OFF + MAX_SPARSE_TILES * 2);
-  if (p.mask_kind == MASK_BLOCK && warp == 0) {
+  if ((p.mask_kind & MASK_BLOCK) && warp == 0) {
     const int n = build_sparse_column(p, kt, list, lane);
     if (lane == 0) *list_count = n;
   }
@@ -236,7 +238,7 @@ __global__ void __launch_bounds__(448, 1) fa_bwd_kernel(const __grid_constant__ 
   const uint32_t tmem = *tmem_slot;
   const WaitCtx wc{abort_flag, p.status, p.timeout_ns};
 
-  const int n_steps = p.mask_kind == MASK_BLOCK ? *list_count * StepSched<BQ>::SUB : n_qi - qi_begin;
+  const int n_steps = (p.mask_kind & MASK_BLOCK) ? *list_count * StepSched<BQ>::SUB : n_qi - qi_begin;
   const StepSched<BQ> sched{list, p.mask_kind, qi_begin, n_steps};
 
   if (warp == L::W_TMA) {
@@ -418,7 +420,7 @@ __global__ void __launch_bounds__(448, 1) fa_bwd_kernel(const __grid_constant__ 
       // d=128: dS^T into buffer i % 2; d=64: P^T in the first half, dS^T in the second
       uint8_t* const pt = area;
       uint8_t* const dsT = L::P_TMEM ? area + (i & 1) * L::PT_BYTES : area + L::PT_BYTES;
-      const bool causal = p.mask_kind == MASK_CAUSAL;
+      const bool causal = (p.mask_kind & MASK_CAUSAL) != 0;
       const bool key_ok = key < p.N;
       const bool need_mask = (causal && qi * BQ < kt * TILE + TILE) || !key_ok || qi * BQ + BQ > p.N;
       constexpr int COLS = BQ / 2;                           // query columns of this warp

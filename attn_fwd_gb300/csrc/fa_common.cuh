@@ -9,7 +9,9 @@
 
 namespace fa {
 
-enum MaskKind : int { MASK_NONE = 0, MASK_CAUSAL = 1, MASK_BLOCK = 2 };
+// Mask kinds are bit flags: causal (key j visible to query i iff j <= i) and
+// block (a 128 x 128 block mask); both together keep what both keep.
+enum MaskKind : int { MASK_NONE = 0, MASK_CAUSAL = 1, MASK_BLOCK = 2, MASK_BLOCK_CAUSAL = 3 };
 
 // Tile sizes along the sequence: B_r = B_c = 128 (one tensor-memory lane per
 // query row, one 128-byte swizzle span per 64 head-dim columns).

@@ -76,14 +76,16 @@ constexpr float RESCALE_THRESHOLD = 8.0f;
 
 // Block-sparse masks: which key tiles a query tile visits, as one bit per key
 // tile, copied once per CTA from the mask row into shared memory by one warp
-// (a ballot per 32 tiles).  Roles walk the set bits in increasing order.
+// (a ballot per 32 tiles); with the causal flag, tiles above the diagonal are
+// dropped too.  Roles walk the set bits in increasing order.
 __device__ __forceinline__ void build_sparse_bits(const FwdParams& p, int qt, uint32_t* bits, int* count,
                                                   uint32_t lane) {
   int n = 0;
   const int nw = (p.n_qt + 31) / 32;
   for (int wd = 0; wd < nw; ++wd) {
     const int kt = wd * 32 + static_cast<int>(lane);
-    const bool v = qt < p.n_qt && kt < p.n_qt && __ldg(p.block_mask + static_cast<size_t>(qt) * p.n_qt + kt) != 0;
+    const bool v = qt < p.n_qt && kt < p.n_qt && (!(p.mask_kind & MASK_CAUSAL) || kt <= qt) &&
+                   __ldg(p.block_mask + static_cast<size_t>(qt) * p.n_qt + kt) != 0;
     const uint32_t m = __ballot_sync(0xffffffffu, v);
     if (lane == 0) bits[wd] = m;
     n += __popc(m);
@@ -102,6 +104,13 @@ __device__ __forceinline__ int next_visible(const uint32_t* bits, int from, int 
     m = bits[wd];
   }
   return wd * 32 + __ffs(m) - 1;
+}
+
+// The last visible key tile, or -1.
+__device__ __forceinline__ int last_visible(const uint32_t* bits, int n_kt) {
+  for (int wd = (n_kt + 31) / 32 - 1; wd >= 0; --wd)
+    if (bits[wd]) return wd * 32 + 31 - __clz(bits[wd]);
+  return -1;
 }
 
 // No mask or causal: the two query tiles of a CTA share one key-tile
@@ -135,7 +144,7 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
   const uint32_t lane = lane_id();
   const int bh = blockIdx.x % p.BH;
   int pair = blockIdx.x / p.BH;
-  if (p.mask_kind == MASK_CAUSAL) pair = p.n_pairs - 1 - pair;  // longest rows first
+  if (p.mask_kind & MASK_CAUSAL) pair = p.n_pairs - 1 - pair;  // longest rows first
   const int qt0 = 2 * pair;
   const int qt1 = 2 * pair + 1;
   const int kt_end = (p.mask_kind == MASK_CAUSAL) ? min(qt1, p.n_qt - 1) + 1 : p.n_qt;
@@ -452,24 +461,24 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
       bool ok = true;
       uint32_t sphase = 0;
       const int n_vis = w ? nv1 : nv0;
-      const uint32_t* my_bits = w ? bits1 : bits0;
-      int kt = SPARSE ? next_visible(my_bits, 0, p.n_qt) : 0;
-      for (int rr = 0; rr < n_vis; ++rr, kt = SPARSE ? next_visible(my_bits, kt + 1, p.n_qt) : kt + 1) {
+      // Only the last visited key tile can need a per-element mask: the causal
+      // diagonal and the ragged tile holding key N-1 are each the highest
+      // visible tile index.  Keys at or past last_lim (a column in that tile)
+      // are masked to -inf.
+      const int last_kt = SPARSE ? last_visible(w ? bits1 : bits0, p.n_qt) : n_vis - 1;
+      int last_lim = p.N - last_kt * TILE;
+      if ((p.mask_kind & MASK_CAUSAL) && last_kt == qt) last_lim = min(last_lim, row + 1);
+      for (int rr = 0; rr < n_vis; ++rr) {
         if (!mbar_wait_warp(bar(L::B_S + w), sphase, wc)) { ok = false; break; }
         sphase ^= 1u;
         tc_fence_after();
         uint32_t r[128];
         tmem_ld_x128(s_addr, r);
         float* s = reinterpret_cast<float*>(r);
-        // keys beyond N (ragged last tile) and, on the causal diagonal, keys
-        // after the query are masked to -inf
-        const bool diag = !SPARSE && p.mask_kind == MASK_CAUSAL && kt == qt;
-        if (diag || (kt + 1) * TILE > p.N) {
-          const int kv_lim = p.N - kt * TILE;
-          const int col_lim = diag ? min(row + 1, kv_lim) : kv_lim;
+        if (rr == n_vis - 1 && last_lim < TILE) {
 #pragma unroll
           for (int c = 0; c < 128; ++c)
-            if (c >= col_lim) s[c] = -INFINITY;
+            if (c >= last_lim) s[c] = -INFINITY;
         }
         // row max: 3-input max over four independent chains
         float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
@@ -594,7 +603,7 @@ static int launch_fwd_t(const FwdParams& p, cudaStream_t stream) {
 }
 
 int launch_fwd(const FwdParams& p, int d, cudaStream_t stream) {
-  const bool sparse = p.mask_kind == MASK_BLOCK;
+  const bool sparse = (p.mask_kind & MASK_BLOCK) != 0;
   if (d == 128) return sparse ? launch_fwd_t<128, true>(p, stream) : launch_fwd_t<128, false>(p, stream);
   if (d == 64) return sparse ? launch_fwd_t<64, true>(p, stream) : launch_fwd_t<64, false>(p, stream);
   return -2;

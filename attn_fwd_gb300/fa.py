@@ -25,7 +25,7 @@ FA_ERR_TIMEOUT = -5
 FA_ERR_CUDA = -6
 FA_ERR_SCRATCH = -7
 
-MASK_NONE, MASK_CAUSAL, MASK_BLOCK = 0, 1, 2
+MASK_NONE, MASK_CAUSAL, MASK_BLOCK, MASK_BLOCK_CAUSAL = 0, 1, 2, 3
 
 _lib = None
 _lock = threading.Lock()
@@ -35,14 +35,16 @@ _SIGS = {
     "fa_version": (_i, []),
     "fa_status_string": (ctypes.c_char_p, [_i]),
     "fa_fwd": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp]),
-    "fa_fwd_blocksparse": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _vp]),
+    "fa_fwd_blocksparse": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp]),
     "fa_bwd_workspace_bytes": (_sz, [_i, _i, _i, _i]),
     "fa_bwd": (_i, [_vp] * 10 + [_i, _i, _i, _i, _f, _i, _vp]),
-    "fa_bwd_blocksparse": (_i, [_vp] * 11 + [_i, _i, _i, _i, _f, _vp]),
+    "fa_bwd_blocksparse": (_i, [_vp] * 11 + [_i, _i, _i, _i, _f, _i, _vp]),
     "fa_bwd_preprocess": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp]),
     "fa_bwd_main": (_i, [_vp] * 8 + [_i, _i, _i, _i, _f, _i, _vp]),
     "fa_bwd_dq_convert": (_i, [_vp, _vp, _i, _i, _i, _i, _f, _vp]),
     "fa_bwd_noalloc": (_i, [_vp] * 9 + [_i, _i, _i, _i, _f, _i, _vp]),
+    "fa_block_mask_window": (_i, [_vp, _i, _i, _i]),
+    "fa_block_mask_dilated": (_i, [_vp, _i, _i, _i, _i]),
     "fa_get_device_error": (_i, [_vp]),
     "fa_set_wait_timeout_ns": (_i, [_u64]),
     "fa_debug_wait_timeout": (_i, [_u64, _vp]),
@@ -130,11 +132,11 @@ def fa_fwd(q, k, v, o, lse, scale, causal=False, stream=None):
     _check("fa_fwd", rc)
 
 
-def fa_fwd_blocksparse(q, k, v, o, lse, block_mask, scale, stream=None):
+def fa_fwd_blocksparse(q, k, v, o, lse, block_mask, scale, causal=False, stream=None):
     B, H, N, d = q.shape
     rc = load().fa_fwd_blocksparse(_bf16(q, "q"), _bf16(k, "k"), _bf16(v, "v"), _bf16(o, "o"),
                                    _f32(lse, "lse"), _mask_ptr(block_mask), B, H, N, d, float(scale),
-                                   _stream(stream))
+                                   int(bool(causal)), _stream(stream))
     _check("fa_fwd_blocksparse", rc)
 
 
@@ -151,13 +153,13 @@ def fa_bwd(q, k, v, o, do, lse, dq, dk, dv, workspace, scale, causal=False, stre
     _check("fa_bwd", rc)
 
 
-def fa_bwd_blocksparse(q, k, v, o, do, lse, block_mask, dq, dk, dv, workspace, scale, stream=None):
+def fa_bwd_blocksparse(q, k, v, o, do, lse, block_mask, dq, dk, dv, workspace, scale, causal=False, stream=None):
     B, H, N, d = q.shape
     rc = load().fa_bwd_blocksparse(_bf16(q, "q"), _bf16(k, "k"), _bf16(v, "v"), _bf16(o, "o"),
                                    _bf16(do, "do"), _f32(lse, "lse"), _mask_ptr(block_mask),
                                    _bf16(dq, "dq"), _bf16(dk, "dk"), _bf16(dv, "dv"),
                                    ctypes.c_void_p(workspace.data_ptr()), B, H, N, d, float(scale),
-                                   _stream(stream))
+                                   int(bool(causal)), _stream(stream))
     _check("fa_bwd_blocksparse", rc)
 
 
@@ -194,6 +196,23 @@ def fa_bwd_noalloc(q, k, v, o, do, lse, dq, dk, dv, scale, causal=False, stream=
     _check("fa_bwd_noalloc", rc)
 
 
+def fa_block_mask_window(N, left, right) -> torch.Tensor:
+    """Sliding-window block mask, uint8 [nb, nb] on the host (see include/fa.h)."""
+    nb = (N + 127) // 128
+    m = torch.empty((max(nb, 1), max(nb, 1)), dtype=torch.uint8)
+    _check("fa_block_mask_window", load().fa_block_mask_window(ctypes.c_void_p(m.data_ptr()), N, left, right))
+    return m
+
+
+def fa_block_mask_dilated(N, window, dilation, causal=False) -> torch.Tensor:
+    """Dilated-window block mask, uint8 [nb, nb] on the host (see include/fa.h)."""
+    nb = (N + 127) // 128
+    m = torch.empty((max(nb, 1), max(nb, 1)), dtype=torch.uint8)
+    _check("fa_block_mask_dilated", load().fa_block_mask_dilated(ctypes.c_void_p(m.data_ptr()), N, window,
+                                                                 dilation, int(bool(causal))))
+    return m
+
+
 def fa_get_device_error(stream=None) -> int:
     return load().fa_get_device_error(_stream(stream))
 
@@ -216,7 +235,7 @@ def forward(q, k, v, causal=False, scale=None, block_mask=None, stream=None):
     o = torch.empty_like(q)
     lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
     if block_mask is not None:
-        fa_fwd_blocksparse(q, k, v, o, lse, block_mask, scale, stream)
+        fa_fwd_blocksparse(q, k, v, o, lse, block_mask, scale, causal, stream)
     else:
         fa_fwd(q, k, v, o, lse, scale, causal, stream)
     return o, lse
@@ -236,7 +255,7 @@ def backward(q, k, v, o, lse, do, causal=False, scale=None, block_mask=None, ws=
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     ws = workspace(B, H, N, d, q.device) if ws is None else ws
     if block_mask is not None:
-        fa_bwd_blocksparse(q, k, v, o, do, lse, block_mask, dq, dk, dv, ws, scale, stream)
+        fa_bwd_blocksparse(q, k, v, o, do, lse, block_mask, dq, dk, dv, ws, scale, causal, stream)
     else:
         fa_bwd(q, k, v, o, do, lse, dq, dk, dv, ws, scale, causal, stream)
     return dq, dk, dv

@@ -16,6 +16,8 @@ configurations describe):
 * A block-sparse workload draws its mask from a fresh generator seeded with the
   same seed: ``rand(nb, nb) < p`` per 128x128 block, then every diagonal block
   is switched on.  One mask is shared by all (batch, head) pairs.
+* A sliding-window workload's mask is a band of 128x128 blocks: query block i
+  keeps key blocks i - left .. i + right (no random draw).
 """
 from __future__ import annotations
 
@@ -40,6 +42,7 @@ class Workload:
     backward: bool = True
     amplitude: float = 1.0
     block_sparse_p: float | None = None  # keep-probability of an off-diagonal block
+    window: tuple[int, int] | None = None  # (left, right) extent of a block band
     note: str = field(default="", compare=False)
 
     @property
@@ -48,8 +51,10 @@ class Workload:
 
     @property
     def mask_kind(self) -> str:
+        if self.window is not None:
+            return "causal+window" if self.causal else "window"
         if self.block_sparse_p is not None:
-            return "block"
+            return "causal+block" if self.causal else "block"
         return "causal" if self.causal else "none"
 
 
@@ -72,6 +77,11 @@ WORKLOADS = {
         "fwdbwd_b1h16n8192d128_blocksparse", 1, 16, 8192, 128, seed=4,
         block_sparse_p=0.25,
         note="forward + backward, 128x128 block mask, p=0.25 + diagonal"),
+    # beyond the five: a causal sliding window of 2048 keys (16 blocks)
+    "fwdbwd_b1h16n16384d128_causal_window2k": Workload(
+        "fwdbwd_b1h16n16384d128_causal_window2k", 1, 16, 16384, 128, seed=5, causal=True,
+        window=(15, 0),
+        note="forward + backward, causal, sliding window of 16 key blocks"),
 }
 
 
@@ -100,6 +110,12 @@ def make_block_mask(N: int, seed: int, p: float, block: int = BLOCK) -> torch.Te
     return keep
 
 
+def make_window_mask(N: int, left: int, right: int, block: int = BLOCK) -> torch.Tensor:
+    """Band of blocks as uint8 [nb, nb]: query block i keeps i - left .. i + right."""
+    nb = -(-N // block)
+    return torch.ones((nb, nb), dtype=torch.uint8).tril(right).triu(-left).contiguous()
+
+
 def make_workload_inputs(w: Workload, heads: slice | None = None) -> dict[str, torch.Tensor]:
     """All inputs of a workload (CPU).  ``heads`` optionally keeps a head slice."""
     t = make_qkvdo(w.B, w.H, w.N, w.d, w.seed, w.amplitude, with_dout=w.backward)
@@ -107,4 +123,6 @@ def make_workload_inputs(w: Workload, heads: slice | None = None) -> dict[str, t
         t = {k: v[:, heads].contiguous() for k, v in t.items()}
     if w.block_sparse_p is not None:
         t["block_mask"] = make_block_mask(w.N, w.seed, w.block_sparse_p)
+    if w.window is not None:
+        t["block_mask"] = make_window_mask(w.N, *w.window)
     return t

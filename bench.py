@@ -71,15 +71,27 @@ def whole_job_tflops(world_size: int, flops_per_rank_step: float, ms_per_step: f
 
 
 def _flops(w, density):
+    """With a block mask, `density` already carries the causal halving (see
+    _density), so the causal factor is applied only without one."""
     import oracle
-    f_fwd = oracle.flops(w.B, w.H, w.N, w.d, causal=w.causal, density=density)
-    f_bwd = oracle.flops(w.B, w.H, w.N, w.d, causal=w.causal, backward=True, density=density) if w.backward else 0.0
+    causal = w.causal and density is None
+    f_fwd = oracle.flops(w.B, w.H, w.N, w.d, causal=causal, density=density)
+    f_bwd = oracle.flops(w.B, w.H, w.N, w.d, causal=causal, backward=True, density=density) if w.backward else 0.0
     return f_fwd, f_bwd
 
 
-def _density(t):
+def _density(t, causal=False):
+    """Fraction of the N x N scores a block mask keeps.  With the causal flag,
+    blocks above the diagonal count 0 and diagonal blocks 1/2, the same
+    halving as the causal FLOP convention (all blocks kept -> exactly 1/2)."""
+    import torch
     bm = t.get("block_mask")
-    return None if bm is None else float(bm.float().mean())
+    if bm is None:
+        return None
+    m = bm.float()
+    if not causal:
+        return float(m.mean())
+    return float((torch.tril(m, -1).sum() + 0.5 * torch.diagonal(m).sum()) / m.numel())
 
 
 def _config(w, density, extra=None):
@@ -173,8 +185,7 @@ def _oracle_sample(w, t, budget_s=15.0, max_heads=None):
         if w.backward:
             oracle.backward(q, k, v, t["do"][sl].double().numpy(), w.scale, causal=w.causal, block_mask=bmn)
         heads += 1
-        dens = None if bm is None else float(bm.float().mean())
-        ff, fb = _flops(type(w)(**{**w.__dict__, "B": 1, "H": 1}), dens)
+        ff, fb = _flops(type(w)(**{**w.__dict__, "B": 1, "H": 1}), _density(t, w.causal))
         flops += ff + fb
         el = time.perf_counter() - t0
         if el >= budget_s or (max_heads and heads >= max_heads):
@@ -229,7 +240,7 @@ def run_reference(args):
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": total / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
-            "config": _config(w, _density(t)),
+            "config": _config(w, _density(t, w.causal)),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": _CORES, "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -286,12 +297,12 @@ def run_cuda(args):
 
     w = WORKLOADS[args.workload]
     t = make_workload_inputs(w)
-    density = _density(t)
+    density = _density(t, w.causal)
     f_fwd, f_bwd = _flops(w, density)
     q, k, v = (t[n].to(dev) for n in ("q", "k", "v"))
     do = t["do"].to(dev) if w.backward else None
     bm = t["block_mask"].to(dev) if "block_mask" in t else None
-    mask_kind = fa.MASK_BLOCK if bm is not None else (fa.MASK_CAUSAL if w.causal else fa.MASK_NONE)
+    mask_kind = (fa.MASK_BLOCK if bm is not None else 0) | (fa.MASK_CAUSAL if w.causal else 0)
     o = torch.empty_like(q)
     lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev)
     if w.backward:
@@ -301,7 +312,7 @@ def run_cuda(args):
 
     def fwd():
         if bm is not None:
-            fa.fa_fwd_blocksparse(q, k, v, o, lse, bm, w.scale)
+            fa.fa_fwd_blocksparse(q, k, v, o, lse, bm, w.scale, causal=w.causal)
         else:
             fa.fa_fwd(q, k, v, o, lse, w.scale, causal=w.causal)
 

@@ -99,11 +99,13 @@ FA_API int fa_fwd(const void *q, const void *k, const void *v, void *o, float *l
 /*
  * Forward with a 128 x 128 block mask (block-sparse attention, "FlashAttention"
  * notes, "Block-sparse Flashattention"): blocks whose mask byte is 0 are
- * skipped and add nothing to m, l or O.
+ * skipped and add nothing to m, l or O.  causal != 0 also applies the causal
+ * mask (key j visible to query i iff j <= i and the block is kept): with the
+ * window masks below this is causal sliding-window or dilated attention.
  */
 FA_API int fa_fwd_blocksparse(const void *q, const void *k, const void *v, void *o, float *lse,
                        const uint8_t *block_mask, int B, int H, int N, int d, float scale,
-                       fa_stream_t stream);
+                       int causal, fa_stream_t stream);
 
 /*
  * Bytes of device workspace that fa_bwd needs: an fp32 dQ accumulator
@@ -123,11 +125,11 @@ FA_API int fa_bwd(const void *q, const void *k, const void *v, const void *o, co
            const float *lse, void *dq, void *dk, void *dv, void *workspace,
            int B, int H, int N, int d, float scale, int causal, fa_stream_t stream);
 
-/* Backward with the block mask of fa_fwd_blocksparse. */
+/* Backward with the block mask (and causal flag) of fa_fwd_blocksparse. */
 FA_API int fa_bwd_blocksparse(const void *q, const void *k, const void *v, const void *o,
                        const void *dout, const float *lse, const uint8_t *block_mask,
                        void *dq, void *dk, void *dv, void *workspace,
-                       int B, int H, int N, int d, float scale, fa_stream_t stream);
+                       int B, int H, int N, int d, float scale, int causal, fa_stream_t stream);
 
 /*
  * Backward stage 1 of 3: D_i = sum_c dO[i,c] O[i,c] in fp32, stored as -D_i
@@ -142,7 +144,8 @@ FA_API int fa_bwd_preprocess(const void *o, const void *dout, const float *lse, 
  * Backward stage 2 of 3: per 128-key tile, recompute P from Q, K and the
  * workspace's LSE, accumulate dK, dV (written as bf16) and add dS K into the
  * workspace's dQ accumulator.  Needs the workspace as stage 1 left it.
- * mask_kind: 0 none, 1 causal, 2 block (block_mask required).
+ * mask_kind: 0 none, 1 causal, 2 block (block_mask required), 3 causal and
+ * block.
  */
 FA_API int fa_bwd_main(const void *q, const void *k, const void *v, const void *dout,
                 const uint8_t *block_mask, void *dk, void *dv,
@@ -152,6 +155,27 @@ FA_API int fa_bwd_main(const void *q, const void *k, const void *v, const void *
 /* Backward stage 3 of 3: dQ = bf16(scale * accumulator). */
 FA_API int fa_bwd_dq_convert(const void *workspace, void *dq, int B, int H, int N, int d,
                       float scale, fa_stream_t stream);
+
+/*
+ * Block masks for the sparse patterns that block-sparse attention serves
+ * ("Как работает FlashAttention математически", section 9: block-sparse
+ * FlashAttention for sliding-window and dilated attention), at the 128 x 128
+ * block granularity of fa_fwd_blocksparse.  Host functions: `mask` is HOST
+ * memory of nb * nb bytes, nb = ceil(N / 128), row = query block, written
+ * with 0 / 1; copy it to the device before use.  No GPU is touched.
+ *
+ * fa_block_mask_window: query block i keeps key block j iff
+ *   i - left <= j <= i + right   (left, right >= 0, in blocks).
+ *   right = 0 with causal = 1 in the attention call is causal sliding-window
+ *   attention over the previous `left` blocks and the query's own block.
+ * fa_block_mask_dilated: query block i keeps key block j iff
+ *   j = i + t * dilation for an integer t with |t| <= window (t <= 0 when
+ *   causal != 0)   (window >= 0, dilation >= 1; dilation 1 is the window).
+ * Return FA_OK, FA_ERR_INVALID (null mask, N < 1, negative extents,
+ * dilation < 1) or FA_ERR_UNSUPPORTED (nb > 1024, beyond the kernels' limit).
+ */
+FA_API int fa_block_mask_window(uint8_t *mask, int N, int left, int right);
+FA_API int fa_block_mask_dilated(uint8_t *mask, int N, int window, int dilation, int causal);
 
 /*
  * Size of the device scratch array behind fa_bwd_noalloc: 64 MiB per device.

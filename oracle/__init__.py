@@ -11,8 +11,10 @@ from .attention import (  # noqa: F401
     flops,
     forward,
     forward_rows,
+    dilated_block_mask,
     head_probs,
     merge_stats,
     tiled_forward,
     visible,
+    window_block_mask,
 )

@@ -27,7 +27,11 @@ notes):
 * Masked entries are -inf (they add nothing to m, l or O); [P2]'s block-sparse
   text writes 0, which would not skip anything.
 * Causal: key j is visible to query i iff j <= i (equal query/key lengths).
-* Block-sparse: mask[i // block, j // block] keeps or drops a whole block.
+* Block-sparse: mask[i // block, j // block] keeps or drops a whole block;
+  causal and a block mask together keep what both keep.
+* Sliding-window and dilated patterns are block masks (one bit per block),
+  the granularity at which the pages place them under block-sparse attention;
+  dilated: key block i + t * dilation for |t| <= window.
 * A row with no visible key gets O = 0, LSE = -inf and zero gradients.
 * LSE = m + ln(l), natural log.
 
@@ -62,6 +66,39 @@ def visible(nq: int, nk: int, causal: bool = False, block_mask=None,
         bm = np.asarray(block_mask).astype(bool)
         vis &= bm[rows[:, None] // block, cols[None, :] // block]
     return vis
+
+
+def window_block_mask(N: int, left: int, right: int, block: int = 128) -> np.ndarray:
+    """Sliding window at block granularity, uint8 [nb, nb], nb = ceil(N / block).
+
+    ["Как работает FlashAttention математически" section 9: block-sparse
+    FlashAttention serves sliding-window patterns.]  Query block i keeps the
+    key blocks i - left, ..., i + right that exist.
+    """
+    nb = -(-N // block)
+    m = np.zeros((nb, nb), dtype=np.uint8)
+    for i in range(nb):
+        for j in range(max(0, i - left), min(nb, i + right + 1)):
+            m[i, j] = 1
+    return m
+
+
+def dilated_block_mask(N: int, window: int, dilation: int, causal: bool = False,
+                       block: int = 128) -> np.ndarray:
+    """Dilated window at block granularity, uint8 [nb, nb].
+
+    [Same section: dilated attention as a block-sparse pattern.]  Query block i
+    keeps key blocks i + t * dilation for t = -window .. window (t <= 0 when
+    causal), those that exist.
+    """
+    nb = -(-N // block)
+    m = np.zeros((nb, nb), dtype=np.uint8)
+    for i in range(nb):
+        for t in range(-window, (0 if causal else window) + 1):
+            j = i + t * dilation
+            if 0 <= j < nb:
+                m[i, j] = 1
+    return m
 
 
 # --------------------------------------------------------------------------- #

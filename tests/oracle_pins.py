@@ -265,5 +265,53 @@ def pin_library(orc):
         np.testing.assert_allclose(dv, tv.grad.numpy(), atol=1e-11)
 
 
+def pin_block_masks(orc):
+    """Sliding-window and dilated block masks against library routines
+    (np.tril / np.triu band, np.eye, a parity checkerboard from np.indices),
+    closed-form row counts, and attention-level special cases."""
+    for N, left, right in ((1, 0, 0), (128, 0, 0), (129, 1, 0), (1000, 2, 1), (2048, 3, 5), (4096, 40, 40)):
+        nb = -(-N // 128)
+        band = np.triu(np.tril(np.ones((nb, nb), np.uint8), right), -left)
+        np.testing.assert_array_equal(orc.window_block_mask(N, left, right), band)
+    nb = 12
+    N = nb * 128 - 5                                          # ragged last block
+    np.testing.assert_array_equal(orc.window_block_mask(N, 0, 0), np.eye(nb, dtype=np.uint8))
+    np.testing.assert_array_equal(orc.window_block_mask(N, nb, 0), np.tril(np.ones((nb, nb), np.uint8)))
+    np.testing.assert_array_equal(orc.window_block_mask(N, 0, nb), np.triu(np.ones((nb, nb), np.uint8)))
+    for w in (0, 1, 3):
+        np.testing.assert_array_equal(orc.dilated_block_mask(N, w, 1), orc.window_block_mask(N, w, w))
+        np.testing.assert_array_equal(orc.dilated_block_mask(N, w, 1, causal=True), orc.window_block_mask(N, w, 0))
+    ii, jj = np.indices((nb, nb))
+    np.testing.assert_array_equal(orc.dilated_block_mask(N, nb, 2), ((ii + jj) % 2 == 0).astype(np.uint8))
+    nb2 = 64
+    for w, r in ((1, 2), (3, 4), (2, 7)):
+        m = orc.dilated_block_mask(nb2 * 128, w, r)
+        mc = orc.dilated_block_mask(nb2 * 128, w, r, causal=True)
+        np.testing.assert_array_equal(m, m.T)
+        np.testing.assert_array_equal(mc, np.tril(m))
+        interior = slice(w * r, nb2 - w * r)
+        assert np.all(m[interior].sum(axis=1) == 2 * w + 1)
+        assert np.all(mc[w * r:].sum(axis=1) == w + 1)
+        i2, j2 = np.indices((nb2, nb2))
+        assert np.all(m[i2 - j2 == r] == 1) and np.all(m[i2 - j2 == r + 1] == (1 if r == 1 else 0))
+    # attention level: a causal window over every block is plain causal attention,
+    # and a window of width 0 is causal attention inside each block independently
+    r = _rng(11)
+    blk, nbk = 8, 4
+    N = blk * nbk - 3
+    q, k, v = (r.standard_normal((1, 2, N, 4)) for _ in range(3))
+    full = orc.window_block_mask(N, nbk, 0, block=blk)
+    o_w, l_w = orc.forward(q, k, v, 0.5, causal=True, block_mask=full, block=blk)
+    o_c, l_c = orc.forward(q, k, v, 0.5, causal=True)
+    np.testing.assert_allclose(o_w, o_c, atol=1e-14)
+    np.testing.assert_allclose(l_w, l_c, atol=1e-14)
+    diag = orc.window_block_mask(N, 0, 0, block=blk)
+    o_d, _ = orc.forward(q, k, v, 0.5, causal=True, block_mask=diag, block=blk)
+    for b0 in range(0, N, blk):
+        sl = slice(b0, min(N, b0 + blk))
+        o_b, _ = orc.forward(q[:, :, sl], k[:, :, sl], v[:, :, sl], 0.5, causal=True)
+        np.testing.assert_allclose(o_d[:, :, sl], o_b, atol=1e-14)
+
+
 ALL_PINS = [pin_worked_example, pin_closed_forms, pin_invariants, pin_backward_fd,
-            pin_dvec, pin_backward_rows, pin_library]
+            pin_dvec, pin_backward_rows, pin_library, pin_block_masks]

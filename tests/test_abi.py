@@ -85,8 +85,10 @@ def test_fwd_rejects_bad_arguments(lib, args, expect):
 
 
 def test_blocksparse_requires_mask(lib):
-    assert lib.fa_fwd_blocksparse(P, P, P, P, P, NULL, 1, 1, 128, 64, 0.125, NULL) == -1
-    assert lib.fa_bwd_blocksparse(P, P, P, P, P, P, NULL, P, P, P, P, 1, 1, 128, 64, 0.125, NULL) == -1
+    assert lib.fa_fwd_blocksparse(P, P, P, P, P, NULL, 1, 1, 128, 64, 0.125, 0, NULL) == -1
+    assert lib.fa_fwd_blocksparse(P, P, P, P, P, NULL, 1, 1, 128, 64, 0.125, 1, NULL) == -1
+    assert lib.fa_bwd_blocksparse(P, P, P, P, P, P, NULL, P, P, P, P, 1, 1, 128, 64, 0.125, 0, NULL) == -1
+    assert lib.fa_bwd_main(P, P, P, P, NULL, P, P, P, 1, 1, 128, 64, 0.125, 3, NULL) == -1
 
 
 def test_bwd_rejects_bad_arguments(lib):
@@ -94,11 +96,12 @@ def test_bwd_rejects_bad_arguments(lib):
     assert lib.fa_bwd(P, P, P, P, P, P, P, P, P, NULL, 1, 1, 128, 64, 0.125, 0, NULL) == -1
     assert lib.fa_bwd_main(P, P, P, P, NULL, P, P, ws, 1, 1, 128, 64, 0.125, 0, NULL) == -1
     assert lib.fa_bwd_main(P, P, P, P, NULL, P, P, P, 1, 1, 128, 64, 0.125, 7, NULL) == -1
+    assert lib.fa_bwd_main(P, P, P, P, NULL, P, P, P, 1, 1, 128, 64, 0.125, 4, NULL) == -1
     assert lib.fa_bwd_main(P, P, P, P, NULL, P, P, P, 1, 1, 128, 64, 0.125, 2, NULL) == -1
     assert lib.fa_bwd_preprocess(P, P, P, P, 1, 1, 100, 96, NULL) == -2
     assert lib.fa_bwd_preprocess(P, P, NULL, P, 1, 1, 100, 64, NULL) == -1    # lse required here
     # block masks are limited to 1024 tiles per row
-    assert lib.fa_fwd_blocksparse(P, P, P, P, P, P, 1, 1, 1024 * 128 + 1, 64, 0.125, NULL) == -2
+    assert lib.fa_fwd_blocksparse(P, P, P, P, P, P, 1, 1, 1024 * 128 + 1, 64, 0.125, 0, NULL) == -2
     assert lib.fa_bwd_dq_convert(P, P, 1, 1, 128, 64, 0.0, NULL) == -1
 
 
@@ -117,3 +120,41 @@ def test_valid_call_without_gpu_fails_loudly(lib):
         pytest.skip("a GPU is present")
     rc = lib.fa_fwd(P, P, P, P, P, 1, 1, 128, 64, 0.125, 0, NULL)
     assert rc in (-6, -3)
+
+
+# --------------------------------------------------------------------------- #
+# block-mask generators (host functions: no GPU needed), against the oracle's
+# own construction from the definitions
+# --------------------------------------------------------------------------- #
+@pytest.mark.parametrize("N,left,right", [
+    (1, 0, 0), (128, 3, 0), (300, 1, 1), (1000, 2, 0), (1024, 0, 3), (4096, 5, 2),
+    (8192, 64, 64), (131072, 16, 0),
+])
+def test_window_mask_matches_oracle(lib, N, left, right):
+    import numpy as np
+    import attn_fwd_gb300.fa as fa
+    import oracle
+    got = fa.fa_block_mask_window(N, left, right).numpy()
+    np.testing.assert_array_equal(got, oracle.window_block_mask(N, left, right))
+
+
+@pytest.mark.parametrize("N,window,dilation,causal", [
+    (1, 0, 1, 0), (640, 2, 1, 0), (1000, 3, 2, 1), (4096, 4, 3, 0), (8192, 2, 5, 1),
+    (8192, 100, 7, 0), (20000, 1, 160, 0),
+])
+def test_dilated_mask_matches_oracle(lib, N, window, dilation, causal):
+    import numpy as np
+    import attn_fwd_gb300.fa as fa
+    import oracle
+    got = fa.fa_block_mask_dilated(N, window, dilation, causal).numpy()
+    np.testing.assert_array_equal(got, oracle.dilated_block_mask(N, window, dilation, bool(causal)))
+
+
+def test_mask_generators_reject_bad_arguments(lib):
+    buf = ctypes.create_string_buffer(16)
+    assert lib.fa_block_mask_window(NULL, 128, 1, 1) == -1
+    assert lib.fa_block_mask_window(buf, 0, 1, 1) == -1
+    assert lib.fa_block_mask_window(buf, 128, -1, 1) == -1
+    assert lib.fa_block_mask_dilated(buf, 128, 1, 0, 0) == -1
+    assert lib.fa_block_mask_dilated(buf, 128, -1, 1, 0) == -1
+    assert lib.fa_block_mask_window(buf, 1024 * 128 + 1, 1, 1) == -2

@@ -9,7 +9,7 @@ from tests import oracle_pins as pins
 
 _real = {name: getattr(orc, name) for name in
          ("_scores", "_apply_mask", "_row_softmax", "_softmax_backward", "visible",
-          "forward", "backward", "tiled_forward", "_lse")}
+          "forward", "backward", "tiled_forward", "_lse", "window_block_mask", "dilated_block_mask")}
 
 
 def _m_no_scale(q, k, scale):
@@ -114,6 +114,28 @@ def _m_lse_log2(m, l):
     return np.where(l > 0, m + np.log2(np.where(l > 0, l, 1.0)), -np.inf)
 
 
+def _m_window_right_short(N, left, right, block=128):
+    m = _real["window_block_mask"](N, left, right, block)
+    nb = m.shape[0]
+    for i in range(nb):
+        if right > 0 and i + right < nb:
+            m[i, i + right] = 0                      # the window stops one block early
+    return m
+
+
+def _m_window_swapped(N, left, right, block=128):
+    return _real["window_block_mask"](N, right, left, block)
+
+
+def _m_dilated_no_dilation(N, window, dilation, causal=False, block=128):
+    return _real["dilated_block_mask"](N, window, 1, causal, block)
+
+
+def _m_dilated_causal_flipped(N, window, dilation, causal=False, block=128):
+    m = _real["dilated_block_mask"](N, window, dilation, False, block)
+    return np.triu(m) if causal else m
+
+
 MUTANTS = {
     "scale_dropped": ("_scores", _m_no_scale),
     "scores_transposed": ("_scores", _m_transposed_scores),
@@ -128,6 +150,10 @@ MUTANTS = {
     "dQ_dS_transposed": ("backward", _m_bwd_dq_transposed),
     "tiled_l_rescale_dropped": ("tiled_forward", _m_tiled_l_no_alpha),
     "lse_wrong_base": ("_lse", _m_lse_log2),
+    "window_right_short": ("window_block_mask", _m_window_right_short),
+    "window_sides_swapped": ("window_block_mask", _m_window_swapped),
+    "dilated_without_dilation": ("dilated_block_mask", _m_dilated_no_dilation),
+    "dilated_causal_flipped": ("dilated_block_mask", _m_dilated_causal_flipped),
 }
 
 

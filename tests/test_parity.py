@@ -411,3 +411,74 @@ def test_ragged_outputs_stay_inside_their_rows(fa):
     assert torch.all(obuf[n:] == 3.0) and torch.all(lbuf[B * H * N:] == 3.0)
     for g in grads:
         assert torch.all(g[n:] == 3.0)
+
+
+# --------------------------------------------------------------------------- #
+# sliding-window and dilated block masks, and a block mask with the causal flag
+# (masks from the library's host generators, checked against the oracle's own
+# construction, then both paths run on them)
+# --------------------------------------------------------------------------- #
+PATTERNS = [
+    # B, H, N, d, pattern, args, causal
+    (1, 2, 1000, 64, "window", (2, 0), True),
+    (1, 2, 2048, 128, "window", (3, 1), False),
+    (1, 1, 1500, 128, "dilated", (2, 2), True),
+    (2, 1, 1024, 64, "dilated", (3, 3), False),
+    (1, 2, 777, 128, "window", (1, 0), True),
+    (1, 1, 2560, 128, "random", 0.3, True),
+    (1, 2, 1280, 64, "random", 0.5, True),
+]
+
+
+def _pattern_masks(fa, N, pattern, args):
+    if pattern == "window":
+        return fa.fa_block_mask_window(N, *args), oracle.window_block_mask(N, *args)
+    if pattern == "dilated":
+        return (fa.fa_block_mask_dilated(N, *args, causal=False),
+                oracle.dilated_block_mask(N, *args, causal=False))
+    nb = (N + 127) // 128
+    g = torch.Generator().manual_seed(N)
+    bm = (torch.rand((nb, nb), generator=g) < args).to(torch.uint8)
+    bm.fill_diagonal_(1)
+    return bm, bm.numpy()
+
+
+@pytest.mark.parametrize("B,H,N,d,pattern,args,causal", PATTERNS)
+def test_window_dilated_and_causal_block_masks(fa, B, H, N, d, pattern, args, causal):
+    bm, bm_ref = _pattern_masks(fa, N, pattern, args)
+    np.testing.assert_array_equal(bm.numpy(), bm_ref)
+    t = make_qkvdo(B, H, N, d, seed=60 + N)
+    scale = 1 / math.sqrt(d)
+    q, k, v, do = (_dev(t[n]) for n in ("q", "k", "v", "do"))
+    o, lse = fa.forward(q, k, v, causal=causal, scale=scale, block_mask=_dev(bm))
+    dq, dk, dv = fa.backward(q, k, v, o, lse, do, causal=causal, scale=scale, block_mask=_dev(bm))
+    _check_device_status(fa)
+    f64 = {n: _np64(t[n]) for n in ("q", "k", "v", "do")}
+    what = f"N={N} d={d} {pattern}{args} causal={causal}"
+    ro, rl = oracle.forward(f64["q"], f64["k"], f64["v"], scale, causal=causal, block_mask=bm_ref)
+    _check_fwd(o, lse, ro, rl, what)
+    ref = oracle.backward(f64["q"], f64["k"], f64["v"], f64["do"], scale, causal=causal, block_mask=bm_ref)[:3]
+    _check_bwd((dq, dk, dv), ref, what)
+
+
+def test_causal_window_long_sequence_sampled_rows(fa):
+    """Causal sliding window (16 blocks back) at N = 16384, d = 128: sampled
+    query rows of two heads through the oracle, forward and backward dQ."""
+    B, H, N, d = 1, 2, 16384, 128
+    t = make_qkvdo(B, H, N, d, seed=77)
+    scale = 1 / math.sqrt(d)
+    bm = fa.fa_block_mask_window(N, 16, 0)
+    q, k, v, do = (_dev(t[n]) for n in ("q", "k", "v", "do"))
+    o, lse = fa.forward(q, k, v, causal=True, scale=scale, block_mask=_dev(bm))
+    dq, dk, dv = fa.backward(q, k, v, o, lse, do, causal=True, scale=scale, block_mask=_dev(bm))
+    _check_device_status(fa)
+    bm_ref = oracle.window_block_mask(N, 16, 0)
+    rows = np.array([0, 1, 127, 128, 2047, 2048, 5000, 9999, 16256, 16383])
+    for h in range(H):
+        f64 = {n: _np64(t[n][:, h:h + 1]) for n in ("q", "k", "v", "do")}
+        ro, rl = oracle.forward_rows(f64["q"], f64["k"], f64["v"], scale, 0, 0, rows, causal=True, block_mask=bm_ref)
+        _check_fwd(o[0, h, rows], lse[0, h, rows], ro, rl, f"causal window N=16384 head {h}")
+        rdq = oracle.backward_rows_dq(f64["q"], f64["k"], f64["v"], f64["do"], scale, 0, 0, rows,
+                                      causal=True, block_mask=bm_ref)
+        err = _rel_l2(dq[0, h, rows], rdq)
+        assert err <= GRAD_RTOL, f"h={h} dQ rows rel-L2 {err}"
