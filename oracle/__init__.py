@@ -8,6 +8,9 @@ from .attention import (  # noqa: F401
     backward,
     backward_rows,
     backward_rows_dq,
+    decode,
+    decode_split,
+    decode_visible,
     flops,
     forward,
     forward_rows,

@@ -290,6 +290,75 @@ def tiled_forward(q, k, v, scale, Br: int, Bc: int, causal=False, block_mask=Non
     return o_all, lse_all
 
 
+# --------------------------------------------------------------------------- #
+# decoding: the newest query tokens against a cache of keys and values
+# --------------------------------------------------------------------------- #
+def decode_visible(nq: int, L: int, causal: bool = False) -> np.ndarray:
+    """Boolean [nq, L]: which of the L cached keys each of the nq newest query
+    tokens may attend to.  Query i sits at sequence position L - nq + i; with
+    the causal mask it sees keys 0 .. L - nq + i, else all L."""
+    vis = np.ones((nq, L), dtype=bool)
+    if causal:
+        pos = L - nq + np.arange(nq)
+        vis &= np.arange(L)[None, :] <= pos[:, None]
+    return vis
+
+
+def decode(q, k, v, scale, seqlens=None, causal=False):
+    """O and LSE of q [B, H, Nq, d] against a cache k, v [B, H, Nk, d] whose
+    first seqlens[b] rows are valid (all Nk without seqlens), materialised
+    ["Как работает FlashAttention математически" section 9: FlashDecoding,
+    K and V cached, Q the newest token(s); the softmax is the plain definition
+    of "FlashAttention" notes, "Standard Attention Implementation"]."""
+    q, k, v = (np.asarray(x, dtype=np.float64) for x in (q, k, v))
+    B, H, nq, _ = q.shape
+    o = np.zeros(q.shape[:3] + (v.shape[-1],))
+    lse = np.full((B, H, nq), NEG_INF)
+    for b in range(B):
+        L = k.shape[2] if seqlens is None else int(seqlens[b])
+        if L == 0:
+            continue
+        for h in range(H):
+            s = _apply_mask(_scores(q[b, h], k[b, h, :L], scale), decode_visible(nq, L, causal))
+            p, m, l = _row_softmax(s)
+            o[b, h] = p @ v[b, h, :L]
+            lse[b, h] = _lse(m, l)
+    return o, lse
+
+
+def decode_split(q, k, v, scale, chunk: int, seqlens=None, causal=False):
+    """The split-KV form of decode: each chunk of `chunk` cached keys gives its
+    own normalised O_c and LSE_c (the plain softmax over that chunk); the
+    chunks are merged with the statistics merge of "FlashAttention" notes,
+    "Tiling" -- M = max_c LSE_c, w_c = exp(LSE_c - M), O = sum w_c O_c / sum w_c,
+    LSE = M + ln(sum w_c).  Chunks with no visible key carry LSE_c = -inf."""
+    q, k, v = (np.asarray(x, dtype=np.float64) for x in (q, k, v))
+    B, H, nq, _ = q.shape
+    o = np.zeros(q.shape[:3] + (v.shape[-1],))
+    lse = np.full((B, H, nq), NEG_INF)
+    for b in range(B):
+        L = k.shape[2] if seqlens is None else int(seqlens[b])
+        vis = decode_visible(nq, L, causal)
+        for h in range(H):
+            parts = []
+            for c0 in range(0, L, chunk):
+                cols = np.arange(c0, min(L, c0 + chunk))
+                s = _apply_mask(_scores(q[b, h], k[b, h, cols], scale), vis[:, cols])
+                p, m, l = _row_softmax(s)
+                parts.append((p @ v[b, h, cols], _lse(m, l)))
+            if not parts:
+                continue
+            lses = np.stack([pl for _, pl in parts])               # [chunks, nq]
+            M = lses.max(axis=0)
+            fin = np.isfinite(M)
+            w = np.exp(lses - np.where(fin, M, 0.0)[None, :])      # exp(-inf) = 0
+            W = w.sum(axis=0)
+            acc = sum(wc[:, None] * oc for wc, (oc, _) in zip(w, parts))
+            o[b, h] = np.where(fin[:, None], acc / np.where(fin, W, 1.0)[:, None], 0.0)
+            lse[b, h] = np.where(fin, M + np.log(np.where(fin, W, 1.0)), NEG_INF)
+    return o, lse
+
+
 def merge_stats(m1, l1, m2, l2):
     """Merge (m, l) of two parts of a row [P2 "Tiling"]:
     m = max(m1, m2);  l = exp(m1 - m) l1 + exp(m2 - m) l2."""

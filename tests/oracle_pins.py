@@ -313,5 +313,56 @@ def pin_block_masks(orc):
         np.testing.assert_allclose(o_d[:, :, sl], o_b, atol=1e-14)
 
 
+def pin_decode(orc):
+    """Decoding against a key/value cache: the square causal case is the
+    forward; one query token sees the whole cache either way; a short cache is
+    the forward over its valid rows; PyTorch's fp64 attention with a
+    bottom-right causal mask built by torch ops; rows with no visible key; and
+    the split-KV merge equals the whole for every chunk size."""
+    r = _rng(21)
+    B, H, d = 2, 3, 8
+    # square, causal: query i of N at position i
+    N = 37
+    q, k, v = (r.standard_normal((B, H, N, d)) for _ in range(3))
+    o, l = orc.decode(q, k, v, 0.4, causal=True)
+    of, lf = orc.forward(q, k, v, 0.4, causal=True)
+    np.testing.assert_allclose(o, of, atol=1e-13)
+    np.testing.assert_allclose(l, lf, atol=1e-13)
+    # one token: causal and non-causal agree
+    q1 = r.standard_normal((B, H, 1, d))
+    o1c, l1c = orc.decode(q1, k, v, 0.4, causal=True)
+    o1, l1 = orc.decode(q1, k, v, 0.4)
+    np.testing.assert_allclose(o1c, o1, atol=1e-14)
+    np.testing.assert_allclose(l1c, l1, atol=1e-14)
+    # a short cache: only its first L rows count
+    seq = [11, 30]
+    q4 = r.standard_normal((B, H, 4, d))
+    o4, l4 = orc.decode(q4, k, v, 0.4, seqlens=seq)
+    for b, L in enumerate(seq):
+        ob, lb = orc.forward(q4[b:b + 1], k[b:b + 1, :, :L], v[b:b + 1, :, :L], 0.4)
+        np.testing.assert_allclose(o4[b], ob[0], atol=1e-13)
+        np.testing.assert_allclose(l4[b], lb[0], atol=1e-13)
+    # library: torch SDPA with a bottom-right causal mask from torch.tril
+    o4c, _ = orc.decode(q4, k, v, 0.4, seqlens=seq, causal=True)
+    for b, L in enumerate(seq):
+        am = torch.ones(4, L, dtype=torch.bool).tril(L - 4)
+        ref = torch.nn.functional.scaled_dot_product_attention(
+            torch.tensor(q4[b]), torch.tensor(k[b, :, :L]), torch.tensor(v[b, :, :L]), attn_mask=am, scale=0.4)
+        np.testing.assert_allclose(o4c[b], ref.numpy(), atol=1e-13)
+    # no visible key: a cache shorter than the query block, and an empty cache
+    q6 = r.standard_normal((B, H, 6, d))
+    o6, l6 = orc.decode(q6, k, v, 0.4, seqlens=[3, 0], causal=True)
+    assert np.all(o6[0, :, :3] == 0) and np.all(np.isneginf(l6[0, :, :3]))   # positions -3..-1
+    assert np.all(np.isfinite(l6[0, :, 3:]))
+    assert np.all(o6[1] == 0) and np.all(np.isneginf(l6[1]))
+    # the split-KV merge is exact for any chunk size
+    for causal in (False, True):
+        ow, lw = orc.decode(q6, k, v, 0.4, seqlens=[37, 9], causal=causal)
+        for chunk in (1, 3, 8, 64):
+            os_, ls_ = orc.decode_split(q6, k, v, 0.4, chunk, seqlens=[37, 9], causal=causal)
+            np.testing.assert_allclose(os_, ow, atol=1e-13)
+            np.testing.assert_allclose(ls_, lw, atol=1e-13)
+
+
 ALL_PINS = [pin_worked_example, pin_closed_forms, pin_invariants, pin_backward_fd,
-            pin_dvec, pin_backward_rows, pin_library, pin_block_masks]
+            pin_dvec, pin_backward_rows, pin_library, pin_block_masks, pin_decode]

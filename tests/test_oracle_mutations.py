@@ -9,7 +9,8 @@ from tests import oracle_pins as pins
 
 _real = {name: getattr(orc, name) for name in
          ("_scores", "_apply_mask", "_row_softmax", "_softmax_backward", "visible",
-          "forward", "backward", "tiled_forward", "_lse", "window_block_mask", "dilated_block_mask")}
+          "forward", "backward", "tiled_forward", "_lse", "window_block_mask", "dilated_block_mask",
+          "decode_visible", "decode", "decode_split")}
 
 
 def _m_no_scale(q, k, scale):
@@ -136,6 +137,44 @@ def _m_dilated_causal_flipped(N, window, dilation, causal=False, block=128):
     return np.triu(m) if causal else m
 
 
+def _m_decode_top_left(nq, L, causal=False):
+    vis = np.ones((nq, L), dtype=bool)
+    if causal:
+        vis &= np.arange(L)[None, :] <= np.arange(nq)[:, None]     # query i at position i
+    return vis
+
+
+def _m_decode_strict(nq, L, causal=False):
+    vis = _real["decode_visible"](nq, L, causal)
+    if causal:
+        pos = L - nq + np.arange(nq)
+        vis &= np.arange(L)[None, :] < np.maximum(pos[:, None], 1)
+    return vis
+
+
+def _m_decode_no_seqlens(q, k, v, scale, seqlens=None, causal=False):
+    return _real["decode"](q, k, v, scale, None, causal)
+
+
+def _m_split_unweighted(q, k, v, scale, chunk, seqlens=None, causal=False):
+    """Split-KV merge that averages the chunks' outputs with equal weights."""
+    q, k, v = (np.asarray(x, dtype=np.float64) for x in (q, k, v))
+    o, lse = _real["decode_split"](q, k, v, scale, chunk, seqlens, causal)
+    B, H, nq, _ = q.shape
+    for b in range(B):
+        L = k.shape[2] if seqlens is None else int(seqlens[b])
+        for h in range(H):
+            outs = []
+            for c0 in range(0, L, chunk):
+                cols = np.arange(c0, min(L, c0 + chunk))
+                oc, _ = _real["decode"](q[b:b + 1, h:h + 1], k[b:b + 1, h:h + 1, cols], v[b:b + 1, h:h + 1, cols],
+                                        scale)
+                outs.append(oc[0, 0])
+            if len(outs) > 1:
+                o[b, h] = np.mean(outs, axis=0)
+    return o, lse
+
+
 MUTANTS = {
     "scale_dropped": ("_scores", _m_no_scale),
     "scores_transposed": ("_scores", _m_transposed_scores),
@@ -154,6 +193,10 @@ MUTANTS = {
     "window_sides_swapped": ("window_block_mask", _m_window_swapped),
     "dilated_without_dilation": ("dilated_block_mask", _m_dilated_no_dilation),
     "dilated_causal_flipped": ("dilated_block_mask", _m_dilated_causal_flipped),
+    "decode_causal_top_left": ("decode_visible", _m_decode_top_left),
+    "decode_causal_strict": ("decode_visible", _m_decode_strict),
+    "decode_ignores_seqlens": ("decode", _m_decode_no_seqlens),
+    "decode_split_unweighted": ("decode_split", _m_split_unweighted),
 }
 
 
