@@ -272,6 +272,82 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* o, const v
   return convert_impl(workspace, dq, B, H, N, d, scale, stream);
 }
 
+// Decoding: split the cache into chunks of a whole number of 64-key tiles so
+// that the grid of (batch * head * chunk) CTAs fills about six waves of two
+// CTAs on each of the 152 SMs, with at most 4096 keys per chunk.  The plan
+// depends only on the sizes, so the workspace query and the call agree.
+constexpr long long kPlanSMs = 152;
+
+struct DecodePlan {
+  int splits;
+  int chunk;
+};
+
+DecodePlan decode_plan(int B, int H, int Nk) {
+  const long long tiles = (static_cast<long long>(Nk) + fa::DEC_TILE - 1) / fa::DEC_TILE;
+  long long per = static_cast<long long>(B) * H * tiles / (kPlanSMs * 2 * 6);
+  per = per < 1 ? 1 : (per > 64 ? 64 : per);
+  const int chunk = static_cast<int>(per) * fa::DEC_TILE;
+  return {static_cast<int>((static_cast<long long>(Nk) + chunk - 1) / chunk), chunk};
+}
+
+int check_decode_shape(int B, int H, int Nq, int Nk, int d) {
+  if (B < 1 || H < 1 || Nq < 1 || Nk < 1 || d < 1) return FA_ERR_INVALID;
+  if (static_cast<long long>(B) * H * Nk * d >= (1ll << 31)) return FA_ERR_INVALID;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  if (Nq > fa::DEC_MAX_Q) return FA_ERR_UNSUPPORTED;
+  return FA_OK;
+}
+
+size_t decode_workspace_bytes(int B, int H, int Nq, int Nk, int d) {
+  const DecodePlan plan = decode_plan(B, H, Nk);
+  if (plan.splits == 1) return 0;
+  const size_t rows = static_cast<size_t>(B) * H * plan.splits * Nq;
+  return align256(rows * d * sizeof(float)) + align256(rows * sizeof(float));
+}
+
+int decode_impl(const void* q, const void* k, const void* v, void* o, float* lse, const int* seqlens, int B, int H,
+                int Nq, int Nk, int d, float scale, int causal, void* workspace, fa_stream_t stream) {
+  int rc;
+  if ((rc = check_ptrs({q, k, v, o, lse})) != FA_OK) return rc;
+  if (seqlens != nullptr && (reinterpret_cast<uintptr_t>(seqlens) & 3u) != 0) return FA_ERR_INVALID;
+  if ((rc = check_decode_shape(B, H, Nq, Nk, d)) != FA_OK) return rc;
+  if ((rc = check_scale(scale)) != FA_OK) return rc;
+  const DecodePlan plan = decode_plan(B, H, Nk);
+  if (plan.splits > 1 && (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0))
+    return FA_ERR_INVALID;
+  int* status = nullptr;
+  if ((rc = device_ready(&status)) != FA_OK) return rc;
+  fa::DecParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.q = static_cast<const __nv_bfloat16*>(q);
+  p.k = static_cast<const __nv_bfloat16*>(k);
+  p.v = static_cast<const __nv_bfloat16*>(v);
+  p.o = static_cast<__nv_bfloat16*>(o);
+  p.lse = lse;
+  if (plan.splits > 1) {
+    const size_t rows = static_cast<size_t>(B) * H * plan.splits * Nq;
+    char* base = static_cast<char*>(workspace);
+    p.o_part = reinterpret_cast<float*>(base);
+    p.lse_part = reinterpret_cast<float*>(base + align256(rows * d * sizeof(float)));
+  }
+  p.seqlens = seqlens;
+  p.status = status;
+  p.timeout_ns = g_timeout_ns.load(std::memory_order_relaxed);
+  p.BH = B * H;
+  p.H = H;
+  p.Nq = Nq;
+  p.Nk = Nk;
+  p.splits = plan.splits;
+  p.chunk = plan.chunk;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.causal = causal ? 1 : 0;
+  if (log_enabled())
+    std::fprintf(stderr, "[fa] decode B=%d H=%d Nq=%d Nk=%d d=%d splits=%d chunk=%d\n", B, H, Nq, Nk, d, plan.splits,
+                 plan.chunk);
+  return fa::launch_decode(p, d, reinterpret_cast<cudaStream_t>(stream));
+}
+
 }  // namespace
 
 // --------------------------------------------------------------------------
@@ -363,6 +439,16 @@ int fa_bwd_main(const void* q, const void* k, const void* v, const void* dout, c
 
 int fa_bwd_dq_convert(const void* workspace, void* dq, int B, int H, int N, int d, float scale, fa_stream_t stream) {
   return convert_impl(workspace, dq, B, H, N, d, scale, stream);
+}
+
+size_t fa_decode_workspace_bytes(int B, int H, int Nq, int Nk, int d) {
+  if (check_decode_shape(B, H, Nq, Nk, d) != FA_OK) return 0;
+  return decode_workspace_bytes(B, H, Nq, Nk, d);
+}
+
+int fa_decode(const void* q, const void* k, const void* v, void* o, float* lse, const int* seqlens_k, int B, int H,
+              int Nq, int Nk, int d, float scale, int causal, void* workspace, fa_stream_t stream) {
+  return decode_impl(q, k, v, o, lse, seqlens_k, B, H, Nq, Nk, d, scale, causal, workspace, stream);
 }
 
 int fa_block_mask_window(uint8_t* mask, int N, int left, int right) {

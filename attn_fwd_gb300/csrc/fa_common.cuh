@@ -65,7 +65,34 @@ struct BwdParams {
   int mask_kind;
 };
 
+// Decoding against a key/value cache: keys per shared-memory stage, and the
+// largest number of query tokens per (batch, head).
+constexpr int DEC_TILE = 64;
+constexpr int DEC_MAX_Q = 8;
+
+struct DecParams {
+  const __nv_bfloat16* q;    // [B*H][Nq][d]
+  const __nv_bfloat16* k;    // [B*H][Nk][d]
+  const __nv_bfloat16* v;    // [B*H][Nk][d]
+  __nv_bfloat16* o;          // [B*H][Nq][d]
+  float* lse;                // [B*H][Nq], natural log
+  float* o_part;             // [B*H][splits][Nq][d] fp32, normalised per chunk (splits > 1)
+  float* lse_part;           // [B*H][splits][Nq], log2 units (splits > 1)
+  const int* seqlens;        // [B] valid cache rows, or null for all Nk
+  int* status;
+  uint64_t timeout_ns;
+  int BH;
+  int H;
+  int Nq;
+  int Nk;
+  int splits;                // chunks of the cache per (batch, head)
+  int chunk;                 // keys per chunk, a multiple of DEC_TILE
+  float scale_log2;
+  int causal;
+};
+
 int launch_fwd(const FwdParams& p, int d, cudaStream_t stream);
+int launch_decode(const DecParams& p, int d, cudaStream_t stream);
 int launch_bwd_preprocess(const __nv_bfloat16* o, const __nv_bfloat16* dout, const float* lse, float* nd,
                           float* nlse, float* dq_acc, int BH, int N, int npad, int d, cudaStream_t stream);
 int launch_bwd_main(const BwdParams& p, int d, cudaStream_t stream);

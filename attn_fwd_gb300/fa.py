@@ -43,6 +43,8 @@ _SIGS = {
     "fa_bwd_main": (_i, [_vp] * 8 + [_i, _i, _i, _i, _f, _i, _vp]),
     "fa_bwd_dq_convert": (_i, [_vp, _vp, _i, _i, _i, _i, _f, _vp]),
     "fa_bwd_noalloc": (_i, [_vp] * 9 + [_i, _i, _i, _i, _f, _i, _vp]),
+    "fa_decode_workspace_bytes": (_sz, [_i, _i, _i, _i, _i]),
+    "fa_decode": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _vp, _vp]),
     "fa_block_mask_window": (_i, [_vp, _i, _i, _i]),
     "fa_block_mask_dilated": (_i, [_vp, _i, _i, _i, _i]),
     "fa_get_device_error": (_i, [_vp]),
@@ -196,6 +198,28 @@ def fa_bwd_noalloc(q, k, v, o, do, lse, dq, dk, dv, scale, causal=False, stream=
     _check("fa_bwd_noalloc", rc)
 
 
+def fa_decode_workspace_bytes(B, H, Nq, Nk, d) -> int:
+    return load().fa_decode_workspace_bytes(B, H, Nq, Nk, d)
+
+
+def fa_decode(q, k, v, o, lse, seqlens_k, scale, causal=False, workspace=None, stream=None):
+    """q, o [B,H,Nq,d]; k, v [B,H,Nk,d]; lse [B,H,Nq]; seqlens_k int32 [B] or None."""
+    B, H, Nq, d = q.shape
+    Nk = k.shape[2]
+    if tuple(k.shape) != (B, H, Nk, d) or tuple(v.shape) != (B, H, Nk, d):
+        raise ValueError("k and v must be [B, H, Nk, d] like q")
+    if seqlens_k is not None:
+        if seqlens_k.dtype != torch.int32 or not seqlens_k.is_cuda or seqlens_k.numel() != B:
+            raise ValueError("seqlens_k must be a CUDA int32 tensor of B entries")
+        sl = ctypes.c_void_p(seqlens_k.data_ptr())
+    else:
+        sl = ctypes.c_void_p(0)
+    ws = ctypes.c_void_p(workspace.data_ptr()) if workspace is not None else ctypes.c_void_p(0)
+    rc = load().fa_decode(_bf16(q, "q"), _bf16(k, "k"), _bf16(v, "v"), _bf16(o, "o"), _f32(lse, "lse"), sl,
+                          B, H, Nq, Nk, d, float(scale), int(bool(causal)), ws, _stream(stream))
+    _check("fa_decode", rc)
+
+
 def fa_block_mask_window(N, left, right) -> torch.Tensor:
     """Sliding-window block mask, uint8 [nb, nb] on the host (see include/fa.h)."""
     nb = (N + 127) // 128
@@ -238,6 +262,19 @@ def forward(q, k, v, causal=False, scale=None, block_mask=None, stream=None):
         fa_fwd_blocksparse(q, k, v, o, lse, block_mask, scale, causal, stream)
     else:
         fa_fwd(q, k, v, o, lse, scale, causal, stream)
+    return o, lse
+
+
+def decode(q, k, v, seqlens_k=None, causal=False, scale=None, ws=None, stream=None):
+    """Returns (O bf16 [B,H,Nq,d], LSE fp32 [B,H,Nq]) of q against the cache k, v."""
+    B, H, Nq, d = q.shape
+    scale = (1.0 / d ** 0.5) if scale is None else scale
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
+    if ws is None:
+        n = fa_decode_workspace_bytes(B, H, Nq, k.shape[2], d)
+        ws = torch.empty(n, dtype=torch.uint8, device=q.device) if n else None
+    fa_decode(q, k, v, o, lse, seqlens_k, scale, causal, ws, stream)
     return o, lse
 
 

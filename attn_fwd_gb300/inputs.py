@@ -99,6 +99,16 @@ def make_qkvdo(B: int, H: int, N: int, d: int, seed: int, amplitude: float = 1.0
     return out
 
 
+def make_decode_inputs(B: int, H: int, Nq: int, Nk: int, d: int, seed: int) -> dict[str, torch.Tensor]:
+    """Decoding inputs as CPU bf16 tensors: q [B, H, Nq, d] (the newest tokens)
+    and the cache k, v [B, H, Nk, d], drawn in that order from one generator."""
+    g = torch.Generator(device="cpu").manual_seed(seed)
+    out = {"q": torch.randn((B, H, Nq, d), generator=g, dtype=torch.float32).to(torch.bfloat16)}
+    for nm in ("k", "v"):
+        out[nm] = torch.randn((B, H, Nk, d), generator=g, dtype=torch.float32).to(torch.bfloat16)
+    return out
+
+
 def make_block_mask(N: int, seed: int, p: float, block: int = BLOCK) -> torch.Tensor:
     """Block mask as uint8 [N/block, N/block]; diagonal blocks are always kept."""
     if N % block:

@@ -178,6 +178,31 @@ FA_API int fa_block_mask_window(uint8_t *mask, int N, int left, int right);
 FA_API int fa_block_mask_dilated(uint8_t *mask, int N, int window, int dilation, int causal);
 
 /*
+ * Decoding: the Nq newest query tokens of each (b, h) against a key/value
+ * cache ("Как работает FlashAttention математически", section 9:
+ * FlashDecoding -- K and V cached, Q the newest token).  The cache is split
+ * into chunks processed in parallel; each chunk's O and LSE are merged with
+ * the statistics merge of "FlashAttention" notes, "Tiling" (exact up to
+ * rounding).
+ *
+ *   q, o        : bf16 [B, H, Nq, d] device memory; lse: fp32 [B, H, Nq]
+ *   k, v        : bf16 [B, H, Nk, d] device memory, the cache's capacity Nk
+ *   seqlens_k   : int32 [B] device memory, the valid cache rows of each batch
+ *                 (clamped to [0, Nk]); NULL means all Nk rows are valid
+ *   causal      : query i sits at position L - Nq + i of a cache of L valid
+ *                 rows and sees keys 0 .. L - Nq + i; without it all L keys.
+ *                 A query that sees no key gets O = 0, LSE = -inf.
+ *   workspace   : device memory of fa_decode_workspace_bytes(B, H, Nq, Nk, d)
+ *                 bytes, 256-byte aligned (may be NULL when that is 0)
+ * Supported: 1 <= Nq <= 8, Nk >= 1, d in {64, 128}, B * H * Nk * d < 2^31.
+ * Errors and asynchrony as for the other compute calls.
+ */
+FA_API size_t fa_decode_workspace_bytes(int B, int H, int Nq, int Nk, int d);
+FA_API int fa_decode(const void *q, const void *k, const void *v, void *o, float *lse,
+                     const int *seqlens_k, int B, int H, int Nq, int Nk, int d, float scale,
+                     int causal, void *workspace, fa_stream_t stream);
+
+/*
  * Size of the device scratch array behind fa_bwd_noalloc: 64 MiB per device.
  * fa_bwd_noalloc accepts a problem when fa_bwd_workspace_bytes(B, H, N, d) is
  * at most this: B * H * N * d up to about 16.5 million elements at d = 128

@@ -158,3 +158,20 @@ def test_mask_generators_reject_bad_arguments(lib):
     assert lib.fa_block_mask_dilated(buf, 128, 1, 0, 0) == -1
     assert lib.fa_block_mask_dilated(buf, 128, -1, 1, 0) == -1
     assert lib.fa_block_mask_window(buf, 1024 * 128 + 1, 1, 1) == -2
+
+
+def test_decode_workspace_and_validation(lib):
+    import attn_fwd_gb300.fa as fa
+    assert fa.fa_decode_workspace_bytes(1, 1, 1, 64, 128) == 0          # one chunk: no workspace
+    n = fa.fa_decode_workspace_bytes(8, 32, 1, 32768, 128)
+    assert n > 0 and n % 256 == 0
+    assert fa.fa_decode_workspace_bytes(1, 1, 9, 1024, 128) == 0         # Nq > 8 unsupported
+    assert fa.fa_decode_workspace_bytes(1, 1, 1, 1024, 96) == 0
+    sl = ctypes.c_void_p(4096 + 2)                                      # not 4-byte aligned
+    assert lib.fa_decode(NULL, P, P, P, P, NULL, 1, 1, 1, 64, 128, 0.1, 0, NULL, NULL) == -1
+    assert lib.fa_decode(P, P, P, P, P, sl, 1, 1, 1, 64, 128, 0.1, 0, NULL, NULL) == -1
+    assert lib.fa_decode(P, P, P, P, P, NULL, 1, 1, 9, 64, 128, 0.1, 0, NULL, NULL) == -2
+    assert lib.fa_decode(P, P, P, P, P, NULL, 1, 1, 0, 64, 128, 0.1, 0, NULL, NULL) == -1
+    assert lib.fa_decode(P, P, P, P, P, NULL, 1, 1, 1, 64, 128, -1.0, 0, NULL, NULL) == -1
+    # several chunks need a workspace
+    assert lib.fa_decode(P, P, P, P, P, NULL, 8, 32, 1, 32768, 128, 0.1, 0, NULL, NULL) == -1
