@@ -27,7 +27,8 @@ struct DecLayout {
   static constexpr int KT = DEC_TILE;                      // keys per stage
   static constexpr int ROW = D * 2;                        // bytes per key row
   static constexpr int TILE_BYTES = KT * ROW;              // K (or V) of one stage
-  static constexpr int STAGES = D == 128 ? 3 : 6;          // 96 KB of K/V per CTA
+  static constexpr int STAGES = 3;                         // 96 KB (d=128) / 48 KB (d=64) of K/V:
+                                                           // 2 / 4 CTAs per SM
   static constexpr int K_OFF = 0;
   static constexpr int V_OFF = STAGES * TILE_BYTES;
   static constexpr int MERGE_OFF = 2 * STAGES * TILE_BYTES;            // warp 1's state

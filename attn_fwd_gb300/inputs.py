@@ -85,6 +85,57 @@ WORKLOADS = {
 }
 
 
+@dataclass(frozen=True)
+class DecodeWorkload:
+    """The newest nq query tokens of each (batch, head) against a key/value
+    cache of capacity N; `ragged` draws each batch's valid length uniformly
+    from [N/4, N] (else every cache is full)."""
+
+    name: str
+    B: int
+    H: int
+    nq: int
+    N: int
+    d: int
+    seed: int
+    causal: bool = False
+    ragged: bool = False
+    note: str = field(default="", compare=False)
+    backward: bool = False
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / (self.d ** 0.5)
+
+    @property
+    def mask_kind(self) -> str:
+        return "causal" if self.causal else "none"
+
+
+DECODE_WORKLOADS = {
+    "decode_b8h32q1n32768d128": DecodeWorkload(
+        "decode_b8h32q1n32768d128", 8, 32, 1, 32768, 128, seed=6,
+        note="one new token per sequence, full 32k caches"),
+    "decode_b16h32q1n8192d128_ragged": DecodeWorkload(
+        "decode_b16h32q1n8192d128_ragged", 16, 32, 1, 8192, 128, seed=7, ragged=True,
+        note="one new token, cache lengths uniform in [2k, 8k]"),
+    "decode_b8h32q4n32768d128_causal": DecodeWorkload(
+        "decode_b8h32q4n32768d128_causal", 8, 32, 4, 32768, 128, seed=8, causal=True,
+        note="four new tokens (speculative decoding), causal among themselves"),
+}
+
+
+def make_decode_workload_inputs(w: DecodeWorkload) -> dict[str, torch.Tensor]:
+    """q, k, v (CPU bf16) and seqlens (CPU int32 [B]) of a decode workload."""
+    t = make_decode_inputs(w.B, w.H, w.nq, w.N, w.d, w.seed)
+    if w.ragged:
+        g = torch.Generator(device="cpu").manual_seed(w.seed + 1)
+        t["seqlens"] = torch.randint(w.N // 4, w.N + 1, (w.B,), generator=g, dtype=torch.int32)
+    else:
+        t["seqlens"] = torch.full((w.B,), w.N, dtype=torch.int32)
+    return t
+
+
 def make_qkvdo(B: int, H: int, N: int, d: int, seed: int, amplitude: float = 1.0,
                with_dout: bool = True) -> dict[str, torch.Tensor]:
     """Draw Q, K, V (and dO) as CPU bf16 tensors of shape [B, H, N, d]."""

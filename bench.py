@@ -70,14 +70,44 @@ def whole_job_tflops(world_size: int, flops_per_rank_step: float, ms_per_step: f
     return world_size * flops_per_rank_step / (ms_per_step * 1e-3) / 1e12
 
 
+def _count_flops(B, H, N, d, causal=False, backward=False, density=None) -> float:
+    """The FLOP convention of the measurements: 4 B H N^2 d forward (two N x N
+    x d products), 2.5x that backward (five products), halved when causal,
+    scaled by the kept fraction of a block mask."""
+    f = 4.0 * B * H * N * N * d
+    if backward:
+        f *= 2.5
+    if causal:
+        f *= 0.5
+    if density is not None:
+        f *= density
+    return f
+
+
 def _flops(w, density):
     """With a block mask, `density` already carries the causal halving (see
     _density), so the causal factor is applied only without one."""
-    import oracle
     causal = w.causal and density is None
-    f_fwd = oracle.flops(w.B, w.H, w.N, w.d, causal=causal, density=density)
-    f_bwd = oracle.flops(w.B, w.H, w.N, w.d, causal=causal, backward=True, density=density) if w.backward else 0.0
+    f_fwd = _count_flops(w.B, w.H, w.N, w.d, causal=causal, density=density)
+    f_bwd = _count_flops(w.B, w.H, w.N, w.d, causal=causal, backward=True, density=density) if w.backward else 0.0
     return f_fwd, f_bwd
+
+
+def _decode_pairs(nq, L, causal):
+    """(query, key) pairs a decode step scores: query i of nq sits at position
+    L - nq + i of a cache of L rows; causal keeps keys up to that position."""
+    if not causal:
+        return nq * L
+    return sum(min(max(L - nq + i + 1, 0), L) for i in range(nq))
+
+
+def _decode_work(w, seqlens):
+    """(FLOPs, cache bytes read) of one decode step: 4 d FLOPs per pair, and K
+    and V rows of every valid cache position read once per (batch, head)."""
+    pairs = sum(_decode_pairs(w.nq, int(L), w.causal) for L in seqlens) * w.H
+    cache_bytes = sum(int(L) for L in seqlens) * w.H * w.d * 2 * 2
+    io_bytes = w.B * w.H * w.nq * (w.d * 2 * 2 + 4)       # q in, o and lse out
+    return 4.0 * w.d * pairs, cache_bytes + io_bytes
 
 
 def _density(t, causal=False):
@@ -209,7 +239,9 @@ def run_reference(args):
         return 0
     import numpy as np
     import oracle
-    from attn_fwd_gb300.inputs import WORKLOADS, make_workload_inputs
+    from attn_fwd_gb300.inputs import DECODE_WORKLOADS, WORKLOADS, make_workload_inputs
+    if args.workload in DECODE_WORKLOADS:
+        return _run_reference_decode(args, DECODE_WORKLOADS[args.workload])
     w = WORKLOADS[args.workload]
     t = make_workload_inputs(w, heads=slice(0, 1))
     q, k, v = (t[n][:1].double().numpy() for n in ("q", "k", "v"))
@@ -280,9 +312,182 @@ def source_sha256(files):
     return hh.hexdigest()
 
 
+def _oracle_decode_sample(w, t, budget_s=15.0):
+    """Time the fp64 oracle's decode (batch, head) by (batch, head) until
+    `budget_s` has passed.  Returns (TFLOPS, seconds, heads)."""
+    import oracle
+    heads, flops = 0, 0.0
+    t0 = time.perf_counter()
+    for hh in range(w.B * w.H):
+        b, h = divmod(hh, w.H)
+        sl = (slice(b, b + 1), slice(h, h + 1))
+        L = int(t["seqlens"][b])
+        q, k, v = (t[n][sl].double().numpy() for n in ("q", "k", "v"))
+        oracle.decode(q, k, v, w.scale, seqlens=[L], causal=w.causal)
+        flops += 4.0 * w.d * _decode_pairs(w.nq, L, w.causal)
+        heads += 1
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    el = time.perf_counter() - t0
+    return flops / el / 1e12, el, heads
+
+
+def _run_reference_decode(args, w):
+    """Reference arm for a decode workload: each step decodes one (batch, head)
+    with the fp64 oracle, cycling through the pairs."""
+    import oracle
+    from attn_fwd_gb300.inputs import make_decode_workload_inputs
+    t = make_decode_workload_inputs(w)
+
+    def one(step):
+        hh = step % (w.B * w.H)
+        b, h = divmod(hh, w.H)
+        sl = (slice(b, b + 1), slice(h, h + 1))
+        L = int(t["seqlens"][b])
+        q, k, v = (t[n][sl].double().numpy() for n in ("q", "k", "v"))
+        oracle.decode(q, k, v, w.scale, seqlens=[L], causal=w.causal)
+        return 4.0 * w.d * _decode_pairs(w.nq, L, w.causal)
+
+    for i in range(args.warmup):
+        one(i)
+    flops = 0.0
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        flops += one(i)
+    total = time.perf_counter() - t0
+    value = flops / total / 1e12
+    sample = (f"per step: one (batch, head) of {w.B * w.H}, {w.nq} query token(s) against its cache, fp64; "
+              f"steps cycle through the pairs")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": total / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": _decode_config(w),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": _CORES, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def _decode_config(w):
+    return {"workload": w.name, "B": w.B, "H": w.H, "Nq": w.nq, "N_cache": w.N, "d": w.d, "causal": w.causal,
+            "cache_lengths": "uniform in [N/4, N]" if w.ragged else "full",
+            "l2": "flushed (256 MiB write) between timed steps", "parallelism": "replica per GPU"}
+
+
+def run_cuda_decode(args, w):
+    """Decoding: fa_decode (split kernel + chunk merge) per step, the cache
+    resident in HBM; roofline against the measured HBM copy bandwidth."""
+    import torch
+    import torch.distributed as dist
+
+    ws, rank, local = _dist()
+    if ws > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    import __graft_entry__
+    __graft_entry__.build()
+    import attn_fwd_gb300.fa as fa
+    from attn_fwd_gb300.inputs import make_decode_workload_inputs
+
+    t = make_decode_workload_inputs(w)
+    flops, nbytes = _decode_work(w, t["seqlens"].tolist())
+    q, k, v = (t[n].to(dev) for n in ("q", "k", "v"))
+    sl = t["seqlens"].to(dev)
+    o = torch.empty_like(q)
+    lse = torch.empty((w.B, w.H, w.nq), dtype=torch.float32, device=dev)
+    nws = fa.fa_decode_workspace_bytes(w.B, w.H, w.nq, w.N, w.d)
+    wsp = torch.empty(nws, dtype=torch.uint8, device=dev) if nws else None
+    launches_per_step = 2 if nws else 1
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    def step():
+        fa.fa_decode(q, k, v, o, lse, sl, w.scale, causal=w.causal, workspace=wsp)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    rc = fa.fa_get_device_error()
+    if rc != 0:
+        raise RuntimeError(f"device status after warm-up: {fa.status_string(rc)}")
+    uuid = None
+    try:
+        uuid = str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        pass
+    sampler = ClockSampler(uuid) if rank == 0 else None
+    if sampler:
+        sampler.start()
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+    if ws > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    for i in range(args.steps):
+        flush.zero_()
+        events[i][0].record()
+        step()
+        events[i][1].record()
+    torch.cuda.synchronize()
+    if ws > 1:
+        dist.barrier()
+    clocks = sampler.stop() if sampler else None
+    rc = fa.fa_get_device_error()
+    if rc != 0:
+        raise RuntimeError(f"device status after timing: {fa.status_string(rc)}")
+    step_ms = [e[0].elapsed_time(e[1]) for e in events]
+    ms_per_step = max_over_ranks(sum(step_ms), dev) / args.steps
+    value = whole_job_tflops(ws, flops, ms_per_step)
+
+    # end to end: the new query tokens in from pinned host memory, O and LSE back
+    hq = t["q"].pin_memory()
+    ho, hl = torch.empty(o.shape, dtype=o.dtype).pin_memory(), torch.empty(lse.shape).pin_memory()
+    e2e_steps = max(3, min(args.steps, 50))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record()
+    for _ in range(e2e_steps):
+        q.copy_(hq, non_blocking=True)
+        step()
+        ho.copy_(o, non_blocking=True)
+        hl.copy_(lse, non_blocking=True)
+    e1.record()
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, dev)
+
+    peaks, peak_src = _peaks()
+    peak = float(peaks["hbm_gbs"])
+    achieved = nbytes / (ms_per_step * 1e-3) / 1e9
+    roofline = {"bound": "hbm", "kernel": "fa_decode_kernel", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                "frac": achieved / peak, "peak_source": f"{peak_src} HBM copy bandwidth",
+                "traffic": _profile_traffic("fa_decode_kernel", w.name),
+                "algorithmic_bytes_per_step": nbytes,
+                "note": "split kernel and chunk merge timed together (one step)"}
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": _decode_config(w),
+            "e2e": {"value": whole_job_tflops(ws, flops, e2e_ms), "unit": UNIT,
+                    "h2d_bytes_per_step": hq.numel() * hq.element_size(),
+                    "d2h_bytes_per_step": ho.numel() * ho.element_size() + hl.numel() * hl.element_size(),
+                    "ms_per_step": e2e_ms},
+            "gpu_launches": launches_per_step * args.steps, "roofline": roofline, "clocks": clocks}
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        tf, el, heads = _oracle_decode_sample(w, t, budget_s=args.cpu_budget)
+        line["cpu_baseline"] = {"value": tf, "unit": UNIT, "cores": _CORES, "kind": "oracle",
+                                "sample": f"{heads} of {w.B * w.H} (batch, head) pairs, decode, fp64, {el:.1f} s"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        dist.destroy_process_group()
+    return 0
+
+
 def run_cuda(args):
     import torch
     import torch.distributed as dist
+    from attn_fwd_gb300.inputs import DECODE_WORKLOADS
+    if args.workload in DECODE_WORKLOADS:
+        return run_cuda_decode(args, DECODE_WORKLOADS[args.workload])
 
     ws, rank, local = _dist()
     if ws > 1:
