@@ -7,16 +7,22 @@ from .attention import (  # noqa: F401
     NEG_INF,
     backward,
     backward_rows,
+    backward_dropout,
     backward_rows_dq,
     decode,
     decode_split,
     decode_visible,
+    dropout_bytes,
+    dropout_keep,
+    dropout_threshold,
     flops,
+    forward_dropout,
     forward,
     forward_rows,
     dilated_block_mask,
     head_probs,
     merge_stats,
+    philox4x32_10,
     tiled_forward,
     visible,
     window_block_mask,

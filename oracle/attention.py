@@ -291,6 +291,110 @@ def tiled_forward(q, k, v, scale, Br: int, Bc: int, causal=False, block_mask=Non
 
 
 # --------------------------------------------------------------------------- #
+# dropout with regenerated masks
+# --------------------------------------------------------------------------- #
+# The pages keep only O(N) statistics and regenerate the random dropout masks
+# in the backward instead of storing them ("Как работает FlashAttention
+# математически", section 5; "FlashAttention" notes, "Backward Pass of
+# flashattention").  They name no generator; the reading here: the
+# counter-based generator Philox4x32-10 of Salmon, Moraes, Dror and Shaw,
+# "Parallel random numbers: as easy as 1, 2, 3" (SC'11), key = the 64-bit
+# seed, counter = (j // 4, i // 4, h, b) for query i and key j, so one call
+# covers a 4 x 4 block; element (i, j) takes byte j % 4 (little-endian) of
+# output word i % 4 and is kept iff that byte >= t = round(256 p), t <= 255;
+# kept entries are scaled by 256 / (256 - t).
+
+_PHILOX_M = (0xD2511F53, 0xCD9E8D57)        # round multipliers
+_PHILOX_W = (0x9E3779B9, 0xBB67AE85)        # key increments (Weyl sequence)
+
+
+def philox4x32_10(ctr, key):
+    """Philox4x32 with 10 rounds on uint32 counters [..., 4] and a key (k0, k1):
+    each round multiplies words 0 and 2 by the two constants, and the new
+    words are (hi(M1 c2) ^ c1 ^ k0, lo(M1 c2), hi(M0 c0) ^ c3 ^ k1, lo(M0 c0));
+    the key advances by the Weyl increments between rounds."""
+    c = np.array(ctr, dtype=np.uint64) & 0xFFFFFFFF
+    k0, k1 = int(key[0]) & 0xFFFFFFFF, int(key[1]) & 0xFFFFFFFF
+    mask = np.uint64(0xFFFFFFFF)
+    for r in range(10):
+        if r:
+            k0 = (k0 + _PHILOX_W[0]) & 0xFFFFFFFF
+            k1 = (k1 + _PHILOX_W[1]) & 0xFFFFFFFF
+        p0 = c[..., 0] * np.uint64(_PHILOX_M[0])
+        p1 = c[..., 2] * np.uint64(_PHILOX_M[1])
+        hi0, lo0 = p0 >> np.uint64(32), p0 & mask
+        hi1, lo1 = p1 >> np.uint64(32), p1 & mask
+        c = np.stack([hi1 ^ c[..., 1] ^ np.uint64(k0), lo1, hi0 ^ c[..., 3] ^ np.uint64(k1), lo0], axis=-1)
+    return c.astype(np.uint32)
+
+
+def dropout_threshold(p: float) -> int:
+    """Byte threshold t = round(256 p), at most 255: a byte below t drops."""
+    if not 0.0 <= p < 1.0:
+        raise ValueError("dropout probability must be in [0, 1)")
+    return min(255, int(np.floor(256.0 * p + 0.5)))
+
+
+def dropout_bytes(b: int, h: int, rows, cols, seed: int) -> np.ndarray:
+    """uint8 [len(rows), len(cols)]: the random byte of each (query, key) pair
+    of head (b, h): byte j % 4 of word i % 4 of Philox(counter (j//4, i//4, h, b))."""
+    rows, cols = np.asarray(rows, dtype=np.int64), np.asarray(cols, dtype=np.int64)
+    ii, jj = np.meshgrid(rows, cols, indexing="ij")
+    ctr = np.stack([jj // 4, ii // 4, np.full_like(ii, h), np.full_like(ii, b)], axis=-1)
+    words = philox4x32_10(ctr, (seed & 0xFFFFFFFF, (seed >> 32) & 0xFFFFFFFF))
+    word = np.take_along_axis(words, (ii % 4)[..., None], axis=-1)[..., 0]
+    return ((word >> (8 * (jj % 4)).astype(np.uint32)) & 0xFF).astype(np.uint8)
+
+
+def dropout_keep(b: int, h: int, rows, cols, p: float, seed: int) -> np.ndarray:
+    """Boolean [len(rows), len(cols)]: which (query, key) pairs of head (b, h)
+    dropout keeps (random byte >= round(256 p))."""
+    return dropout_bytes(b, h, rows, cols, seed) >= dropout_threshold(p)
+
+
+def forward_dropout(q, k, v, scale, p: float, seed: int, causal=False, block_mask=None, block=128):
+    """O = (P o Z) V * 256 / (256 - t) with P the plain softmax and Z the
+    regenerated keep mask; LSE is that of P (dropout acts after the softmax)."""
+    q, k, v = (np.asarray(x, dtype=np.float64) for x in (q, k, v))
+    B, H, N, _ = q.shape
+    Nk = k.shape[2]
+    inv_keep = 256.0 / (256 - dropout_threshold(p))
+    o = np.zeros(q.shape[:3] + (v.shape[-1],))
+    lse = np.zeros((B, H, N))
+    for b in range(B):
+        for h in range(H):
+            pr, lse[b, h] = head_probs(q[b, h], k[b, h], scale, causal, block_mask, block)
+            z = dropout_keep(b, h, np.arange(N), np.arange(Nk), p, seed)
+            o[b, h] = (pr * z * inv_keep) @ v[b, h]
+    return o, lse
+
+
+def backward_dropout(q, k, v, do, scale, p: float, seed: int, causal=False, block_mask=None, block=128):
+    """Gradients of forward_dropout ["FlashAttention" notes, "Backward Pass of
+    flashattention", with the dropped probabilities P~ = P o Z * c]:
+    dV = P~^T dO;  dP = (dO V^T) o Z * c;  D_i = sum_j P_ij dP_ij;
+    dS = P o (dP - D);  dQ = scale * dS K;  dK = scale * dS^T Q."""
+    q, k, v, do = (np.asarray(x, dtype=np.float64) for x in (q, k, v, do))
+    B, H, N, _ = q.shape
+    Nk = k.shape[2]
+    inv_keep = 256.0 / (256 - dropout_threshold(p))
+    dq, dk, dv = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
+    dvec = np.zeros((B, H, N))
+    for b in range(B):
+        for h in range(H):
+            pr, _ = head_probs(q[b, h], k[b, h], scale, causal, block_mask, block)
+            zc = dropout_keep(b, h, np.arange(N), np.arange(Nk), p, seed) * inv_keep
+            dv[b, h] = (pr * zc).T @ do[b, h]
+            dp = (do[b, h] @ v[b, h].T) * zc
+            d_row = (pr * dp).sum(axis=1)
+            ds = _softmax_backward(pr, dp, d_row)
+            dq[b, h] = scale * (ds @ k[b, h])
+            dk[b, h] = scale * (ds.T @ q[b, h])
+            dvec[b, h] = d_row
+    return dq, dk, dv, dvec
+
+
+# --------------------------------------------------------------------------- #
 # decoding: the newest query tokens against a cache of keys and values
 # --------------------------------------------------------------------------- #
 def decode_visible(nq: int, L: int, causal: bool = False) -> np.ndarray:

@@ -364,5 +364,103 @@ def pin_decode(orc):
             np.testing.assert_allclose(ls_, lw, atol=1e-13)
 
 
+def pin_philox(orc):
+    """Philox4x32-10 against its published known-answer vectors, and the
+    element-to-counter mapping of the dropout bytes against the same vectors:
+    counter (j//4, i//4, h, b) and key (seed low, seed high) reproduce each
+    vector's four output words as the 4 x 4 block of bytes (row i%4 = word,
+    column j%4 = byte, little-endian)."""
+    with open(os.path.join(GOLDEN, "philox4x32_10_kat.json")) as f:
+        kat = json.load(f)["vectors"]
+    for vec in kat:
+        ctr = np.array([int(x, 16) for x in vec["ctr"]], dtype=np.uint64)
+        key = [int(x, 16) for x in vec["key"]]
+        out = [int(x, 16) for x in vec["out"]]
+        assert [int(x) for x in orc.philox4x32_10(ctr, key)] == out
+        c0, c1, c2, c3 = (int(x) for x in ctr)
+        seed = key[0] | (key[1] << 32)
+        rows = 4 * c1 + np.arange(4)
+        cols = 4 * c0 + np.arange(4)
+        got = orc.dropout_bytes(c3, c2, rows, cols, seed)
+        want = np.array([[(w >> (8 * j)) & 0xFF for j in range(4)] for w in out], dtype=np.uint8)
+        np.testing.assert_array_equal(got, want)
+
+
+def pin_dropout(orc):
+    """Dropout: p = 0 is plain attention; keep rates and cross-head agreement
+    match the binomial law; averaging over seeds gives the undropped output
+    (unbiased); PyTorch autograd of softmax(S) o Z c V with the oracle's mask;
+    central finite differences of the backward with a fixed mask."""
+    r = _rng(31)
+    B, H, N, d = 1, 2, 24, 4
+    q, k, v, do = (r.standard_normal((B, H, N, d)) for _ in range(4))
+    o0, l0 = orc.forward(q, k, v, 0.5, causal=True)
+    od, ld = orc.forward_dropout(q, k, v, 0.5, 0.0, 7, causal=True)
+    np.testing.assert_array_equal(od, o0)
+    np.testing.assert_array_equal(ld, l0)
+    g0 = orc.backward(q, k, v, do, 0.5, causal=True)
+    gd = orc.backward_dropout(q, k, v, do, 0.5, 0.0, 7, causal=True)
+    for a, b_ in zip(g0, gd):
+        np.testing.assert_allclose(b_, a, atol=1e-14)
+    assert orc.dropout_threshold(0.1) == 26 and orc.dropout_threshold(0.5) == 128
+    # keep rate and independence (binomial bounds, 6 sigma)
+    n = 256
+    for pdrop in (0.1, 0.5):
+        t = orc.dropout_threshold(pdrop)
+        keep = 1 - t / 256
+        z0 = orc.dropout_keep(0, 0, np.arange(n), np.arange(n), pdrop, 123)
+        z1 = orc.dropout_keep(0, 1, np.arange(n), np.arange(n), pdrop, 123)
+        z2 = orc.dropout_keep(1, 0, np.arange(n), np.arange(n), pdrop, 123)
+        z3 = orc.dropout_keep(0, 0, np.arange(n), np.arange(n), pdrop, 124)
+        m = n * n
+        assert abs(z0.mean() - keep) <= 6 * math.sqrt(keep * (1 - keep) / m)
+        agree = keep ** 2 + (1 - keep) ** 2
+        for other in (z1, z2, z3, z0.T):
+            assert abs((z0 == other).mean() - agree) <= 6 * math.sqrt(agree * (1 - agree) / m)
+        # any sub-block is the same pairs' slice of the whole
+        np.testing.assert_array_equal(orc.dropout_keep(0, 0, np.arange(5, 21), np.arange(3, 41), pdrop, 123),
+                                      z0[5:21, 3:41])
+    # unbiased: the mean over seeds approaches the undropped output
+    acc = np.zeros_like(o0)
+    S = 400
+    for sd in range(S):
+        acc += orc.forward_dropout(q, k, v, 0.5, 0.3, 1000 + sd, causal=True)[0]
+    err = np.abs(acc / S - o0).max()
+    assert err < 6 * np.abs(v).max() / math.sqrt(S), err
+    # library: torch autograd of the dropped expression with the oracle's mask
+    pdrop, seed = 0.25, 99
+    c = 256.0 / (256 - orc.dropout_threshold(pdrop))
+    tq, tk, tv = (torch.tensor(x, requires_grad=True) for x in (q, k, v))
+    z = torch.stack([torch.stack([torch.tensor(orc.dropout_keep(b_, h, np.arange(N), np.arange(N), pdrop, seed))
+                                  for h in range(H)]) for b_ in range(B)])
+    s_ = 0.5 * tq @ tk.transpose(-1, -2)
+    s_ = s_.masked_fill(~torch.ones(N, N, dtype=torch.bool).tril(), float("-inf"))
+    out = (torch.softmax(s_, dim=-1) * z * c) @ tv
+    out.backward(torch.tensor(do))
+    o_d, _ = orc.forward_dropout(q, k, v, 0.5, pdrop, seed, causal=True)
+    dq, dk, dv, _ = orc.backward_dropout(q, k, v, do, 0.5, pdrop, seed, causal=True)
+    np.testing.assert_allclose(o_d, out.detach().numpy(), atol=1e-13)
+    np.testing.assert_allclose(dq, tq.grad.numpy(), atol=1e-12)
+    np.testing.assert_allclose(dk, tk.grad.numpy(), atol=1e-12)
+    np.testing.assert_allclose(dv, tv.grad.numpy(), atol=1e-12)
+    # finite differences with the mask fixed by the seed
+    qs, ks, vs, dos = (x[:, :1, :9, :3].copy() for x in (q, k, v, do))
+    g = orc.backward_dropout(qs, ks, vs, dos, 0.7, 0.4, 5)
+    eps = 1e-6
+    for idx, x in enumerate((qs, ks, vs)):
+        num = np.zeros_like(x)
+        it = np.nditer(x, flags=["multi_index"])
+        for _ in it:
+            mi = it.multi_index
+            x[mi] += eps
+            fp = (orc.forward_dropout(qs, ks, vs, 0.7, 0.4, 5)[0] * dos).sum()
+            x[mi] -= 2 * eps
+            fm = (orc.forward_dropout(qs, ks, vs, 0.7, 0.4, 5)[0] * dos).sum()
+            x[mi] += eps
+            num[mi] = (fp - fm) / (2 * eps)
+        rel = np.linalg.norm(num - g[idx]) / max(np.linalg.norm(num), 1e-30)
+        assert rel < 1e-6, (idx, rel)
+
+
 ALL_PINS = [pin_worked_example, pin_closed_forms, pin_invariants, pin_backward_fd,
-            pin_dvec, pin_backward_rows, pin_library, pin_block_masks, pin_decode]
+            pin_dvec, pin_backward_rows, pin_library, pin_block_masks, pin_decode, pin_philox, pin_dropout]

@@ -10,7 +10,8 @@ from tests import oracle_pins as pins
 _real = {name: getattr(orc, name) for name in
          ("_scores", "_apply_mask", "_row_softmax", "_softmax_backward", "visible",
           "forward", "backward", "tiled_forward", "_lse", "window_block_mask", "dilated_block_mask",
-          "decode_visible", "decode", "decode_split")}
+          "decode_visible", "decode", "decode_split", "philox4x32_10", "dropout_bytes",
+          "forward_dropout", "backward_dropout")}
 
 
 def _m_no_scale(q, k, scale):
@@ -175,6 +176,48 @@ def _m_split_unweighted(q, k, v, scale, chunk, seqlens=None, causal=False):
     return o, lse
 
 
+def _m_philox_no_bump(ctr, key):
+    """Philox with the key held fixed across rounds."""
+    c = np.array(ctr, dtype=np.uint64) & 0xFFFFFFFF
+    k0, k1 = int(key[0]) & 0xFFFFFFFF, int(key[1]) & 0xFFFFFFFF
+    mask = np.uint64(0xFFFFFFFF)
+    for _ in range(10):
+        p0 = c[..., 0] * np.uint64(0xD2511F53)
+        p1 = c[..., 2] * np.uint64(0xCD9E8D57)
+        c = np.stack([(p1 >> np.uint64(32)) ^ c[..., 1] ^ np.uint64(k0), p1 & mask,
+                      (p0 >> np.uint64(32)) ^ c[..., 3] ^ np.uint64(k1), p0 & mask], axis=-1)
+    return c.astype(np.uint32)
+
+
+def _m_dropout_transposed(b, h, rows, cols, seed):
+    return _real["dropout_bytes"](b, h, cols, rows, seed).T
+
+
+def _m_dropout_unscaled(q, k, v, scale, p, seed, causal=False, block_mask=None, block=128):
+    o, lse = _real["forward_dropout"](q, k, v, scale, p, seed, causal, block_mask, block)
+    return o * (256 - orc.dropout_threshold(p)) / 256.0, lse
+
+
+def _m_dropout_bwd_no_mask_in_dp(q, k, v, do, scale, p, seed, causal=False, block_mask=None, block=128):
+    q, k, v, do = (np.asarray(x, dtype=np.float64) for x in (q, k, v, do))
+    B, H, N, _ = q.shape
+    c = 256.0 / (256 - orc.dropout_threshold(p))
+    dq, dk, dv = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
+    dvec = np.zeros((B, H, N))
+    for b in range(B):
+        for h in range(H):
+            pr, _ = orc.head_probs(q[b, h], k[b, h], scale, causal, block_mask, block)
+            zc = orc.dropout_keep(b, h, np.arange(N), np.arange(k.shape[2]), p, seed) * c
+            dv[b, h] = (pr * zc).T @ do[b, h]
+            dp = do[b, h] @ v[b, h].T                       # planted mistake: mask not applied
+            d_row = (pr * dp).sum(axis=1)
+            ds = pr * (dp - d_row[:, None])
+            dq[b, h] = scale * (ds @ k[b, h])
+            dk[b, h] = scale * (ds.T @ q[b, h])
+            dvec[b, h] = d_row
+    return dq, dk, dv, dvec
+
+
 MUTANTS = {
     "scale_dropped": ("_scores", _m_no_scale),
     "scores_transposed": ("_scores", _m_transposed_scores),
@@ -197,6 +240,10 @@ MUTANTS = {
     "decode_causal_strict": ("decode_visible", _m_decode_strict),
     "decode_ignores_seqlens": ("decode", _m_decode_no_seqlens),
     "decode_split_unweighted": ("decode_split", _m_split_unweighted),
+    "philox_key_not_advanced": ("philox4x32_10", _m_philox_no_bump),
+    "dropout_mask_transposed": ("dropout_bytes", _m_dropout_transposed),
+    "dropout_output_unscaled": ("forward_dropout", _m_dropout_unscaled),
+    "dropout_grad_mask_missing": ("backward_dropout", _m_dropout_bwd_no_mask_in_dp),
 }
 
 
