@@ -110,6 +110,20 @@ int check_shape(int B, int H, int N, int d) {
 
 int check_scale(float scale) { return (std::isfinite(scale) && scale > 0.f) ? FA_OK : FA_ERR_INVALID; }
 
+int check_dropout(float p) { return (std::isfinite(p) && p >= 0.f && p < 1.f) ? FA_OK : FA_ERR_INVALID; }
+
+// Byte threshold t = round(256 p) (at most 255), and the keep scale 256 / (256 - t).
+fa::Dropout make_dropout(float p, unsigned long long seed) {
+  fa::Dropout d;
+  const double t = std::floor(256.0 * static_cast<double>(p) + 0.5);
+  d.t = static_cast<uint32_t>(t > 255.0 ? 255.0 : t);
+  d.add = (256u - d.t) * 0x00010001u;
+  d.scale = static_cast<float>(256.0 / (256.0 - d.t));
+  d.seed_lo = static_cast<uint32_t>(seed & 0xFFFFFFFFull);
+  d.seed_hi = static_cast<uint32_t>(seed >> 32);
+  return d;
+}
+
 int check_ptrs(std::initializer_list<const void*> ps) {
   for (const void* p : ps)
     if (p == nullptr || !aligned16(p)) return FA_ERR_INVALID;
@@ -151,8 +165,10 @@ Workspace carve(void* ws, int B, int H, int N, int d) {
 }
 
 int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, const uint8_t* block_mask,
-             int B, int H, int N, int d, float scale, int mask_kind, fa_stream_t stream) {
+             int B, int H, int N, int d, float scale, int mask_kind, float dropout_p, unsigned long long seed,
+             fa_stream_t stream) {
   int rc;
+  if ((rc = check_dropout(dropout_p)) != FA_OK) return rc;
   if ((rc = check_ptrs({q, k, v, o, lse})) != FA_OK) return rc;
   if ((mask_kind & fa::MASK_BLOCK) && block_mask == nullptr) return FA_ERR_INVALID;
   if ((rc = check_shape(B, H, N, d)) != FA_OK) return rc;
@@ -179,6 +195,8 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, c
   p.n_pairs = (p.n_qt + 1) / 2;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.mask_kind = mask_kind;
+  p.H = H;
+  p.drop = make_dropout(dropout_p, seed);
   if (log_enabled())
     std::fprintf(stderr, "[fa] fwd B=%d H=%d N=%d d=%d mask=%d grid=%d\n", B, H, N, d, mask_kind, p.n_pairs * BH);
   return fa::launch_fwd(p, d, reinterpret_cast<cudaStream_t>(stream));
@@ -186,8 +204,9 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, c
 
 int bwd_main_impl(const void* q, const void* k, const void* v, const void* dout, const uint8_t* block_mask,
                   void* dk, void* dv, void* workspace, int B, int H, int N, int d, float scale, int mask_kind,
-                  fa_stream_t stream) {
+                  float dropout_p, unsigned long long seed, fa_stream_t stream) {
   int rc;
+  if ((rc = check_dropout(dropout_p)) != FA_OK) return rc;
   if ((rc = check_ptrs({q, k, v, dout, dk, dv, workspace})) != FA_OK) return rc;
   if (mask_kind < 0 || mask_kind > 3) return FA_ERR_INVALID;
   if ((mask_kind & fa::MASK_BLOCK) && block_mask == nullptr) return FA_ERR_INVALID;
@@ -222,6 +241,8 @@ int bwd_main_impl(const void* q, const void* k, const void* v, const void* dout,
   p.scale = scale;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.mask_kind = mask_kind;
+  p.H = H;
+  p.drop = make_dropout(dropout_p, seed);
   if (log_enabled())
     std::fprintf(stderr, "[fa] bwd B=%d H=%d N=%d d=%d mask=%d bq=%d\n", B, H, N, d, mask_kind, bq);
   return fa::launch_bwd_main(p, d, reinterpret_cast<cudaStream_t>(stream));
@@ -257,8 +278,9 @@ int convert_impl(const void* workspace, void* dq, int B, int H, int N, int d, fl
 
 int bwd_impl(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
              const uint8_t* block_mask, void* dq, void* dk, void* dv, void* workspace, int B, int H, int N, int d,
-             float scale, int mask_kind, fa_stream_t stream) {
+             float scale, int mask_kind, float dropout_p, unsigned long long seed, fa_stream_t stream) {
   int rc;
+  if ((rc = check_dropout(dropout_p)) != FA_OK) return rc;
   // validate everything first so that nothing is enqueued on a bad call
   if ((rc = check_ptrs({q, k, v, o, dout, lse, dq, dk, dv, workspace})) != FA_OK) return rc;
   if ((mask_kind & fa::MASK_BLOCK) && block_mask == nullptr) return FA_ERR_INVALID;
@@ -266,8 +288,8 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* o, const v
   if ((rc = check_scale(scale)) != FA_OK) return rc;
   if ((mask_kind & fa::MASK_BLOCK) && tiles(N) > fa::MAX_SPARSE_TILES) return FA_ERR_UNSUPPORTED;
   if ((rc = preprocess_impl(o, dout, lse, workspace, B, H, N, d, stream)) != FA_OK) return rc;
-  if ((rc = bwd_main_impl(q, k, v, dout, block_mask, dk, dv, workspace, B, H, N, d, scale, mask_kind,
-                          stream)) != FA_OK)
+  if ((rc = bwd_main_impl(q, k, v, dout, block_mask, dk, dv, workspace, B, H, N, d, scale, mask_kind, dropout_p,
+                          seed, stream)) != FA_OK)
     return rc;
   return convert_impl(workspace, dq, B, H, N, d, scale, stream);
 }
@@ -409,13 +431,14 @@ const char* fa_status_string(int status) {
 
 int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
            float scale, int causal, fa_stream_t stream) {
-  return fwd_impl(q, k, v, o, lse, nullptr, B, H, N, d, scale, causal ? fa::MASK_CAUSAL : fa::MASK_NONE, stream);
+  return fwd_impl(q, k, v, o, lse, nullptr, B, H, N, d, scale, causal ? fa::MASK_CAUSAL : fa::MASK_NONE, 0.f, 0,
+                  stream);
 }
 
 int fa_fwd_blocksparse(const void* q, const void* k, const void* v, void* o, float* lse, const uint8_t* block_mask,
                        int B, int H, int N, int d, float scale, int causal, fa_stream_t stream) {
   return fwd_impl(q, k, v, o, lse, block_mask, B, H, N, d, scale, causal ? fa::MASK_BLOCK_CAUSAL : fa::MASK_BLOCK,
-                  stream);
+                  0.f, 0, stream);
 }
 
 size_t fa_bwd_workspace_bytes(int B, int H, int N, int d) {
@@ -428,14 +451,14 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
            void* dk, void* dv, void* workspace, int B, int H, int N, int d, float scale, int causal,
            fa_stream_t stream) {
   return bwd_impl(q, k, v, o, dout, lse, nullptr, dq, dk, dv, workspace, B, H, N, d, scale,
-                  causal ? fa::MASK_CAUSAL : fa::MASK_NONE, stream);
+                  causal ? fa::MASK_CAUSAL : fa::MASK_NONE, 0.f, 0, stream);
 }
 
 int fa_bwd_blocksparse(const void* q, const void* k, const void* v, const void* o, const void* dout,
                        const float* lse, const uint8_t* block_mask, void* dq, void* dk, void* dv, void* workspace,
                        int B, int H, int N, int d, float scale, int causal, fa_stream_t stream) {
   return bwd_impl(q, k, v, o, dout, lse, block_mask, dq, dk, dv, workspace, B, H, N, d, scale,
-                  causal ? fa::MASK_BLOCK_CAUSAL : fa::MASK_BLOCK, stream);
+                  causal ? fa::MASK_BLOCK_CAUSAL : fa::MASK_BLOCK, 0.f, 0, stream);
 }
 
 int fa_bwd_preprocess(const void* o, const void* dout, const float* lse, void* workspace, int B, int H, int N, int d,
@@ -444,9 +467,25 @@ int fa_bwd_preprocess(const void* o, const void* dout, const float* lse, void* w
 }
 
 int fa_bwd_main(const void* q, const void* k, const void* v, const void* dout, const uint8_t* block_mask, void* dk,
-                void* dv, void* workspace, int B, int H, int N, int d, float scale, int mask_kind,
-                fa_stream_t stream) {
-  return bwd_main_impl(q, k, v, dout, block_mask, dk, dv, workspace, B, H, N, d, scale, mask_kind, stream);
+                void* dv, void* workspace, int B, int H, int N, int d, float scale, int mask_kind, float dropout_p,
+                unsigned long long seed, fa_stream_t stream) {
+  return bwd_main_impl(q, k, v, dout, block_mask, dk, dv, workspace, B, H, N, d, scale, mask_kind, dropout_p, seed,
+                       stream);
+}
+
+int fa_fwd_dropout(const void* q, const void* k, const void* v, void* o, float* lse, const uint8_t* block_mask, int B,
+                   int H, int N, int d, float scale, int causal, float dropout_p, unsigned long long seed,
+                   fa_stream_t stream) {
+  const int kind = (block_mask ? fa::MASK_BLOCK : 0) | (causal ? fa::MASK_CAUSAL : 0);
+  return fwd_impl(q, k, v, o, lse, block_mask, B, H, N, d, scale, kind, dropout_p, seed, stream);
+}
+
+int fa_bwd_dropout(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
+                   const uint8_t* block_mask, void* dq, void* dk, void* dv, void* workspace, int B, int H, int N, int d,
+                   float scale, int causal, float dropout_p, unsigned long long seed, fa_stream_t stream) {
+  const int kind = (block_mask ? fa::MASK_BLOCK : 0) | (causal ? fa::MASK_CAUSAL : 0);
+  return bwd_impl(q, k, v, o, dout, lse, block_mask, dq, dk, dv, workspace, B, H, N, d, scale, kind, dropout_p, seed,
+                  stream);
 }
 
 int fa_bwd_dq_convert(const void* workspace, void* dq, int B, int H, int N, int d, float scale, fa_stream_t stream) {
@@ -564,5 +603,5 @@ extern "C" int fa_bwd_noalloc(const void* q, const void* k, const void* v, const
   void* ws = nullptr;
   if ((rc = scratch_ready(&ws)) != FA_OK) return rc;
   return bwd_impl(q, k, v, o, dout, lse, nullptr, dq, dk, dv, ws, B, H, N, d, scale,
-                  causal ? fa::MASK_CAUSAL : fa::MASK_NONE, stream);
+                  causal ? fa::MASK_CAUSAL : fa::MASK_NONE, 0.f, 0, stream);
 }

@@ -33,6 +33,7 @@
 // tensor memory into the fp32 accumulator; 12 issues MMAs; 13 loads K_j, V_j
 // once and Q_i, dO_i, LSE_i, D_i per step into a two-stage ring.
 #include "fa_common.cuh"
+#include "fa_dropout.cuh"
 #include "fa_ptx.cuh"
 
 namespace fa {
@@ -145,11 +146,14 @@ __device__ __forceinline__ void mbar_drain_b(uint32_t bar, uint32_t parity, uint
 // P = exp2(S^T * scale * log2 e - LSE * log2 e), dS = P (dP - D), packed as
 // bf16 pairs.  nlse and nd hold -LSE * log2 e and -D per query column.
 // MASKED: P = 0 where the query q (q_base + column) is at or past q_end, or,
-// causal, where q < key.
-template <bool MASKED>
+// causal, where q < key.  DROP: with Z the keep bit of the pair (keep_bit
+// layout of `keep`) and c the dropout scale, the dV operand is P Z c and
+// dS = P (Z c dP~ - D), dP~ = dO V^T being the gradient of the dropped P.
+template <bool MASKED, bool DROP>
 __device__ __forceinline__ void recompute32(const uint32_t (&sr)[32], const uint32_t (&dr)[32], const float* nlse,
                                             const float* nd, int c0, float2 sl2v, int q_base, int q_end, int key,
-                                            bool causal, uint32_t (&pt_pk)[16], uint32_t (&ds_pk)[16]) {
+                                            bool causal, uint32_t keep, float dscale, uint32_t (&pt_pk)[16],
+                                            uint32_t (&ds_pk)[16]) {
 #pragma unroll
   for (int j = 0; j < 4; ++j) {                        // 8 queries per group
     const int cq = c0 + 8 * j;
@@ -171,14 +175,24 @@ __device__ __forceinline__ void recompute32(const uint32_t (&sr)[32], const uint
         if (!(q0 < q_end && (!causal || q0 >= key))) pv.x = 0.f;
         if (!(q0 + 1 < q_end && (!causal || q0 + 1 >= key))) pv.y = 0.f;
       }
-      const float2 ds = fmul2(pv, fadd2(make_float2(__uint_as_float(dr[k]), __uint_as_float(dr[k + 1])), ndv[e]));
-      pt_pk[4 * j + e] = pack_bf16x2(pv.x, pv.y);
-      ds_pk[4 * j + e] = pack_bf16x2(ds.x, ds.y);
+      const float2 dpv = make_float2(__uint_as_float(dr[k]), __uint_as_float(dr[k + 1]));
+      if constexpr (DROP) {
+        const uint32_t f = keep >> keep_bit(k);             // columns k, k + 1: adjacent bits
+        const float2 zc = make_float2((f & 1u) ? dscale : 0.f, (f & 2u) ? dscale : 0.f);
+        const float2 ptv = fmul2(pv, zc);
+        const float2 ds = fmul2(pv, ffma2(zc, dpv, ndv[e]));
+        pt_pk[4 * j + e] = pack_bf16x2(ptv.x, ptv.y);
+        ds_pk[4 * j + e] = pack_bf16x2(ds.x, ds.y);
+      } else {
+        const float2 ds = fmul2(pv, fadd2(dpv, ndv[e]));
+        pt_pk[4 * j + e] = pack_bf16x2(pv.x, pv.y);
+        ds_pk[4 * j + e] = pack_bf16x2(ds.x, ds.y);
+      }
     }
   }
 }
 
-template <int D>
+template <int D, bool DROP>
 __global__ void __launch_bounds__(448, 1) fa_bwd_kernel(const __grid_constant__ BwdParams p) {
   using L = BwdLayout<D>;
   constexpr int BQ = L::BQ;
@@ -407,10 +421,24 @@ __global__ void __launch_bounds__(448, 1) fa_bwd_kernel(const __grid_constant__ 
     const int key = kt * TILE + r;
     const uint32_t lane_base = quarter * 32;
     const float2 sl2v = make_float2(p.scale_log2, p.scale_log2);
+    const uint32_t hd = static_cast<uint32_t>(bh % p.H), bd = static_cast<uint32_t>(bh / p.H);
     bool ok = true;
     for (int i = 0; i < n_steps && ok; ++i) {
       const int qi = sched.qi(i);
       const int st = i % L::STAGES;
+      constexpr int COLS = BQ / 2;                           // query columns of this warp
+      // dropout keep bits of this key row for the warp's query columns, made
+      // before S^T and dP^T are waited for
+      uint32_t keep[COLS / 32];
+      if constexpr (DROP) {
+#pragma unroll
+        for (int cc = 0; cc < COLS / 32; ++cc)
+          keep[cc] = keep_bits_col(key, qi * BQ + half * COLS + 32 * cc, hd, bd, p.drop.seed_lo, p.drop.seed_hi,
+                                   p.drop.add, lane & 3u);
+      } else {
+#pragma unroll
+        for (int cc = 0; cc < COLS / 32; ++cc) keep[cc] = 0;
+      }
       if (!(ok = mbar_wait_warp(bar(L::B_SDP), i & 1, wc))) break;
       tc_fence_after();
       const uint8_t* stage = smem + L::RING_OFF + st * L::STAGE_BYTES;
@@ -423,7 +451,6 @@ __global__ void __launch_bounds__(448, 1) fa_bwd_kernel(const __grid_constant__ 
       const bool causal = (p.mask_kind & MASK_CAUSAL) != 0;
       const bool key_ok = key < p.N;
       const bool need_mask = (causal && qi * BQ < kt * TILE + TILE) || !key_ok || qi * BQ + BQ > p.N;
-      constexpr int COLS = BQ / 2;                           // query columns of this warp
 #pragma unroll 1
       for (int c0 = half * COLS; c0 < (half + 1) * COLS; c0 += 32) {
         uint32_t sr[32], dr[32];
@@ -438,10 +465,12 @@ __global__ void __launch_bounds__(448, 1) fa_bwd_kernel(const __grid_constant__ 
         // shared-memory stores in between, so the LSE/D loads can be hoisted);
         // the masked form only for steps that need it (causal diagonal, past N)
         uint32_t pt_pk[16], ds_pk[16];
+        const uint32_t kp = keep[(c0 - half * COLS) / 32];
         if (need_mask)
-          recompute32<true>(sr, dr, lse, dvec, c0, sl2v, qi * BQ, key_ok ? p.N : -1, key, causal, pt_pk, ds_pk);
+          recompute32<true, DROP>(sr, dr, lse, dvec, c0, sl2v, qi * BQ, key_ok ? p.N : -1, key, causal, kp,
+                                  p.drop.scale, pt_pk, ds_pk);
         else
-          recompute32<false>(sr, dr, lse, dvec, c0, sl2v, 0, 0, 0, false, pt_pk, ds_pk);
+          recompute32<false, DROP>(sr, dr, lse, dvec, c0, sl2v, 0, 0, 0, false, kp, p.drop.scale, pt_pk, ds_pk);
         // pass 2: stores, once the buffers they overwrite have been consumed
         if (c0 == half * COLS) {
           if constexpr (L::P_TMEM) {
@@ -576,21 +605,22 @@ __global__ void __launch_bounds__(448, 1) fa_bwd_kernel(const __grid_constant__ 
   }
 }
 
-template <int D>
+template <int D, bool DROP>
 static int launch_bwd_t(const BwdParams& p, cudaStream_t stream) {
   using L = BwdLayout<D>;
   static_assert(L::SMEM_BYTES <= 232448, "shared memory budget");
-  if (cudaFuncSetAttribute(fa_bwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM_BYTES) !=
+  if (cudaFuncSetAttribute(fa_bwd_kernel<D, DROP>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM_BYTES) !=
       cudaSuccess)
     return -4;
   const unsigned grid = static_cast<unsigned>(p.n_kt) * static_cast<unsigned>(p.BH);
-  fa_bwd_kernel<D><<<grid, L::THREADS, L::SMEM_BYTES, stream>>>(p);
+  fa_bwd_kernel<D, DROP><<<grid, L::THREADS, L::SMEM_BYTES, stream>>>(p);
   return cudaGetLastError() == cudaSuccess ? 0 : -4;
 }
 
 int launch_bwd_main(const BwdParams& p, int d, cudaStream_t stream) {
-  if (d == 128) return launch_bwd_t<128>(p, stream);
-  if (d == 64) return launch_bwd_t<64>(p, stream);
+  const bool drop = p.drop.t != 0;
+  if (d == 128) return drop ? launch_bwd_t<128, true>(p, stream) : launch_bwd_t<128, false>(p, stream);
+  if (d == 64) return drop ? launch_bwd_t<64, true>(p, stream) : launch_bwd_t<64, false>(p, stream);
   return -2;
 }
 

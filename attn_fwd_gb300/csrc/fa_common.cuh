@@ -22,6 +22,16 @@ constexpr int TILE = 128;
 // (N <= 131072).
 constexpr int MAX_SPARSE_TILES = 1024;
 
+// Dropout with regenerated masks (fa_dropout.cuh): kept iff the pair's random
+// byte >= t, values scaled by 256 / (256 - t).  t = 0 switches it off.
+struct Dropout {
+  uint32_t t;                // byte threshold, 0..255
+  uint32_t add;              // (256 - t) in both 16-bit halves
+  float scale;               // 256 / (256 - t)
+  uint32_t seed_lo;
+  uint32_t seed_hi;
+};
+
 // Forward launch parameters.  Tensor maps describe Q, K, V as 3-D bf16
 // arrays [B*H][N][d] with a {64, 128, 1} box and 128-byte swizzle.
 struct FwdParams {
@@ -39,6 +49,8 @@ struct FwdParams {
   int n_pairs;               // ceil(n_qt / 2): each CTA owns two query tiles
   float scale_log2;          // scale * log2(e)
   int mask_kind;
+  int H;                     // heads: (b, h) = divmod(bh, H) keys the dropout generator
+  Dropout drop;
 };
 
 // Backward main-kernel parameters.  Q and dO use a {64, BQ, 1} box, K and V a
@@ -63,6 +75,8 @@ struct BwdParams {
   float scale;
   float scale_log2;
   int mask_kind;
+  int H;
+  Dropout drop;
 };
 
 // Decoding against a key/value cache: keys per shared-memory stage, and the

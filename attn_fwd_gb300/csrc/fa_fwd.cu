@@ -35,6 +35,7 @@
 // columns of S_w.  tcgen05 MMAs issued by one thread execute in order, so the
 // next S_w(j+1) never overwrites P_w(j) before O_w += P_w(j) V_j has read it.
 #include "fa_common.cuh"
+#include "fa_dropout.cuh"
 #include "fa_ptx.cuh"
 
 namespace fa {
@@ -129,7 +130,7 @@ __device__ __forceinline__ void mbar_drain(uint32_t bar, uint32_t parity, uint64
   }
 }
 
-template <int D, bool SPARSE>
+template <int D, bool SPARSE, bool DROP>
 __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ FwdParams p) {
   using L = FwdLayout<D, SPARSE>;
   extern __shared__ uint8_t smem_raw[];
@@ -468,7 +469,20 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
       const int last_kt = SPARSE ? last_visible(w ? bits1 : bits0, p.n_qt) : n_vis - 1;
       int last_lim = p.N - last_kt * TILE;
       if ((p.mask_kind & MASK_CAUSAL) && last_kt == qt) last_lim = min(last_lim, row + 1);
+      // dropout: key tile of this round (only tracked when needed) and the
+      // keep bits of this row's 128 columns, made before S is waited for
+      int kt_d = DROP ? (SPARSE ? next_visible(w ? bits1 : bits0, 0, p.n_qt) : 0) : 0;
+      const uint32_t bh_u = static_cast<uint32_t>(blockIdx.x % p.BH);
+      const uint32_t hd = bh_u % static_cast<uint32_t>(p.H), bd = bh_u / static_cast<uint32_t>(p.H);
       for (int rr = 0; rr < n_vis; ++rr) {
+        uint32_t dbits[4];
+        if constexpr (DROP) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            dbits[q] = keep_bits_row(qt * TILE + row, kt_d * TILE + 32 * q, hd, bd, p.drop.seed_lo, p.drop.seed_hi,
+                                     p.drop.add, lane & 3u);
+          kt_d = SPARSE ? next_visible(w ? bits1 : bits0, kt_d + 1, p.n_qt) : kt_d + 1;
+        }
         if (!mbar_wait_warp(bar(L::B_S + w), sphase, wc)) { ok = false; break; }
         sphase ^= 1u;
         tc_fence_after();
@@ -502,7 +516,8 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
         // bf16 pairs go to tensor memory 32 columns at a time while the next
         // 32 are computed.  l sums the fp32 values (for LSE); lr sums the
         // bf16-rounded values that P V multiplies, so O / lr weighs the V rows
-        // with weights summing to exactly one.
+        // with weights summing to exactly one.  Dropout zeroes the dropped
+        // pairs of the P V operand only: l and lr are the softmax's own sums.
         const float2 sl2v = make_float2(sl2, sl2);
         const float2 negm = make_float2(-m, -m);
         float2 la = make_float2(0.f, 0.f), lb = la, ra = la, rb = la;
@@ -513,13 +528,19 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
           for (int e = 0; e < 16; ++e) {
             const float2 x = ffma2(make_float2(s[32 * q + 2 * e], s[32 * q + 2 * e + 1]), sl2v, negm);
             const float2 pv = make_float2(ex2_approx(x.x), ex2_approx(x.y));
-            pk[e] = pack_bf16x2(pv.x, pv.y);
+            const uint32_t pku = pack_bf16x2(pv.x, pv.y);
             if (e & 1) {
               lb = fadd2(lb, pv);
-              add_bf16x2_to_f32(rb, pk[e]);
+              add_bf16x2_to_f32(rb, pku);
             } else {
               la = fadd2(la, pv);
-              add_bf16x2_to_f32(ra, pk[e]);
+              add_bf16x2_to_f32(ra, pku);
+            }
+            if constexpr (DROP) {
+              const uint32_t f = dbits[q] >> keep_bit(2 * e);   // columns 2e, 2e+1: adjacent bits
+              pk[e] = pku & (((f & 1u) ? 0x0000FFFFu : 0u) | ((f & 2u) ? 0xFFFF0000u : 0u));
+            } else {
+              pk[e] = pku;
             }
           }
           tmem_st_x16_async(s_addr + 16 * q, pk);
@@ -553,7 +574,7 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
           ok = mbar_wait_warp(bar(L::B_O + w), 0, wc);
           if (ok) {
             tc_fence_after();
-            const float inv_l = 1.f / lr;
+            const float inv_l = DROP ? p.drop.scale / lr : 1.f / lr;
 #pragma unroll 1
             for (int c = 0; c < D; c += 32) {
               uint32_t ov[32];
@@ -590,22 +611,29 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
   }
 }
 
-template <int D, bool SPARSE>
+template <int D, bool SPARSE, bool DROP>
 static int launch_fwd_t(const FwdParams& p, cudaStream_t stream) {
   using L = FwdLayout<D, SPARSE>;
   static_assert(L::SMEM_BYTES <= 232448, "shared memory budget");
-  cudaError_t e = cudaFuncSetAttribute(fa_fwd_kernel<D, SPARSE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaError_t e = cudaFuncSetAttribute(fa_fwd_kernel<D, SPARSE, DROP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        L::SMEM_BYTES);
   if (e != cudaSuccess) return -4;
   const unsigned grid = static_cast<unsigned>(p.n_pairs) * static_cast<unsigned>(p.BH);
-  fa_fwd_kernel<D, SPARSE><<<grid, L::THREADS, L::SMEM_BYTES, stream>>>(p);
+  fa_fwd_kernel<D, SPARSE, DROP><<<grid, L::THREADS, L::SMEM_BYTES, stream>>>(p);
   return cudaGetLastError() == cudaSuccess ? 0 : -4;
 }
 
 int launch_fwd(const FwdParams& p, int d, cudaStream_t stream) {
   const bool sparse = (p.mask_kind & MASK_BLOCK) != 0;
-  if (d == 128) return sparse ? launch_fwd_t<128, true>(p, stream) : launch_fwd_t<128, false>(p, stream);
-  if (d == 64) return sparse ? launch_fwd_t<64, true>(p, stream) : launch_fwd_t<64, false>(p, stream);
+  const bool drop = p.drop.t != 0;
+  if (d == 128) {
+    if (drop) return sparse ? launch_fwd_t<128, true, true>(p, stream) : launch_fwd_t<128, false, true>(p, stream);
+    return sparse ? launch_fwd_t<128, true, false>(p, stream) : launch_fwd_t<128, false, false>(p, stream);
+  }
+  if (d == 64) {
+    if (drop) return sparse ? launch_fwd_t<64, true, true>(p, stream) : launch_fwd_t<64, false, true>(p, stream);
+    return sparse ? launch_fwd_t<64, true, false>(p, stream) : launch_fwd_t<64, false, false>(p, stream);
+  }
   return -2;
 }
 

@@ -40,7 +40,9 @@ _SIGS = {
     "fa_bwd": (_i, [_vp] * 10 + [_i, _i, _i, _i, _f, _i, _vp]),
     "fa_bwd_blocksparse": (_i, [_vp] * 11 + [_i, _i, _i, _i, _f, _i, _vp]),
     "fa_bwd_preprocess": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp]),
-    "fa_bwd_main": (_i, [_vp] * 8 + [_i, _i, _i, _i, _f, _i, _vp]),
+    "fa_bwd_main": (_i, [_vp] * 8 + [_i, _i, _i, _i, _f, _i, _f, _u64, _vp]),
+    "fa_fwd_dropout": (_i, [_vp] * 6 + [_i, _i, _i, _i, _f, _i, _f, _u64, _vp]),
+    "fa_bwd_dropout": (_i, [_vp] * 11 + [_i, _i, _i, _i, _f, _i, _f, _u64, _vp]),
     "fa_bwd_dq_convert": (_i, [_vp, _vp, _i, _i, _i, _i, _f, _vp]),
     "fa_bwd_noalloc": (_i, [_vp] * 9 + [_i, _i, _i, _i, _f, _i, _vp]),
     "fa_decode_workspace_bytes": (_sz, [_i, _i, _i, _i, _i]),
@@ -172,13 +174,32 @@ def fa_bwd_preprocess(o, do, lse, workspace, stream=None):
     _check("fa_bwd_preprocess", rc)
 
 
-def fa_bwd_main(q, k, v, do, block_mask, dk, dv, workspace, scale, mask_kind, stream=None):
+def fa_bwd_main(q, k, v, do, block_mask, dk, dv, workspace, scale, mask_kind, dropout_p=0.0, seed=0,
+                stream=None):
     B, H, N, d = q.shape
     rc = load().fa_bwd_main(_bf16(q, "q"), _bf16(k, "k"), _bf16(v, "v"), _bf16(do, "do"),
                             _mask_ptr(block_mask), _bf16(dk, "dk"), _bf16(dv, "dv"),
                             ctypes.c_void_p(workspace.data_ptr()), B, H, N, d, float(scale), int(mask_kind),
-                            _stream(stream))
+                            float(dropout_p), int(seed) & (2 ** 64 - 1), _stream(stream))
     _check("fa_bwd_main", rc)
+
+
+def fa_fwd_dropout(q, k, v, o, lse, block_mask, scale, causal, dropout_p, seed, stream=None):
+    B, H, N, d = q.shape
+    rc = load().fa_fwd_dropout(_bf16(q, "q"), _bf16(k, "k"), _bf16(v, "v"), _bf16(o, "o"), _f32(lse, "lse"),
+                               _mask_ptr(block_mask), B, H, N, d, float(scale), int(bool(causal)),
+                               float(dropout_p), int(seed) & (2 ** 64 - 1), _stream(stream))
+    _check("fa_fwd_dropout", rc)
+
+
+def fa_bwd_dropout(q, k, v, o, do, lse, block_mask, dq, dk, dv, workspace, scale, causal, dropout_p, seed,
+                   stream=None):
+    B, H, N, d = q.shape
+    rc = load().fa_bwd_dropout(_bf16(q, "q"), _bf16(k, "k"), _bf16(v, "v"), _bf16(o, "o"), _bf16(do, "do"),
+                               _f32(lse, "lse"), _mask_ptr(block_mask), _bf16(dq, "dq"), _bf16(dk, "dk"),
+                               _bf16(dv, "dv"), ctypes.c_void_p(workspace.data_ptr()), B, H, N, d, float(scale),
+                               int(bool(causal)), float(dropout_p), int(seed) & (2 ** 64 - 1), _stream(stream))
+    _check("fa_bwd_dropout", rc)
 
 
 def fa_bwd_dq_convert(workspace, dq, scale, stream=None):
@@ -252,13 +273,15 @@ def fa_debug_wait_timeout(ns: int, stream=None) -> int:
 # --------------------------------------------------------------------------- #
 # conveniences that allocate outputs
 # --------------------------------------------------------------------------- #
-def forward(q, k, v, causal=False, scale=None, block_mask=None, stream=None):
+def forward(q, k, v, causal=False, scale=None, block_mask=None, dropout_p=0.0, seed=0, stream=None):
     """Returns (O bf16 [B,H,N,d], LSE fp32 [B,H,N])."""
     B, H, N, d = q.shape
     scale = (1.0 / d ** 0.5) if scale is None else scale
     o = torch.empty_like(q)
     lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
-    if block_mask is not None:
+    if dropout_p:
+        fa_fwd_dropout(q, k, v, o, lse, block_mask, scale, causal, dropout_p, seed, stream)
+    elif block_mask is not None:
         fa_fwd_blocksparse(q, k, v, o, lse, block_mask, scale, causal, stream)
     else:
         fa_fwd(q, k, v, o, lse, scale, causal, stream)
@@ -285,13 +308,16 @@ def workspace(B, H, N, d, device) -> torch.Tensor:
     return torch.empty(n, dtype=torch.uint8, device=device)
 
 
-def backward(q, k, v, o, lse, do, causal=False, scale=None, block_mask=None, ws=None, stream=None):
+def backward(q, k, v, o, lse, do, causal=False, scale=None, block_mask=None, ws=None, dropout_p=0.0, seed=0,
+             stream=None):
     """Returns (dQ, dK, dV), bf16 [B,H,N,d]."""
     B, H, N, d = q.shape
     scale = (1.0 / d ** 0.5) if scale is None else scale
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     ws = workspace(B, H, N, d, q.device) if ws is None else ws
-    if block_mask is not None:
+    if dropout_p:
+        fa_bwd_dropout(q, k, v, o, do, lse, block_mask, dq, dk, dv, ws, scale, causal, dropout_p, seed, stream)
+    elif block_mask is not None:
         fa_bwd_blocksparse(q, k, v, o, do, lse, block_mask, dq, dk, dv, ws, scale, causal, stream)
     else:
         fa_bwd(q, k, v, o, do, lse, dq, dk, dv, ws, scale, causal, stream)

@@ -145,16 +145,44 @@ FA_API int fa_bwd_preprocess(const void *o, const void *dout, const float *lse, 
  * workspace's LSE, accumulate dK, dV (written as bf16) and add dS K into the
  * workspace's dQ accumulator.  Needs the workspace as stage 1 left it.
  * mask_kind: 0 none, 1 causal, 2 block (block_mask required), 3 causal and
- * block.
+ * block.  dropout_p, seed: as for fa_bwd_dropout (0 for none).
  */
 FA_API int fa_bwd_main(const void *q, const void *k, const void *v, const void *dout,
                 const uint8_t *block_mask, void *dk, void *dv,
                 void *workspace, int B, int H, int N, int d, float scale, int mask_kind,
-                fa_stream_t stream);
+                float dropout_p, unsigned long long seed, fa_stream_t stream);
 
 /* Backward stage 3 of 3: dQ = bf16(scale * accumulator). */
 FA_API int fa_bwd_dq_convert(const void *workspace, void *dq, int B, int H, int N, int d,
                       float scale, fa_stream_t stream);
+
+/*
+ * Attention with dropout on the probabilities, the masks regenerated in the
+ * backward instead of stored ("Как работает FlashAttention математически",
+ * section 5: only the statistics and the random masks' generator state are
+ * kept; "FlashAttention" notes, "Backward Pass of flashattention": masks are
+ * regenerated).  O = (P o Z) V / (1 - p'), with P the softmax (LSE is P's),
+ * Z the keep mask and p' the effective drop probability.
+ *
+ * Generator (the pages name none): Philox4x32-10 (Salmon, Moraes, Dror, Shaw,
+ * "Parallel random numbers: as easy as 1, 2, 3", SC'11), key = seed (low
+ * word first), counter = (j / 4, i / 4, h, b) for query i, key j; pair (i, j)
+ * takes byte j % 4 of output word i % 4 and is kept iff that byte >= t with
+ * t = round(256 dropout_p) (at most 255), so p' = t / 256 and kept values
+ * are scaled by 256 / (256 - t).  The same (seed, dropout_p) in the forward
+ * and the backward give the same mask.
+ *
+ * block_mask may be NULL (no block mask); causal as for fa_fwd.  dropout_p in
+ * [0, 1), else FA_ERR_INVALID.  Everything else as for fa_fwd / fa_bwd.
+ */
+FA_API int fa_fwd_dropout(const void *q, const void *k, const void *v, void *o, float *lse,
+                          const uint8_t *block_mask, int B, int H, int N, int d, float scale,
+                          int causal, float dropout_p, unsigned long long seed, fa_stream_t stream);
+FA_API int fa_bwd_dropout(const void *q, const void *k, const void *v, const void *o,
+                          const void *dout, const float *lse, const uint8_t *block_mask,
+                          void *dq, void *dk, void *dv, void *workspace,
+                          int B, int H, int N, int d, float scale, int causal,
+                          float dropout_p, unsigned long long seed, fa_stream_t stream);
 
 /*
  * Block masks for the sparse patterns that block-sparse attention serves

@@ -352,9 +352,12 @@ def dropout_keep(b: int, h: int, rows, cols, p: float, seed: int) -> np.ndarray:
     return dropout_bytes(b, h, rows, cols, seed) >= dropout_threshold(p)
 
 
-def forward_dropout(q, k, v, scale, p: float, seed: int, causal=False, block_mask=None, block=128):
+def forward_dropout(q, k, v, scale, p: float, seed: int, causal=False, block_mask=None, block=128,
+                    b0: int = 0, h0: int = 0):
     """O = (P o Z) V * 256 / (256 - t) with P the plain softmax and Z the
-    regenerated keep mask; LSE is that of P (dropout acts after the softmax)."""
+    regenerated keep mask; LSE is that of P (dropout acts after the softmax).
+    Input head (b, h) is head (b0 + b, h0 + h) of the whole problem (the mask
+    depends on it)."""
     q, k, v = (np.asarray(x, dtype=np.float64) for x in (q, k, v))
     B, H, N, _ = q.shape
     Nk = k.shape[2]
@@ -364,12 +367,13 @@ def forward_dropout(q, k, v, scale, p: float, seed: int, causal=False, block_mas
     for b in range(B):
         for h in range(H):
             pr, lse[b, h] = head_probs(q[b, h], k[b, h], scale, causal, block_mask, block)
-            z = dropout_keep(b, h, np.arange(N), np.arange(Nk), p, seed)
+            z = dropout_keep(b0 + b, h0 + h, np.arange(N), np.arange(Nk), p, seed)
             o[b, h] = (pr * z * inv_keep) @ v[b, h]
     return o, lse
 
 
-def backward_dropout(q, k, v, do, scale, p: float, seed: int, causal=False, block_mask=None, block=128):
+def backward_dropout(q, k, v, do, scale, p: float, seed: int, causal=False, block_mask=None, block=128,
+                     b0: int = 0, h0: int = 0):
     """Gradients of forward_dropout ["FlashAttention" notes, "Backward Pass of
     flashattention", with the dropped probabilities P~ = P o Z * c]:
     dV = P~^T dO;  dP = (dO V^T) o Z * c;  D_i = sum_j P_ij dP_ij;
@@ -383,7 +387,7 @@ def backward_dropout(q, k, v, do, scale, p: float, seed: int, causal=False, bloc
     for b in range(B):
         for h in range(H):
             pr, _ = head_probs(q[b, h], k[b, h], scale, causal, block_mask, block)
-            zc = dropout_keep(b, h, np.arange(N), np.arange(Nk), p, seed) * inv_keep
+            zc = dropout_keep(b0 + b, h0 + h, np.arange(N), np.arange(Nk), p, seed) * inv_keep
             dv[b, h] = (pr * zc).T @ do[b, h]
             dp = (do[b, h] @ v[b, h].T) * zc
             d_row = (pr * dp).sum(axis=1)

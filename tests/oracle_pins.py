@@ -443,6 +443,10 @@ def pin_dropout(orc):
     np.testing.assert_allclose(dq, tq.grad.numpy(), atol=1e-12)
     np.testing.assert_allclose(dk, tk.grad.numpy(), atol=1e-12)
     np.testing.assert_allclose(dv, tv.grad.numpy(), atol=1e-12)
+    # a head evaluated alone with its offsets equals that head of the whole
+    full = orc.forward_dropout(q, k, v, 0.5, 0.3, 17)[0]
+    alone = orc.forward_dropout(q[:, 1:2], k[:, 1:2], v[:, 1:2], 0.5, 0.3, 17, h0=1)[0]
+    np.testing.assert_array_equal(alone[:, 0], full[:, 1])
     # finite differences with the mask fixed by the seed
     qs, ks, vs, dos = (x[:, :1, :9, :3].copy() for x in (q, k, v, do))
     g = orc.backward_dropout(qs, ks, vs, dos, 0.7, 0.4, 5)

@@ -88,16 +88,16 @@ def test_blocksparse_requires_mask(lib):
     assert lib.fa_fwd_blocksparse(P, P, P, P, P, NULL, 1, 1, 128, 64, 0.125, 0, NULL) == -1
     assert lib.fa_fwd_blocksparse(P, P, P, P, P, NULL, 1, 1, 128, 64, 0.125, 1, NULL) == -1
     assert lib.fa_bwd_blocksparse(P, P, P, P, P, P, NULL, P, P, P, P, 1, 1, 128, 64, 0.125, 0, NULL) == -1
-    assert lib.fa_bwd_main(P, P, P, P, NULL, P, P, P, 1, 1, 128, 64, 0.125, 3, NULL) == -1
+    assert lib.fa_bwd_main(P, P, P, P, NULL, P, P, P, 1, 1, 128, 64, 0.125, 3, 0.0, 0, NULL) == -1
 
 
 def test_bwd_rejects_bad_arguments(lib):
     ws = ctypes.c_void_p(4096 + 16)       # 16- but not 256-byte aligned
     assert lib.fa_bwd(P, P, P, P, P, P, P, P, P, NULL, 1, 1, 128, 64, 0.125, 0, NULL) == -1
-    assert lib.fa_bwd_main(P, P, P, P, NULL, P, P, ws, 1, 1, 128, 64, 0.125, 0, NULL) == -1
-    assert lib.fa_bwd_main(P, P, P, P, NULL, P, P, P, 1, 1, 128, 64, 0.125, 7, NULL) == -1
-    assert lib.fa_bwd_main(P, P, P, P, NULL, P, P, P, 1, 1, 128, 64, 0.125, 4, NULL) == -1
-    assert lib.fa_bwd_main(P, P, P, P, NULL, P, P, P, 1, 1, 128, 64, 0.125, 2, NULL) == -1
+    assert lib.fa_bwd_main(P, P, P, P, NULL, P, P, ws, 1, 1, 128, 64, 0.125, 0, 0.0, 0, NULL) == -1
+    assert lib.fa_bwd_main(P, P, P, P, NULL, P, P, P, 1, 1, 128, 64, 0.125, 7, 0.0, 0, NULL) == -1
+    assert lib.fa_bwd_main(P, P, P, P, NULL, P, P, P, 1, 1, 128, 64, 0.125, 4, 0.0, 0, NULL) == -1
+    assert lib.fa_bwd_main(P, P, P, P, NULL, P, P, P, 1, 1, 128, 64, 0.125, 2, 0.0, 0, NULL) == -1
     assert lib.fa_bwd_preprocess(P, P, P, P, 1, 1, 100, 96, NULL) == -2
     assert lib.fa_bwd_preprocess(P, P, NULL, P, 1, 1, 100, 64, NULL) == -1    # lse required here
     # block masks are limited to 1024 tiles per row
@@ -175,3 +175,12 @@ def test_decode_workspace_and_validation(lib):
     assert lib.fa_decode(P, P, P, P, P, NULL, 1, 1, 1, 64, 128, -1.0, 0, NULL, NULL) == -1
     # several chunks need a workspace
     assert lib.fa_decode(P, P, P, P, P, NULL, 8, 32, 1, 32768, 128, 0.1, 0, NULL, NULL) == -1
+
+
+def test_dropout_argument_checks(lib):
+    # dropout probability outside [0, 1) or not finite
+    for pdrop in (-0.1, 1.0, float("nan")):
+        assert lib.fa_fwd_dropout(P, P, P, P, P, NULL, 1, 1, 128, 64, 0.125, 0, pdrop, 1, NULL) == -1
+        assert lib.fa_bwd_dropout(P, P, P, P, P, P, NULL, P, P, P, P, 1, 1, 128, 64, 0.125, 0, pdrop, 1, NULL) == -1
+        assert lib.fa_bwd_main(P, P, P, P, NULL, P, P, P, 1, 1, 128, 64, 0.125, 0, pdrop, 1, NULL) == -1
+    assert lib.fa_fwd_dropout(NULL, P, P, P, P, NULL, 1, 1, 128, 64, 0.125, 0, 0.1, 1, NULL) == -1

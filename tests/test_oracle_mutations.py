@@ -193,12 +193,13 @@ def _m_dropout_transposed(b, h, rows, cols, seed):
     return _real["dropout_bytes"](b, h, cols, rows, seed).T
 
 
-def _m_dropout_unscaled(q, k, v, scale, p, seed, causal=False, block_mask=None, block=128):
-    o, lse = _real["forward_dropout"](q, k, v, scale, p, seed, causal, block_mask, block)
+def _m_dropout_unscaled(q, k, v, scale, p, seed, causal=False, block_mask=None, block=128, b0=0, h0=0):
+    o, lse = _real["forward_dropout"](q, k, v, scale, p, seed, causal, block_mask, block, b0, h0)
     return o * (256 - orc.dropout_threshold(p)) / 256.0, lse
 
 
-def _m_dropout_bwd_no_mask_in_dp(q, k, v, do, scale, p, seed, causal=False, block_mask=None, block=128):
+def _m_dropout_bwd_no_mask_in_dp(q, k, v, do, scale, p, seed, causal=False, block_mask=None, block=128, b0=0,
+                                 h0=0):
     q, k, v, do = (np.asarray(x, dtype=np.float64) for x in (q, k, v, do))
     B, H, N, _ = q.shape
     c = 256.0 / (256 - orc.dropout_threshold(p))
@@ -207,7 +208,7 @@ def _m_dropout_bwd_no_mask_in_dp(q, k, v, do, scale, p, seed, causal=False, bloc
     for b in range(B):
         for h in range(H):
             pr, _ = orc.head_probs(q[b, h], k[b, h], scale, causal, block_mask, block)
-            zc = orc.dropout_keep(b, h, np.arange(N), np.arange(k.shape[2]), p, seed) * c
+            zc = orc.dropout_keep(b0 + b, h0 + h, np.arange(N), np.arange(k.shape[2]), p, seed) * c
             dv[b, h] = (pr * zc).T @ do[b, h]
             dp = do[b, h] @ v[b, h].T                       # planted mistake: mask not applied
             d_row = (pr * dp).sum(axis=1)
