@@ -43,6 +43,7 @@ class Workload:
     amplitude: float = 1.0
     block_sparse_p: float | None = None  # keep-probability of an off-diagonal block
     window: tuple[int, int] | None = None  # (left, right) extent of a block band
+    dropout_p: float = 0.0                 # dropout on P (mask seed = the workload's seed)
     note: str = field(default="", compare=False)
 
     @property
@@ -77,7 +78,11 @@ WORKLOADS = {
         "fwdbwd_b1h16n8192d128_blocksparse", 1, 16, 8192, 128, seed=4,
         block_sparse_p=0.25,
         note="forward + backward, 128x128 block mask, p=0.25 + diagonal"),
-    # beyond the five: a causal sliding window of 2048 keys (16 blocks)
+    # beyond the five: the headline shape with dropout 0.1 on P
+    "fwdbwd_b2h16n4096d128_causal_dropout": Workload(
+        "fwdbwd_b2h16n4096d128_causal_dropout", 2, 16, 4096, 128, seed=2, causal=True, dropout_p=0.1,
+        note="forward + backward, causal, dropout 0.1 with regenerated masks"),
+    # a causal sliding window of 2048 keys (16 blocks)
     "fwdbwd_b1h16n16384d128_causal_window2k": Workload(
         "fwdbwd_b1h16n16384d128_causal_window2k", 1, 16, 16384, 128, seed=5, causal=True,
         window=(15, 0),

@@ -130,6 +130,8 @@ def _config(w, density, extra=None):
          "l2": "flushed (256 MiB write) between timed steps", "parallelism": "replica per GPU"}
     if density is not None:
         c["block_density"] = round(density, 4)
+    if getattr(w, "dropout_p", 0.0):
+        c["dropout_p"] = w.dropout_p
     if extra:
         c.update(extra)
     return c
@@ -211,9 +213,16 @@ def _oracle_sample(w, t, budget_s=15.0, max_heads=None):
         b, h = divmod(hh, w.H)
         sl = (slice(b, b + 1), slice(h, h + 1))
         q, k, v = (t[n][sl].double().numpy() for n in ("q", "k", "v"))
-        oracle.forward(q, k, v, w.scale, causal=w.causal, block_mask=bmn, row_chunk=2048 if w.N > 8192 else None)
-        if w.backward:
-            oracle.backward(q, k, v, t["do"][sl].double().numpy(), w.scale, causal=w.causal, block_mask=bmn)
+        if w.dropout_p:
+            oracle.forward_dropout(q, k, v, w.scale, w.dropout_p, w.seed, causal=w.causal, block_mask=bmn, b0=b, h0=h)
+            if w.backward:
+                oracle.backward_dropout(q, k, v, t["do"][sl].double().numpy(), w.scale, w.dropout_p, w.seed,
+                                        causal=w.causal, block_mask=bmn, b0=b, h0=h)
+        else:
+            oracle.forward(q, k, v, w.scale, causal=w.causal, block_mask=bmn,
+                           row_chunk=2048 if w.N > 8192 else None)
+            if w.backward:
+                oracle.backward(q, k, v, t["do"][sl].double().numpy(), w.scale, causal=w.causal, block_mask=bmn)
         heads += 1
         ff, fb = _flops(type(w)(**{**w.__dict__, "B": 1, "H": 1}), _density(t, w.causal))
         flops += ff + fb
@@ -253,9 +262,11 @@ def run_reference(args):
         rows = np.arange((step % nblk) * REF_ROWS, min(w.N, (step % nblk + 1) * REF_ROWS))
         pairs = float(oracle.visible(w.N, w.N, w.causal, bm, rows=rows).sum())
         if w.backward:
-            oracle.backward_rows(q, k, v, do, w.scale, 0, 0, rows, causal=w.causal, block_mask=bm)
+            oracle.backward_rows(q, k, v, do, w.scale, 0, 0, rows, causal=w.causal, block_mask=bm,
+                                 dropout_p=w.dropout_p, seed=w.seed)
             return pairs * 4.0 * w.d * 3.5
-        oracle.forward_rows(q, k, v, w.scale, 0, 0, rows, causal=w.causal, block_mask=bm)
+        oracle.forward_rows(q, k, v, w.scale, 0, 0, rows, causal=w.causal, block_mask=bm,
+                            dropout_p=w.dropout_p, seed=w.seed)
         return pairs * 4.0 * w.d
 
     for i in range(args.warmup):
@@ -516,7 +527,9 @@ def run_cuda(args):
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
 
     def fwd():
-        if bm is not None:
+        if w.dropout_p:
+            fa.fa_fwd_dropout(q, k, v, o, lse, bm, w.scale, w.causal, w.dropout_p, w.seed)
+        elif bm is not None:
             fa.fa_fwd_blocksparse(q, k, v, o, lse, bm, w.scale, causal=w.causal)
         else:
             fa.fa_fwd(q, k, v, o, lse, w.scale, causal=w.causal)
@@ -531,7 +544,7 @@ def run_cuda(args):
             fa.fa_bwd_preprocess(o, do, lse, wsp)
             if ev:
                 ev[2].record()
-            fa.fa_bwd_main(q, k, v, do, bm, dk, dv, wsp, w.scale, mask_kind)
+            fa.fa_bwd_main(q, k, v, do, bm, dk, dv, wsp, w.scale, mask_kind, w.dropout_p, w.seed)
             if ev:
                 ev[3].record()
             fa.fa_bwd_dq_convert(wsp, dq, w.scale)

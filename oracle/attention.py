@@ -165,11 +165,16 @@ def forward(q, k, v, scale, causal=False, block_mask=None, block=128,
     return o, lse
 
 
-def forward_rows(q, k, v, scale, b, h, rows, causal=False, block_mask=None, block=128):
+def forward_rows(q, k, v, scale, b, h, rows, causal=False, block_mask=None, block=128,
+                 dropout_p: float = 0.0, seed: int = 0):
     """O and LSE of selected query rows of head (b, h) only: for sampled checks
-    of workloads too large to materialise."""
+    of workloads too large to materialise.  With dropout_p, the rows of
+    forward_dropout."""
     q, k, v = (np.asarray(x, dtype=np.float64) for x in (q[b, h], k[b, h], v[b, h]))
     p, lse = head_probs(q, k, scale, causal, block_mask, block, rows)
+    if dropout_p:
+        p = p * dropout_keep(b, h, rows, np.arange(k.shape[0]), dropout_p, seed) * (
+            256.0 / (256 - dropout_threshold(dropout_p)))
     return p @ v, lse
 
 
@@ -215,20 +220,26 @@ def backward_rows_dq(q, k, v, do, scale, b, h, rows, causal=False, block_mask=No
     return scale * (_softmax_backward(p, dp, d_row) @ k)
 
 
-def backward_rows(q, k, v, do, scale, b, h, rows, causal=False, block_mask=None, block=128):
+def backward_rows(q, k, v, do, scale, b, h, rows, causal=False, block_mask=None, block=128,
+                  dropout_p: float = 0.0, seed: int = 0):
     """The backward restricted to selected query rows of head (b, h): dQ of
     those rows and their contributions to dK and dV [P2 "Backward Pass of
     flashattention": dv_j = sum_i P_ij do_i, dk_j = sum_i dS_ij q_i, both sums
-    over query rows i, so a partition of the rows splits them exactly].
+    over query rows i, so a partition of the rows splits them exactly].  With
+    dropout_p, the rows of backward_dropout.
     Returns (dq_rows, dk_part, dv_part, o_rows, lse_rows)."""
     q, k, v, do = (np.asarray(x, dtype=np.float64) for x in (q[b, h], k[b, h], v[b, h], do[b, h]))
     rows = np.asarray(rows)
     p, lse = head_probs(q, k, scale, causal, block_mask, block, rows)
-    o = p @ v
-    dp = do[rows] @ v.T
+    zc = 1.0
+    if dropout_p:
+        zc = dropout_keep(b, h, rows, np.arange(k.shape[0]), dropout_p, seed) * (
+            256.0 / (256 - dropout_threshold(dropout_p)))
+    o = (p * zc) @ v
+    dp = (do[rows] @ v.T) * zc
     d_row = (p * dp).sum(axis=1)
     ds = _softmax_backward(p, dp, d_row)
-    return scale * (ds @ k), scale * (ds.T @ q[rows]), p.T @ do[rows], o, lse
+    return scale * (ds @ k), scale * (ds.T @ q[rows]), (p * zc).T @ do[rows], o, lse
 
 
 # --------------------------------------------------------------------------- #
@@ -339,11 +350,14 @@ def dropout_bytes(b: int, h: int, rows, cols, seed: int) -> np.ndarray:
     """uint8 [len(rows), len(cols)]: the random byte of each (query, key) pair
     of head (b, h): byte j % 4 of word i % 4 of Philox(counter (j//4, i//4, h, b))."""
     rows, cols = np.asarray(rows, dtype=np.int64), np.asarray(cols, dtype=np.int64)
-    ii, jj = np.meshgrid(rows, cols, indexing="ij")
-    ctr = np.stack([jj // 4, ii // 4, np.full_like(ii, h), np.full_like(ii, b)], axis=-1)
-    words = philox4x32_10(ctr, (seed & 0xFFFFFFFF, (seed >> 32) & 0xFFFFFFFF))
-    word = np.take_along_axis(words, (ii % 4)[..., None], axis=-1)[..., 0]
-    return ((word >> (8 * (jj % 4)).astype(np.uint32)) & 0xFF).astype(np.uint8)
+    # one generator call per 4 x 4 block that the pairs touch
+    rb, ri = np.unique(rows // 4, return_inverse=True)
+    cb, ci = np.unique(cols // 4, return_inverse=True)
+    gr, gc = np.meshgrid(rb, cb, indexing="ij")
+    ctr = np.stack([gc, gr, np.full_like(gr, h), np.full_like(gr, b)], axis=-1)
+    words = philox4x32_10(ctr, (seed & 0xFFFFFFFF, (seed >> 32) & 0xFFFFFFFF))   # [blocks_i, blocks_j, 4]
+    word = words[ri[:, None], ci[None, :], (rows % 4)[:, None]]
+    return ((word >> (8 * (cols % 4))[None, :].astype(np.uint32)) & 0xFF).astype(np.uint8)
 
 
 def dropout_keep(b: int, h: int, rows, cols, p: float, seed: int) -> np.ndarray:

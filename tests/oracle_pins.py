@@ -238,6 +238,21 @@ def pin_backward_rows(orc):
         sdv += dvp
     np.testing.assert_allclose(sdk, dk[0, 1], atol=1e-12)
     np.testing.assert_allclose(sdv, dv[0, 1], atol=1e-12)
+    # the same with dropout: the row blocks partition backward_dropout
+    dq, dk, dv, _ = orc.backward_dropout(q, k, v, do, 0.5, 0.3, 77, causal=True)
+    o, lse = orc.forward_dropout(q, k, v, 0.5, 0.3, 77, causal=True)
+    sdk, sdv = np.zeros_like(dk[0, 1]), np.zeros_like(dv[0, 1])
+    for blk in (range(0, 13), range(13, 29)):
+        dqr, dkp, dvp, orr, lr = orc.backward_rows(q, k, v, do, 0.5, 0, 1, list(blk), causal=True,
+                                                   dropout_p=0.3, seed=77)
+        np.testing.assert_allclose(dqr, dq[0, 1, list(blk)], atol=1e-13)
+        np.testing.assert_allclose(orr, o[0, 1, list(blk)], atol=1e-13)
+        ofr, lfr = orc.forward_rows(q, k, v, 0.5, 0, 1, list(blk), causal=True, dropout_p=0.3, seed=77)
+        np.testing.assert_allclose(ofr, o[0, 1, list(blk)], atol=1e-13)
+        sdk += dkp
+        sdv += dvp
+    np.testing.assert_allclose(sdk, dk[0, 1], atol=1e-12)
+    np.testing.assert_allclose(sdv, dv[0, 1], atol=1e-12)
 
 
 # --------------------------------------------------------------------------- #
