@@ -413,6 +413,61 @@ def backward_dropout(q, k, v, do, scale, p: float, seed: int, causal=False, bloc
 
 
 # --------------------------------------------------------------------------- #
+# 8-bit (e4m3) inputs
+# --------------------------------------------------------------------------- #
+# The pages name 8-bit tensor-core arithmetic only as the FlashAttention-3
+# extension ("Как работает FlashAttention математически", section 9).  The
+# reading here: inputs are e4m3 bytes with per-(batch, head) descale factors,
+# the real input is byte value x descale, and the result to reproduce is exact
+# attention on those real inputs; the kernel's rounding of P to e4m3 is an
+# approximation whose error fp8_error_model bounds.
+
+def e4m3_decode(codes) -> np.ndarray:
+    """Value of e4m3 bytes (1 sign bit, 4 exponent bits with bias 7, 3
+    mantissa bits; exponent 0 is subnormal: m/8 * 2^-6; no infinities; the
+    codes 0x7F and 0xFF are NaN)."""
+    c = np.asarray(codes, dtype=np.uint8).astype(np.int64)
+    sign = np.where(c & 0x80, -1.0, 1.0)
+    e = (c >> 3) & 0xF
+    m = (c & 0x7).astype(np.float64)
+    val = np.where(e == 0, m / 8.0 * 2.0 ** -6, (1.0 + m / 8.0) * np.exp2(e.astype(np.float64) - 7.0))
+    val = np.where((c & 0x7F) == 0x7F, np.nan, val)
+    return sign * val
+
+
+def forward_fp8(q8, k8, v8, q_descale, k_descale, v_descale, scale, causal=False):
+    """Exact attention on the real inputs q8 dq, k8 dk, v8 dv (q8, k8, v8: e4m3
+    bytes [B, H, N, d] as uint8; descales [B, H]).  Returns (O, LSE, P) with P
+    the per-head probabilities [B, H, N, N] (for the error model)."""
+    dq, dk, dv = (np.asarray(x, dtype=np.float64)[..., None, None] for x in (q_descale, k_descale, v_descale))
+    q, k, v = e4m3_decode(q8) * dq, e4m3_decode(k8) * dk, e4m3_decode(v8) * dv
+    B, H, N, _ = q.shape
+    o, lse = forward(q, k, v, scale, causal=causal)
+    probs = np.zeros((B, H, N, k.shape[2]))
+    for b in range(B):
+        for h in range(H):
+            probs[b, h], _ = head_probs(q[b, h], k[b, h], scale, causal)
+    return o, lse, probs, v
+
+
+def fp8_error_model(o, probs, v, rel: float = 2.0 ** -4):
+    """Effect on O of perturbing every attention weight by a relative error of
+    at most `rel` (the rounding of P to e4m3: 3 mantissa bits) and
+    renormalising: O' - O = sum_j w_j d_j (v_j - O) / (1 + sum_j w_j d_j).
+    Returns (bound, sigma): the worst case rel / (1 - rel) * sum_j w_j |v_j - O|
+    plus the flush of weights below 2^-17 of the row maximum (at most
+    n 2^-17 max_j |v_j - O|), and the standard deviation when the d_j are
+    independent and uniform on [-rel, rel]:
+    rel / sqrt(3) * sqrt(sum_j w_j^2 (v_j - O)^2)."""
+    dev = v[:, :, None, :, :] - o[:, :, :, None, :]                     # [B,H,N,Nk,d]
+    bound = rel / (1 - rel) * np.einsum("bhij,bhijc->bhic", probs, np.abs(dev))
+    n_vis = (probs > 0).sum(axis=-1)[..., None]
+    bound = bound + n_vis * 2.0 ** -17 * np.abs(dev).max(axis=3)
+    sigma = rel / np.sqrt(3.0) * np.sqrt(np.einsum("bhij,bhijc->bhic", probs ** 2, dev ** 2))
+    return bound, sigma
+
+
+# --------------------------------------------------------------------------- #
 # decoding: the newest query tokens against a cache of keys and values
 # --------------------------------------------------------------------------- #
 def decode_visible(nq: int, L: int, causal: bool = False) -> np.ndarray:

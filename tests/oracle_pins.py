@@ -481,5 +481,49 @@ def pin_dropout(orc):
         assert rel < 1e-6, (idx, rel)
 
 
+def pin_fp8(orc):
+    """8-bit inputs: e4m3 decoding against PyTorch's float8_e4m3fn for all 256
+    codes and the format's landmarks; the 8-bit forward against PyTorch's fp64
+    attention on the dequantised inputs; round-to-nearest e4m3 stays within a
+    relative 2^-4; the error model's bound holds and its sigma matches the
+    spread of randomly perturbed, renormalised weights."""
+    codes = np.arange(256, dtype=np.uint8)
+    mine = orc.e4m3_decode(codes)
+    ref = torch.tensor(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    assert np.array_equal(np.isnan(mine), np.isnan(ref))
+    np.testing.assert_array_equal(mine[~np.isnan(mine)], ref[~np.isnan(ref)])
+    assert mine[0x38] == 1.0 and mine[0x7E] == 448.0 and mine[0x01] == 2.0 ** -9 and mine[0x08] == 2.0 ** -6
+    assert mine[0xB8] == -1.0 and np.isnan(mine[0x7F]) and np.isnan(mine[0xFF])
+    # relative rounding error of e4m3 on its normal range
+    r = _rng(41)
+    x = np.exp2(r.uniform(-5.9, 8.7, 20000))
+    xr = torch.tensor(x).to(torch.float8_e4m3fn).to(torch.float64).numpy()
+    assert np.max(np.abs(xr - x) / x) <= 2.0 ** -4
+    # the 8-bit forward is attention on the dequantised inputs
+    B, H, N, d = 1, 2, 40, 16
+    q8, k8, v8 = (torch.randn(B, H, N, d, generator=torch.Generator().manual_seed(s_)).mul(3).to(torch.float8_e4m3fn)
+                  for s_ in (1, 2, 3))
+    qd, kd, vd = (r.uniform(0.01, 0.5, (B, H)) for _ in range(3))
+    u8 = [t.view(torch.uint8).numpy() for t in (q8, k8, v8)]
+    o, lse, probs, vv = orc.forward_fp8(*u8, qd, kd, vd, 0.25, causal=True)
+    tq, tk, tv = (t.to(torch.float64) * torch.tensor(s_)[..., None, None] for t, s_ in zip((q8, k8, v8), (qd, kd, vd)))
+    am = torch.ones(N, N, dtype=torch.bool).tril()
+    ref_o = torch.nn.functional.scaled_dot_product_attention(tq, tk, tv, attn_mask=am, scale=0.25).numpy()
+    np.testing.assert_allclose(o, ref_o, atol=1e-13)
+    # error model: worst case holds, sigma is the spread of random perturbations
+    bound, sigma = orc.fp8_error_model(o, probs, vv)
+    rel = 2.0 ** -4
+    sq = np.zeros_like(o)
+    S = 300
+    for _ in range(S):
+        w = probs * (1 + r.uniform(-rel, rel, probs.shape))
+        w = w / w.sum(axis=-1, keepdims=True)
+        do_ = np.einsum("bhij,bhjc->bhic", w, vv) - o
+        assert np.all(np.abs(do_) <= bound + 1e-15)
+        sq += do_ ** 2
+    ratio = np.sqrt(sq.mean() / S) / np.sqrt((sigma ** 2).mean())
+    assert 0.85 < ratio < 1.15, ratio
+
+
 ALL_PINS = [pin_worked_example, pin_closed_forms, pin_invariants, pin_backward_fd,
-            pin_dvec, pin_backward_rows, pin_library, pin_block_masks, pin_decode, pin_philox, pin_dropout]
+            pin_dvec, pin_backward_rows, pin_library, pin_block_masks, pin_decode, pin_philox, pin_dropout, pin_fp8]

@@ -11,7 +11,7 @@ _real = {name: getattr(orc, name) for name in
          ("_scores", "_apply_mask", "_row_softmax", "_softmax_backward", "visible",
           "forward", "backward", "tiled_forward", "_lse", "window_block_mask", "dilated_block_mask",
           "decode_visible", "decode", "decode_split", "philox4x32_10", "dropout_bytes",
-          "forward_dropout", "backward_dropout")}
+          "forward_dropout", "backward_dropout", "e4m3_decode", "forward_fp8", "fp8_error_model")}
 
 
 def _m_no_scale(q, k, scale):
@@ -219,6 +219,31 @@ def _m_dropout_bwd_no_mask_in_dp(q, k, v, do, scale, p, seed, causal=False, bloc
     return dq, dk, dv, dvec
 
 
+def _m_e4m3_bias8(codes):
+    c = np.asarray(codes, dtype=np.uint8).astype(np.int64)
+    sign = np.where(c & 0x80, -1.0, 1.0)
+    e, m = (c >> 3) & 0xF, (c & 0x7).astype(np.float64)
+    val = np.where(e == 0, m / 8.0 * 2.0 ** -7, (1.0 + m / 8.0) * np.exp2(e.astype(np.float64) - 8.0))
+    return sign * np.where((c & 0x7F) == 0x7F, np.nan, val)
+
+
+def _m_e4m3_no_subnormal(codes):
+    c = np.asarray(codes, dtype=np.uint8).astype(np.int64)
+    sign = np.where(c & 0x80, -1.0, 1.0)
+    e, m = (c >> 3) & 0xF, (c & 0x7).astype(np.float64)
+    val = (1.0 + m / 8.0) * np.exp2(e.astype(np.float64) - 7.0)
+    return sign * np.where((c & 0x7F) == 0x7F, np.nan, val)
+
+
+def _m_fp8_v_descale_dropped(q8, k8, v8, qd, kd, vd, scale, causal=False):
+    return _real["forward_fp8"](q8, k8, v8, qd, kd, np.ones_like(np.asarray(vd)), scale, causal)
+
+
+def _m_fp8_sigma_halved(o, probs, v, rel=2.0 ** -4):
+    bound, sigma = _real["fp8_error_model"](o, probs, v, rel)
+    return bound, sigma / 2
+
+
 MUTANTS = {
     "scale_dropped": ("_scores", _m_no_scale),
     "scores_transposed": ("_scores", _m_transposed_scores),
@@ -245,6 +270,10 @@ MUTANTS = {
     "dropout_mask_transposed": ("dropout_bytes", _m_dropout_transposed),
     "dropout_output_unscaled": ("forward_dropout", _m_dropout_unscaled),
     "dropout_grad_mask_missing": ("backward_dropout", _m_dropout_bwd_no_mask_in_dp),
+    "e4m3_exponent_bias_8": ("e4m3_decode", _m_e4m3_bias8),
+    "e4m3_subnormals_as_normal": ("e4m3_decode", _m_e4m3_no_subnormal),
+    "fp8_v_descale_dropped": ("forward_fp8", _m_fp8_v_descale_dropped),
+    "fp8_sigma_halved": ("fp8_error_model", _m_fp8_sigma_halved),
 }
 
 
