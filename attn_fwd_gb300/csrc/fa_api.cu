@@ -81,14 +81,64 @@ int encoder_ready() {
   return g_encode ? FA_OK : FA_ERR_CUDA;
 }
 
+// Encoded tensor maps are a pure function of (address, sizes, box), so a
+// direct-mapped table of recent ones saves the host the encoding on repeated
+// calls over the same buffers (a training loop's steady state).
+struct MapKey {
+  const void* ptr;
+  int BH, N, d, box_rows;
+  bool operator==(const MapKey& o) const {
+    return ptr == o.ptr && BH == o.BH && N == o.N && d == o.d && box_rows == o.box_rows;
+  }
+};
+struct MapSlot {
+  MapKey key;
+  CUtensorMap map;
+  bool valid;
+};
+constexpr int kMapSlots = 256;
+MapSlot g_map_slots[kMapSlots];
+std::mutex g_map_mu;
+
+int map_slot(const MapKey& k) {
+  uint64_t h = reinterpret_cast<uintptr_t>(k.ptr) >> 8;
+  h = h * 0x9E3779B97F4A7C15ull ^ (static_cast<uint64_t>(k.N) << 20) ^ (static_cast<uint64_t>(k.BH) << 4) ^
+      static_cast<uint64_t>(k.d + k.box_rows);
+  return static_cast<int>((h ^ (h >> 29)) % kMapSlots);
+}
+
 // 3-D map over a bf16 array [BH][N][d]: box {64, box_rows, 1}, 128-byte
 // swizzle, zero fill outside the array.
 int make_map_bf16(CUtensorMap* m, const void* ptr, int BH, int N, int d, int box_rows) {
+  const MapKey key{ptr, BH, N, d, box_rows};
+  const int slot = map_slot(key);
+  {
+    std::lock_guard<std::mutex> lk(g_map_mu);
+    if (g_map_slots[slot].valid && g_map_slots[slot].key == key) {
+      *m = g_map_slots[slot].map;
+      return FA_OK;
+    }
+  }
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(BH)};
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(N) * d * 2};
   cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_rows), 1};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return FA_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_map_mu);
+  g_map_slots[slot] = MapSlot{key, *m, true};
+  return FA_OK;
+}
+
+// 3-D map over a byte array [BH][rows][cols]: box {128, 128, 1}, 128-byte swizzle.
+int make_map_u8(CUtensorMap* m, const void* ptr, int BH, int rows, int cols) {
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(BH)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows) * cols};
+  cuuint32_t box[3] = {128, 128, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(ptr), dims, strides, box, estr,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
@@ -382,6 +432,56 @@ int decode_impl(const void* q, const void* k, const void* v, void* o, float* lse
   return fa::launch_decode(p, d, reinterpret_cast<cudaStream_t>(stream));
 }
 
+// FP8 forward: V^T workspace [B*H][128][npad] bytes, npad = N rounded up to 16
+// (the row pitch of a TMA map must be a multiple of 16 bytes).
+int fp8_npad(int N) { return (N + 15) / 16 * 16; }
+
+size_t fp8_workspace_bytes(int B, int H, int N, int d) {
+  if (B < 1 || H < 1 || N < 1 || d != 128) return 0;
+  if (static_cast<long long>(B) * H * N * d >= (1ll << 31)) return 0;
+  return align256(static_cast<size_t>(B) * H * 128 * fp8_npad(N));
+}
+
+int fwd_fp8_impl(const void* q, const void* k, const void* v, void* o, float* lse, const float* qd, const float* kd,
+                 const float* vd, int B, int H, int N, int d, float scale, int causal, void* workspace,
+                 fa_stream_t stream) {
+  int rc;
+  if ((rc = check_ptrs({q, k, v, o, lse, workspace})) != FA_OK) return rc;
+  for (const float* x : {qd, kd, vd})
+    if (x != nullptr && (reinterpret_cast<uintptr_t>(x) & 3u) != 0) return FA_ERR_INVALID;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return FA_ERR_INVALID;
+  if ((rc = check_shape(B, H, N, d)) != FA_OK) return rc;
+  if (d != 128) return FA_ERR_UNSUPPORTED;
+  if ((rc = check_scale(scale)) != FA_OK) return rc;
+  int* status = nullptr;
+  if ((rc = device_ready(&status)) != FA_OK) return rc;
+  if ((rc = encoder_ready()) != FA_OK) return rc;
+  const int BH = B * H;
+  const int npad = fp8_npad(N);
+  uint8_t* vt = static_cast<uint8_t*>(workspace);
+  fa::Fp8Params p;
+  std::memset(&p, 0, sizeof(p));
+  if (make_map_u8(&p.tm_q, q, BH, N, 128) != FA_OK || make_map_u8(&p.tm_k, k, BH, N, 128) != FA_OK ||
+      make_map_u8(&p.tm_vt, vt, BH, 128, npad) != FA_OK)
+    return FA_ERR_CUDA;
+  p.o = static_cast<__nv_bfloat16*>(o);
+  p.lse = lse;
+  p.q_descale = qd;
+  p.k_descale = kd;
+  p.v_descale = vd;
+  p.status = status;
+  p.timeout_ns = g_timeout_ns.load(std::memory_order_relaxed);
+  p.N = N;
+  p.BH = BH;
+  p.n_qt = tiles(N);
+  p.n_pairs = (p.n_qt + 1) / 2;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.causal = causal ? 1 : 0;
+  const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (fa::launch_fp8_transpose_v(static_cast<const uint8_t*>(v), vt, BH, N, npad, st) != 0) return FA_ERR_LAUNCH;
+  return fa::launch_fwd_fp8(p, st) == 0 ? FA_OK : FA_ERR_LAUNCH;
+}
+
 }  // namespace
 
 // --------------------------------------------------------------------------
@@ -500,6 +600,15 @@ size_t fa_decode_workspace_bytes(int B, int H, int Nq, int Nk, int d) {
 int fa_decode(const void* q, const void* k, const void* v, void* o, float* lse, const int* seqlens_k, int B, int H,
               int Nq, int Nk, int d, float scale, int causal, void* workspace, fa_stream_t stream) {
   return decode_impl(q, k, v, o, lse, seqlens_k, B, H, Nq, Nk, d, scale, causal, workspace, stream);
+}
+
+size_t fa_fwd_fp8_workspace_bytes(int B, int H, int N, int d) { return fp8_workspace_bytes(B, H, N, d); }
+
+int fa_fwd_fp8(const void* q, const void* k, const void* v, void* o, float* lse, const float* q_descale,
+               const float* k_descale, const float* v_descale, int B, int H, int N, int d, float scale, int causal,
+               void* workspace, fa_stream_t stream) {
+  return fwd_fp8_impl(q, k, v, o, lse, q_descale, k_descale, v_descale, B, H, N, d, scale, causal, workspace,
+                      stream);
 }
 
 int fa_block_mask_window(uint8_t* mask, int N, int left, int right) {

@@ -609,9 +609,8 @@ template <int D, bool DROP>
 static int launch_bwd_t(const BwdParams& p, cudaStream_t stream) {
   using L = BwdLayout<D>;
   static_assert(L::SMEM_BYTES <= 232448, "shared memory budget");
-  if (cudaFuncSetAttribute(fa_bwd_kernel<D, DROP>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM_BYTES) !=
-      cudaSuccess)
-    return -4;
+  static SmemAttrOnce attr;
+  if (!attr.ensure(reinterpret_cast<const void*>(fa_bwd_kernel<D, DROP>), L::SMEM_BYTES)) return -4;
   const unsigned grid = static_cast<unsigned>(p.n_kt) * static_cast<unsigned>(p.BH);
   fa_bwd_kernel<D, DROP><<<grid, L::THREADS, L::SMEM_BYTES, stream>>>(p);
   return cudaGetLastError() == cudaSuccess ? 0 : -4;

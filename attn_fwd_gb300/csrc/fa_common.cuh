@@ -2,6 +2,7 @@
 // kernels of libfa.so.
 #pragma once
 
+#include <atomic>
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -105,7 +106,45 @@ struct DecParams {
   int causal;
 };
 
+// Raises a kernel's dynamic shared-memory limit once per device (the
+// attribute is per device context), instead of on every launch.
+struct SmemAttrOnce {
+  std::atomic<uint64_t> done{0};   // bit per device ordinal below 64
+  bool ensure(const void* kernel, int bytes) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return false;
+    const uint64_t bit = dev < 64 ? (1ull << dev) : 0;
+    if (bit && (done.load(std::memory_order_acquire) & bit)) return true;
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess) return false;
+    done.fetch_or(bit, std::memory_order_release);
+    return true;
+  }
+};
+
+// FP8 (e4m3) forward, d = 128: Q, K as 3-D byte arrays [B*H][N][128] with a
+// {128, 128, 1} box, V transposed to [B*H][128][npad] with the same box.
+struct Fp8Params {
+  CUtensorMap tm_q;
+  CUtensorMap tm_k;
+  CUtensorMap tm_vt;
+  __nv_bfloat16* o;          // [B*H][N][128]
+  float* lse;                // [B*H][N]
+  const float* q_descale;    // [B*H] or null (1)
+  const float* k_descale;
+  const float* v_descale;
+  int* status;
+  uint64_t timeout_ns;
+  int N;
+  int BH;
+  int n_qt;
+  int n_pairs;
+  float scale_log2;          // scale * log2(e), before the descales
+  int causal;
+};
+
 int launch_fwd(const FwdParams& p, int d, cudaStream_t stream);
+int launch_fwd_fp8(const Fp8Params& p, cudaStream_t stream);
+int launch_fp8_transpose_v(const uint8_t* v, uint8_t* vt, int BH, int N, int npad, cudaStream_t stream);
 int launch_decode(const DecParams& p, int d, cudaStream_t stream);
 int launch_bwd_preprocess(const __nv_bfloat16* o, const __nv_bfloat16* dout, const float* lse, float* nd,
                           float* nlse, float* dq_acc, int BH, int N, int npad, int d, cudaStream_t stream);

@@ -338,9 +338,8 @@ __global__ void __launch_bounds__(128) fa_decode_combine_kernel(const __grid_con
 template <int D, int NQ>
 int launch_decode_t(const DecParams& p, cudaStream_t stream) {
   using L = DecLayout<D>;
-  cudaError_t e = cudaFuncSetAttribute(fa_decode_kernel<D, NQ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       L::SMEM_BYTES);
-  if (e != cudaSuccess) return -4;
+  static SmemAttrOnce attr;
+  if (!attr.ensure(reinterpret_cast<const void*>(fa_decode_kernel<D, NQ>), L::SMEM_BYTES)) return -4;
   const unsigned grid = static_cast<unsigned>(p.BH) * static_cast<unsigned>(p.splits);
   fa_decode_kernel<D, NQ><<<grid, L::THREADS, L::SMEM_BYTES, stream>>>(p);
   if (cudaGetLastError() != cudaSuccess) return -4;

@@ -615,9 +615,8 @@ template <int D, bool SPARSE, bool DROP>
 static int launch_fwd_t(const FwdParams& p, cudaStream_t stream) {
   using L = FwdLayout<D, SPARSE>;
   static_assert(L::SMEM_BYTES <= 232448, "shared memory budget");
-  cudaError_t e = cudaFuncSetAttribute(fa_fwd_kernel<D, SPARSE, DROP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       L::SMEM_BYTES);
-  if (e != cudaSuccess) return -4;
+  static SmemAttrOnce attr;
+  if (!attr.ensure(reinterpret_cast<const void*>(fa_fwd_kernel<D, SPARSE, DROP>), L::SMEM_BYTES)) return -4;
   const unsigned grid = static_cast<unsigned>(p.n_pairs) * static_cast<unsigned>(p.BH);
   fa_fwd_kernel<D, SPARSE, DROP><<<grid, L::THREADS, L::SMEM_BYTES, stream>>>(p);
   return cudaGetLastError() == cudaSuccess ? 0 : -4;

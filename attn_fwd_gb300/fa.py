@@ -47,6 +47,8 @@ _SIGS = {
     "fa_bwd_noalloc": (_i, [_vp] * 9 + [_i, _i, _i, _i, _f, _i, _vp]),
     "fa_decode_workspace_bytes": (_sz, [_i, _i, _i, _i, _i]),
     "fa_decode": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _vp, _vp]),
+    "fa_fwd_fp8_workspace_bytes": (_sz, [_i, _i, _i, _i]),
+    "fa_fwd_fp8": (_i, [_vp] * 8 + [_i, _i, _i, _i, _f, _i, _vp, _vp]),
     "fa_block_mask_window": (_i, [_vp, _i, _i, _i]),
     "fa_block_mask_dilated": (_i, [_vp, _i, _i, _i, _i]),
     "fa_get_device_error": (_i, [_vp]),
@@ -239,6 +241,47 @@ def fa_decode(q, k, v, o, lse, seqlens_k, scale, causal=False, workspace=None, s
     rc = load().fa_decode(_bf16(q, "q"), _bf16(k, "k"), _bf16(v, "v"), _bf16(o, "o"), _f32(lse, "lse"), sl,
                           B, H, Nq, Nk, d, float(scale), int(bool(causal)), ws, _stream(stream))
     _check("fa_decode", rc)
+
+
+def fa_fwd_fp8_workspace_bytes(B, H, N, d) -> int:
+    return load().fa_fwd_fp8_workspace_bytes(B, H, N, d)
+
+
+def _fp8(t, name):
+    if not (t.is_cuda and t.dtype == torch.float8_e4m3fn and t.is_contiguous() and t.dim() == 4):
+        raise ValueError(f"{name} must be a contiguous float8_e4m3fn CUDA tensor [B, H, N, d]")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _descale(t, name, n):
+    if t is None:
+        return ctypes.c_void_p(0)
+    if not (t.is_cuda and t.dtype == torch.float32 and t.is_contiguous() and t.numel() == n):
+        raise ValueError(f"{name} must be a contiguous fp32 CUDA tensor of B*H entries")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def fa_fwd_fp8(q, k, v, o, lse, q_descale, k_descale, v_descale, scale, causal, workspace, stream=None):
+    B, H, N, d = q.shape
+    rc = load().fa_fwd_fp8(_fp8(q, "q"), _fp8(k, "k"), _fp8(v, "v"), _bf16(o, "o"), _f32(lse, "lse"),
+                           _descale(q_descale, "q_descale", B * H), _descale(k_descale, "k_descale", B * H),
+                           _descale(v_descale, "v_descale", B * H), B, H, N, d, float(scale), int(bool(causal)),
+                           ctypes.c_void_p(workspace.data_ptr()), _stream(stream))
+    _check("fa_fwd_fp8", rc)
+
+
+def forward_fp8(q, k, v, q_descale=None, k_descale=None, v_descale=None, causal=False, scale=None, stream=None):
+    """8-bit forward: returns (O bf16 [B,H,N,d], LSE fp32 [B,H,N])."""
+    B, H, N, d = q.shape
+    scale = (1.0 / d ** 0.5) if scale is None else scale
+    o = torch.empty((B, H, N, d), dtype=torch.bfloat16, device=q.device)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    n = fa_fwd_fp8_workspace_bytes(B, H, N, d)
+    if n == 0:
+        raise ValueError("unsupported sizes for the 8-bit forward (d must be 128)")
+    ws = torch.empty(n, dtype=torch.uint8, device=q.device)
+    fa_fwd_fp8(q, k, v, o, lse, q_descale, k_descale, v_descale, scale, causal, ws, stream)
+    return o, lse
 
 
 def fa_block_mask_window(N, left, right) -> torch.Tensor:

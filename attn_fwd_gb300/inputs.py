@@ -44,6 +44,7 @@ class Workload:
     block_sparse_p: float | None = None  # keep-probability of an off-diagonal block
     window: tuple[int, int] | None = None  # (left, right) extent of a block band
     dropout_p: float = 0.0                 # dropout on P (mask seed = the workload's seed)
+    fp8: bool = False                      # e4m3 inputs with per-head descales (forward only)
     note: str = field(default="", compare=False)
 
     @property
@@ -82,6 +83,10 @@ WORKLOADS = {
     "fwdbwd_b2h16n4096d128_causal_dropout": Workload(
         "fwdbwd_b2h16n4096d128_causal_dropout", 2, 16, 4096, 128, seed=2, causal=True, dropout_p=0.1,
         note="forward + backward, causal, dropout 0.1 with regenerated masks"),
+    # the headline shape's forward with 8-bit (e4m3) Q, K, V
+    "fwd_b2h16n4096d128_causal_fp8": Workload(
+        "fwd_b2h16n4096d128_causal_fp8", 2, 16, 4096, 128, seed=2, causal=True, backward=False, fp8=True,
+        note="forward only, causal, e4m3 inputs with per-(batch, head) descales"),
     # a causal sliding window of 2048 keys (16 blocks)
     "fwdbwd_b1h16n16384d128_causal_window2k": Workload(
         "fwdbwd_b1h16n16384d128_causal_window2k", 1, 16, 16384, 128, seed=5, causal=True,
@@ -165,6 +170,21 @@ def make_decode_inputs(B: int, H: int, Nq: int, Nk: int, d: int, seed: int) -> d
     return out
 
 
+def make_fp8_inputs(B: int, H: int, N: int, d: int, seed: int) -> dict[str, torch.Tensor]:
+    """8-bit inputs: Q, K, V drawn as for make_qkvdo (fp32 randn in that order),
+    then each (batch, head) of each tensor stored as e4m3 after division by
+    its descale amax / 448 (so it fills the e4m3 range).  Returns q8, k8, v8
+    (float8_e4m3fn, CPU) and qd, kd, vd (fp32 [B, H])."""
+    g = torch.Generator(device="cpu").manual_seed(seed)
+    out = {}
+    for nm in ("q", "k", "v"):
+        x = torch.randn((B, H, N, d), generator=g, dtype=torch.float32)
+        ds = x.abs().amax(dim=(2, 3)) / 448.0
+        out[nm + "8"] = (x / ds[..., None, None]).to(torch.float8_e4m3fn)
+        out[nm + "d"] = ds.contiguous()
+    return out
+
+
 def make_block_mask(N: int, seed: int, p: float, block: int = BLOCK) -> torch.Tensor:
     """Block mask as uint8 [N/block, N/block]; diagonal blocks are always kept."""
     if N % block:
@@ -184,7 +204,10 @@ def make_window_mask(N: int, left: int, right: int, block: int = BLOCK) -> torch
 
 def make_workload_inputs(w: Workload, heads: slice | None = None) -> dict[str, torch.Tensor]:
     """All inputs of a workload (CPU).  ``heads`` optionally keeps a head slice."""
-    t = make_qkvdo(w.B, w.H, w.N, w.d, w.seed, w.amplitude, with_dout=w.backward)
+    if w.fp8:
+        t = make_fp8_inputs(w.B, w.H, w.N, w.d, w.seed)
+    else:
+        t = make_qkvdo(w.B, w.H, w.N, w.d, w.seed, w.amplitude, with_dout=w.backward)
     if heads is not None:
         t = {k: v[:, heads].contiguous() for k, v in t.items()}
     if w.block_sparse_p is not None:

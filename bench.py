@@ -204,6 +204,7 @@ def _oracle_sample(w, t, budget_s=15.0, max_heads=None):
     """Time the fp64 oracle (forward + backward) head by head until `budget_s`
     has passed.  Returns (TFLOPS, seconds, heads)."""
     import oracle
+    import torch
     bm = t.get("block_mask")
     bmn = None if bm is None else bm.numpy()
     heads = 0
@@ -212,6 +213,16 @@ def _oracle_sample(w, t, budget_s=15.0, max_heads=None):
     for hh in range(w.B * w.H):
         b, h = divmod(hh, w.H)
         sl = (slice(b, b + 1), slice(h, h + 1))
+        if w.fp8:
+            u8 = [t[n][sl].contiguous().view(torch.uint8).numpy() for n in ("q8", "k8", "v8")]
+            qd, kd, vd = (t[n][sl].double().numpy() for n in ("qd", "kd", "vd"))
+            oracle.forward_fp8(*u8, qd, kd, vd, w.scale, causal=w.causal)
+            heads += 1
+            ff, fb = _flops(type(w)(**{**w.__dict__, "B": 1, "H": 1}), None)
+            flops += ff
+            if time.perf_counter() - t0 >= budget_s or (max_heads and heads >= max_heads):
+                break
+            continue
         q, k, v = (t[n][sl].double().numpy() for n in ("q", "k", "v"))
         if w.dropout_p:
             oracle.forward_dropout(q, k, v, w.scale, w.dropout_p, w.seed, causal=w.causal, block_mask=bmn, b0=b, h0=h)
@@ -247,13 +258,18 @@ def run_reference(args):
     if rank != 0:
         return 0
     import numpy as np
+    import torch
     import oracle
     from attn_fwd_gb300.inputs import DECODE_WORKLOADS, WORKLOADS, make_workload_inputs
     if args.workload in DECODE_WORKLOADS:
         return _run_reference_decode(args, DECODE_WORKLOADS[args.workload])
     w = WORKLOADS[args.workload]
     t = make_workload_inputs(w, heads=slice(0, 1))
-    q, k, v = (t[n][:1].double().numpy() for n in ("q", "k", "v"))
+    if w.fp8:      # the real inputs: e4m3 values times their descales
+        q, k, v = (oracle.e4m3_decode(t[n + "8"][:1].contiguous().view(torch.uint8).numpy())
+                   * t[n + "d"][:1].double().numpy()[..., None, None] for n in ("q", "k", "v"))
+    else:
+        q, k, v = (t[n][:1].double().numpy() for n in ("q", "k", "v"))
     do = t["do"][:1].double().numpy() if w.backward else None
     bm = t["block_mask"].numpy() if "block_mask" in t else None
     nblk = max(1, w.N // REF_ROWS)
@@ -493,6 +509,95 @@ def run_cuda_decode(args, w):
     return 0
 
 
+def _run_cuda_fp8(args, w, t, f_fwd, fa, dev, ws, rank):
+    """8-bit forward: fa_fwd_fp8 (V transpose + forward kernel) per step;
+    roofline against the 8-bit tensor peak = measured bf16 peak x 2 (the
+    nominal dense fp8 : bf16 ratio, 4.5 : 2.25 PFLOP/s)."""
+    import torch
+    import torch.distributed as dist
+    d8 = {n: t[n].to(dev) for n in ("q8", "k8", "v8", "qd", "kd", "vd")}
+    o = torch.empty((w.B, w.H, w.N, w.d), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev)
+    wsp = torch.empty(fa.fa_fwd_fp8_workspace_bytes(w.B, w.H, w.N, w.d), dtype=torch.uint8, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    def step():
+        fa.fa_fwd_fp8(d8["q8"], d8["k8"], d8["v8"], o, lse, d8["qd"], d8["kd"], d8["vd"], w.scale, w.causal, wsp)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    if fa.fa_get_device_error() != 0:
+        raise RuntimeError("device status after warm-up")
+    uuid = None
+    try:
+        uuid = str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        pass
+    sampler = ClockSampler(uuid) if rank == 0 else None
+    if sampler:
+        sampler.start()
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+    if ws > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    for i in range(args.steps):
+        flush.zero_()
+        events[i][0].record()
+        step()
+        events[i][1].record()
+    torch.cuda.synchronize()
+    if ws > 1:
+        dist.barrier()
+    clocks = sampler.stop() if sampler else None
+    if fa.fa_get_device_error() != 0:
+        raise RuntimeError("device status after timing")
+    ms_per_step = max_over_ranks(sum(e[0].elapsed_time(e[1]) for e in events), dev) / args.steps
+    value = whole_job_tflops(ws, f_fwd, ms_per_step)
+    host_in = {n: t[n].pin_memory() for n in d8}
+    ho, hl = torch.empty(o.shape, dtype=o.dtype).pin_memory(), torch.empty(lse.shape).pin_memory()
+    e2e_steps = max(3, min(args.steps, 20))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record()
+    for _ in range(e2e_steps):
+        for n, x in host_in.items():
+            d8[n].copy_(x, non_blocking=True)
+        step()
+        ho.copy_(o, non_blocking=True)
+        hl.copy_(lse, non_blocking=True)
+    e1.record()
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, dev)
+    peaks, peak_src = _peaks()
+    peak = 2.0 * float(peaks["bf16_tflops"])
+    achieved = f_fwd / (ms_per_step * 1e-3) / 1e12
+    roofline = {"bound": "tensor", "kernel": "fa_fwd_fp8_kernel", "achieved": achieved, "peak": peak,
+                "unit": "TFLOP/s", "frac": achieved / peak,
+                "peak_source": f"{peak_src} bf16 dense (burst) x 2, the nominal e4m3 : bf16 ratio",
+                "traffic": _profile_traffic("fa_fwd_fp8_kernel", w.name), "algorithmic_flops_per_launch": f_fwd,
+                "note": "timed with the V transpose launch that precedes it"}
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "e4m3", "data": "synthetic", "config": {**_config(w, None), "inputs":
+            f"N(0,1) seed {w.seed}, e4m3 with per-(batch, head) descale amax/448"},
+            "e2e": {"value": whole_job_tflops(ws, f_fwd, e2e_ms), "unit": UNIT,
+                    "h2d_bytes_per_step": sum(x.numel() * x.element_size() for x in host_in.values()),
+                    "d2h_bytes_per_step": ho.numel() * ho.element_size() + hl.numel() * hl.element_size(),
+                    "ms_per_step": e2e_ms},
+            "gpu_launches": 2 * args.steps, "roofline": roofline, "clocks": clocks}
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        tf, el, heads = _oracle_sample(w, t, budget_s=args.cpu_budget)
+        line["cpu_baseline"] = {"value": tf, "unit": UNIT, "cores": _CORES, "kind": "oracle",
+                                "sample": f"{heads} of {w.B * w.H} (batch, head) pairs, 8-bit forward, fp64, {el:.1f} s"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        dist.destroy_process_group()
+    return 0
+
+
 def run_cuda(args):
     import torch
     import torch.distributed as dist
@@ -515,6 +620,8 @@ def run_cuda(args):
     t = make_workload_inputs(w)
     density = _density(t, w.causal)
     f_fwd, f_bwd = _flops(w, density)
+    if w.fp8:
+        return _run_cuda_fp8(args, w, t, f_fwd, fa, dev, ws, rank)
     q, k, v = (t[n].to(dev) for n in ("q", "k", "v"))
     do = t["do"].to(dev) if w.backward else None
     bm = t["block_mask"].to(dev) if "block_mask" in t else None

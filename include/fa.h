@@ -185,6 +185,29 @@ FA_API int fa_bwd_dropout(const void *q, const void *k, const void *v, const voi
                           float dropout_p, unsigned long long seed, fa_stream_t stream);
 
 /*
+ * Forward with 8-bit inputs: q, k, v hold e4m3 values (1 byte each, [B, H, N,
+ * d] contiguous) whose real values are q * q_descale[b*H + h] (likewise k, v;
+ * a NULL descale array means 1).  Both products run on the 8-bit tensor-core
+ * path ("Как работает FlashAttention математически", section 9, names 8-bit
+ * tensor-core arithmetic as the FlashAttention-3 extension; the pages give no
+ * scaling convention, so the per-(b, h) descale is this library's):
+ *   S = scale * dq * dk * (q k^T), softmax as for fa_fwd, P rounded to e4m3
+ *   (scaled so a row's largest P is in [16, 256]), O = dv * (P8 v) / l with
+ *   l the exact row sum, written as bf16 [B, H, N, d]; LSE (fp32) of the
+ *   exact softmax.
+ * The e4m3 rounding of P (3 mantissa bits) perturbs each attention weight by
+ * at most 2^-4 relative, so |O - O_exact| <= 2^-4 * sum_j P_ij |v_j dv| plus
+ * weights below 2^-14 of the row maximum and O's own bf16 rounding.  d must be 128.  workspace: device memory of
+ * fa_fwd_fp8_workspace_bytes(B, H, N, d) bytes, 256-byte aligned (it receives
+ * v transposed).  Other arguments, errors and asynchrony as for fa_fwd.
+ */
+FA_API size_t fa_fwd_fp8_workspace_bytes(int B, int H, int N, int d);
+FA_API int fa_fwd_fp8(const void *q, const void *k, const void *v, void *o, float *lse,
+                      const float *q_descale, const float *k_descale, const float *v_descale,
+                      int B, int H, int N, int d, float scale, int causal, void *workspace,
+                      fa_stream_t stream);
+
+/*
  * Block masks for the sparse patterns that block-sparse attention serves
  * ("Как работает FlashAttention математически", section 9: block-sparse
  * FlashAttention for sliding-window and dilated attention), at the 128 x 128

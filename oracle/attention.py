@@ -450,20 +450,30 @@ def forward_fp8(q8, k8, v8, q_descale, k_descale, v_descale, scale, causal=False
     return o, lse, probs, v
 
 
-def fp8_error_model(o, probs, v, rel: float = 2.0 ** -4):
-    """Effect on O of perturbing every attention weight by a relative error of
-    at most `rel` (the rounding of P to e4m3: 3 mantissa bits) and
-    renormalising: O' - O = sum_j w_j d_j (v_j - O) / (1 + sum_j w_j d_j).
-    Returns (bound, sigma): the worst case rel / (1 - rel) * sum_j w_j |v_j - O|
-    plus the flush of weights below 2^-17 of the row maximum (at most
-    n 2^-17 max_j |v_j - O|), and the standard deviation when the d_j are
-    independent and uniform on [-rel, rel]:
-    rel / sqrt(3) * sqrt(sum_j w_j^2 (v_j - O)^2)."""
-    dev = v[:, :, None, :, :] - o[:, :, :, None, :]                     # [B,H,N,Nk,d]
-    bound = rel / (1 - rel) * np.einsum("bhij,bhijc->bhic", probs, np.abs(dev))
-    n_vis = (probs > 0).sum(axis=-1)[..., None]
-    bound = bound + n_vis * 2.0 ** -17 * np.abs(dev).max(axis=3)
-    sigma = rel / np.sqrt(3.0) * np.sqrt(np.einsum("bhij,bhijc->bhic", probs ** 2, dev ** 2))
+def fp8_error_model(o, probs, v, rel: float = 2.0 ** -4, row_chunk: int = 64):
+    """Effect on O of rounding every attention weight to e4m3 (relative error
+    d_j at most `rel`: 3 mantissa bits) while O is still divided by the exact
+    row sum: O' - O = sum_j w_j d_j v_j.  Weights below 2^-14 of the row's
+    largest are flushed or rounded with an absolute error up to 2^-14 of it
+    (e4m3's subnormal step against a row maximum of at least 16).
+    Returns (bound, sigma): the worst case rel * sum_j w_j |v_j| + n 2^-14
+    max_j |v_j|, and the standard deviation when the d_j are independent and
+    uniform on [-rel, rel]: rel / sqrt(3) * sqrt(sum_j w_j^2 v_j^2).  Rows are
+    taken in chunks."""
+    B, H, N, d = o.shape
+    bound = np.zeros_like(o)
+    sigma = np.zeros_like(o)
+    for b in range(B):
+        for h in range(H):
+            av = np.abs(v[b, h])
+            for r0 in range(0, N, row_chunk):
+                rows = slice(r0, min(N, r0 + row_chunk))
+                w = probs[b, h, rows]                                    # [r, Nk]
+                n_vis = (w > 0).sum(axis=1)[:, None]
+                vis_max = np.stack([av[w[i] > 0].max(axis=0) if n_vis[i, 0] else np.zeros(d)
+                                    for i in range(w.shape[0])])
+                bound[b, h, rows] = rel * (w @ av) + n_vis * 2.0 ** -14 * vis_max
+                sigma[b, h, rows] = rel / np.sqrt(3.0) * np.sqrt((w ** 2) @ (v[b, h] ** 2))
     return bound, sigma
 
 

@@ -184,3 +184,13 @@ def test_dropout_argument_checks(lib):
         assert lib.fa_bwd_dropout(P, P, P, P, P, P, NULL, P, P, P, P, 1, 1, 128, 64, 0.125, 0, pdrop, 1, NULL) == -1
         assert lib.fa_bwd_main(P, P, P, P, NULL, P, P, P, 1, 1, 128, 64, 0.125, 0, pdrop, 1, NULL) == -1
     assert lib.fa_fwd_dropout(NULL, P, P, P, P, NULL, 1, 1, 128, 64, 0.125, 0, 0.1, 1, NULL) == -1
+
+
+def test_fp8_workspace_and_validation(lib):
+    import attn_fwd_gb300.fa as fa
+    assert fa.fa_fwd_fp8_workspace_bytes(2, 3, 300, 128) == 2 * 3 * 128 * 304 + (256 - (2 * 3 * 128 * 304) % 256) % 256
+    assert fa.fa_fwd_fp8_workspace_bytes(1, 1, 128, 64) == 0          # d must be 128
+    assert lib.fa_fwd_fp8(P, P, P, P, P, NULL, NULL, NULL, 1, 1, 128, 64, 0.1, 0, P, NULL) == -2
+    assert lib.fa_fwd_fp8(P, P, P, P, P, NULL, NULL, NULL, 1, 1, 128, 128, 0.1, 0, NULL, NULL) == -1
+    assert lib.fa_fwd_fp8(P, P, P, P, P, ctypes.c_void_p(4096 + 2), NULL, NULL, 1, 1, 128, 128, 0.1, 0, P, NULL) == -1
+    assert lib.fa_fwd_fp8(P, P, P, P, P, NULL, NULL, NULL, 1, 1, 128, 128, 0.0, 0, P, NULL) == -1
