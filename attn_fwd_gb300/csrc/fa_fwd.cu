@@ -472,7 +472,7 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
       // dropout: key tile of this round (only tracked when needed) and the
       // keep bits of this row's 128 columns, made before S is waited for
       int kt_d = DROP ? (SPARSE ? next_visible(w ? bits1 : bits0, 0, p.n_qt) : 0) : 0;
-      const uint32_t bh_u = static_cast<uint32_t>(blockIdx.x % p.BH);
+      const uint32_t bh_u = static_cast<uint32_t>(bh);
       const uint32_t hd = bh_u % static_cast<uint32_t>(p.H), bd = bh_u / static_cast<uint32_t>(p.H);
       for (int rr = 0; rr < n_vis; ++rr) {
         uint32_t dbits[4];

@@ -46,6 +46,31 @@ def _peaks():
         return PEAKS_FALLBACK, "fallback"
 
 
+# tcgen05 bf16 rate of one SM, measured on this GPU with a microbenchmark of
+# back-to-back 128 x 128 x 16 MMAs: 64 cycles each, i.e. 8192 FLOP per clock.
+BF16_FLOP_PER_CLK_PER_SM = 8192
+
+
+def _other_peaks(achieved, peaks, clocks, dev):
+    """The achieved rate against the measured sustained peak and against the
+    theoretical peak at the median SM clock of the timed region."""
+    import torch
+    out = {}
+    if "bf16_tflops_sustained" in peaks:
+        ps = float(peaks["bf16_tflops_sustained"])
+        out["sustained"] = {"peak": ps, "frac": achieved / ps, "source": "measured bf16 dense (sustained)"}
+    try:
+        sms = torch.cuda.get_device_properties(dev).multi_processor_count
+        mhz = float(clocks["sm_mhz"]) if clocks and clocks.get("sm_mhz") else None
+        if mhz:
+            pt = BF16_FLOP_PER_CLK_PER_SM * sms * mhz * 1e6 / 1e12
+            out["theoretical_at_clock"] = {"peak": pt, "frac": achieved / pt, "sms": sms, "sm_mhz": mhz,
+                                           "source": "8192 FLOP/clk/SM (measured MMA rate) x SMs x median clock"}
+    except Exception:
+        pass
+    return out
+
+
 def _dist():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -747,7 +772,8 @@ def run_cuda(args):
     roofline = {"bound": "tensor", "kernel": tag, "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                 "frac": achieved / peak, "peak_source": f"{peak_src} bf16 dense (burst)",
                 "traffic": _profile_traffic(tag, w.name),
-                "algorithmic_flops_per_launch": algo[dom]}
+                "algorithmic_flops_per_launch": algo[dom],
+                "other_peaks": _other_peaks(achieved, peaks, clocks, dev)}
     kernels = {kname: {"ms": avg[kname], "share": avg[kname] / ms_per_step if ms_per_step else 0.0}
                for kname in avg if per[kname]}
     kernels["fwd"]["tflops"] = f_fwd / (avg["fwd"] * 1e-3) / 1e12
@@ -780,6 +806,28 @@ def run_cuda(args):
     return 0
 
 
+def _apply_overrides(args, ap):
+    """--set K=V,...: a copy of the workload with some sizes replaced, under
+    the name '<workload>@<overrides>' (no stored profile matches it)."""
+    import dataclasses
+    from attn_fwd_gb300.inputs import DECODE_WORKLOADS, WORKLOADS
+    table = DECODE_WORKLOADS if args.workload in DECODE_WORKLOADS else WORKLOADS
+    if args.workload not in table:
+        ap.error(f"unknown workload {args.workload}")
+    w = table[args.workload]
+    kw = {}
+    for item in args.set.split(","):
+        key, _, val = item.partition("=")
+        if not hasattr(w, key) or key in ("name", "note"):
+            ap.error(f"--set: unknown field {key}")
+        cur = getattr(w, key)
+        kw[key] = (val.lower() in ("1", "true", "yes")) if isinstance(cur, bool) else type(cur)(val) \
+            if cur is not None else float(val)
+    name = f"{w.name}@{args.set}"
+    table[name] = dataclasses.replace(w, name=name, **kw)
+    args.workload = name
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -789,9 +837,13 @@ def main():
     ap.add_argument("--impl", choices=("cuda", "reference"), default="cuda")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle time for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--set", default="", metavar="K=V,...",
+                    help="override sizes of the workload, e.g. N=2048,H=16 (an ad-hoc shape with its recipe)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
+    if args.set:
+        _apply_overrides(args, ap)
     if args.impl == "reference":
         return run_reference(args)
     return run_cuda(args)
