@@ -345,8 +345,8 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* o, const v
 }
 
 // Decoding: split the cache into chunks of a whole number of 64-key tiles.
-// The split kernel keeps 2 CTAs per SM at d=128 and 4 at d=64 (shared memory),
-// so 152 SMs run `slots` CTAs at once; the chunk size (1..64 tiles) minimises
+// The split kernel keeps 2 CTAs per SM at d=128 with one query token, 3 with
+// several, and 4 at d=64 (shared memory), so 152 SMs run `slots` CTAs at once; the chunk size (1..64 tiles) minimises
 // waves * (tiles per chunk + 1), the +1 standing for a CTA's pipeline ramp,
 // and prefers fewer chunks on ties.  The plan depends only on the sizes, so
 // the workspace query and the call agree.
@@ -357,9 +357,9 @@ struct DecodePlan {
   int chunk;
 };
 
-DecodePlan decode_plan(int B, int H, int Nk, int d) {
+DecodePlan decode_plan(int B, int H, int Nq, int Nk, int d) {
   const long long tiles = (static_cast<long long>(Nk) + fa::DEC_TILE - 1) / fa::DEC_TILE;
-  const long long slots = kPlanSMs * (d == 128 ? 2 : 4);
+  const long long slots = kPlanSMs * (d == 128 ? (Nq > 1 ? 3 : 2) : 4);
   const long long bh = static_cast<long long>(B) * H;
   long long best_per = 1, best_cost = -1;
   for (long long per = 1; per <= 64 && per <= tiles; ++per) {
@@ -384,7 +384,7 @@ int check_decode_shape(int B, int H, int Nq, int Nk, int d) {
 }
 
 size_t decode_workspace_bytes(int B, int H, int Nq, int Nk, int d) {
-  const DecodePlan plan = decode_plan(B, H, Nk, d);
+  const DecodePlan plan = decode_plan(B, H, Nq, Nk, d);
   if (plan.splits == 1) return 0;
   const size_t rows = static_cast<size_t>(B) * H * plan.splits * Nq;
   return align256(rows * d * sizeof(float)) + align256(rows * sizeof(float));
@@ -397,7 +397,7 @@ int decode_impl(const void* q, const void* k, const void* v, void* o, float* lse
   if (seqlens != nullptr && (reinterpret_cast<uintptr_t>(seqlens) & 3u) != 0) return FA_ERR_INVALID;
   if ((rc = check_decode_shape(B, H, Nq, Nk, d)) != FA_OK) return rc;
   if ((rc = check_scale(scale)) != FA_OK) return rc;
-  const DecodePlan plan = decode_plan(B, H, Nk, d);
+  const DecodePlan plan = decode_plan(B, H, Nq, Nk, d);
   if (plan.splits > 1 && (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0))
     return FA_ERR_INVALID;
   int* status = nullptr;
