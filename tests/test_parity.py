@@ -482,3 +482,35 @@ def test_causal_window_long_sequence_sampled_rows(fa):
                                       causal=True, block_mask=bm_ref)
         err = _rel_l2(dq[0, h, rows], rdq)
         assert err <= GRAD_RTOL, f"h={h} dQ rows rel-L2 {err}"
+
+
+# --------------------------------------------------------------------------- #
+# the largest size the ABI accepts: B*H*N*d just under 2^31 elements, where
+# any 32-bit offset would overflow (inputs drawn on the device from a seeded
+# generator; sampled rows of two heads through the oracle)
+# --------------------------------------------------------------------------- #
+def test_forward_backward_at_the_index_limit(fa):
+    B, H, N, d = 1, 127, 131072, 128
+    assert B * H * N * d < 2 ** 31 and B * (H + 1) * N * d >= 2 ** 31
+    g = torch.Generator(device="cuda").manual_seed(2024)
+    q, k, v, do = (torch.randn((B, H, N, d), generator=g, device="cuda").to(torch.bfloat16) for _ in range(4))
+    scale = 1 / math.sqrt(d)
+    o, lse = fa.forward(q, k, v, causal=True, scale=scale)
+    dq, dk, dv = fa.backward(q, k, v, o, lse, do, causal=True, scale=scale)
+    _check_device_status(fa)
+    tail = np.arange(N - 256, N)
+    for h in (0, H - 1):
+        f64 = {n: x[:, h:h + 1].double().cpu().numpy() for n, x in (("q", q), ("k", k), ("v", v), ("do", do))}
+        rows = np.array([0, 1, 127, 128, 65535, 65536, N - 129, N - 1])
+        ro, rl = oracle.forward_rows(f64["q"], f64["k"], f64["v"], scale, 0, 0, rows, causal=True)
+        _check_fwd(o[0, h, rows], lse[0, h, rows], ro, rl, f"index limit head {h}")
+        rdq = oracle.backward_rows_dq(f64["q"], f64["k"], f64["v"], f64["do"], scale, 0, 0, rows, causal=True)
+        assert _rel_l2(dq[0, h, rows], rdq) <= GRAD_RTOL, f"index limit head {h}: dQ rows"
+        # keys N-256.. are seen only by query rows N-256.. (causal): their
+        # dK and dV are exactly the contributions of those rows
+        _, dkp, dvp, _, _ = oracle.backward_rows(f64["q"], f64["k"], f64["v"], f64["do"], scale, 0, 0, tail,
+                                                 causal=True)
+        assert _rel_l2(dk[0, h, tail], dkp[tail]) <= GRAD_RTOL, f"index limit head {h}: dK tail"
+        assert _rel_l2(dv[0, h, tail], dvp[tail]) <= GRAD_RTOL, f"index limit head {h}: dV tail"
+    del q, k, v, do, o, lse, dq, dk, dv
+    torch.cuda.empty_cache()
