@@ -345,8 +345,8 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* o, const v
 }
 
 // Decoding: split the cache into chunks of a whole number of 64-key tiles.
-// The split kernel keeps 2 CTAs per SM at d=128 with one query token, 3 with
-// several, and 4 at d=64 (shared memory), so 152 SMs run `slots` CTAs at once; the chunk size (1..64 tiles) minimises
+// The split kernel keeps fa::dec_ctas_per_sm CTAs on an SM (its shared
+// memory), so 152 SMs run `slots` CTAs at once; the chunk size (1..64 tiles) minimises
 // waves * (tiles per chunk + 1), the +1 standing for a CTA's pipeline ramp,
 // and prefers fewer chunks on ties.  The plan depends only on the sizes, so
 // the workspace query and the call agree.
@@ -359,7 +359,7 @@ struct DecodePlan {
 
 DecodePlan decode_plan(int B, int H, int Nq, int Nk, int d) {
   const long long tiles = (static_cast<long long>(Nk) + fa::DEC_TILE - 1) / fa::DEC_TILE;
-  const long long slots = kPlanSMs * (d == 128 ? (Nq > 1 ? 3 : 2) : 4);
+  const long long slots = kPlanSMs * fa::dec_ctas_per_sm(d);
   const long long bh = static_cast<long long>(B) * H;
   long long best_per = 1, best_cost = -1;
   for (long long per = 1; per <= 64 && per <= tiles; ++per) {
@@ -405,8 +405,6 @@ int decode_impl(const void* q, const void* k, const void* v, void* o, float* lse
   fa::DecParams p;
   std::memset(&p, 0, sizeof(p));
   p.q = static_cast<const __nv_bfloat16*>(q);
-  p.k = static_cast<const __nv_bfloat16*>(k);
-  p.v = static_cast<const __nv_bfloat16*>(v);
   p.o = static_cast<__nv_bfloat16*>(o);
   p.lse = lse;
   if (plan.splits > 1) {
@@ -426,6 +424,10 @@ int decode_impl(const void* q, const void* k, const void* v, void* o, float* lse
   p.chunk = plan.chunk;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.causal = causal ? 1 : 0;
+  // the cache tiles go through TMA with 128-byte swizzle
+  if ((rc = encoder_ready()) != FA_OK) return rc;
+  if ((rc = make_map_bf16(&p.tm_k, k, B * H, Nk, d, fa::DEC_TILE)) != FA_OK) return rc;
+  if ((rc = make_map_bf16(&p.tm_v, v, B * H, Nk, d, fa::DEC_TILE)) != FA_OK) return rc;
   if (log_enabled())
     std::fprintf(stderr, "[fa] decode B=%d H=%d Nq=%d Nk=%d d=%d splits=%d chunk=%d\n", B, H, Nq, Nk, d, plan.splits,
                  plan.chunk);

@@ -85,10 +85,15 @@ struct BwdParams {
 constexpr int DEC_TILE = 64;
 constexpr int DEC_MAX_Q = 8;
 
+// CTAs of the decode split kernel that fit on one SM (shared memory: a
+// 3-stage ring of 64-key K and V tiles, 101 KB at d = 128, 53 KB at d = 64);
+// the host-side planner sizes its chunks with the same number.
+__host__ __device__ constexpr int dec_ctas_per_sm(int d) { return d == 128 ? 2 : 4; }
+
 struct DecParams {
+  CUtensorMap tm_k;          // K, V as [B*H][Nk][d], box {64, 64, 1}, 128-byte swizzle
+  CUtensorMap tm_v;
   const __nv_bfloat16* q;    // [B*H][Nq][d]
-  const __nv_bfloat16* k;    // [B*H][Nk][d]
-  const __nv_bfloat16* v;    // [B*H][Nk][d]
   __nv_bfloat16* o;          // [B*H][Nq][d]
   float* lse;                // [B*H][Nq], natural log
   float* o_part;             // [B*H][splits][Nq][d] fp32, normalised per chunk (splits > 1)

@@ -2,20 +2,21 @@
 // cache, split over the cache ("Как работает FlashAttention математически",
 // section 9: FlashDecoding -- K and V are cached, Q is the newest token).
 //
-// The work is bound by reading K and V once from HBM, so it runs on CUDA
-// cores: one CTA per (batch, head, chunk of the cache); a producer lane
-// streams 64-key tiles of K and V with 1-D bulk copies (each tile is a
-// contiguous run of rows) into a shared-memory ring; two consumer warps take
-// 32 keys of each tile.  For S = scale * q k^T lane j owns key j: it reads
-// its key row once, in 16-byte chunks taken in a lane-rotated order (so the
-// 32 rows hit different banks), and forms every query's dot product against
-// q kept in shared memory as fp32, two products per packed FMA.  The online
-// softmax ("FlashAttention" notes, "Tiling"; the aivaro.ru page, sections
-// 3-4) keeps the running max m, the row sum l and the output per query; for
-// O += p V lane t owns d/32 columns, reads each V row once and updates two
-// queries per packed FMA with their p broadcast by shuffle.  Each chunk writes its
-// normalised O and its LSE; a second kernel merges the chunks with the
-// statistics merge of "FlashAttention" notes, "Tiling":
+// The work is bound by reading K and V once from HBM.  One CTA per (batch,
+// head, chunk of the cache): a producer lane streams 64-key tiles of K and V
+// by TMA into a shared-memory ring; two consumer warps take 32 keys of each
+// tile and keep the online softmax per query token ("FlashAttention" notes,
+// "Tiling"; the aivaro.ru page, sections 3-4): running max m, row sum l and
+// the output.  For 1 to 8 tokens the scores S^T = K q^T (keys x tokens) and
+// the output O^T += V^T P^T (head dim x tokens) are matrix products with a
+// short side; they go to warp-level m16n8k16 tensor-core MMAs with the keys
+// (or head-dim rows) in M and the tokens in N = 8, which leaves CUDA cores
+// only the softmax, so the kernel runs at the HBM bound for any token count.
+// K and V tiles arrive with 128-byte swizzle (boxes of 64 keys x 64
+// columns), so the fragment loads hit 8 different bank groups.
+//
+// Each chunk writes its normalised O and its LSE; a second kernel merges the
+// chunks with the statistics merge of "FlashAttention" notes, "Tiling":
 // M = max LSE_c, w_c = exp(LSE_c - M), O = sum w_c O_c / sum w_c,
 // LSE = M + ln sum w_c.  With a single chunk the first kernel writes O and
 // LSE itself.
@@ -24,70 +25,10 @@
 
 namespace fa {
 
-template <int D, int NQ>
-struct DecLayout {
-  static constexpr int KT = DEC_TILE;                      // keys per stage
-  static constexpr int ROW = D * 2;                        // bytes per key row
-  static constexpr int TILE_BYTES = KT * ROW;              // K (or V) of one stage
-  // 3 stages: 96 KB (d=128) / 48 KB (d=64) of K/V, 2 / 4 CTAs per SM; with
-  // several query tokens at d=128, 2 stages and 3 CTAs per SM, so more
-  // consumer warps hide the per-key latency of the longer score loop
-  static constexpr int STAGES = (D == 128 && NQ > 1) ? 2 : 3;
-  static constexpr int K_OFF = 0;
-  static constexpr int V_OFF = STAGES * TILE_BYTES;
-  static constexpr int MERGE_OFF = 2 * STAGES * TILE_BYTES;            // warp 1's state
-  static constexpr int MERGE_BYTES = DEC_MAX_Q * (D + 2) * 4;
-  static constexpr int QS_OFF = MERGE_OFF + MERGE_BYTES;               // q, fp32, pre-scaled
-  static constexpr int QS_BYTES = DEC_MAX_Q * D * 4;
-  static constexpr int BAR_OFF = QS_OFF + QS_BYTES;
-  static constexpr int B_FULL = 0;
-  static constexpr int B_EMPTY = STAGES;
-  static constexpr int NBARS = 2 * STAGES;
-  static constexpr int SMEM_BYTES = BAR_OFF + NBARS * 8 + 16 + 128;   // + abort flag, + alignment slack
-  static constexpr int THREADS = 96;                       // warps 0-1 consume, warp 2 loads
-  static constexpr int E = D / 32;                         // head-dim columns per lane
-};
-
-// Sum over the 32 lanes of v[j] for each j, leaving the total of entry `lane`
-// in v[0]: at each step a lane keeps the half of its entries selected by its
-// lane bit and adds the partner's copy of that half (31 shuffles in all).
-template <int OFF>
-__device__ __forceinline__ void xpose_step(float (&v)[32], uint32_t lane) {
-  const bool up = (lane & OFF) != 0;
-#pragma unroll
-  for (int t = 0; t < OFF; ++t) {
-    const float send = up ? v[t] : v[t + OFF];
-    const float keep = up ? v[t + OFF] : v[t];
-    v[t] = keep + __shfl_xor_sync(0xffffffffu, send, OFF);
-  }
-}
-
 __device__ __forceinline__ float warp_max(float x) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
   return x;
-}
-
-__device__ __forceinline__ float warp_sum(float x) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
-  return x;
-}
-
-// E consecutive bf16 of a row as floats (E = 2 or 4).
-template <int E>
-__device__ __forceinline__ void load_bf16(const uint8_t* p, float (&f)[E]) {
-  if constexpr (E == 4) {
-    const uint2 w = *reinterpret_cast<const uint2*>(p);
-    f[0] = __uint_as_float(w.x << 16);
-    f[1] = __uint_as_float(w.x & 0xffff0000u);
-    f[2] = __uint_as_float(w.y << 16);
-    f[3] = __uint_as_float(w.y & 0xffff0000u);
-  } else {
-    const uint32_t w = *reinterpret_cast<const uint32_t*>(p);
-    f[0] = __uint_as_float(w << 16);
-    f[1] = __uint_as_float(w & 0xffff0000u);
-  }
 }
 
 __device__ __forceinline__ void dec_drain(uint32_t bar, uint32_t parity, uint64_t ns) {
@@ -97,226 +38,38 @@ __device__ __forceinline__ void dec_drain(uint32_t bar, uint32_t parity, uint64_
   }
 }
 
-// One query token: lane t holds d/32 columns of q and of O; scores by a
-// transposing butterfly reduction over the lanes.
-template <int D, int NQ>
-__device__ __forceinline__ void consume_one(const DecParams& p, uint8_t* smem, uint64_t* bars, const WaitCtx& wc,
-                                        uint32_t warp, uint32_t lane, int bh, int len, int k_begin, int k_end,
-                                        int n_tiles, float (&o)[NQ][D / 32], float (&m)[NQ], float (&l)[NQ],
-                                        bool& ok) {
-  using L = DecLayout<D, NQ>;
-  constexpr int E = L::E;
-  auto bar = [&](int i) { return smem_u32(bars + i); };
-  // q pre-scaled by scale * log2(e): scores come out in exp2 units
-  float qf[NQ][E];
-  const int nq = p.Nq;
-#pragma unroll
-  for (int i = 0; i < NQ; ++i) {
-    if (i < nq) {
-      load_bf16<E>(reinterpret_cast<const uint8_t*>(p.q + (static_cast<size_t>(bh) * nq + i) * D + lane * E), qf[i]);
-#pragma unroll
-      for (int e = 0; e < E; ++e) qf[i][e] *= p.scale_log2;
-    }
-  }
-#pragma unroll
-  for (int i = 0; i < NQ; ++i) {
-    m[i] = -INFINITY;
-    l[i] = 0.f;
-#pragma unroll
-    for (int e = 0; e < E; ++e) o[i][e] = 0.f;
-  }
-  // the last key query i may see (bottom-right causal alignment)
-  const int last_key0 = p.causal ? len - nq : len - 1;
-  ok = true;
-  for (int t = 0; t < n_tiles; ++t) {
-    const int s = t % L::STAGES;
-    if (!(ok = mbar_wait_warp(bar(L::B_FULL + s), (t / L::STAGES) & 1, wc))) break;
-    const int kb = k_begin + t * L::KT + 32 * static_cast<int>(warp);   // this warp's first key
-    const int nv = min(max(k_end - kb, 0), 32);                         // its valid keys
-    const uint8_t* ks = smem + L::K_OFF + s * L::TILE_BYTES + (32 * warp) * L::ROW + lane * E * 2;
-    const uint8_t* vs = smem + L::V_OFF + s * L::TILE_BYTES + (32 * warp) * L::ROW + lane * E * 2;
-    if (nv > 0) {
-#pragma unroll
-      for (int i = 0; i < NQ; ++i) {
-        if (i >= nq) break;
-        float part[32];
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          float kf[E];
-          load_bf16<E>(ks + j * L::ROW, kf);
-          float acc = qf[i][0] * kf[0];
-#pragma unroll
-          for (int e = 1; e < E; ++e) acc = fmaf(qf[i][e], kf[e], acc);
-          part[j] = acc;
-        }
-        xpose_step<16>(part, lane);
-        xpose_step<8>(part, lane);
-        xpose_step<4>(part, lane);
-        xpose_step<2>(part, lane);
-        xpose_step<1>(part, lane);
-        const int key = kb + static_cast<int>(lane);
-        const bool vis = static_cast<int>(lane) < nv && key <= last_key0 + (p.causal ? i : 0);
-        const float sc = vis ? part[0] : -INFINITY;
-        const float m_new = fmaxf(m[i], warp_max(sc));
-        if (m_new == -INFINITY) continue;                  // nothing visible yet (warp-uniform)
-        const float alpha = ex2_approx(m[i] - m_new);      // 0 when m was -inf
-        const float pj = ex2_approx(sc - m_new);           // 0 for masked keys
-        m[i] = m_new;
-        l[i] = l[i] * alpha + pj;
-#pragma unroll
-        for (int e = 0; e < E; ++e) o[i][e] *= alpha;
-        // O += p V over this warp's keys; rows past nv are stale and never read
-        if (nv == 32) {
-#pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const float w = __shfl_sync(0xffffffffu, pj, j);
-            float vf[E];
-            load_bf16<E>(vs + j * L::ROW, vf);
-#pragma unroll
-            for (int e = 0; e < E; ++e) o[i][e] = fmaf(w, vf[e], o[i][e]);
-          }
-        } else {
-          for (int j = 0; j < nv; ++j) {
-            const float w = __shfl_sync(0xffffffffu, pj, j);
-            float vf[E];
-            load_bf16<E>(vs + j * L::ROW, vf);
-#pragma unroll
-            for (int e = 0; e < E; ++e) o[i][e] = fmaf(w, vf[e], o[i][e]);
-          }
-        }
-      }
-    }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(bar(L::B_EMPTY + s));
-  }
+template <int D>
+struct DecLayout {
+  static constexpr int KT = DEC_TILE;                      // keys per stage
+  static constexpr int BOX_BYTES = KT * 128;               // 64 keys x 64 columns
+  static constexpr int TILE_BYTES = KT * D * 2;            // K (or V) of one stage
+  static constexpr int STAGES = 3;                         // 96 KB (d=128) / 48 KB (d=64)
+  static constexpr int K_OFF = 0;
+  static constexpr int V_OFF = STAGES * TILE_BYTES;
+  static constexpr int MS = D + 4;                         // merge row stride (floats)
+  static constexpr int MERGE_OFF = 2 * STAGES * TILE_BYTES;
+  static constexpr int MERGE_BYTES = (DEC_MAX_Q * MS + 2 * DEC_MAX_Q) * 4;   // O, then m, l
+  static constexpr int BAR_OFF = MERGE_OFF + MERGE_BYTES;
+  static constexpr int B_FULL = 0;
+  static constexpr int B_EMPTY = STAGES;
+  static constexpr int NBARS = 2 * STAGES;
+  static constexpr int SMEM_BYTES = BAR_OFF + NBARS * 8 + 16 + 1024;  // + abort flag, + 1 KB alignment slack
+  static constexpr int THREADS = 96;                       // warps 0-1 consume, warp 2 loads
+};
+
+// Byte offset of 16-byte chunk j (columns 8j..8j+7) of key row r in a tile
+// stored as D/64 boxes of [64 rows][128 B] with 128-byte swizzle.
+template <int D>
+__device__ __forceinline__ uint32_t sw_chunk(int r, int j) {
+  return static_cast<uint32_t>((j >> 3) * DecLayout<D>::BOX_BYTES + r * 128 + (((j & 7) ^ (r & 7)) << 4));
 }
 
-// Several query tokens: lane j scores key j against every query; O columns
-// per lane, two queries per packed FMA.
-template <int D, int NQ>
-__device__ __forceinline__ void consume_many(const DecParams& p, uint8_t* smem, uint64_t* bars, const WaitCtx& wc,
-                                        uint32_t warp, uint32_t lane, int bh, int len, int k_begin, int k_end,
-                                        int n_tiles, float (&o)[NQ][D / 32], float (&m)[NQ], float (&l)[NQ],
-                                        bool& ok) {
-  using L = DecLayout<D, NQ>;
-  constexpr int E = L::E;
-  auto bar = [&](int i) { return smem_u32(bars + i); };
-  // q pre-scaled by scale * log2(e) (scores come out in exp2 units), fp32 in
-  // shared memory: [query][d]
-  const int nq = p.Nq;
-  float* qs = reinterpret_cast<float*>(smem + L::QS_OFF);
-  for (int x = static_cast<int>(threadIdx.x); x < nq * D; x += 64) {
-    const float f = __bfloat162float(p.q[static_cast<size_t>(bh) * nq * D + x]);
-    qs[x] = f * p.scale_log2;
-  }
-  named_bar_sync(2, 64);
-  constexpr int NP = NQ > 1 ? NQ / 2 : 1;                 // query pairs
-  float2 o2[NP][E];                                       // (query 2r, query 2r+1) per column
-#pragma unroll
-  for (int i = 0; i < NQ; ++i) {
-    m[i] = -INFINITY;
-    l[i] = 0.f;
-  }
-#pragma unroll
-  for (int r = 0; r < NP; ++r)
-#pragma unroll
-    for (int e = 0; e < E; ++e) o2[r][e] = make_float2(0.f, 0.f);
-  // the last key query i may see (bottom-right causal alignment)
-  const int last_key0 = p.causal ? len - nq : len - 1;
-  constexpr int CH = D / 8;                                // 16-byte chunks per key row
-  ok = true;
-  for (int t = 0; t < n_tiles; ++t) {
-    const int s = t % L::STAGES;
-    if (!(ok = mbar_wait_warp(bar(L::B_FULL + s), (t / L::STAGES) & 1, wc))) break;
-    const int kb = k_begin + t * L::KT + 32 * static_cast<int>(warp);   // this warp's first key
-    const int nv = min(max(k_end - kb, 0), 32);                         // its valid keys
-    const uint8_t* krow = smem + L::K_OFF + s * L::TILE_BYTES + (32 * warp + lane) * L::ROW;
-    const uint8_t* vs = smem + L::V_OFF + s * L::TILE_BYTES + (32 * warp) * L::ROW + lane * E * 2;
-    if (nv > 0) {
-      // scores: lane = key; rows past nv are stale, their scores are masked below
-      float2 acc[NQ];
-#pragma unroll
-      for (int i = 0; i < NQ; ++i) acc[i] = make_float2(0.f, 0.f);
-#pragma unroll
-      for (int c = 0; c < CH; ++c) {
-        const int cc = (c + static_cast<int>(lane)) & (CH - 1);
-        const uint4 kw = *reinterpret_cast<const uint4*>(krow + cc * 16);
-        const float2 k0 = make_float2(__uint_as_float(kw.x << 16), __uint_as_float(kw.x & 0xffff0000u));
-        const float2 k1 = make_float2(__uint_as_float(kw.y << 16), __uint_as_float(kw.y & 0xffff0000u));
-        const float2 k2 = make_float2(__uint_as_float(kw.z << 16), __uint_as_float(kw.z & 0xffff0000u));
-        const float2 k3 = make_float2(__uint_as_float(kw.w << 16), __uint_as_float(kw.w & 0xffff0000u));
-#pragma unroll
-        for (int i = 0; i < NQ; ++i) {
-          if (i < nq) {
-            const float4 qa = *reinterpret_cast<const float4*>(qs + i * D + cc * 8);
-            const float4 qb = *reinterpret_cast<const float4*>(qs + i * D + cc * 8 + 4);
-            acc[i] = ffma2(make_float2(qa.x, qa.y), k0, acc[i]);
-            acc[i] = ffma2(make_float2(qa.z, qa.w), k1, acc[i]);
-            acc[i] = ffma2(make_float2(qb.x, qb.y), k2, acc[i]);
-            acc[i] = ffma2(make_float2(qb.z, qb.w), k3, acc[i]);
-          }
-        }
-      }
-      // online softmax per query; pj = this lane's key weight
-      const int key = kb + static_cast<int>(lane);
-      float pj[NQ], alpha[NQ];
-#pragma unroll
-      for (int i = 0; i < NQ; ++i) {
-        pj[i] = 0.f;
-        alpha[i] = 1.f;
-        if (i < nq) {
-          const bool vis = static_cast<int>(lane) < nv && key <= last_key0 + (p.causal ? i : 0);
-          const float sc = vis ? acc[i].x + acc[i].y : -INFINITY;
-          const float m_new = fmaxf(m[i], warp_max(sc));
-          if (m_new != -INFINITY) {                        // warp-uniform
-            alpha[i] = ex2_approx(m[i] - m_new);           // 0 when m was -inf
-            pj[i] = ex2_approx(sc - m_new);                // 0 for masked keys
-            m[i] = m_new;
-            l[i] = l[i] * alpha[i] + pj[i];
-          }
-        }
-      }
-#pragma unroll
-      for (int r = 0; r < NP; ++r) {
-        const float2 a2 = make_float2(alpha[2 * r], NQ > 1 ? alpha[2 * r + 1] : 1.f);
-#pragma unroll
-        for (int e = 0; e < E; ++e) o2[r][e] = fmul2(o2[r][e], a2);
-      }
-      // O += p V over this warp's keys; rows past nv are stale and never read
-      auto pv_row = [&](int j) {
-        float vf[E];
-        load_bf16<E>(vs + j * L::ROW, vf);
-#pragma unroll
-        for (int r = 0; r < NP; ++r) {
-          const float wa = __shfl_sync(0xffffffffu, pj[2 * r], j);
-          const float wb = NQ > 1 ? __shfl_sync(0xffffffffu, pj[2 * r + 1], j) : 0.f;
-          const float2 w2 = make_float2(wa, wb);
-#pragma unroll
-          for (int e = 0; e < E; ++e) o2[r][e] = ffma2(w2, make_float2(vf[e], vf[e]), o2[r][e]);
-        }
-      };
-      if (nv == 32) {
-#pragma unroll
-        for (int j = 0; j < 32; ++j) pv_row(j);
-      } else {
-        for (int j = 0; j < nv; ++j) pv_row(j);
-      }
-    }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(bar(L::B_EMPTY + s));
-  }
-#pragma unroll
-  for (int i = 0; i < NQ; ++i)
-#pragma unroll
-    for (int e = 0; e < E; ++e) o[i][e] = (i & 1) ? o2[i / 2][e].y : o2[i / 2][e].x;
-}
-
-template <int D, int NQ>
+template <int D>
 __global__ void __launch_bounds__(96) fa_decode_kernel(const __grid_constant__ DecParams p) {
-  using L = DecLayout<D, NQ>;
-  constexpr int E = L::E;
+  using L = DecLayout<D>;
+  constexpr int KS = D / 16;                               // 16-column steps of the head dim
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::BAR_OFF);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + L::NBARS);
   auto bar = [&](int i) { return smem_u32(bars + i); };
@@ -342,23 +95,27 @@ __global__ void __launch_bounds__(96) fa_decode_kernel(const __grid_constant__ D
   }
   __syncthreads();
   const WaitCtx wc{abort_flag, p.status, p.timeout_ns};
-  const size_t head_rows = static_cast<size_t>(bh) * p.Nk;
 
   if (warp == 2) {
     // ------------------------------------------------------------ producer
+    // Whole 64-key boxes: rows past the cache's end (Nk) are zero-filled;
+    // rows past this batch's length are read and masked by the consumers.
     if (lane == 0) {
       uint32_t issued[L::STAGES] = {};
       bool ok = true;
+      const uint64_t pol = l2_policy_evict_first();          // K and V are read once
       for (int t = 0; t < n_tiles; ++t) {
         const int s = t % L::STAGES;
         if (!mbar_wait(bar(L::B_EMPTY + s), ((t / L::STAGES) & 1) ^ 1, wc)) { ok = false; break; }
         const int k0 = k_begin + t * L::KT;
-        const int rows = min(L::KT, k_end - k0);
-        const uint32_t bytes = static_cast<uint32_t>(rows * L::ROW);    // a multiple of 128
-        const size_t off = (head_rows + static_cast<size_t>(k0)) * D;
-        mbar_arrive_expect_tx(bar(L::B_FULL + s), 2 * bytes);
-        bulk_load(smem_u32(smem + L::K_OFF + s * L::TILE_BYTES), p.k + off, bytes, bar(L::B_FULL + s));
-        bulk_load(smem_u32(smem + L::V_OFF + s * L::TILE_BYTES), p.v + off, bytes, bar(L::B_FULL + s));
+        mbar_arrive_expect_tx(bar(L::B_FULL + s), 2 * L::TILE_BYTES);
+#pragma unroll
+        for (int h = 0; h < D / 64; ++h) {
+          tma_load_3d(smem_u32(smem + L::K_OFF + s * L::TILE_BYTES + h * L::BOX_BYTES), &p.tm_k, bar(L::B_FULL + s),
+                      64 * h, k0, bh, pol);
+          tma_load_3d(smem_u32(smem + L::V_OFF + s * L::TILE_BYTES + h * L::BOX_BYTES), &p.tm_v, bar(L::B_FULL + s),
+                      64 * h, k0, bh, pol);
+        }
         ++issued[s];
       }
       if (!ok) {
@@ -370,75 +127,226 @@ __global__ void __launch_bounds__(96) fa_decode_kernel(const __grid_constant__ D
   }
 
   // -------------------------------------------------------------- consumers
-  // One token: the transposing-reduction form (its loop is short enough for
-  // one consumer warp per SM sub-partition to keep up with HBM).  Several
-  // tokens: lane-per-key scores with shared K and V reads.
-  float o[NQ][E], m[NQ], l[NQ];
-  bool ok = true;
+  // Warp w takes keys 32w..32w+31 of every tile.  Fragment coordinates:
+  // g = lane / 4 (a row of M), tq = lane % 4 (query columns 2tq, 2tq+1).
   const int nq = p.Nq;
-  if constexpr (NQ == 1) {
-    consume_one<D, NQ>(p, smem, bars, wc, warp, lane, bh, len, k_begin, k_end, n_tiles, o, m, l, ok);
-  } else {
-    consume_many<D, NQ>(p, smem, bars, wc, warp, lane, bh, len, k_begin, k_end, n_tiles, o, m, l, ok);
+  const int g = static_cast<int>(lane >> 2), tq = static_cast<int>(lane & 3);
+  // q^T as the B operand of S^T = K q^T, for every 16-column step kk:
+  // (q[g][16kk + 2tq, +1], q[g][16kk + 8 + 2tq, +1]); zero for absent tokens
+  uint32_t qb[KS][2];
+  {
+    const uint32_t* qrow = reinterpret_cast<const uint32_t*>(p.q + (static_cast<size_t>(bh) * nq + g) * D);
+#pragma unroll
+    for (int kk = 0; kk < KS; ++kk) {
+      qb[kk][0] = g < nq ? __ldg(qrow + 8 * kk + tq) : 0u;
+      qb[kk][1] = g < nq ? __ldg(qrow + 8 * kk + 4 + tq) : 0u;
+    }
   }
-  // ------------------------------------------ merge the two warps' states
-  float* mg = reinterpret_cast<float*>(smem + L::MERGE_OFF);   // [DEC_MAX_Q][D + 2]
+  // running max (exp2 units), this lane's part of the row sum, and O^T
+  // fragments: oacc[dm] holds O^T[16dm + g (+8)][2tq, 2tq+1]
+  float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
+  float oacc[KS][4];
 #pragma unroll
-  for (int i = 0; i < NQ; ++i) l[i] = warp_sum(l[i]);
-  if (warp == 1) {
+  for (int dm = 0; dm < KS; ++dm)
 #pragma unroll
-    for (int i = 0; i < NQ; ++i) {
-      if (i < nq) {
-        float* r = mg + i * (D + 2);
+    for (int e = 0; e < 4; ++e) oacc[dm][e] = 0.f;
+  // the last key each of this lane's two queries may see (bottom-right causal
+  // alignment); query columns past nq compute on zeros and are never stored
+  const int last_key0 = p.causal ? len - nq : len - 1;
+  const int lim0 = last_key0 + (p.causal ? 2 * tq : 0);
+  const int lim1 = last_key0 + (p.causal ? 2 * tq + 1 : 0);
+  const uint32_t sk0 = smem_u32(smem + L::K_OFF), sv0 = smem_u32(smem + L::V_OFF);
+  const int rw = 32 * static_cast<int>(warp);                // this warp's first row in a tile
+  bool ok = true;
+  for (int t = 0; t < n_tiles; ++t) {
+    const int s = t % L::STAGES;
+    if (!(ok = mbar_wait_warp(bar(L::B_FULL + s), (t / L::STAGES) & 1, wc))) break;
+    const int kb = k_begin + t * L::KT + rw;                 // this warp's first key
+    const int nv = min(max(k_end - kb, 0), 32);              // its valid keys
+    if (nv > 0) {
+      const uint32_t kt = sk0 + s * L::TILE_BYTES, vt = sv0 + s * L::TILE_BYTES;
+      if (nv < 32) {
+        // rows past the batch's length hold whatever the cache holds there:
+        // zero this warp's V rows past nv (P is 0 there, but 0 * NaN is not)
+        uint8_t* vrow = smem + L::V_OFF + s * L::TILE_BYTES;
+        for (int x = static_cast<int>(lane); x < (32 - nv) * (D / 8); x += 32) {
+          const int r = rw + nv + x / (D / 8), j = x % (D / 8);
+          *reinterpret_cast<uint4*>(vrow + (j >> 3) * L::BOX_BYTES + r * 128 + ((j & 7) << 4)) =
+              make_uint4(0, 0, 0, 0);
+        }
+        __syncwarp();
+      }
+      // S^T for the warp's two 16-key row blocks
+      float sacc[2][4];
 #pragma unroll
-        for (int e = 0; e < E; ++e) r[lane * E + e] = o[i][e];
-        if (lane == 0) {
-          r[D] = m[i];
-          r[D + 1] = l[i];
+      for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) sacc[mt][e] = 0.f;
+#pragma unroll
+      for (int kk = 0; kk < KS; ++kk) {
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt) {
+          // matrices: rows +0 / +8 of the block, columns 16kk / 16kk + 8
+          const int r = rw + 16 * mt + static_cast<int>(lane & 7) + static_cast<int>((lane >> 3) & 1) * 8;
+          const int j = 2 * kk + static_cast<int>(lane >> 4);
+          uint32_t a[4];
+          ldsm_x4(kt + sw_chunk<D>(r, j), a);
+          mma_16816(sacc[mt], a, qb[kk][0], qb[kk][1]);
         }
       }
+      // online softmax per query column: mask, max over the 32 keys (this
+      // lane's 4 rows, then the 8 lanes sharing tq), exp2
+      float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+      for (int mt = 0; mt < 2; ++mt) {
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          const int kr = 16 * mt + 8 * hh + g;               // key row within the warp's 32
+          const bool in = kr < nv;
+          const int key = kb + kr;
+          sacc[mt][2 * hh] = (in && key <= lim0) ? sacc[mt][2 * hh] * p.scale_log2 : -INFINITY;
+          sacc[mt][2 * hh + 1] = (in && key <= lim1) ? sacc[mt][2 * hh + 1] * p.scale_log2 : -INFINITY;
+          mx0 = fmaxf(mx0, sacc[mt][2 * hh]);
+          mx1 = fmaxf(mx1, sacc[mt][2 * hh + 1]);
+        }
+      }
+#pragma unroll
+      for (int o = 4; o < 32; o <<= 1) {
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+      }
+      const float mn0 = fmaxf(m[0], mx0), mn1 = fmaxf(m[1], mx1);
+      // a column with nothing visible yet keeps m = -inf, p = 0, alpha = 1
+      const float al0 = mn0 == -INFINITY ? 1.f : ex2_approx(m[0] - mn0);
+      const float al1 = mn1 == -INFINITY ? 1.f : ex2_approx(m[1] - mn1);
+      const float mb0 = mn0 == -INFINITY ? 0.f : mn0, mb1 = mn1 == -INFINITY ? 0.f : mn1;
+      float ps0 = 0.f, ps1 = 0.f;
+#pragma unroll
+      for (int mt = 0; mt < 2; ++mt) {
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          sacc[mt][2 * hh] = ex2_approx(sacc[mt][2 * hh] - mb0);          // 0 where masked
+          sacc[mt][2 * hh + 1] = ex2_approx(sacc[mt][2 * hh + 1] - mb1);
+          ps0 += sacc[mt][2 * hh];
+          ps1 += sacc[mt][2 * hh + 1];
+        }
+      }
+      m[0] = mn0;
+      m[1] = mn1;
+      l[0] = l[0] * al0 + ps0;
+      l[1] = l[1] * al1 + ps1;
+#pragma unroll
+      for (int dm = 0; dm < KS; ++dm) {
+        oacc[dm][0] *= al0;
+        oacc[dm][1] *= al1;
+        oacc[dm][2] *= al0;
+        oacc[dm][3] *= al1;
+      }
+      // O^T += V^T P^T: per 16-key step mt, P^T as the B operand is the
+      // transpose of the score fragments (keys x queries -> queries x keys)
+#pragma unroll
+      for (int mt = 0; mt < 2; ++mt) {
+        const uint32_t b0 = movm_t(pack_bf16x2(sacc[mt][0], sacc[mt][1]));
+        const uint32_t b1 = movm_t(pack_bf16x2(sacc[mt][2], sacc[mt][3]));
+#pragma unroll
+        for (int dm = 0; dm < KS; ++dm) {
+          // matrices (transposed): keys +0 / +8 of the step, columns 16dm / 16dm + 8
+          const int r = rw + 16 * mt + static_cast<int>(lane & 7) + static_cast<int>((lane >> 4) & 1) * 8;
+          const int j = 2 * dm + static_cast<int>((lane >> 3) & 1);
+          uint32_t a[4];
+          ldsm_x4_t(vt + sw_chunk<D>(r, j), a);
+          mma_16816(oacc[dm], a, b0, b1);
+        }
+      }
+      // the generic zero stores above precede the stage's next TMA refill
+      if (nv < 32) fence_proxy_async_smem();
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar(L::B_EMPTY + s));
+  }
+  // ------------------------------------------ merge the two warps' states
+#pragma unroll
+  for (int o = 4; o < 32; o <<= 1) {
+    l[0] += __shfl_xor_sync(0xffffffffu, l[0], o);
+    l[1] += __shfl_xor_sync(0xffffffffu, l[1], o);
+  }
+  float* mg = reinterpret_cast<float*>(smem + L::MERGE_OFF);   // [DEC_MAX_Q][MS] O, then m, l
+  float* mm = mg + DEC_MAX_Q * L::MS;
+  const int q0 = 2 * tq, q1 = 2 * tq + 1;
+  if (warp == 1) {
+#pragma unroll
+    for (int dm = 0; dm < KS; ++dm) {
+      mg[q0 * L::MS + 16 * dm + g] = oacc[dm][0];
+      mg[q1 * L::MS + 16 * dm + g] = oacc[dm][1];
+      mg[q0 * L::MS + 16 * dm + g + 8] = oacc[dm][2];
+      mg[q1 * L::MS + 16 * dm + g + 8] = oacc[dm][3];
+    }
+    if (g == 0) {
+      mm[q0] = m[0];
+      mm[q1] = m[1];
+      mm[DEC_MAX_Q + q0] = l[0];
+      mm[DEC_MAX_Q + q1] = l[1];
     }
   }
   named_bar_sync(1, 64);
   if (warp != 0) return;
-  const bool failed = !ok || *abort_flag;
-  if (failed) return;                                      // the status word says why
-  const size_t out_q = static_cast<size_t>(bh) * nq;
+  if (!ok || *abort_flag) return;                          // the status word says why
+  // combined and normalised O^T back into the merge buffer (each position
+  // is read and written by one lane), then stored row by row
+  float lse2[2];
 #pragma unroll
-  for (int i = 0; i < NQ; ++i) {
-    if (i >= nq) break;
-    const float* r = mg + i * (D + 2);
-    const float m1 = r[D], l1 = r[D + 1];
-    const float M = fmaxf(m[i], m1);
-    float lsum = 0.f, ov[E];
-    if (M == -INFINITY) {
-#pragma unroll
-      for (int e = 0; e < E; ++e) ov[e] = 0.f;
-    } else {
-      const float a0 = ex2_approx(m[i] - M), a1 = ex2_approx(m1 - M);
-      lsum = a0 * l[i] + a1 * l1;
-      const float inv = 1.f / lsum;
-#pragma unroll
-      for (int e = 0; e < E; ++e) ov[e] = (a0 * o[i][e] + a1 * r[lane * E + e]) * inv;
+  for (int c = 0; c < 2; ++c) {
+    const int qc = 2 * tq + c;
+    const float m1 = mm[qc], l1 = mm[DEC_MAX_Q + qc];
+    const float M = fmaxf(m[c], m1);
+    float a0 = 0.f, a1 = 0.f, lsum = 0.f;
+    if (M != -INFINITY) {
+      a0 = ex2_approx(m[c] - M);
+      a1 = ex2_approx(m1 - M);
+      lsum = a0 * l[c] + a1 * l1;
     }
-    const float lse2 = M == -INFINITY ? -INFINITY : M + __log2f(lsum);   // log2 units
-    if (p.splits == 1) {
-      __nv_bfloat16* dst = p.o + (out_q + i) * D + lane * E;
-      if constexpr (E == 4) {
-        uint2 w;
-        w.x = pack_bf16x2(ov[0], ov[1]);
-        w.y = pack_bf16x2(ov[2], ov[3]);
-        *reinterpret_cast<uint2*>(dst) = w;
-      } else {
-        *reinterpret_cast<uint32_t*>(dst) = pack_bf16x2(ov[0], ov[1]);
-      }
-      if (lane == 0) p.lse[out_q + i] = lse2 * 0.69314718055994530942f;
-    } else {
-      const size_t part_row = (static_cast<size_t>(bh) * p.splits + split) * nq + i;
-      float* dst = p.o_part + part_row * D + lane * E;
+    const float iv = lsum > 0.f ? 1.f / lsum : 0.f;
+    lse2[c] = M == -INFINITY ? -INFINITY : M + __log2f(lsum);          // log2 units
+    // scale factors for this warp's and the other warp's parts
+    m[c] = a0 * iv;
+    l[c] = a1 * iv;
+  }
 #pragma unroll
-      for (int e = 0; e < E; ++e) dst[e] = ov[e];
-      if (lane == 0) p.lse_part[part_row] = lse2;
+  for (int dm = 0; dm < KS; ++dm) {
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int qc = 2 * tq + (e & 1);
+      float* x = mg + qc * L::MS + 16 * dm + g + 8 * (e >> 1);
+      *x = oacc[dm][e] * m[e & 1] + *x * l[e & 1];
+    }
+  }
+  __syncwarp();
+  const size_t out_q = static_cast<size_t>(bh) * nq;
+  if (g == 0) {
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+      const int qc = 2 * tq + c;
+      if (qc < nq) {
+        if (p.splits == 1) {
+          p.lse[out_q + qc] = lse2[c] * 0.69314718055994530942f;
+        } else {
+          p.lse_part[(static_cast<size_t>(bh) * p.splits + split) * nq + qc] = lse2[c];
+        }
+      }
+    }
+  }
+  // rows of O: lane x covers 4 consecutive columns
+  for (int x = static_cast<int>(lane); x < nq * (D / 4); x += 32) {
+    const int qc = x / (D / 4), c4 = (x % (D / 4)) * 4;
+    const float4 v = *reinterpret_cast<const float4*>(mg + qc * L::MS + c4);
+    if (p.splits == 1) {
+      uint2 w;
+      w.x = pack_bf16x2(v.x, v.y);
+      w.y = pack_bf16x2(v.z, v.w);
+      *reinterpret_cast<uint2*>(p.o + (out_q + qc) * D + c4) = w;
+    } else {
+      const size_t part_row = (static_cast<size_t>(bh) * p.splits + split) * nq + qc;
+      *reinterpret_cast<float4*>(p.o_part + part_row * D + c4) = v;
     }
   }
 }
@@ -482,14 +390,8 @@ __global__ void __launch_bounds__(128) fa_decode_combine_kernel(const __grid_con
   if (lane == 0) p.lse[row] = W > 0.f ? (M + __log2f(W)) * 0.69314718055994530942f : -INFINITY;
 }
 
-template <int D, int NQ>
-int launch_decode_t(const DecParams& p, cudaStream_t stream) {
-  using L = DecLayout<D, NQ>;
-  static SmemAttrOnce attr;
-  if (!attr.ensure(reinterpret_cast<const void*>(fa_decode_kernel<D, NQ>), L::SMEM_BYTES)) return -4;
-  const unsigned grid = static_cast<unsigned>(p.BH) * static_cast<unsigned>(p.splits);
-  fa_decode_kernel<D, NQ><<<grid, L::THREADS, L::SMEM_BYTES, stream>>>(p);
-  if (cudaGetLastError() != cudaSuccess) return -4;
+template <int D>
+int launch_decode_combine(const DecParams& p, cudaStream_t stream) {
   if (p.splits > 1) {
     const long long rows = static_cast<long long>(p.BH) * p.Nq;
     fa_decode_combine_kernel<D><<<static_cast<unsigned>((rows + 3) / 4), 128, 0, stream>>>(p);
@@ -500,10 +402,13 @@ int launch_decode_t(const DecParams& p, cudaStream_t stream) {
 
 template <int D>
 int launch_decode_d(const DecParams& p, cudaStream_t stream) {
-  if (p.Nq <= 1) return launch_decode_t<D, 1>(p, stream);
-  if (p.Nq <= 2) return launch_decode_t<D, 2>(p, stream);
-  if (p.Nq <= 4) return launch_decode_t<D, 4>(p, stream);
-  return launch_decode_t<D, 8>(p, stream);
+  using L = DecLayout<D>;
+  static SmemAttrOnce attr;
+  if (!attr.ensure(reinterpret_cast<const void*>(fa_decode_kernel<D>), L::SMEM_BYTES)) return -4;
+  const unsigned grid = static_cast<unsigned>(p.BH) * static_cast<unsigned>(p.splits);
+  fa_decode_kernel<D><<<grid, L::THREADS, L::SMEM_BYTES, stream>>>(p);
+  if (cudaGetLastError() != cudaSuccess) return -4;
+  return launch_decode_combine<D>(p, stream);
 }
 
 int launch_decode(const DecParams& p, int d, cudaStream_t stream) {

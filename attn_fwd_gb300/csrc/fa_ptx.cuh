@@ -233,6 +233,42 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
 }
 
 // ------------------------------------------------------------------------- //
+// warp-level MMA (m16n8k16, bf16 operands, fp32 accumulators) and the
+// shared-memory fragment loads it takes: for products too small for tcgen05
+// (a handful of query tokens against a cache tile)
+// ------------------------------------------------------------------------- //
+// Four 8 x 8 b16 matrices; lanes 8i..8i+7 give the row addresses of matrix i,
+// and register i of a lane receives row lane / 4, columns 2 (lane % 4) + {0, 1}.
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr)
+               : "memory");
+}
+// The same with each matrix transposed: register i receives column lane / 4,
+// rows 2 (lane % 4) + {0, 1}.
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr)
+               : "memory");
+}
+// Transpose of an 8 x 8 b16 matrix held one row pair per lane.
+__device__ __forceinline__ uint32_t movm_t(uint32_t x) {
+  uint32_t y;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
+}
+// c += a b for a 16 x 16 row-major A, a 16 x 8 column-major B.
+__device__ __forceinline__ void mma_16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// ------------------------------------------------------------------------- //
 // tcgen05: tensor memory, MMA, commit
 // ------------------------------------------------------------------------- //
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {

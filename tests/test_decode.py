@@ -52,6 +52,12 @@ CASES = [
     (2, 2, 5, 3000, 128, [2999, 65], False),
     (1, 8, 2, 65536, 128, None, False),        # hundreds of chunks
     (2, 16, 1, 32768, 128, [32768, 20001], True),
+    # several tokens, two keys per lane: one tile (the second warp idle),
+    # partial last tiles with both key groups, odd tile counts
+    (1, 3, 4, 50, 128, None, True),
+    (2, 2, 8, 200, 64, [200, 97], True),
+    (1, 4, 6, 4133, 128, None, False),
+    (2, 2, 7, 64, 128, [64, 33], True),
 ]
 
 
