@@ -716,3 +716,164 @@ extern "C" int fa_bwd_noalloc(const void* q, const void* k, const void* v, const
   return bwd_impl(q, k, v, o, dout, lse, nullptr, dq, dk, dv, ws, B, H, N, d, scale,
                   causal ? fa::MASK_CAUSAL : fa::MASK_NONE, 0.f, 0, stream);
 }
+
+// --------------------------------------------------------------------------
+// fa_fwd_bwd_host: forward and backward of tensors in (pinned) host memory,
+// streamed through the device in chunks of heads.  Three library-owned
+// streams per device overlap the copies in of chunk c + 1, the kernels of
+// chunk c and the copies out of chunk c - 1 (the link carries both
+// directions at once); two device buffer sets alternate between chunks.
+// --------------------------------------------------------------------------
+namespace {
+
+// Heads per chunk: enough key tiles for two waves of the backward on 152
+// SMs (a chunk's kernels then run near full speed), at most 8 chunks, and
+// the heads spread evenly over the chunks.  (Measured on B2 H16 N4096 d128:
+// chunks of 8 heads beat chunks of 16, whose longer first copy and last copy
+// back are not overlapped, and chunks of 4, whose kernels run half empty.)
+long long host_chunk_heads(int B, int H, int N) {
+  const long long bh = static_cast<long long>(B) * H;
+  const long long waves = (2 * kPlanSMs + tiles(N) - 1) / tiles(N);
+  long long g = waves > (bh + 7) / 8 ? waves : (bh + 7) / 8;
+  if (g > bh) g = bh;
+  const long long chunks = (bh + g - 1) / g;
+  return (bh + chunks - 1) / chunks;
+}
+
+// One buffer set: q, k, v, dO, O, dQ, dK, dV [G][N][d] bf16, LSE [G][N]
+// fp32, then the backward workspace of G heads.
+struct HostSet {
+  char* t[8];
+  float* lse;
+  void* ws;
+};
+
+size_t host_set_bytes(long long G, int N, int d) {
+  const size_t t = align256(static_cast<size_t>(G) * N * d * 2);
+  return 8 * t + align256(static_cast<size_t>(G) * N * sizeof(float)) +
+         align256(workspace_bytes(1, static_cast<int>(G), N, d));
+}
+
+HostSet host_carve(char* base, long long G, int N, int d) {
+  const size_t t = align256(static_cast<size_t>(G) * N * d * 2);
+  HostSet s;
+  for (int i = 0; i < 8; ++i) s.t[i] = base + i * t;
+  s.lse = reinterpret_cast<float*>(base + 8 * t);
+  s.ws = base + 8 * t + align256(static_cast<size_t>(G) * N * sizeof(float));
+  return s;
+}
+
+struct HostStreams {
+  std::once_flag once;
+  std::mutex mu;                // one caller enqueues at a time on a device
+  cudaStream_t in = nullptr, cmp = nullptr, out = nullptr;
+  cudaEvent_t start = nullptr, in_done[2] = {}, cmp_done[2] = {}, out_done[2] = {};
+  cudaError_t err = cudaSuccess;
+};
+HostStreams g_host[kMaxDevices];
+
+int host_streams(HostStreams** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FA_ERR_CUDA;
+  HostStreams& h = g_host[dev];
+  std::call_once(h.once, [&] {
+    cudaError_t e = cudaSuccess;
+    for (cudaStream_t* s : {&h.in, &h.cmp, &h.out})
+      if (e == cudaSuccess) e = cudaStreamCreateWithFlags(s, cudaStreamNonBlocking);
+    for (cudaEvent_t* ev : {&h.start, &h.in_done[0], &h.in_done[1], &h.cmp_done[0], &h.cmp_done[1],
+                            &h.out_done[0], &h.out_done[1]})
+      if (e == cudaSuccess) e = cudaEventCreateWithFlags(ev, cudaEventDisableTiming);
+    h.err = e;
+  });
+  if (h.err != cudaSuccess) return FA_ERR_CUDA;
+  *out = &h;
+  return FA_OK;
+}
+
+}  // namespace
+
+extern "C" size_t fa_fwd_bwd_host_workspace_bytes(int B, int H, int N, int d) {
+  if (check_shape(B, H, N, d) != FA_OK) return 0;
+  return 2 * host_set_bytes(host_chunk_heads(B, H, N), N, d);
+}
+
+extern "C" int fa_fwd_bwd_host(const void* q, const void* k, const void* v, const void* dout, void* o, float* lse,
+                               void* dq, void* dk, void* dv, const uint8_t* block_mask, void* workspace,
+                               size_t workspace_size, int B, int H, int N, int d, float scale, int causal,
+                               fa_stream_t stream) {
+  int rc;
+  for (const void* ptr : {q, k, v, dout, static_cast<const void*>(o), static_cast<const void*>(lse),
+                          static_cast<const void*>(dq), static_cast<const void*>(dk), static_cast<const void*>(dv),
+                          static_cast<const void*>(workspace)})
+    if (ptr == nullptr) return FA_ERR_INVALID;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return FA_ERR_INVALID;
+  if ((rc = check_shape(B, H, N, d)) != FA_OK) return rc;
+  if ((rc = check_scale(scale)) != FA_OK) return rc;
+  const int mask_kind = (block_mask ? fa::MASK_BLOCK : 0) | (causal ? fa::MASK_CAUSAL : 0);
+  if ((mask_kind & fa::MASK_BLOCK) && tiles(N) > fa::MAX_SPARSE_TILES) return FA_ERR_UNSUPPORTED;
+  if (workspace_size < fa_fwd_bwd_host_workspace_bytes(B, H, N, d)) return FA_ERR_INVALID;
+  int* status = nullptr;
+  if ((rc = device_ready(&status)) != FA_OK) return rc;
+  HostStreams* hs = nullptr;
+  if ((rc = host_streams(&hs)) != FA_OK) return rc;
+  std::lock_guard<std::mutex> lk(hs->mu);
+  const cudaStream_t caller = reinterpret_cast<cudaStream_t>(stream);
+  const long long BH = static_cast<long long>(B) * H;
+  const long long G = host_chunk_heads(B, H, N);
+  const size_t set_bytes = host_set_bytes(G, N, d);
+  const size_t head_elems = static_cast<size_t>(N) * d;
+  auto cu = [](cudaError_t e) { return e == cudaSuccess ? FA_OK : FA_ERR_CUDA; };
+  // everything starts after the work already queued on the caller's stream
+  if ((rc = cu(cudaEventRecord(hs->start, caller))) != FA_OK) return rc;
+  for (cudaStream_t s : {hs->in, hs->cmp, hs->out})
+    if ((rc = cu(cudaStreamWaitEvent(s, hs->start, 0))) != FA_OK) return rc;
+  const void* hin[4] = {q, k, v, dout};
+  void* hout[4] = {o, dq, dk, dv};
+  // chunks of G heads, except a first chunk of G / 2 when there are several
+  // (the pipeline fills and drains faster); the last takes the rest
+  long long c = 0;
+  for (long long h0 = 0; h0 < BH; ++c) {
+    const int b = static_cast<int>(c & 1);
+    long long gc = (c == 0 && BH > G) ? (G + 1) / 2 : G;
+    if (gc > BH - h0) gc = BH - h0;
+    const int g = static_cast<int>(gc);
+    const HostSet s = host_carve(static_cast<char*>(workspace) + b * set_bytes, G, N, d);
+    const size_t bytes = static_cast<size_t>(g) * head_elems * 2;
+    const size_t off = static_cast<size_t>(h0) * head_elems * 2;
+    // copies in, once the kernels of chunk c - 2 are done with this set's
+    // inputs (its outputs may still be on their way out)
+    if (c >= 2 && (rc = cu(cudaStreamWaitEvent(hs->in, hs->cmp_done[b], 0))) != FA_OK) return rc;
+    for (int i = 0; i < 4; ++i)
+      if ((rc = cu(cudaMemcpyAsync(s.t[i], static_cast<const char*>(hin[i]) + off, bytes, cudaMemcpyHostToDevice,
+                                   hs->in))) != FA_OK)
+        return rc;
+    if ((rc = cu(cudaEventRecord(hs->in_done[b], hs->in))) != FA_OK) return rc;
+    // kernels: forward (O, LSE), then the three backward stages, once the
+    // inputs are in and chunk c - 2's outputs have left this set
+    if ((rc = cu(cudaStreamWaitEvent(hs->cmp, hs->in_done[b], 0))) != FA_OK) return rc;
+    if (c >= 2 && (rc = cu(cudaStreamWaitEvent(hs->cmp, hs->out_done[b], 0))) != FA_OK) return rc;
+    const fa_stream_t cs = reinterpret_cast<fa_stream_t>(hs->cmp);
+    if ((rc = fwd_impl(s.t[0], s.t[1], s.t[2], s.t[4], s.lse, block_mask, 1, g, N, d, scale, mask_kind, 0.f, 0,
+                       cs)) != FA_OK)
+      return rc;
+    if ((rc = bwd_impl(s.t[0], s.t[1], s.t[2], s.t[4], s.t[3], s.lse, block_mask, s.t[5], s.t[6], s.t[7], s.ws, 1,
+                       g, N, d, scale, mask_kind, 0.f, 0, cs)) != FA_OK)
+      return rc;
+    if ((rc = cu(cudaEventRecord(hs->cmp_done[b], hs->cmp))) != FA_OK) return rc;
+    // copies out
+    if ((rc = cu(cudaStreamWaitEvent(hs->out, hs->cmp_done[b], 0))) != FA_OK) return rc;
+    const char* dsrc[4] = {s.t[4], s.t[5], s.t[6], s.t[7]};
+    for (int i = 0; i < 4; ++i)
+      if ((rc = cu(cudaMemcpyAsync(static_cast<char*>(hout[i]) + off, dsrc[i], bytes, cudaMemcpyDeviceToHost,
+                                   hs->out))) != FA_OK)
+        return rc;
+    if ((rc = cu(cudaMemcpyAsync(lse + h0 * N, s.lse, static_cast<size_t>(g) * N * sizeof(float),
+                                 cudaMemcpyDeviceToHost, hs->out))) != FA_OK)
+      return rc;
+    if ((rc = cu(cudaEventRecord(hs->out_done[b], hs->out))) != FA_OK) return rc;
+    h0 += gc;
+  }
+  // the caller's stream continues once the last copies out are done (the
+  // out stream runs the chunks in order)
+  return cu(cudaStreamWaitEvent(caller, hs->out_done[(c - 1) & 1], 0));
+}

@@ -54,6 +54,8 @@ _SIGS = {
     "fa_get_device_error": (_i, [_vp]),
     "fa_set_wait_timeout_ns": (_i, [_u64]),
     "fa_debug_wait_timeout": (_i, [_u64, _vp]),
+    "fa_fwd_bwd_host_workspace_bytes": (_sz, [_i, _i, _i, _i]),
+    "fa_fwd_bwd_host": (_i, [_vp] * 11 + [_sz, _i, _i, _i, _i, _f, _i, _vp]),
 }
 
 
@@ -221,6 +223,29 @@ def fa_bwd_noalloc(q, k, v, o, do, lse, dq, dk, dv, scale, causal=False, stream=
     _check("fa_bwd_noalloc", rc)
 
 
+def _host(t: torch.Tensor, name: str, dtype=torch.bfloat16, dim=4):
+    if t.is_cuda or t.dtype != dtype or not t.is_contiguous() or t.dim() != dim:
+        raise ValueError(f"{name} must be a contiguous {dtype} host tensor with {dim} dimensions")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def fa_fwd_bwd_host_workspace_bytes(B, H, N, d) -> int:
+    return load().fa_fwd_bwd_host_workspace_bytes(B, H, N, d)
+
+
+def fa_fwd_bwd_host(q, k, v, do, o, lse, dq, dk, dv, block_mask, workspace, scale, causal=False, stream=None):
+    """Forward and backward of host tensors (pinned for overlap), streamed
+    through the device in chunks of heads; see include/fa.h."""
+    B, H, N, d = q.shape
+    if not (workspace.is_cuda and workspace.dtype == torch.uint8):
+        raise ValueError("workspace must be a uint8 CUDA tensor")
+    rc = load().fa_fwd_bwd_host(_host(q, "q"), _host(k, "k"), _host(v, "v"), _host(do, "do"), _host(o, "o"),
+                                _host(lse, "lse", torch.float32, 3), _host(dq, "dq"), _host(dk, "dk"),
+                                _host(dv, "dv"), _mask_ptr(block_mask), ctypes.c_void_p(workspace.data_ptr()),
+                                workspace.numel(), B, H, N, d, float(scale), int(bool(causal)), _stream(stream))
+    _check("fa_fwd_bwd_host", rc)
+
+
 def fa_decode_workspace_bytes(B, H, Nq, Nk, d) -> int:
     return load().fa_decode_workspace_bytes(B, H, Nq, Nk, d)
 
@@ -365,6 +390,20 @@ def backward(q, k, v, o, lse, do, causal=False, scale=None, block_mask=None, ws=
     else:
         fa_bwd(q, k, v, o, do, lse, dq, dk, dv, ws, scale, causal, stream)
     return dq, dk, dv
+
+
+def forward_backward_host(q, k, v, do, causal=False, scale=None, block_mask=None, ws=None, stream=None):
+    """Forward and backward of host tensors; returns pinned host (O, LSE, dQ,
+    dK, dV).  ``ws``: a device workspace of fa_fwd_bwd_host_workspace_bytes
+    bytes (allocated when omitted)."""
+    B, H, N, d = q.shape
+    scale = (1.0 / d ** 0.5) if scale is None else scale
+    o, dq, dk, dv = (torch.empty(q.shape, dtype=q.dtype).pin_memory() for _ in range(4))
+    lse = torch.empty((B, H, N), dtype=torch.float32).pin_memory()
+    if ws is None:
+        ws = torch.empty(fa_fwd_bwd_host_workspace_bytes(B, H, N, d), dtype=torch.uint8, device="cuda")
+    fa_fwd_bwd_host(q, k, v, do, o, lse, dq, dk, dv, block_mask, ws, scale, causal, stream)
+    return o, lse, dq, dk, dv
 
 
 def fa_status_string(code: int) -> str:

@@ -745,17 +745,32 @@ def run_cuda(args):
     if w.backward:
         dev_out.update({"dq": dq, "dk": dk, "dv": dv})
     e2e_steps = max(3, min(args.steps, 20))
+    # forward + backward without dropout: the library's host-streamed entry
+    # point (copies in, kernels and copies out of successive chunks of heads
+    # overlap); otherwise pinned copies around the device-resident step
+    streamed = w.backward and not w.dropout_p
+    if streamed:
+        hws = torch.empty(fa.fa_fwd_bwd_host_workspace_bytes(w.B, w.H, w.N, w.d), dtype=torch.uint8, device=dev)
+
+        def e2e_step():
+            fa.fa_fwd_bwd_host(host_in["q"], host_in["k"], host_in["v"], host_in["do"], host_out["o"],
+                               host_out["lse"], host_out["dq"], host_out["dk"], host_out["dv"], bm, hws, w.scale,
+                               w.causal)
+    else:
+        def e2e_step():
+            for n, x in host_in.items():
+                dev_in[n].copy_(x, non_blocking=True)
+            step()
+            for n, x in dev_out.items():
+                host_out[n].copy_(x, non_blocking=True)
+    e2e_step()                                  # warm-up (streams, tensor maps)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if ws > 1:
         dist.barrier()
     torch.cuda.synchronize()
     e0.record()
     for _ in range(e2e_steps):
-        for n, x in host_in.items():
-            dev_in[n].copy_(x, non_blocking=True)
-        step()
-        for n, x in dev_out.items():
-            host_out[n].copy_(x, non_blocking=True)
+        e2e_step()
     e1.record()
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, dev)
@@ -790,7 +805,9 @@ def run_cuda(args):
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": _config(w, density),
             "frac_of_peak": value / ws / peak,
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                    "ms_per_step": e2e_ms},
+                    "ms_per_step": e2e_ms,
+                    "call": ("fa_fwd_bwd_host: chunks of heads, copies overlapped with the kernels" if streamed
+                             else "pinned copies in, device-resident step, copies out")},
             "gpu_launches": launches_per_step * args.steps, "roofline": roofline, "kernels": kernels,
             "clocks": clocks}
 

@@ -292,6 +292,45 @@ FA_API int fa_bwd_noalloc(const void *q, const void *k, const void *v, const voi
                           int B, int H, int N, int d, float scale, int causal, fa_stream_t stream);
 
 /*
+ * Forward and backward of tensors that live in host memory: the call a
+ * training step makes when its Q, K, V and dO arrive from the host and
+ * O, LSE, dQ, dK and dV go back.  The same computation as fa_fwd followed by
+ * fa_bwd (fa_fwd_blocksparse / fa_bwd_blocksparse when block_mask is given),
+ * done in chunks of whole heads: the copies into the device of chunk c + 1,
+ * the kernels of chunk c and the copies back of chunk c - 1 run at the same
+ * time on three streams that the library owns (one set per device), through
+ * two device buffer sets in `workspace`.  (A data-movement entry point for
+ * callers; the attention pages do not describe it.)
+ *
+ *   q, k, v, dout   : bf16 [B, H, N, d] in host memory
+ *   o, dq, dk, dv   : bf16 [B, H, N, d] in host memory, written
+ *   lse             : fp32 [B, H, N] in host memory, written
+ *   block_mask      : NULL, or device uint8 [N/128][N/128] as for
+ *                     fa_fwd_blocksparse (combined with `causal`)
+ *   workspace       : device memory, 256-byte aligned, of at least
+ *                     fa_fwd_bwd_host_workspace_bytes(B, H, N, d) bytes
+ *   workspace_size  : its size in bytes
+ * Host buffers should be page-locked (cudaHostAlloc / pinned): the copies
+ * then run asynchronously at full link speed.  Pageable buffers work, but
+ * the copies stage through the driver and do not overlap.
+ *
+ * Ordering: the work starts after everything already queued on `stream` and
+ * `stream` waits for its end (the last copy back), so a synchronisation of
+ * `stream` makes the host outputs readable.  The host inputs must stay
+ * unchanged, and the outputs unread, until then.  Calls from several host
+ * threads on one device are serialised while they enqueue; the workspace of
+ * a call must not be in use by other work.
+ * Returns FA_ERR_INVALID for a null pointer, an unaligned or too small
+ * workspace, bad sizes or scale; FA_ERR_UNSUPPORTED as fa_fwd; FA_ERR_CUDA
+ * when a stream, event or copy call fails.  Dropout is not offered here.
+ */
+FA_API size_t fa_fwd_bwd_host_workspace_bytes(int B, int H, int N, int d);
+FA_API int fa_fwd_bwd_host(const void *q, const void *k, const void *v, const void *dout, void *o,
+                           float *lse, void *dq, void *dk, void *dv, const uint8_t *block_mask,
+                           void *workspace, size_t workspace_size, int B, int H, int N, int d,
+                           float scale, int causal, fa_stream_t stream);
+
+/*
  * Synchronises `stream`, then returns and clears the current device's status
  * word: FA_OK, or FA_ERR_TIMEOUT when a kernel wait gave up.  Returns
  * FA_ERR_CUDA when the synchronisation itself fails.

@@ -105,6 +105,39 @@ def test_bwd_rejects_bad_arguments(lib):
     assert lib.fa_bwd_dq_convert(P, P, 1, 1, 128, 64, 0.0, NULL) == -1
 
 
+def test_host_streamed_entry_checks(lib):
+    """fa_fwd_bwd_host: workspace sizing and argument checks on the host."""
+    import attn_fwd_gb300.fa as fa
+    # two buffer sets of G heads: 8 bf16 tensors, LSE and the backward workspace
+    # each; G covers two backward waves (2 * 152 / key tiles), at most 8
+    # chunks, heads spread evenly: 4 chunks of 8 here
+    B, H, N, d = 2, 16, 4096, 128
+    G = 8
+    per_set = 8 * G * N * d * 2 + G * N * 4 + fa.fa_bwd_workspace_bytes(1, G, N, d)
+    assert fa.fa_fwd_bwd_host_workspace_bytes(B, H, N, d) == 2 * per_set
+    assert fa.fa_fwd_bwd_host_workspace_bytes(1, 1, 128, 64) == 2 * (8 * 128 * 64 * 2 + 512 +
+                                                                      fa.fa_bwd_workspace_bytes(1, 1, 128, 64))
+    assert fa.fa_fwd_bwd_host_workspace_bytes(0, 1, 128, 64) == 0
+    assert fa.fa_fwd_bwd_host_workspace_bytes(1, 1, 128, 96) == 0
+    ws = ctypes.c_void_p(4096)
+    big = 1 << 40
+    args = [P] * 9 + [NULL, ws, big, 1, 1, 128, 64, 0.125, 1, NULL]
+    for i in range(9):                                  # each host buffer is required
+        a = list(args)
+        a[i] = NULL
+        assert lib.fa_fwd_bwd_host(*a) == -1
+    a = list(args); a[10] = NULL
+    assert lib.fa_fwd_bwd_host(*a) == -1                # no workspace
+    a = list(args); a[10] = ctypes.c_void_p(4096 + 16)
+    assert lib.fa_fwd_bwd_host(*a) == -1                # workspace not 256-byte aligned
+    a = list(args); a[11] = 1024
+    assert lib.fa_fwd_bwd_host(*a) == -1                # workspace too small
+    a = list(args); a[15] = 96
+    assert lib.fa_fwd_bwd_host(*a) == -2                # head dim not built
+    a = list(args); a[16] = 0.0
+    assert lib.fa_fwd_bwd_host(*a) == -1                # scale
+
+
 def test_timeout_setter(lib):
     assert lib.fa_set_wait_timeout_ns(0) == -1
     assert lib.fa_set_wait_timeout_ns(2_000_000_000) == 0
