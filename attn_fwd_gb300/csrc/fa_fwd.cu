@@ -107,6 +107,104 @@ __device__ __forceinline__ int next_visible(const uint32_t* bits, int from, int 
   return wd * 32 + __ffs(m) - 1;
 }
 
+// Key tiles of a CTA's two query tiles by class: mode 0 those only tile 0
+// visits (x and not y), mode 1 only tile 1 (y and not x), mode 2 both; the
+// first one at or after `from`, or -1.
+__device__ __forceinline__ int next_in_class(const uint32_t* x, const uint32_t* y, int mode, int from, int n_kt) {
+  if (from >= n_kt) return -1;
+  auto word = [&](int wd) {
+    const uint32_t a = x[wd], b = y[wd];
+    return mode == 0 ? (a & ~b) : (mode == 1 ? (b & ~a) : (a & b));
+  };
+  int wd = from >> 5;
+  uint32_t m = word(wd) & (0xffffffffu << (from & 31));
+  const int nw = (n_kt + 31) >> 5;
+  while (m == 0) {
+    if (++wd >= nw) return -1;
+    m = word(wd);
+  }
+  return wd * 32 + __ffs(m) - 1;
+}
+
+// Round schedule of a block-sparse CTA.  When the two query tiles share at
+// least as many key tiles as either visits alone (sliding windows: all but
+// one), the rounds take first the tiles only one query tile visits, tile 0's
+// r-th paired with tile 1's r-th (rounds 0 .. split-1), then the shared tiles
+// in increasing order, where one K and one V load serve both.  Otherwise
+// (scattered masks, where reordering only loses L2 locality) round r pairs
+// the r-th visible tile of each, in increasing order.  Every role walks the
+// same schedule.
+struct SparsePlan {
+  int na, nb, nc;        // tiles only tile 0 / only tile 1 / both visit
+  bool shared_first;
+};
+
+__device__ __forceinline__ SparsePlan sparse_plan(const uint32_t* x, const uint32_t* y, int n_kt) {
+  SparsePlan pl{0, 0, 0, false};
+  for (int wd = 0; wd < (n_kt + 31) / 32; ++wd) {
+    pl.na += __popc(x[wd] & ~y[wd]);
+    pl.nb += __popc(y[wd] & ~x[wd]);
+    pl.nc += __popc(x[wd] & y[wd]);
+  }
+  pl.shared_first = pl.nc >= (pl.na > pl.nb ? pl.na : pl.nb);
+  return pl;
+}
+
+struct SparseRounds {
+  const uint32_t* x;
+  const uint32_t* y;
+  int n_kt, split, ca, cb, cc;
+  bool shared_first;
+  __device__ __forceinline__ SparseRounds(const uint32_t* x_, const uint32_t* y_, int n) : x(x_), y(y_), n_kt(n) {
+    const SparsePlan pl = sparse_plan(x, y, n);
+    shared_first = pl.shared_first;
+    split = pl.na > pl.nb ? pl.na : pl.nb;
+    ca = cb = cc = 0;
+  }
+  // the key tiles (a for query tile 0, b for tile 1; -1 for none) of round r,
+  // called once per round in increasing r
+  __device__ __forceinline__ void next(int r, int& a, int& b) {
+    if (!shared_first) {
+      a = next_visible(x, ca, n_kt);
+      b = next_visible(y, cb, n_kt);
+      if (a >= 0) ca = a + 1;
+      if (b >= 0) cb = b + 1;
+    } else if (r < split) {
+      a = next_in_class(x, y, 0, ca, n_kt);
+      b = next_in_class(x, y, 1, cb, n_kt);
+      if (a >= 0) ca = a + 1;
+      if (b >= 0) cb = b + 1;
+    } else {
+      a = b = next_in_class(x, y, 2, cc, n_kt);
+      if (a >= 0) cc = a + 1;
+    }
+  }
+};
+
+// Query tile w's key tiles in the order of SparseRounds (for dropout, which
+// needs each round's tile index): class w, then class 2 when shared-first;
+// mode 3 (all of tile w's tiles, increasing) otherwise.  x, y: the bits of
+// query tiles 0 and 1.
+struct SparseTileSeq {
+  int mode, cur;
+  __device__ __forceinline__ int next(const uint32_t* x, const uint32_t* y, int w, int n_kt) {
+    if (mode == 3) {
+      const int kt = next_visible(w ? y : x, cur, n_kt);
+      cur = kt + 1;
+      return kt;
+    }
+    for (;;) {
+      const int kt = next_in_class(x, y, mode, cur, n_kt);
+      if (kt >= 0 || mode == 2) {
+        cur = kt + 1;
+        return kt;
+      }
+      mode = 2;
+      cur = 0;
+    }
+  }
+};
+
 // The last visible key tile, or -1.
 __device__ __forceinline__ int last_visible(const uint32_t* bits, int n_kt) {
   for (int wd = (n_kt + 31) / 32 - 1; wd >= 0; --wd)
@@ -192,10 +290,10 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
   const uint32_t* bits0 = bits;
   const uint32_t* bits1 = bits + L::BITS_WORDS;
   const int rounds = nv0 > nv1 ? nv0 : nv1;
-  // Round r pairs tile 0's r-th key tile a_r with tile 1's r-th key tile b_r
-  // (-1 when a tile has no more).  The producer loads, per round, K(a) K(b)
-  // V(a) V(b) into consecutive ring slots, once when a_r == b_r; the MMA
-  // issuer walks the same sequence.
+  // Block-sparse: round r pairs key tile a_r of query tile 0 with b_r of tile
+  // 1 (-1 when a tile has none), in the order of SparseRounds.  The producer
+  // loads, per round, K(a) K(b) V(a) V(b) into consecutive ring slots, once
+  // when a_r == b_r; the MMA issuer walks the same sequence.
 
   if (warp == 9) {
     // ------------------------------------------------------------ producer
@@ -249,12 +347,11 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
       // STAGES slots keeps STAGES - 1 tiles in flight ahead: per round r,
       // V(a_{r-1}), K(a_r), V(b_{r-1}), K(b_r) -- a tile both query tiles
       // use is loaded once -- and after the last round the last V tiles.
-      int cur0 = next_visible(bits0, 0, p.n_qt), cur1 = next_visible(bits1, 0, p.n_qt);
+      SparseRounds sched(bits0, bits1, p.n_qt);
       int pa = -1, pb = -1;                 // previous round's key tiles
       for (int r = 0; r <= rounds && ok; ++r) {
-        const int a = r < rounds ? cur0 : -1, b = r < rounds ? cur1 : -1;
-        if (a >= 0) cur0 = next_visible(bits0, a + 1, p.n_qt);
-        if (b >= 0) cur1 = next_visible(bits1, b + 1, p.n_qt);
+        int a = -1, b = -1;
+        if (r < rounds) sched.next(r, a, b);
         if (pa >= 0) ok = load(&p.tm_v, pa);
         if (ok && a >= 0) ok = load(&p.tm_k, a);
         if (ok && pb >= 0 && pb != pa) ok = load(&p.tm_v, pb);
@@ -391,12 +488,11 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
     int cnt = 0;                       // tiles taken so far, in load order
     uint32_t pph0 = 0, pph1 = 0;       // phases of the P barriers
     int done0 = 0, done1 = 0;          // PV products issued per tile
-    int cur0 = next_visible(bits0, 0, p.n_qt), cur1 = next_visible(bits1, 0, p.n_qt);
+    SparseRounds sched(bits0, bits1, p.n_qt);
     int pa = -1, pb = -1;              // previous round's key tiles
     for (int r = 0; r <= rounds && ok; ++r) {
-      const int a = r < rounds ? cur0 : -1, b = r < rounds ? cur1 : -1;
-      if (a >= 0) cur0 = next_visible(bits0, a + 1, p.n_qt);
-      if (b >= 0) cur1 = next_visible(bits1, b + 1, p.n_qt);
+      int a = -1, b = -1;
+      if (r < rounds) sched.next(r, a, b);
       const bool vshared = pb >= 0 && pb == pa;   // tile 1 reuses tile 0's V of the previous round
       const bool kshared = b >= 0 && b == a;      // and its K of this round
       const int nva = pa >= 0 ? cnt++ : -1;
@@ -462,26 +558,39 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
       bool ok = true;
       uint32_t sphase = 0;
       const int n_vis = w ? nv1 : nv0;
-      // Only the last visited key tile can need a per-element mask: the causal
-      // diagonal and the ragged tile holding key N-1 are each the highest
-      // visible tile index.  Keys at or past last_lim (a column in that tile)
-      // are masked to -inf.
+      // Only the highest visible key tile can need a per-element mask: the
+      // causal diagonal and the ragged tile holding key N-1.  Keys at or past
+      // last_lim (a column in that tile) are masked to -inf.  Dense: the
+      // tiles come in increasing order, so that is the last round; sparse:
+      // the round whose tile is last_kt (SparseRounds' order).
       const int last_kt = SPARSE ? last_visible(w ? bits1 : bits0, p.n_qt) : n_vis - 1;
       int last_lim = p.N - last_kt * TILE;
       if ((p.mask_kind & MASK_CAUSAL) && last_kt == qt) last_lim = min(last_lim, row + 1);
-      // dropout: key tile of this round (only tracked when needed) and the
-      // keep bits of this row's 128 columns, made before S is waited for
-      int kt_d = DROP ? (SPARSE ? next_visible(w ? bits1 : bits0, 0, p.n_qt) : 0) : 0;
+      // the round (of this tile's own) that holds last_kt: the last one, or,
+      // shared-first, the last of its own tiles when the other tile does not
+      // visit last_kt
+      int mask_rr = n_vis - 1;
+      const uint32_t* other = w ? bits0 : bits1;
+      SparseTileSeq seq{3, 0};
+      if constexpr (SPARSE) {
+        const SparsePlan pl = sparse_plan(bits0, bits1, p.n_qt);
+        if (pl.shared_first) {
+          seq.mode = w;
+          if (last_kt >= 0 && !((other[last_kt >> 5] >> (last_kt & 31)) & 1u)) mask_rr = (w ? pl.nb : pl.na) - 1;
+        }
+      }
       const uint32_t bh_u = static_cast<uint32_t>(bh);
       const uint32_t hd = bh_u % static_cast<uint32_t>(p.H), bd = bh_u / static_cast<uint32_t>(p.H);
       for (int rr = 0; rr < n_vis; ++rr) {
         uint32_t dbits[4];
         if constexpr (DROP) {
+          // keep bits of this row's 128 columns for this round's key tile,
+          // made before S is waited for
+          const int kt = SPARSE ? seq.next(bits0, bits1, w, p.n_qt) : rr;
 #pragma unroll
           for (int q = 0; q < 4; ++q)
-            dbits[q] = keep_bits_row(qt * TILE + row, kt_d * TILE + 32 * q, hd, bd, p.drop.seed_lo, p.drop.seed_hi,
+            dbits[q] = keep_bits_row(qt * TILE + row, kt * TILE + 32 * q, hd, bd, p.drop.seed_lo, p.drop.seed_hi,
                                      p.drop.add, lane & 3u);
-          kt_d = SPARSE ? next_visible(w ? bits1 : bits0, kt_d + 1, p.n_qt) : kt_d + 1;
         }
         if (!mbar_wait_warp(bar(L::B_S + w), sphase, wc)) { ok = false; break; }
         sphase ^= 1u;
@@ -489,7 +598,7 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
         uint32_t r[128];
         tmem_ld_x128(s_addr, r);
         float* s = reinterpret_cast<float*>(r);
-        if (rr == n_vis - 1 && last_lim < TILE) {
+        if (rr == mask_rr && last_lim < TILE) {
 #pragma unroll
           for (int c = 0; c < 128; ++c)
             if (c >= last_lim) s[c] = -INFINITY;

@@ -47,12 +47,18 @@ CASES = [
     (1, 1, 512, 128, False, 0.2, 0xDEADBEEFCAFEF00D, 0.5),
     (1, 2, 1000, 128, True, 0.1, 5, None),
     (1, 1, 640, 64, True, 0.25, 6, 0.6),
+    # sliding windows: the two query tiles of a CTA share all but one key
+    # tile, so the forward runs its shared-first round order
+    (1, 2, 2048, 128, True, 0.2, 11, ("window", 3, 0)),
+    (1, 1, 1500, 64, False, 0.15, 12, ("window", 2, 2)),
 ]
 
 
 def _mask(N, keep_p, seed):
     if keep_p is None:
         return None
+    if isinstance(keep_p, tuple):
+        return torch.from_numpy(oracle.window_block_mask(N, keep_p[1], keep_p[2]).astype(np.uint8))
     nb = (N + 127) // 128
     g = torch.Generator().manual_seed(seed)
     bm = (torch.rand((nb, nb), generator=g) < keep_p).to(torch.uint8)
