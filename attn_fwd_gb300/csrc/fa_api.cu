@@ -767,7 +767,7 @@ struct HostStreams {
   std::once_flag once;
   std::mutex mu;                // one caller enqueues at a time on a device
   cudaStream_t in = nullptr, cmp = nullptr, out = nullptr;
-  cudaEvent_t start = nullptr, in_done[2] = {}, cmp_done[2] = {}, out_done[2] = {};
+  cudaEvent_t start = nullptr, in_done[2] = {}, cmp_done[2] = {}, out_done[2] = {}, join[3] = {};
   cudaError_t err = cudaSuccess;
 };
 HostStreams g_host[kMaxDevices];
@@ -781,7 +781,7 @@ int host_streams(HostStreams** out) {
     for (cudaStream_t* s : {&h.in, &h.cmp, &h.out})
       if (e == cudaSuccess) e = cudaStreamCreateWithFlags(s, cudaStreamNonBlocking);
     for (cudaEvent_t* ev : {&h.start, &h.in_done[0], &h.in_done[1], &h.cmp_done[0], &h.cmp_done[1],
-                            &h.out_done[0], &h.out_done[1]})
+                            &h.out_done[0], &h.out_done[1], &h.join[0], &h.join[1], &h.join[2]})
       if (e == cudaSuccess) e = cudaEventCreateWithFlags(ev, cudaEventDisableTiming);
     h.err = e;
   });
@@ -825,55 +825,67 @@ extern "C" int fa_fwd_bwd_host(const void* q, const void* k, const void* v, cons
   auto cu = [](cudaError_t e) { return e == cudaSuccess ? FA_OK : FA_ERR_CUDA; };
   // everything starts after the work already queued on the caller's stream
   if ((rc = cu(cudaEventRecord(hs->start, caller))) != FA_OK) return rc;
-  for (cudaStream_t s : {hs->in, hs->cmp, hs->out})
-    if ((rc = cu(cudaStreamWaitEvent(s, hs->start, 0))) != FA_OK) return rc;
-  const void* hin[4] = {q, k, v, dout};
-  void* hout[4] = {o, dq, dk, dv};
-  // chunks of G heads, except a first chunk of G / 2 when there are several
-  // (the pipeline fills and drains faster); the last takes the rest
-  long long c = 0;
-  for (long long h0 = 0; h0 < BH; ++c) {
-    const int b = static_cast<int>(c & 1);
-    long long gc = (c == 0 && BH > G) ? (G + 1) / 2 : G;
-    if (gc > BH - h0) gc = BH - h0;
-    const int g = static_cast<int>(gc);
-    const HostSet s = host_carve(static_cast<char*>(workspace) + b * set_bytes, G, N, d);
-    const size_t bytes = static_cast<size_t>(g) * head_elems * 2;
-    const size_t off = static_cast<size_t>(h0) * head_elems * 2;
-    // copies in, once the kernels of chunk c - 2 are done with this set's
-    // inputs (its outputs may still be on their way out)
-    if (c >= 2 && (rc = cu(cudaStreamWaitEvent(hs->in, hs->cmp_done[b], 0))) != FA_OK) return rc;
-    for (int i = 0; i < 4; ++i)
-      if ((rc = cu(cudaMemcpyAsync(s.t[i], static_cast<const char*>(hin[i]) + off, bytes, cudaMemcpyHostToDevice,
-                                   hs->in))) != FA_OK)
+  auto enqueue = [&]() -> int {
+    int rc;
+    for (cudaStream_t s : {hs->in, hs->cmp, hs->out})
+      if ((rc = cu(cudaStreamWaitEvent(s, hs->start, 0))) != FA_OK) return rc;
+    const void* hin[4] = {q, k, v, dout};
+    void* hout[4] = {o, dq, dk, dv};
+    // chunks of G heads, except a first chunk of G / 2 when there are several
+    // (the pipeline fills and drains faster); the last takes the rest
+    long long c = 0;
+    for (long long h0 = 0; h0 < BH; ++c) {
+      const int b = static_cast<int>(c & 1);
+      long long gc = (c == 0 && BH > G) ? (G + 1) / 2 : G;
+      if (gc > BH - h0) gc = BH - h0;
+      const int g = static_cast<int>(gc);
+      const HostSet s = host_carve(static_cast<char*>(workspace) + b * set_bytes, G, N, d);
+      const size_t bytes = static_cast<size_t>(g) * head_elems * 2;
+      const size_t off = static_cast<size_t>(h0) * head_elems * 2;
+      // copies in, once the kernels of chunk c - 2 are done with this set's
+      // inputs (its outputs may still be on their way out)
+      if (c >= 2 && (rc = cu(cudaStreamWaitEvent(hs->in, hs->cmp_done[b], 0))) != FA_OK) return rc;
+      for (int i = 0; i < 4; ++i)
+        if ((rc = cu(cudaMemcpyAsync(s.t[i], static_cast<const char*>(hin[i]) + off, bytes, cudaMemcpyHostToDevice,
+                                     hs->in))) != FA_OK)
+          return rc;
+      if ((rc = cu(cudaEventRecord(hs->in_done[b], hs->in))) != FA_OK) return rc;
+      // kernels: forward (O, LSE), then the three backward stages, once the
+      // inputs are in and chunk c - 2's outputs have left this set
+      if ((rc = cu(cudaStreamWaitEvent(hs->cmp, hs->in_done[b], 0))) != FA_OK) return rc;
+      if (c >= 2 && (rc = cu(cudaStreamWaitEvent(hs->cmp, hs->out_done[b], 0))) != FA_OK) return rc;
+      const fa_stream_t cs = reinterpret_cast<fa_stream_t>(hs->cmp);
+      if ((rc = fwd_impl(s.t[0], s.t[1], s.t[2], s.t[4], s.lse, block_mask, 1, g, N, d, scale, mask_kind, 0.f, 0,
+                         cs)) != FA_OK)
         return rc;
-    if ((rc = cu(cudaEventRecord(hs->in_done[b], hs->in))) != FA_OK) return rc;
-    // kernels: forward (O, LSE), then the three backward stages, once the
-    // inputs are in and chunk c - 2's outputs have left this set
-    if ((rc = cu(cudaStreamWaitEvent(hs->cmp, hs->in_done[b], 0))) != FA_OK) return rc;
-    if (c >= 2 && (rc = cu(cudaStreamWaitEvent(hs->cmp, hs->out_done[b], 0))) != FA_OK) return rc;
-    const fa_stream_t cs = reinterpret_cast<fa_stream_t>(hs->cmp);
-    if ((rc = fwd_impl(s.t[0], s.t[1], s.t[2], s.t[4], s.lse, block_mask, 1, g, N, d, scale, mask_kind, 0.f, 0,
-                       cs)) != FA_OK)
-      return rc;
-    if ((rc = bwd_impl(s.t[0], s.t[1], s.t[2], s.t[4], s.t[3], s.lse, block_mask, s.t[5], s.t[6], s.t[7], s.ws, 1,
-                       g, N, d, scale, mask_kind, 0.f, 0, cs)) != FA_OK)
-      return rc;
-    if ((rc = cu(cudaEventRecord(hs->cmp_done[b], hs->cmp))) != FA_OK) return rc;
-    // copies out
-    if ((rc = cu(cudaStreamWaitEvent(hs->out, hs->cmp_done[b], 0))) != FA_OK) return rc;
-    const char* dsrc[4] = {s.t[4], s.t[5], s.t[6], s.t[7]};
-    for (int i = 0; i < 4; ++i)
-      if ((rc = cu(cudaMemcpyAsync(static_cast<char*>(hout[i]) + off, dsrc[i], bytes, cudaMemcpyDeviceToHost,
-                                   hs->out))) != FA_OK)
+      if ((rc = bwd_impl(s.t[0], s.t[1], s.t[2], s.t[4], s.t[3], s.lse, block_mask, s.t[5], s.t[6], s.t[7], s.ws, 1,
+                         g, N, d, scale, mask_kind, 0.f, 0, cs)) != FA_OK)
         return rc;
-    if ((rc = cu(cudaMemcpyAsync(lse + h0 * N, s.lse, static_cast<size_t>(g) * N * sizeof(float),
-                                 cudaMemcpyDeviceToHost, hs->out))) != FA_OK)
-      return rc;
-    if ((rc = cu(cudaEventRecord(hs->out_done[b], hs->out))) != FA_OK) return rc;
-    h0 += gc;
+      if ((rc = cu(cudaEventRecord(hs->cmp_done[b], hs->cmp))) != FA_OK) return rc;
+      // copies out
+      if ((rc = cu(cudaStreamWaitEvent(hs->out, hs->cmp_done[b], 0))) != FA_OK) return rc;
+      const char* dsrc[4] = {s.t[4], s.t[5], s.t[6], s.t[7]};
+      for (int i = 0; i < 4; ++i)
+        if ((rc = cu(cudaMemcpyAsync(static_cast<char*>(hout[i]) + off, dsrc[i], bytes, cudaMemcpyDeviceToHost,
+                                     hs->out))) != FA_OK)
+          return rc;
+      if ((rc = cu(cudaMemcpyAsync(lse + h0 * N, s.lse, static_cast<size_t>(g) * N * sizeof(float),
+                                   cudaMemcpyDeviceToHost, hs->out))) != FA_OK)
+        return rc;
+      if ((rc = cu(cudaEventRecord(hs->out_done[b], hs->out))) != FA_OK) return rc;
+      h0 += gc;
+    }
+    return FA_OK;
+  };
+  rc = enqueue();
+  // The caller's stream continues once everything enqueued on the three
+  // streams is done -- also after a failed enqueue, so that no copy or
+  // kernel of this call still runs when the caller reuses its buffers.
+  const cudaStream_t own[3] = {hs->in, hs->cmp, hs->out};
+  for (int i = 0; i < 3; ++i) {
+    const int rj = cu(cudaEventRecord(hs->join[i], own[i]));
+    const int rw = rj == FA_OK ? cu(cudaStreamWaitEvent(caller, hs->join[i], 0)) : rj;
+    if (rc == FA_OK) rc = rw;
   }
-  // the caller's stream continues once the last copies out are done (the
-  // out stream runs the chunks in order)
-  return cu(cudaStreamWaitEvent(caller, hs->out_done[(c - 1) & 1], 0));
+  return rc;
 }

@@ -316,7 +316,9 @@ FA_API int fa_bwd_noalloc(const void *q, const void *k, const void *v, const voi
  *
  * Ordering: the work starts after everything already queued on `stream` and
  * `stream` waits for its end (the last copy back), so a synchronisation of
- * `stream` makes the host outputs readable.  The host inputs must stay
+ * `stream` makes the host outputs readable.  That holds for an error return
+ * too: whatever was enqueued before the failing call finishes before
+ * `stream` goes on.  The host inputs must stay
  * unchanged, and the outputs unread, until then.  Calls from several host
  * threads on one device are serialised while they enqueue; the workspace of
  * a call must not be in use by other work.
