@@ -20,7 +20,8 @@
 //   dP^T = V_j dO_i^T         (M=128, N=BQ, K=d)        A,B K-major
 //   dV  += P^T dO_i           (M=128, N=d, K=BQ)        A = P^T, B MN-major
 //   dK  += dS^T Q_i           (M=128, N=d, K=BQ)        A = dS^T, B MN-major
-// (A of dV and dK from tensor memory at d=128, from shared memory at d=64)
+// (A of dV from tensor memory; A of dK from tensor memory at d=128, from
+// shared memory at d=64, where the 512 columns hold P^T but not dS^T too)
 //   d=128: dQ^T = K_j^T dS^T  (M=d=128, N=BQ=64, K=128) A,B MN-major
 //   d=64:  dQ   = dS K_j      (M=BQ=128, N=d, K=128)    A,B MN-major
 // The d=128 form keeps the head-dim index on the lanes, so each warp's fp32
@@ -29,7 +30,8 @@
 // Warp roles (14 warps): 0-7 recompute P and dS (thread = key row; warps
 // 0-3 take the first half of the step's query columns, 4-7 the second half,
 // so two warps per SM sub-partition share the CUDA-core work) and write P^T
-// and dS^T (bf16, 128-byte swizzle) to shared memory; 8-11 drain dQ from
+// (bf16) to tensor memory and dS^T (bf16, 128-byte swizzle) to a
+// double-buffered shared-memory tile (d=128: to tensor memory too); 8-11 drain dQ from
 // tensor memory into the fp32 accumulator; 12 issues MMAs; 13 loads K_j, V_j
 // once and Q_i, dO_i, LSE_i, D_i per step into a two-stage ring.
 #include "fa_common.cuh"
@@ -55,9 +57,9 @@ struct BwdLayout {
   static constexpr int STAGE_BYTES = ((2 * Q_BYTES + 2 * BQ * 4) + 1023) / 1024 * 1024;
   static constexpr int PT_CHUNK = TILE * 128;               // [128 key rows][64 queries]
   static constexpr int PT_BYTES = (BQ / 64) * PT_CHUNK;     // 128 x BQ bf16
-  // Shared P^T / dS^T area (2 x PT_BYTES): d=64 keeps P^T and dS^T there
-  // (one buffer each); d=128 keeps P^T in tensor memory and double-buffers
-  // dS^T there, so step i+1 can write while dQ(i) still reads step i's.
+  // Shared dS^T area (2 x PT_BYTES): dS^T double-buffered there, so step
+  // i+1 can write while dQ(i) still reads step i's; P^T lives in tensor
+  // memory (and at d=128 a copy of dS^T too).
   static constexpr int PBUFS = 1;
   static constexpr int K_OFF = 0;
   static constexpr int V_OFF = KV_BYTES;
@@ -71,8 +73,8 @@ struct BwdLayout {
   static constexpr int B_SDP = B_EMPTY + STAGES;         // S^T and dP^T of a step in tensor memory
   static constexpr int B_SDP_FREE = B_SDP + 1;           // ... and read out (one arrival per warp)
   static constexpr int B_DS = B_SDP_FREE + 1;            // P^T, dS^T of a step written (one arrival per warp)
-  static constexpr int B_PFREE = B_DS + 1;               // dV, dK done reading them (d=64: dQ too)
-  static constexpr int B_DSF = B_PFREE + 1;              // 2: d=128 dS^T smem buffer b consumed by dQ
+  static constexpr int B_PFREE = B_DS + 1;               // dV, dK done reading P^T (d=128: dS^T) in TMEM
+  static constexpr int B_DSF = B_PFREE + 1;              // 2: dS^T smem buffer b consumed (dQ; d=64: dK too)
   static constexpr int B_DQ = B_DSF + 2;                 // dQ of a step in tensor memory
   static constexpr int B_DQ_FREE = B_DQ + 1;             // ... and read out (one arrival per warp)
   static constexpr int B_DONE = B_DQ_FREE + 1;
@@ -92,8 +94,10 @@ struct BwdLayout {
   // shared memory.  Map at d=128: S^T [0,64) dP^T [64,128) dQ^T [128,192)
   // P^T [192,224) dS^T [224,256) dV [256,384) dK [384,512).  d=64 has no room
   // left (S^T and dP^T take 128 columns each).
-  static constexpr bool P_TMEM = (D == 128);
-  static constexpr uint32_t COL_PT = 192;     // free columns between dQ^T [128,192) and dV [256,384)
+  static constexpr bool DST_TMEM = (D == 128);   // dS^T also in TMEM (dK as a TS product)
+  // P^T: d=128 in the free columns between dQ^T [128,192) and dV [256,384);
+  // d=64 in the last 64 columns, after dK [384,448)
+  static constexpr uint32_t COL_PT = (D == 128) ? 192 : 448;
   static constexpr uint32_t COL_DST = 224;
   static constexpr int THREADS = 448;
   static constexpr int W_DRAIN = 8;      // first drain warp
@@ -316,12 +320,11 @@ __global__ void __launch_bounds__(448, 1) fa_bwd_kernel(const __grid_constant__ 
       const uint64_t dO_kmaj = sdesc_sw128(sbase + L::RING_OFF + L::ST_DO, 16, 1024);   // stage 0 dO, K-major
       const uint64_t dQ_mn = sdesc_sw128(sbase + L::RING_OFF + L::ST_Q, L::Q_CHUNK, 1024);   // stage 0 Q, MN-major
       const uint64_t dO_mn = sdesc_sw128(sbase + L::RING_OFF + L::ST_DO, L::Q_CHUNK, 1024);  // stage 0 dO, MN-major
-      const uint32_t pt = sbase + L::PT_OFF;                                         // single P^T / dS^T buffer
-      const uint64_t dPT_kmaj = sdesc_sw128(pt, 16, 1024);
-      const uint64_t dDS_kmaj = sdesc_sw128(pt + L::PT_BYTES, 16, 1024);
-      // dS^T as the B (d=128) or A (d=64) operand of the dQ product; at d=128
-      // step i uses buffer i % 2 of the area, at d=64 the second half.
-      const uint64_t dDS_mn0 = sdesc_sw128(L::P_TMEM ? pt : pt + L::PT_BYTES, L::PT_CHUNK, 1024);
+      const uint32_t pt = sbase + L::PT_OFF;                                         // dS^T buffers
+      // dS^T, step i in buffer i % 2: K-major as the A operand of dK (d=64),
+      // MN-major as the B (d=128) or A (d=64) operand of the dQ product
+      const uint64_t dDS_kmaj0 = sdesc_sw128(pt, 16, 1024);
+      const uint64_t dDS_mn0 = sdesc_sw128(pt, L::PT_CHUNK, 1024);
       constexpr uint32_t PT16 = L::PT_BYTES >> 4;
       bool ok = mbar_wait_warp(bar(L::B_KV), 0, wc);
 
@@ -366,30 +369,27 @@ __global__ void __launch_bounds__(448, 1) fa_bwd_kernel(const __grid_constant__ 
         // dV += P^T dO_i ; dK += dS^T Q_i   (K = BQ queries, 16 per step)
 #pragma unroll
         for (int k = 0; k < BQ / 16; ++k) {
-          const uint32_t ao = ((k >> 2) * L::PT_CHUNK + (k & 3) * 32) >> 4;
           const uint64_t bd = dO_mn + so + ((k * 2048) >> 4);
-          if constexpr (L::P_TMEM)
-            mma_ts_elect(tmem + L::COL_DV, tmem + L::COL_PT + 8 * k, bd, ID_G, (i > 0 || k > 0) ? 1u : 0u);
-          else
-            mma_ss_elect(tmem + L::COL_DV, dPT_kmaj + ao, bd, ID_G, (i > 0 || k > 0) ? 1u : 0u);
+          mma_ts_elect(tmem + L::COL_DV, tmem + L::COL_PT + 8 * k, bd, ID_G, (i > 0 || k > 0) ? 1u : 0u);
         }
 #pragma unroll
         for (int k = 0; k < BQ / 16; ++k) {
           const uint32_t ao = ((k >> 2) * L::PT_CHUNK + (k & 3) * 32) >> 4;
           const uint64_t bd = dQ_mn + so + ((k * 2048) >> 4);
-          if constexpr (L::P_TMEM)
+          if constexpr (L::DST_TMEM)
             mma_ts_elect(tmem + L::COL_DK, tmem + L::COL_DST + 8 * k, bd, ID_G, (i > 0 || k > 0) ? 1u : 0u);
           else
-            mma_ss_elect(tmem + L::COL_DK, dDS_kmaj + ao, bd, ID_G, (i > 0 || k > 0) ? 1u : 0u);
+            mma_ss_elect(tmem + L::COL_DK, dDS_kmaj0 + static_cast<uint64_t>(i & 1) * PT16 + ao, bd, ID_G,
+                         (i > 0 || k > 0) ? 1u : 0u);
         }
         mma_commit_elect(bar(L::B_EMPTY + st));     // Q_i, dO_i are no longer needed after dV, dK
-        if constexpr (L::P_TMEM) mma_commit_elect(bar(L::B_PFREE));   // P^T, dS^T in TMEM consumed
+        mma_commit_elect(bar(L::B_PFREE));          // P^T (d=128: and dS^T) in TMEM consumed
         // dQ for this step, once the drain warps have read the previous one
         if (i > 0) {
           if (!(ok = mbar_wait_warp(bar(L::B_DQ_FREE), (i - 1) & 1, wc))) break;
           tc_fence_after();
         }
-        const uint64_t dDS_mn = dDS_mn0 + (L::P_TMEM ? static_cast<uint64_t>(i & 1) * PT16 : 0);
+        const uint64_t dDS_mn = dDS_mn0 + static_cast<uint64_t>(i & 1) * PT16;
 #pragma unroll
         for (int k = 0; k < TILE / 16; ++k) {
           const uint32_t o = (k * 2048) >> 4;
@@ -404,10 +404,7 @@ __global__ void __launch_bounds__(448, 1) fa_bwd_kernel(const __grid_constant__ 
           }
         }
         mma_commit_elect(bar(L::B_DQ));
-        if constexpr (L::P_TMEM)
-          mma_commit_elect(bar(L::B_DSF + (i & 1)));   // dS^T buffer i % 2 consumed
-        else
-          mma_commit_elect(bar(L::B_PFREE));           // P^T, dS^T buffer consumed
+        mma_commit_elect(bar(L::B_DSF + (i & 1)));     // dS^T buffer i % 2 consumed (dK, dQ)
       }
       mma_commit_elect(bar(L::B_DONE));
       if (lane == 0) mbar_drain_b(bar(L::B_DONE), 0, 1000000000ull);
@@ -444,10 +441,8 @@ __global__ void __launch_bounds__(448, 1) fa_bwd_kernel(const __grid_constant__ 
       const uint8_t* stage = smem + L::RING_OFF + st * L::STAGE_BYTES;
       const float* lse = reinterpret_cast<const float*>(stage + L::ST_LSE);
       const float* dvec = reinterpret_cast<const float*>(stage + L::ST_DV);
-      uint8_t* const area = smem + L::PT_OFF;
-      // d=128: dS^T into buffer i % 2; d=64: P^T in the first half, dS^T in the second
-      uint8_t* const pt = area;
-      uint8_t* const dsT = L::P_TMEM ? area + (i & 1) * L::PT_BYTES : area + L::PT_BYTES;
+      // dS^T of step i into shared buffer i % 2
+      uint8_t* const dsT = smem + L::PT_OFF + (i & 1) * L::PT_BYTES;
       const bool causal = (p.mask_kind & MASK_CAUSAL) != 0;
       const bool key_ok = key < p.N;
       const bool need_mask = (causal && qi * BQ < kt * TILE + TILE) || !key_ok || qi * BQ + BQ > p.N;
@@ -472,35 +467,25 @@ __global__ void __launch_bounds__(448, 1) fa_bwd_kernel(const __grid_constant__ 
         else
           recompute32<false, DROP>(sr, dr, lse, dvec, c0, sl2v, 0, 0, 0, false, kp, p.drop.scale, pt_pk, ds_pk);
         // pass 2: stores, once the buffers they overwrite have been consumed
-        if (c0 == half * COLS) {
-          if constexpr (L::P_TMEM) {
-            if (i >= 2 && !(ok = mbar_wait_warp(bar(L::B_DSF + (i & 1)), ((i >> 1) - 1) & 1, wc))) break;
-          } else {
-            if (i >= 1 && !(ok = mbar_wait_warp(bar(L::B_PFREE), (i - 1) & 1, wc))) break;
-          }
-        }
-        uint8_t* prow = pt + (c0 >> 6) * L::PT_CHUNK + r * 128;
+        // the dS^T buffer is free once dK(i-2), dQ(i-2) have read it
+        if (c0 == half * COLS && i >= 2 &&
+            !(ok = mbar_wait_warp(bar(L::B_DSF + (i & 1)), ((i >> 1) - 1) & 1, wc)))
+          break;
         uint8_t* drow = dsT + (c0 >> 6) * L::PT_CHUNK + r * 128;
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           const int sw = ((((c0 & 63) >> 3) + j) ^ (r & 7)) << 4;   // 128-byte swizzle of the 16-byte chunk
-          if constexpr (!L::P_TMEM)
-            *reinterpret_cast<uint4*>(prow + sw) = make_uint4(pt_pk[4 * j], pt_pk[4 * j + 1], pt_pk[4 * j + 2], pt_pk[4 * j + 3]);
           *reinterpret_cast<uint4*>(drow + sw) = make_uint4(ds_pk[4 * j], ds_pk[4 * j + 1], ds_pk[4 * j + 2], ds_pk[4 * j + 3]);
         }
-        if constexpr (L::P_TMEM) {
-          // P^T, dS^T in tensor memory are free once dV(i-1), dK(i-1) are done
-          if (i >= 1 && !(ok = mbar_wait_warp(bar(L::B_PFREE), (i - 1) & 1, wc))) break;
-          // 32 query columns = 16 bf16-pair columns of P^T and of dS^T
-          tmem_st_x16_async(tmem_addr(tmem, lane_base, L::COL_PT + c0 / 2), pt_pk);
-          tmem_st_x16_async(tmem_addr(tmem, lane_base, L::COL_DST + c0 / 2), ds_pk);
-        }
+        // P^T (d=128: and dS^T) in tensor memory are free once dV(i-1), dK(i-1) are done
+        if (i >= 1 && !(ok = mbar_wait_warp(bar(L::B_PFREE), (i - 1) & 1, wc))) break;
+        // 32 query columns = 16 bf16-pair columns
+        tmem_st_x16_async(tmem_addr(tmem, lane_base, L::COL_PT + c0 / 2), pt_pk);
+        if constexpr (L::DST_TMEM) tmem_st_x16_async(tmem_addr(tmem, lane_base, L::COL_DST + c0 / 2), ds_pk);
       }
       if (!ok) break;
-      if constexpr (L::P_TMEM) {
-        tmem_wait_st();
-        tc_fence_before();
-      }
+      tmem_wait_st();
+      tc_fence_before();
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(L::B_DS));
