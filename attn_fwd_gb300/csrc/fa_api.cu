@@ -726,40 +726,47 @@ extern "C" int fa_bwd_noalloc(const void* q, const void* k, const void* v, const
 // --------------------------------------------------------------------------
 namespace {
 
-// Heads per chunk: enough key tiles for two waves of the backward on 152
-// SMs (a chunk's kernels then run near full speed), at most 8 chunks, and
-// the heads spread evenly over the chunks.  (Measured on B2 H16 N4096 d128:
-// chunks of 8 heads beat chunks of 16, whose longer first copy and last copy
-// back are not overlapped, and chunks of 4, whose kernels run half empty.)
-long long host_chunk_heads(int B, int H, int N) {
+// Heads per chunk: enough CTAs for two waves on 152 SMs (the backward runs
+// one CTA per key tile, the forward one per pair of query tiles), so a
+// chunk's kernels run near full speed; at most 8 chunks; the heads spread
+// evenly over the chunks.  (Measured on B2 H16 N4096 d128, forward and
+// backward: chunks of 8 heads beat chunks of 16, whose longer first copy in
+// and last copy back are not overlapped, and chunks of 4, whose kernels run
+// half empty.)
+long long host_chunk_heads(int B, int H, int N, bool backward) {
   const long long bh = static_cast<long long>(B) * H;
-  const long long waves = (2 * kPlanSMs + tiles(N) - 1) / tiles(N);
+  const long long per_head = backward ? tiles(N) : (tiles(N) + 1) / 2;
+  const long long waves = (2 * kPlanSMs + per_head - 1) / per_head;
   long long g = waves > (bh + 7) / 8 ? waves : (bh + 7) / 8;
   if (g > bh) g = bh;
   const long long chunks = (bh + g - 1) / g;
   return (bh + chunks - 1) / chunks;
 }
 
-// One buffer set: q, k, v, dO, O, dQ, dK, dV [G][N][d] bf16, LSE [G][N]
-// fp32, then the backward workspace of G heads.
+// One device buffer set for G heads: the bf16 [G][N][d] tensors (forward:
+// q, k, v, O; with the backward: q, k, v, dO, O, dQ, dK, dV), LSE [G][N]
+// fp32, then (backward) the backward workspace of G heads.
 struct HostSet {
   char* t[8];
   float* lse;
   void* ws;
 };
 
-size_t host_set_bytes(long long G, int N, int d) {
+int host_tensors(bool backward) { return backward ? 8 : 4; }
+
+size_t host_set_bytes(long long G, int N, int d, bool backward) {
   const size_t t = align256(static_cast<size_t>(G) * N * d * 2);
-  return 8 * t + align256(static_cast<size_t>(G) * N * sizeof(float)) +
-         align256(workspace_bytes(1, static_cast<int>(G), N, d));
+  return host_tensors(backward) * t + align256(static_cast<size_t>(G) * N * sizeof(float)) +
+         (backward ? align256(workspace_bytes(1, static_cast<int>(G), N, d)) : 0);
 }
 
-HostSet host_carve(char* base, long long G, int N, int d) {
+HostSet host_carve(char* base, long long G, int N, int d, bool backward) {
   const size_t t = align256(static_cast<size_t>(G) * N * d * 2);
-  HostSet s;
-  for (int i = 0; i < 8; ++i) s.t[i] = base + i * t;
-  s.lse = reinterpret_cast<float*>(base + 8 * t);
-  s.ws = base + 8 * t + align256(static_cast<size_t>(G) * N * sizeof(float));
+  const int nt = host_tensors(backward);
+  HostSet s{};
+  for (int i = 0; i < nt; ++i) s.t[i] = base + i * t;
+  s.lse = reinterpret_cast<float*>(base + nt * t);
+  s.ws = backward ? base + nt * t + align256(static_cast<size_t>(G) * N * sizeof(float)) : nullptr;
   return s;
 }
 
@@ -792,35 +799,49 @@ int host_streams(HostStreams** out) {
 
 }  // namespace
 
-extern "C" size_t fa_fwd_bwd_host_workspace_bytes(int B, int H, int N, int d) {
+namespace {
+
+// One host-streamed call: the forward alone, or the forward and the
+// backward, of host-resident tensors.
+struct HostJob {
+  bool backward;
+  const void* in[4];            // q, k, v (, dO)
+  void* out[4];                 // O (, dQ, dK, dV)
+  float* lse;
+  const uint8_t* block_mask;
+  int B, H, N, d;
+  float scale;
+  int mask_kind;
+};
+
+size_t host_workspace_bytes(int B, int H, int N, int d, bool backward) {
   if (check_shape(B, H, N, d) != FA_OK) return 0;
-  return 2 * host_set_bytes(host_chunk_heads(B, H, N), N, d);
+  return 2 * host_set_bytes(host_chunk_heads(B, H, N, backward), N, d, backward);
 }
 
-extern "C" int fa_fwd_bwd_host(const void* q, const void* k, const void* v, const void* dout, void* o, float* lse,
-                               void* dq, void* dk, void* dv, const uint8_t* block_mask, void* workspace,
-                               size_t workspace_size, int B, int H, int N, int d, float scale, int causal,
-                               fa_stream_t stream) {
+int host_stream(const HostJob& j, void* workspace, size_t workspace_size, fa_stream_t stream) {
   int rc;
-  for (const void* ptr : {q, k, v, dout, static_cast<const void*>(o), static_cast<const void*>(lse),
-                          static_cast<const void*>(dq), static_cast<const void*>(dk), static_cast<const void*>(dv),
-                          static_cast<const void*>(workspace)})
-    if (ptr == nullptr) return FA_ERR_INVALID;
+  const int n_in = j.backward ? 4 : 3, n_out = j.backward ? 4 : 1;
+  for (int i = 0; i < n_in; ++i)
+    if (j.in[i] == nullptr) return FA_ERR_INVALID;
+  for (int i = 0; i < n_out; ++i)
+    if (j.out[i] == nullptr) return FA_ERR_INVALID;
+  if (j.lse == nullptr || workspace == nullptr) return FA_ERR_INVALID;
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return FA_ERR_INVALID;
-  if ((rc = check_shape(B, H, N, d)) != FA_OK) return rc;
-  if ((rc = check_scale(scale)) != FA_OK) return rc;
-  const int mask_kind = (block_mask ? fa::MASK_BLOCK : 0) | (causal ? fa::MASK_CAUSAL : 0);
-  if ((mask_kind & fa::MASK_BLOCK) && tiles(N) > fa::MAX_SPARSE_TILES) return FA_ERR_UNSUPPORTED;
-  if (workspace_size < fa_fwd_bwd_host_workspace_bytes(B, H, N, d)) return FA_ERR_INVALID;
+  if ((rc = check_shape(j.B, j.H, j.N, j.d)) != FA_OK) return rc;
+  if ((rc = check_scale(j.scale)) != FA_OK) return rc;
+  if ((j.mask_kind & fa::MASK_BLOCK) && tiles(j.N) > fa::MAX_SPARSE_TILES) return FA_ERR_UNSUPPORTED;
+  if (workspace_size < host_workspace_bytes(j.B, j.H, j.N, j.d, j.backward)) return FA_ERR_INVALID;
   int* status = nullptr;
   if ((rc = device_ready(&status)) != FA_OK) return rc;
   HostStreams* hs = nullptr;
   if ((rc = host_streams(&hs)) != FA_OK) return rc;
   std::lock_guard<std::mutex> lk(hs->mu);
   const cudaStream_t caller = reinterpret_cast<cudaStream_t>(stream);
-  const long long BH = static_cast<long long>(B) * H;
-  const long long G = host_chunk_heads(B, H, N);
-  const size_t set_bytes = host_set_bytes(G, N, d);
+  const int N = j.N, d = j.d;
+  const long long BH = static_cast<long long>(j.B) * j.H;
+  const long long G = host_chunk_heads(j.B, j.H, N, j.backward);
+  const size_t set_bytes = host_set_bytes(G, N, d, j.backward);
   const size_t head_elems = static_cast<size_t>(N) * d;
   auto cu = [](cudaError_t e) { return e == cudaSuccess ? FA_OK : FA_ERR_CUDA; };
   // everything starts after the work already queued on the caller's stream
@@ -829,8 +850,6 @@ extern "C" int fa_fwd_bwd_host(const void* q, const void* k, const void* v, cons
     int rc;
     for (cudaStream_t s : {hs->in, hs->cmp, hs->out})
       if ((rc = cu(cudaStreamWaitEvent(s, hs->start, 0))) != FA_OK) return rc;
-    const void* hin[4] = {q, k, v, dout};
-    void* hout[4] = {o, dq, dk, dv};
     // chunks of G heads, except a first chunk of G / 2 when there are several
     // (the pipeline fills and drains faster); the last takes the rest
     long long c = 0;
@@ -839,37 +858,38 @@ extern "C" int fa_fwd_bwd_host(const void* q, const void* k, const void* v, cons
       long long gc = (c == 0 && BH > G) ? (G + 1) / 2 : G;
       if (gc > BH - h0) gc = BH - h0;
       const int g = static_cast<int>(gc);
-      const HostSet s = host_carve(static_cast<char*>(workspace) + b * set_bytes, G, N, d);
+      const HostSet s = host_carve(static_cast<char*>(workspace) + b * set_bytes, G, N, d, j.backward);
       const size_t bytes = static_cast<size_t>(g) * head_elems * 2;
       const size_t off = static_cast<size_t>(h0) * head_elems * 2;
       // copies in, once the kernels of chunk c - 2 are done with this set's
       // inputs (its outputs may still be on their way out)
       if (c >= 2 && (rc = cu(cudaStreamWaitEvent(hs->in, hs->cmp_done[b], 0))) != FA_OK) return rc;
-      for (int i = 0; i < 4; ++i)
-        if ((rc = cu(cudaMemcpyAsync(s.t[i], static_cast<const char*>(hin[i]) + off, bytes, cudaMemcpyHostToDevice,
-                                     hs->in))) != FA_OK)
+      for (int i = 0; i < n_in; ++i)
+        if ((rc = cu(cudaMemcpyAsync(s.t[i], static_cast<const char*>(j.in[i]) + off, bytes,
+                                     cudaMemcpyHostToDevice, hs->in))) != FA_OK)
           return rc;
       if ((rc = cu(cudaEventRecord(hs->in_done[b], hs->in))) != FA_OK) return rc;
-      // kernels: forward (O, LSE), then the three backward stages, once the
-      // inputs are in and chunk c - 2's outputs have left this set
+      // kernels, once the inputs are in and chunk c - 2's outputs have left
+      // this set: the forward (O, LSE), then the backward stages
       if ((rc = cu(cudaStreamWaitEvent(hs->cmp, hs->in_done[b], 0))) != FA_OK) return rc;
       if (c >= 2 && (rc = cu(cudaStreamWaitEvent(hs->cmp, hs->out_done[b], 0))) != FA_OK) return rc;
       const fa_stream_t cs = reinterpret_cast<fa_stream_t>(hs->cmp);
-      if ((rc = fwd_impl(s.t[0], s.t[1], s.t[2], s.t[4], s.lse, block_mask, 1, g, N, d, scale, mask_kind, 0.f, 0,
-                         cs)) != FA_OK)
+      char* const o_dev = s.t[n_in];                      // O follows the inputs
+      if ((rc = fwd_impl(s.t[0], s.t[1], s.t[2], o_dev, s.lse, j.block_mask, 1, g, N, d, j.scale, j.mask_kind,
+                         0.f, 0, cs)) != FA_OK)
         return rc;
-      if ((rc = bwd_impl(s.t[0], s.t[1], s.t[2], s.t[4], s.t[3], s.lse, block_mask, s.t[5], s.t[6], s.t[7], s.ws, 1,
-                         g, N, d, scale, mask_kind, 0.f, 0, cs)) != FA_OK)
+      if (j.backward &&
+          (rc = bwd_impl(s.t[0], s.t[1], s.t[2], o_dev, s.t[3], s.lse, j.block_mask, s.t[5], s.t[6], s.t[7], s.ws,
+                         1, g, N, d, j.scale, j.mask_kind, 0.f, 0, cs)) != FA_OK)
         return rc;
       if ((rc = cu(cudaEventRecord(hs->cmp_done[b], hs->cmp))) != FA_OK) return rc;
       // copies out
       if ((rc = cu(cudaStreamWaitEvent(hs->out, hs->cmp_done[b], 0))) != FA_OK) return rc;
-      const char* dsrc[4] = {s.t[4], s.t[5], s.t[6], s.t[7]};
-      for (int i = 0; i < 4; ++i)
-        if ((rc = cu(cudaMemcpyAsync(static_cast<char*>(hout[i]) + off, dsrc[i], bytes, cudaMemcpyDeviceToHost,
-                                     hs->out))) != FA_OK)
+      for (int i = 0; i < n_out; ++i)
+        if ((rc = cu(cudaMemcpyAsync(static_cast<char*>(j.out[i]) + off, s.t[n_in + i], bytes,
+                                     cudaMemcpyDeviceToHost, hs->out))) != FA_OK)
           return rc;
-      if ((rc = cu(cudaMemcpyAsync(lse + h0 * N, s.lse, static_cast<size_t>(g) * N * sizeof(float),
+      if ((rc = cu(cudaMemcpyAsync(j.lse + h0 * N, s.lse, static_cast<size_t>(g) * N * sizeof(float),
                                    cudaMemcpyDeviceToHost, hs->out))) != FA_OK)
         return rc;
       if ((rc = cu(cudaEventRecord(hs->out_done[b], hs->out))) != FA_OK) return rc;
@@ -888,4 +908,31 @@ extern "C" int fa_fwd_bwd_host(const void* q, const void* k, const void* v, cons
     if (rc == FA_OK) rc = rw;
   }
   return rc;
+}
+
+}  // namespace
+
+extern "C" size_t fa_fwd_bwd_host_workspace_bytes(int B, int H, int N, int d) {
+  return host_workspace_bytes(B, H, N, d, true);
+}
+
+extern "C" int fa_fwd_bwd_host(const void* q, const void* k, const void* v, const void* dout, void* o, float* lse,
+                               void* dq, void* dk, void* dv, const uint8_t* block_mask, void* workspace,
+                               size_t workspace_size, int B, int H, int N, int d, float scale, int causal,
+                               fa_stream_t stream) {
+  const HostJob j{true, {q, k, v, dout}, {o, dq, dk, dv}, lse, block_mask, B, H, N, d, scale,
+                  (block_mask ? fa::MASK_BLOCK : 0) | (causal ? fa::MASK_CAUSAL : 0)};
+  return host_stream(j, workspace, workspace_size, stream);
+}
+
+extern "C" size_t fa_fwd_host_workspace_bytes(int B, int H, int N, int d) {
+  return host_workspace_bytes(B, H, N, d, false);
+}
+
+extern "C" int fa_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse,
+                           const uint8_t* block_mask, void* workspace, size_t workspace_size, int B, int H, int N,
+                           int d, float scale, int causal, fa_stream_t stream) {
+  const HostJob j{false, {q, k, v, nullptr}, {o, nullptr, nullptr, nullptr}, lse, block_mask, B, H, N, d, scale,
+                  (block_mask ? fa::MASK_BLOCK : 0) | (causal ? fa::MASK_CAUSAL : 0)};
+  return host_stream(j, workspace, workspace_size, stream);
 }

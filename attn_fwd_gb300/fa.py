@@ -56,6 +56,8 @@ _SIGS = {
     "fa_debug_wait_timeout": (_i, [_u64, _vp]),
     "fa_fwd_bwd_host_workspace_bytes": (_sz, [_i, _i, _i, _i]),
     "fa_fwd_bwd_host": (_i, [_vp] * 11 + [_sz, _i, _i, _i, _i, _f, _i, _vp]),
+    "fa_fwd_host_workspace_bytes": (_sz, [_i, _i, _i, _i]),
+    "fa_fwd_host": (_i, [_vp] * 7 + [_sz, _i, _i, _i, _i, _f, _i, _vp]),
 }
 
 
@@ -246,6 +248,23 @@ def fa_fwd_bwd_host(q, k, v, do, o, lse, dq, dk, dv, block_mask, workspace, scal
     _check("fa_fwd_bwd_host", rc)
 
 
+def fa_fwd_host_workspace_bytes(B, H, N, d) -> int:
+    return load().fa_fwd_host_workspace_bytes(B, H, N, d)
+
+
+def fa_fwd_host(q, k, v, o, lse, block_mask, workspace, scale, causal=False, stream=None):
+    """The forward of host tensors (pinned for overlap), streamed through the
+    device in chunks of heads; see include/fa.h."""
+    B, H, N, d = q.shape
+    if not (workspace.is_cuda and workspace.dtype == torch.uint8):
+        raise ValueError("workspace must be a uint8 CUDA tensor")
+    rc = load().fa_fwd_host(_host(q, "q"), _host(k, "k"), _host(v, "v"), _host(o, "o"),
+                            _host(lse, "lse", torch.float32, 3), _mask_ptr(block_mask),
+                            ctypes.c_void_p(workspace.data_ptr()), workspace.numel(), B, H, N, d, float(scale),
+                            int(bool(causal)), _stream(stream))
+    _check("fa_fwd_host", rc)
+
+
 def fa_decode_workspace_bytes(B, H, Nq, Nk, d) -> int:
     return load().fa_decode_workspace_bytes(B, H, Nq, Nk, d)
 
@@ -404,6 +423,20 @@ def forward_backward_host(q, k, v, do, causal=False, scale=None, block_mask=None
         ws = torch.empty(fa_fwd_bwd_host_workspace_bytes(B, H, N, d), dtype=torch.uint8, device="cuda")
     fa_fwd_bwd_host(q, k, v, do, o, lse, dq, dk, dv, block_mask, ws, scale, causal, stream)
     return o, lse, dq, dk, dv
+
+
+def forward_host(q, k, v, causal=False, scale=None, block_mask=None, ws=None, stream=None):
+    """The forward of host tensors; returns pinned host (O, LSE).  ``ws``: a
+    device workspace of fa_fwd_host_workspace_bytes bytes (allocated when
+    omitted)."""
+    B, H, N, d = q.shape
+    scale = (1.0 / d ** 0.5) if scale is None else scale
+    o = torch.empty(q.shape, dtype=q.dtype).pin_memory()
+    lse = torch.empty((B, H, N), dtype=torch.float32).pin_memory()
+    if ws is None:
+        ws = torch.empty(fa_fwd_host_workspace_bytes(B, H, N, d), dtype=torch.uint8, device="cuda")
+    fa_fwd_host(q, k, v, o, lse, block_mask, ws, scale, causal, stream)
+    return o, lse
 
 
 def fa_status_string(code: int) -> str:

@@ -748,14 +748,20 @@ def run_cuda(args):
     # forward + backward without dropout: the library's host-streamed entry
     # point (copies in, kernels and copies out of successive chunks of heads
     # overlap); otherwise pinned copies around the device-resident step
-    streamed = w.backward and not w.dropout_p
-    if streamed:
+    streamed = not w.dropout_p
+    if streamed and w.backward:
         hws = torch.empty(fa.fa_fwd_bwd_host_workspace_bytes(w.B, w.H, w.N, w.d), dtype=torch.uint8, device=dev)
 
         def e2e_step():
             fa.fa_fwd_bwd_host(host_in["q"], host_in["k"], host_in["v"], host_in["do"], host_out["o"],
                                host_out["lse"], host_out["dq"], host_out["dk"], host_out["dv"], bm, hws, w.scale,
                                w.causal)
+    elif streamed:
+        hws = torch.empty(fa.fa_fwd_host_workspace_bytes(w.B, w.H, w.N, w.d), dtype=torch.uint8, device=dev)
+
+        def e2e_step():
+            fa.fa_fwd_host(host_in["q"], host_in["k"], host_in["v"], host_out["o"], host_out["lse"], bm, hws,
+                           w.scale, w.causal)
     else:
         def e2e_step():
             for n, x in host_in.items():
@@ -806,7 +812,8 @@ def run_cuda(args):
             "frac_of_peak": value / ws / peak,
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "ms_per_step": e2e_ms,
-                    "call": ("fa_fwd_bwd_host: chunks of heads, copies overlapped with the kernels" if streamed
+                    "call": ((("fa_fwd_bwd_host" if w.backward else "fa_fwd_host") +
+                              ": chunks of heads, copies overlapped with the kernels") if streamed
                              else "pinned copies in, device-resident step, copies out")},
             "gpu_launches": launches_per_step * args.steps, "roofline": roofline, "kernels": kernels,
             "clocks": clocks}

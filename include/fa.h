@@ -333,6 +333,25 @@ FA_API int fa_fwd_bwd_host(const void *q, const void *k, const void *v, const vo
                            float scale, int causal, fa_stream_t stream);
 
 /*
+ * The forward alone for host-resident tensors, streamed the same way as
+ * fa_fwd_bwd_host: the same computation as fa_fwd (fa_fwd_blocksparse when
+ * block_mask is given), in chunks of whole heads whose copies in, kernels
+ * and copies back overlap on the library's three streams.
+ *
+ *   q, k, v         : bf16 [B, H, N, d] in host memory
+ *   o               : bf16 [B, H, N, d] in host memory, written
+ *   lse             : fp32 [B, H, N] in host memory, written
+ *   block_mask      : NULL, or device uint8 [N/128][N/128] (with `causal`)
+ *   workspace       : device memory, 256-byte aligned, of at least
+ *                     fa_fwd_host_workspace_bytes(B, H, N, d) bytes
+ * Host buffers, ordering, threads and errors: as for fa_fwd_bwd_host.
+ */
+FA_API size_t fa_fwd_host_workspace_bytes(int B, int H, int N, int d);
+FA_API int fa_fwd_host(const void *q, const void *k, const void *v, void *o, float *lse,
+                       const uint8_t *block_mask, void *workspace, size_t workspace_size,
+                       int B, int H, int N, int d, float scale, int causal, fa_stream_t stream);
+
+/*
  * Synchronises `stream`, then returns and clears the current device's status
  * word: FA_OK, or FA_ERR_TIMEOUT when a kernel wait gave up.  Returns
  * FA_ERR_CUDA when the synchronisation itself fails.

@@ -138,6 +138,28 @@ def test_host_streamed_entry_checks(lib):
     assert lib.fa_fwd_bwd_host(*a) == -1                # scale
 
 
+def test_host_streamed_forward_checks(lib):
+    """fa_fwd_host: workspace sizing (two sets of q, k, v, O and LSE for G
+    heads, G covering two forward waves of 152 CTAs) and argument checks."""
+    import attn_fwd_gb300.fa as fa
+    B, H, N, d = 1, 32, 16384, 128
+    G = 5                                    # one CTA per query-tile pair: 64 per head -> 5 heads
+    assert fa.fa_fwd_host_workspace_bytes(B, H, N, d) == 2 * (4 * G * N * d * 2 + G * N * 4)
+    assert fa.fa_fwd_host_workspace_bytes(0, 1, 128, 64) == 0
+    ws = ctypes.c_void_p(4096)
+    args = [P, P, P, P, P, NULL, ws, 1 << 40, 1, 1, 128, 64, 0.125, 1, NULL]
+    for i in range(5):                       # q, k, v, o, lse are required
+        a = list(args)
+        a[i] = NULL
+        assert lib.fa_fwd_host(*a) == -1
+    a = list(args); a[6] = ctypes.c_void_p(4096 + 16)
+    assert lib.fa_fwd_host(*a) == -1         # workspace not 256-byte aligned
+    a = list(args); a[7] = 1024
+    assert lib.fa_fwd_host(*a) == -1         # workspace too small
+    a = list(args); a[11] = 96
+    assert lib.fa_fwd_host(*a) == -2         # head dim not built
+
+
 def test_timeout_setter(lib):
     assert lib.fa_set_wait_timeout_ns(0) == -1
     assert lib.fa_set_wait_timeout_ns(2_000_000_000) == 0

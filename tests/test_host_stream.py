@@ -76,3 +76,32 @@ def test_host_streamed_back_to_back_calls_reuse_the_workspace(fa):
             torch.testing.assert_close(a.float(), b.float(), rtol=2 ** -7, atol=1e-4)
         else:
             assert torch.equal(a, b), name
+
+
+FWD_CASES = [
+    # B, H, N, d, causal, block-mask density (None: no block mask)
+    (1, 32, 4096, 128, True, None),       # 16 CTAs a head: chunks of 8, 16, 8 heads
+    (2, 8, 2048, 64, False, 0.4),         # one chunk, block mask
+    (1, 5, 1000, 128, True, None),        # one chunk, ragged N
+]
+
+
+@pytest.mark.parametrize("B,H,N,d,causal,density", FWD_CASES)
+def test_host_streamed_forward_matches_device_call(fa, B, H, N, d, causal, density):
+    t = make_qkvdo(B, H, N, d, seed=N + 3 * H, with_dout=False)
+    scale = 1 / math.sqrt(d)
+    bm = None
+    if density is not None:
+        nb = -(-N // 128)
+        g = torch.Generator().manual_seed(N + 1)
+        m = (torch.rand((nb, nb), generator=g) < density).to(torch.uint8)
+        m.fill_diagonal_(1)
+        bm = m.cuda()
+    host = {n: t[n].pin_memory() for n in ("q", "k", "v")}
+    o_h, lse_h = fa.forward_host(host["q"], host["k"], host["v"], causal=causal, scale=scale, block_mask=bm)
+    torch.cuda.synchronize()
+    assert fa.fa_get_device_error() == 0
+    o, lse = fa.forward(t["q"].cuda(), t["k"].cuda(), t["v"].cuda(), causal=causal, scale=scale, block_mask=bm)
+    torch.cuda.synchronize()
+    assert torch.equal(o_h, o.cpu())
+    assert torch.equal(lse_h, lse.cpu())
