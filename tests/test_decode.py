@@ -58,6 +58,7 @@ CASES = [
     (2, 2, 8, 200, 64, [200, 97], True),
     (1, 4, 6, 4133, 128, None, False),
     (2, 2, 7, 64, 128, [64, 33], True),
+    (64, 64, 2, 96, 64, None, True),           # 4096 (batch, head) pairs, two tiles each
 ]
 
 

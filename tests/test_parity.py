@@ -514,3 +514,24 @@ def test_forward_backward_at_the_index_limit(fa):
         assert _rel_l2(dv[0, h, tail], dvp[tail]) <= GRAD_RTOL, f"index limit head {h}: dV tail"
     del q, k, v, do, o, lse, dq, dk, dv
     torch.cuda.empty_cache()
+
+
+# --------------------------------------------------------------------------- #
+# many short heads: large grids of one-tile problems
+# --------------------------------------------------------------------------- #
+@pytest.mark.parametrize("d,causal", [(64, False), (128, True)])
+def test_many_short_heads(fa, d, causal):
+    B, H, N = 32, 32, 128
+    t = make_qkvdo(B, H, N, d, seed=500 + d)
+    scale = 1 / math.sqrt(d)
+    q, k, v, do = (_dev(t[n]) for n in ("q", "k", "v", "do"))
+    o, lse = fa.forward(q, k, v, causal=causal, scale=scale)
+    dq, dk, dv = fa.backward(q, k, v, o, lse, do, causal=causal, scale=scale)
+    _check_device_status(fa)
+    for b, h in ((0, 0), (13, 7), (31, 31)):
+        sl = (slice(b, b + 1), slice(h, h + 1))
+        f64 = {n: _np64(t[n][sl]) for n in ("q", "k", "v", "do")}
+        ro, rl = oracle.forward(f64["q"], f64["k"], f64["v"], scale, causal=causal)
+        _check_fwd(o[sl], lse[sl], ro, rl, f"B32 H32 N128 d{d} head ({b}, {h})")
+        ref = oracle.backward(f64["q"], f64["k"], f64["v"], f64["do"], scale, causal=causal)[:3]
+        _check_bwd((dq[sl], dk[sl], dv[sl]), ref, f"B32 H32 N128 d{d} head ({b}, {h})")
