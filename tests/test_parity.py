@@ -394,6 +394,38 @@ def test_ragged_sequence_length(fa, B, H, N, d, mask):
     _check_bwd((dq, dk, dv), ref, f"N={N} d={d} {mask}")
 
 
+ODD_TILE_MASKS = [
+    # B, H, N, d, causal, mask seed: random block masks (p = 0.3) with rows of
+    # unequal length, an odd number of query tiles (the last CTA has one),
+    # the causal flag on top of a block mask, ragged N
+    (1, 2, 1152, 128, False, 1152),
+    (1, 2, 1408, 64, True, 1408),
+    (2, 1, 1100, 128, False, 7),
+]
+
+
+@pytest.mark.parametrize("B,H,N,d,causal,seed", ODD_TILE_MASKS)
+def test_block_mask_odd_tile_counts(fa, B, H, N, d, causal, seed):
+    """Random block masks over an odd number of tiles, forward and backward:
+    every element against the oracle."""
+    nb = (N + 127) // 128
+    g = torch.Generator().manual_seed(seed)
+    bm = (torch.rand((nb, nb), generator=g) < 0.3).to(torch.uint8)
+    bm.fill_diagonal_(1)
+    t = make_qkvdo(B, H, N, d, seed=60 + N)
+    scale = 1 / math.sqrt(d)
+    q, k, v, do = (_dev(t[n]) for n in ("q", "k", "v", "do"))
+    bmd = _dev(bm)
+    o, lse = fa.forward(q, k, v, causal=causal, scale=scale, block_mask=bmd)
+    dq, dk, dv = fa.backward(q, k, v, o, lse, do, causal=causal, scale=scale, block_mask=bmd)
+    _check_device_status(fa)
+    f64 = {n: _np64(t[n]) for n in ("q", "k", "v", "do")}
+    ro, rl = oracle.forward(f64["q"], f64["k"], f64["v"], scale, causal=causal, block_mask=bm.numpy())
+    _check_fwd(o, lse, ro, rl, f"N={N} d={d} odd tiles")
+    ref = oracle.backward(f64["q"], f64["k"], f64["v"], f64["do"], scale, causal=causal, block_mask=bm.numpy())[:3]
+    _check_bwd((dq, dk, dv), ref, f"N={N} d={d} odd tiles")
+
+
 def test_ragged_outputs_stay_inside_their_rows(fa):
     """With N not a multiple of 128, nothing is written past row N - 1."""
     B, H, N, d = 1, 2, 200, 128
