@@ -3,7 +3,10 @@
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
 
 One step = fa_fwd then fa_bwd (its three stages) over one batch of the
-workload, inputs resident in HBM.  `value` is algorithmic TFLOPS (forward
+workload, inputs resident in HBM, captured once into a CUDA graph and timed
+as one replay per step (`--eager`: as eager calls); per-kernel times and the
+roofline come from eager calls with CUDA events between the kernels.
+`value` is algorithmic TFLOPS (forward
 4 B H N^2 d, backward 2.5x that, halved for causal; block-sparse counts the
 kept blocks), summed over ranks under torchrun (each rank runs the whole
 workload on its own GPU: weak scaling, no collective on the data path).
@@ -623,6 +626,39 @@ def _run_cuda_fp8(args, w, t, f_fwd, fa, dev, ws, rank):
     return 0
 
 
+def _graph_ms_per_step(args, step, flush, ws, dev):
+    """Capture step() into a CUDA graph and time one replay per step (CUDA
+    events around each replay, the L2 flushed before each, max over ranks)."""
+    import torch
+    import torch.distributed as dist
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        step()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step()
+    for _ in range(args.warmup):
+        flush.zero_()
+        g.replay()
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+    if ws > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    for ev in events:
+        flush.zero_()
+        ev[0].record()
+        g.replay()
+        ev[1].record()
+    torch.cuda.synchronize()
+    if ws > 1:
+        dist.barrier()
+    total = sum(e0.elapsed_time(e1) for e0, e1 in events)
+    return max_over_ranks(total, dev) / args.steps
+
+
 def run_cuda(args):
     import torch
     import torch.distributed as dist
@@ -711,7 +747,6 @@ def run_cuda(args):
     torch.cuda.synchronize()
     if ws > 1:
         dist.barrier()
-    clocks = sampler.stop() if sampler else None
     rc = fa.fa_get_device_error()
     if rc != 0:
         raise RuntimeError(f"device status after timing: {fa.status_string(rc)}")
@@ -727,6 +762,15 @@ def run_cuda(args):
             per["bwd_dq_convert"].append(ev[3].elapsed_time(ev[4]))
     total_ms = max_over_ranks(sum(step_ms), dev)
     ms_per_step = total_ms / args.steps
+    eager_ms_per_step = ms_per_step
+    if not args.eager:
+        # the same step captured once and replayed: no host work between the
+        # kernels, which is what bounds one-tile and other launch-bound shapes
+        ms_per_step = _graph_ms_per_step(args, step, flush, ws, dev)
+        rc = fa.fa_get_device_error()
+        if rc != 0:
+            raise RuntimeError(f"device status after the graph replays: {fa.status_string(rc)}")
+    clocks = sampler.stop() if sampler else None
     value = whole_job_tflops(ws, f_fwd + f_bwd, ms_per_step)
 
     # ---- end to end through the public binding, host buffers ------------- #
@@ -795,7 +839,7 @@ def run_cuda(args):
                 "traffic": _profile_traffic(tag, w.name),
                 "algorithmic_flops_per_launch": algo[dom],
                 "other_peaks": _other_peaks(achieved, peaks, clocks, dev)}
-    kernels = {kname: {"ms": avg[kname], "share": avg[kname] / ms_per_step if ms_per_step else 0.0}
+    kernels = {kname: {"ms": avg[kname], "share": avg[kname] / eager_ms_per_step if eager_ms_per_step else 0.0}
                for kname in avg if per[kname]}
     kernels["fwd"]["tflops"] = f_fwd / (avg["fwd"] * 1e-3) / 1e12
     kernels["fwd"]["frac_of_peak"] = kernels["fwd"]["tflops"] / peak
@@ -808,7 +852,9 @@ def run_cuda(args):
 
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": _config(w, density),
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": _config(w, density, {"launch": "eager calls" if args.eager else
+                                           "cuda graph of the step, one replay per step"}),
             "frac_of_peak": value / ws / peak,
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "ms_per_step": e2e_ms,
@@ -817,6 +863,8 @@ def run_cuda(args):
                              else "pinned copies in, device-resident step, copies out")},
             "gpu_launches": launches_per_step * args.steps, "roofline": roofline, "kernels": kernels,
             "clocks": clocks}
+    if not args.eager:
+        line["eager_ms_per_step"] = eager_ms_per_step
 
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         tf, el, heads = _oracle_sample(w, t, budget_s=args.cpu_budget)
@@ -861,6 +909,9 @@ def main():
     ap.add_argument("--impl", choices=("cuda", "reference"), default="cuda")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle time for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--eager", action="store_true",
+                    help="time the step as eager calls instead of one replay of a CUDA graph of the step "
+                         "(per-kernel times and the roofline are always taken from eager calls)")
     ap.add_argument("--set", default="", metavar="K=V,...",
                     help="override sizes of the workload, e.g. N=2048,H=16 (an ad-hoc shape with its recipe)")
     args = ap.parse_args()
