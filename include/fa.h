@@ -49,13 +49,15 @@
  * fa_set_wait_timeout_ns) records FA_ERR_TIMEOUT in the status word and
  * returns early; its outputs are then undefined.
  *
- * Stream capture: the device-resident compute calls (fa_fwd*, fa_bwd*,
- * fa_decode) enqueue only kernel launches on `stream` -- no allocation, copy
- * or synchronisation -- so they can be captured into a CUDA graph and
- * replayed.  The first call on a device sets up per-device state, so make one
- * call before capturing.  fa_get_device_error synchronises and the
- * host-streamed calls (fa_fwd_bwd_host, fa_fwd_host) use the library's own
- * streams: neither belongs in a capture.
+ * Stream capture: fa_fwd, fa_fwd_blocksparse, fa_fwd_dropout, fa_bwd,
+ * fa_bwd_blocksparse, fa_bwd_dropout, the three backward stages
+ * (fa_bwd_preprocess, fa_bwd_main, fa_bwd_dq_convert) and fa_decode enqueue
+ * only kernel launches on `stream` -- no allocation, copy or
+ * synchronisation -- so they can be captured into a CUDA graph and replayed.
+ * The first call on a device sets up per-device state, so make one call
+ * before capturing.  fa_get_device_error synchronises and the host-streamed
+ * calls (fa_fwd_bwd_host, fa_fwd_host) use the library's own streams:
+ * neither belongs in a capture.
  */
 #ifndef FA_H_
 #define FA_H_
