@@ -30,6 +30,7 @@ std::atomic<uint64_t> g_timeout_ns{2000000000ull};
 struct DeviceState {
   std::once_flag once;
   int arch_ok = 0;      // 1 when compute capability is 10.3
+  int sms = 0;          // multiprocessors
   int* status = nullptr;
   cudaError_t err = cudaSuccess;
 };
@@ -57,6 +58,7 @@ int device_ready(int** status_out) {
     st.err = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
     if (st.err == cudaSuccess) st.err = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
     st.arch_ok = (major == 10 && minor == 3) ? 1 : 0;
+    if (st.err == cudaSuccess) st.err = cudaDeviceGetAttribute(&st.sms, cudaDevAttrMultiProcessorCount, dev);
     if (st.err == cudaSuccess && st.arch_ok) {
       void* a = nullptr;
       st.err = cudaGetSymbolAddress(&a, g_fa_status);
@@ -67,6 +69,13 @@ int device_ready(int** status_out) {
   if (!st.arch_ok) return FA_ERR_ARCH;
   *status_out = st.status;
   return FA_OK;
+}
+
+// Multiprocessors of the current device (after device_ready succeeded).
+int device_sms() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 1;
+  return g_dev[dev].sms > 0 ? g_dev[dev].sms : 1;
 }
 
 int encoder_ready() {
@@ -247,8 +256,9 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, c
   p.mask_kind = mask_kind;
   p.H = H;
   p.drop = make_dropout(dropout_p, seed);
+  p.max_ctas = device_sms();
   if (log_enabled())
-    std::fprintf(stderr, "[fa] fwd B=%d H=%d N=%d d=%d mask=%d grid=%d\n", B, H, N, d, mask_kind, p.n_pairs * BH);
+    std::fprintf(stderr, "[fa] fwd B=%d H=%d N=%d d=%d mask=%d items=%d\n", B, H, N, d, mask_kind, p.n_pairs * BH);
   return fa::launch_fwd(p, d, reinterpret_cast<cudaStream_t>(stream));
 }
 

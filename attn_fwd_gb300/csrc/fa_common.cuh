@@ -52,6 +52,7 @@ struct FwdParams {
   int mask_kind;
   int H;                     // heads: (b, h) = divmod(bh, H) keys the dropout generator
   Dropout drop;
+  int max_ctas;              // persistent grid size for dense and causal masks (one CTA per SM)
 };
 
 // Backward main-kernel parameters.  Q and dO use a {64, BQ, 1} box, K and V a

@@ -59,7 +59,8 @@ struct FwdLayout {
   static constexpr int B_P = B_S + 2;            // 2
   static constexpr int B_O = B_P + 2;            // 2
   static constexpr int B_DONE = B_O + 2;         // 1
-  static constexpr int NBARS = B_DONE + 1;
+  static constexpr int B_QFREE = B_DONE + 1;     // 1: an item's S products done, Q may be reloaded
+  static constexpr int NBARS = B_QFREE + 1;
   // block-sparse: one bit per key tile for each of the two query tiles, and
   // the two counts
   static constexpr int BITS_OFF = BAR_OFF + NBARS * 8 + 16;
@@ -241,16 +242,47 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
 
   const uint32_t warp = warp_id();
   const uint32_t lane = lane_id();
-  const int bh = blockIdx.x % p.BH;
-  int pair = blockIdx.x / p.BH;
-  if (p.mask_kind & MASK_CAUSAL) pair = p.n_pairs - 1 - pair;  // longest rows first
-  const int qt0 = 2 * pair;
-  const int qt1 = 2 * pair + 1;
-  const int kt_end = (p.mask_kind == MASK_CAUSAL) ? min(qt1, p.n_qt - 1) + 1 : p.n_qt;
+  // Work items: the query-tile pairs j = 0 .. n_items - 1 of all (batch,
+  // head)s, head fastest, pairs in decreasing length when causal.  The grid
+  // is persistent for dense and causal masks (at most one CTA per SM): CTA c
+  // takes items c, 2G - 1 - c, 2G + c, ... (G CTAs), so the long and short
+  // causal pairs even out; one item per CTA with a block mask.
+  const int n_items = p.n_pairs * p.BH;
+  auto item_index = [&](int k) {
+    const int G = static_cast<int>(gridDim.x), c = static_cast<int>(blockIdx.x);
+    const int j = k * G + ((k & 1) ? G - 1 - c : c);
+    return (SPARSE && k > 0) || j >= n_items ? -1 : j;
+  };
   uint32_t* bits = reinterpret_cast<uint32_t*>(smem + L::BITS_OFF);   // [2][BITS_WORDS], then 2 counts
   int* bit_counts = reinterpret_cast<int*>(bits + 2 * L::BITS_WORDS);
+  // item j: (batch, head) bh, query tiles qt0 and qt1 = qt0 + 1, the key-tile
+  // range of the dense schedule, visible key tiles per query tile (a block
+  // mask's bits describe this CTA's single item)
+  struct Item {
+    int bh, qt0, qt1, kt_end, nv0, nv1;
+  };
+  auto item_info = [&](int j) {
+    Item it;
+    it.bh = j % p.BH;
+    int pair = j / p.BH;
+    if (p.mask_kind & MASK_CAUSAL) pair = p.n_pairs - 1 - pair;  // longest rows first
+    it.qt0 = 2 * pair;
+    it.qt1 = 2 * pair + 1;
+    it.kt_end = (p.mask_kind == MASK_CAUSAL) ? min(it.qt1, p.n_qt - 1) + 1 : p.n_qt;
+    if constexpr (SPARSE) {
+      it.nv0 = bit_counts[0];
+      it.nv1 = bit_counts[1];
+    } else {
+      it.nv0 = it.qt0 < p.n_qt ? (p.mask_kind == MASK_CAUSAL ? it.qt0 + 1 : p.n_qt) : 0;
+      it.nv1 = it.qt1 < p.n_qt ? (p.mask_kind == MASK_CAUSAL ? it.qt1 + 1 : p.n_qt) : 0;
+    }
+    return it;
+  };
   if constexpr (SPARSE) {
-    if (warp < 2) build_sparse_bits(p, warp == 0 ? qt0 : qt1, bits + warp * L::BITS_WORDS, bit_counts + warp, lane);
+    const int pair0 = (p.mask_kind & MASK_CAUSAL) ? p.n_pairs - 1 - static_cast<int>(blockIdx.x) / p.BH
+                                                  : static_cast<int>(blockIdx.x) / p.BH;
+    if (warp < 2) build_sparse_bits(p, 2 * pair0 + static_cast<int>(warp), bits + warp * L::BITS_WORDS,
+                                    bit_counts + warp, lane);
   }
 
   if (threadIdx.x == 0) {
@@ -266,6 +298,7 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
       mbar_init(bar(L::B_O + w), 1);
     }
     mbar_init(bar(L::B_DONE), 1);
+    mbar_init(bar(L::B_QFREE), 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -278,18 +311,8 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const WaitCtx wc{abort_flag, p.status, p.timeout_ns};
-  // key tiles visited by each query tile
-  int nv0, nv1;
-  if constexpr (SPARSE) {
-    nv0 = bit_counts[0];
-    nv1 = bit_counts[1];
-  } else {
-    nv0 = qt0 < p.n_qt ? (p.mask_kind == MASK_CAUSAL ? qt0 + 1 : p.n_qt) : 0;
-    nv1 = qt1 < p.n_qt ? (p.mask_kind == MASK_CAUSAL ? qt1 + 1 : p.n_qt) : 0;
-  }
   const uint32_t* bits0 = bits;
   const uint32_t* bits1 = bits + L::BITS_WORDS;
-  const int rounds = nv0 > nv1 ? nv0 : nv1;
   // Block-sparse: round r pairs key tile a_r of query tile 0 with b_r of tile
   // 1 (-1 when a tile has none), in the order of SparseRounds.  The producer
   // loads, per round, K(a) K(b) V(a) V(b) into consecutive ring slots, once
@@ -303,19 +326,30 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
       prefetch_tmap(&p.tm_v);
       const uint64_t pol_q = l2_policy_evict_first();
       const uint64_t pol_kv = l2_policy_evict_last();
-      for (int w = 0; w < 2; ++w) {
-        const int qt = qt0 + w;
-        if (qt >= p.n_qt) continue;
-        mbar_arrive_expect_tx(bar(L::B_Q + w), L::TILE_BYTES);
-        for (int c = 0; c < L::NCH; ++c)
-          tma_load_3d(sbase + L::Q_OFF + w * L::TILE_BYTES + c * L::CHUNK_BYTES, &p.tm_q,
-                      bar(L::B_Q + w), c * 64, qt * TILE, bh, pol_q);
-      }
       int slot = 0;
       uint32_t phase = 0;
       uint32_t issued[L::STAGES];
       for (int s = 0; s < L::STAGES; ++s) issued[s] = 0;
       bool ok = true;
+      for (int k = 0; ok; ++k) {
+      const int j = item_index(k);
+      if (j < 0) break;
+      const Item it = item_info(j);
+      const int bh = it.bh, qt0 = it.qt0, qt1 = it.qt1, kt_end = it.kt_end;
+      const int rounds = it.nv0 > it.nv1 ? it.nv0 : it.nv1;
+      // the Q buffers are free once the previous item's S products are done
+      if (k > 0 && !(ok = mbar_wait(bar(L::B_QFREE), (k - 1) & 1, wc))) break;
+      for (int w = 0; w < 2; ++w) {
+        const int qt = qt0 + w;
+        if (qt >= p.n_qt) {              // no such tile: complete the phase empty
+          mbar_arrive(bar(L::B_Q + w));
+          continue;
+        }
+        mbar_arrive_expect_tx(bar(L::B_Q + w), L::TILE_BYTES);
+        for (int c = 0; c < L::NCH; ++c)
+          tma_load_3d(sbase + L::Q_OFF + w * L::TILE_BYTES + c * L::CHUNK_BYTES, &p.tm_q,
+                      bar(L::B_Q + w), c * 64, qt * TILE, bh, pol_q);
+      }
       if constexpr (!SPARSE) {
       for (int kt = 0; kt < kt_end && ok; ++kt) {
         if (!(dense_visible(p, qt0, kt) || dense_visible(p, qt1, kt))) continue;
@@ -360,6 +394,8 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
         pb = b;
       }
       }
+      if constexpr (SPARSE) break;       // one item per CTA
+      }
       if (!ok) {  // let copies already in flight land before the CTA exits
         for (int s = 0; s < L::STAGES; ++s)
           if (issued[s]) mbar_drain(bar(L::B_FULL + s), (issued[s] - 1) & 1u, 100000000ull);
@@ -373,8 +409,6 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
     constexpr uint32_t IDESC_S = idesc_bf16(128, 128, false, false);
     constexpr uint32_t IDESC_O = idesc_bf16(128, D, false, true);
     bool ok = true;
-    if (nv0 > 0) ok = mbar_wait_warp(bar(L::B_Q + 0), 0, wc);
-    if (ok && nv1 > 0) ok = mbar_wait_warp(bar(L::B_Q + 1), 0, wc);
     const uint64_t dq0 = sdesc_sw128(sbase + L::Q_OFF, 16, 1024);                 // Q tile 0, K-major
     const uint64_t dq1 = sdesc_sw128(sbase + L::Q_OFF + L::TILE_BYTES, 16, 1024);  // Q tile 1
     const uint64_t dk_ring = sdesc_sw128(sbase + L::RING_OFF, 16, 1024);           // ring slot 0 as K (K-major)
@@ -405,6 +439,18 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
     int slot = 0;
     uint32_t phase = 0;
     uint32_t pph0 = 0, pph1 = 0;       // phases of the P barriers
+    for (int k = 0; ok; ++k) {
+    const int j = item_index(k);
+    if (j < 0) break;
+    const Item it = item_info(j);
+    const int qt0 = it.qt0, qt1 = it.qt1, kt_end = it.kt_end, nv0 = it.nv0, nv1 = it.nv1;
+    // Q of both tiles (a missing tile's phase completes empty).  The first
+    // S of this item overwrites the P that the previous item's last P V
+    // reads: issued after it, it runs after it.  Its first P V waits for P
+    // of this item, which its softmax warps publish only after they have
+    // read out the previous item's O.
+    if (!(ok = mbar_wait_warp(bar(L::B_Q + 0), k & 1, wc))) break;
+    if (!(ok = mbar_wait_warp(bar(L::B_Q + 1), k & 1, wc))) break;
     int done0 = 0, done1 = 0;          // PV products issued per tile
     bool has_prev = false, pf0 = false, pf1 = false;
     int pvslot = 0;
@@ -457,10 +503,12 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
       pvslot = vslot;
       pvphase = vphase;
     }
+    if (ok) mma_commit_elect(bar(L::B_QFREE));   // all S of this item issued: Q may be reloaded
     if (ok && has_prev) {
       ok = mbar_wait_warp(bar(L::B_FULL + pvslot), pvphase, wc);
       if (ok && pf0) {
         ok = mbar_wait_warp(bar(L::B_P + 0), pph0, wc);
+        pph0 ^= 1u;                      // the phases continue into the next item
         if (ok) {
           tc_fence_after();
           issue_pv(L::O_COL0, L::S_COL0, pvslot, done0 > 0);
@@ -469,6 +517,7 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
       }
       if (ok && pf1) {
         ok = mbar_wait_warp(bar(L::B_P + 1), pph1, wc);
+        pph1 ^= 1u;
         if (ok) {
           tc_fence_after();
           issue_pv(L::O_COL1, L::S_COL1, pvslot, done1 > 0);
@@ -477,7 +526,13 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
       }
       if (ok) mma_commit_elect(bar(L::B_EMPTY + pvslot));
     }
+    }
     } else {
+    const Item it = item_info(static_cast<int>(blockIdx.x));
+    const int nv0 = it.nv0, nv1 = it.nv1;
+    const int rounds = nv0 > nv1 ? nv0 : nv1;
+    if (nv0 > 0) ok = mbar_wait_warp(bar(L::B_Q + 0), 0, wc);
+    if (ok && nv1 > 0) ok = mbar_wait_warp(bar(L::B_Q + 1), 0, wc);
     // Ring slots in load order (the producer's sequence): the n-th tile
     // loaded sits in slot n % STAGES, and its fill barrier completes for the
     // (n / STAGES)-th time.  Each slot is released right after the MMAs that
@@ -545,7 +600,15 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
     // ------------------------------------------------------------ softmax
     const int w = static_cast<int>(warp >> 2);
     const uint32_t quarter = warp & 3u;
-    const int qt = qt0 + w;
+    uint32_t sphase = 0;   // phase of this tile's S barrier, continued across items
+    int n_out = 0;         // items whose O this group has read (phase of its O barrier)
+    bool ok = true;
+    for (int k = 0; ok; ++k) {
+    const int j = item_index(k);
+    if (j < 0) break;
+    const Item it = item_info(j);
+    const int bh = it.bh, nv0 = it.nv0, nv1 = it.nv1;
+    const int qt = it.qt0 + w;
     if (qt < p.n_qt) {
       const int row = static_cast<int>(quarter * 32 + lane);      // row in tile == TMEM lane
       const uint32_t s_addr = tmem_addr(tmem, quarter * 32, w ? L::S_COL1 : L::S_COL0);
@@ -555,8 +618,6 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
       float l = 0.f;    // row sum of exp2(S - m), fp32
       float lr = 0.f;   // the same sum over the bf16-rounded values used in P V
       bool has_o = false;
-      bool ok = true;
-      uint32_t sphase = 0;
       const int n_vis = w ? nv1 : nv0;
       // Only the highest visible key tile can need a per-element mask: the
       // causal diagonal and the ragged tile holding key N-1.  Keys at or past
@@ -680,7 +741,8 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
         const size_t grow = static_cast<size_t>(bh) * p.N + static_cast<size_t>(qt) * TILE + row;
         __nv_bfloat16* orow = p.o + grow * D;
         if (n_vis > 0) {
-          ok = mbar_wait_warp(bar(L::B_O + w), 0, wc);
+          ok = mbar_wait_warp(bar(L::B_O + w), n_out & 1, wc);
+          ++n_out;
           if (ok) {
             tc_fence_after();
             const float inv_l = DROP ? p.drop.scale / lr : 1.f / lr;
@@ -710,6 +772,8 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
         }
       }
     }
+    if constexpr (SPARSE) break;         // one item per CTA
+    }
   }
 
   tc_fence_before();
@@ -726,8 +790,9 @@ static int launch_fwd_t(const FwdParams& p, cudaStream_t stream) {
   static_assert(L::SMEM_BYTES <= 232448, "shared memory budget");
   static SmemAttrOnce attr;
   if (!attr.ensure(reinterpret_cast<const void*>(fa_fwd_kernel<D, SPARSE, DROP>), L::SMEM_BYTES)) return -4;
-  const unsigned grid = static_cast<unsigned>(p.n_pairs) * static_cast<unsigned>(p.BH);
-  fa_fwd_kernel<D, SPARSE, DROP><<<grid, L::THREADS, L::SMEM_BYTES, stream>>>(p);
+  const long long items = static_cast<long long>(p.n_pairs) * p.BH;
+  const long long grid = SPARSE ? items : (items < p.max_ctas ? items : p.max_ctas);
+  fa_fwd_kernel<D, SPARSE, DROP><<<static_cast<unsigned>(grid), L::THREADS, L::SMEM_BYTES, stream>>>(p);
   return cudaGetLastError() == cudaSuccess ? 0 : -4;
 }
 
