@@ -198,6 +198,34 @@ def test_forward_workload_sampled_heads(fa, name):
         _check_fwd(o[sl], lse[sl], ro, rl, f"{name} head {hh}")
 
 
+PERSISTENT = [
+    # B, H, N, d, causal: more query-tile pairs than SMs, so the forward's
+    # persistent CTAs each walk several; ragged N, and an odd tile count whose
+    # last pair of every head has one tile (its Q phase completes empty)
+    (2, 16, 2000, 128, True),
+    (4, 16, 1100, 64, False),
+    (8, 8, 1100, 128, True),
+]
+
+
+@pytest.mark.parametrize("B,H,N,d,causal", PERSISTENT)
+def test_forward_persistent_items(fa, B, H, N, d, causal):
+    """Every (batch, head) of a multi-item persistent launch written once and
+    right: all heads finite, sampled heads element by element."""
+    n_items = (N + 255) // 256 * B * H
+    assert n_items > 152
+    t = make_qkvdo(B, H, N, d, seed=80 + N, with_dout=False)
+    scale = 1 / math.sqrt(d)
+    o, lse = fa.forward(_dev(t["q"]), _dev(t["k"]), _dev(t["v"]), causal=causal, scale=scale)
+    _check_device_status(fa)
+    assert torch.isfinite(o).all() and torch.isfinite(lse).all()
+    for hh in sorted(set([0, B * H - 1] + _sampled_heads(B * H, 3, seed=N))):
+        b, h = divmod(hh, H)
+        sl = (slice(b, b + 1), slice(h, h + 1))
+        ro, rl = oracle.forward(_np64(t["q"][sl]), _np64(t["k"][sl]), _np64(t["v"][sl]), scale, causal=causal)
+        _check_fwd(o[sl], lse[sl], ro, rl, f"B{B} H{H} N{N} d{d} head {hh}")
+
+
 def test_forward_workload_long_causal_sampled_rows(fa):
     """N=16384 causal with x3 inputs: S would be 16 GiB; check sampled rows of
     sampled heads, including the first and last rows of the sequence."""
