@@ -56,8 +56,9 @@ struct FwdLayout {
   static constexpr int B_FULL = 2;               // STAGES
   static constexpr int B_EMPTY = 2 + STAGES;     // STAGES
   static constexpr int B_S = 2 + 2 * STAGES;     // 2
-  static constexpr int B_P = B_S + 2;            // 2
-  static constexpr int B_O = B_P + 2;            // 2
+  static constexpr int B_P = B_S + 2;            // 2: all of P_w in tensor memory
+  static constexpr int B_PH = B_P + 2;           // 2: its first half (keys 0-63)
+  static constexpr int B_O = B_PH + 2;           // 2
   static constexpr int B_DONE = B_O + 2;         // 1
   static constexpr int B_QFREE = B_DONE + 1;     // 1: an item's S products done, Q may be reloaded
   static constexpr int NBARS = B_QFREE + 1;
@@ -295,6 +296,7 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
     for (int w = 0; w < 2; ++w) {
       mbar_init(bar(L::B_S + w), 1);
       mbar_init(bar(L::B_P + w), 4);      // the four warps of softmax group w
+      mbar_init(bar(L::B_PH + w), 4);
       mbar_init(bar(L::B_O + w), 1);
     }
     mbar_init(bar(L::B_DONE), 1);
@@ -428,11 +430,33 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
     // O_w += P_w V: 128/16 k-steps; P from tensor memory (8 columns of bf16
     // pairs per step), V MN-major (16 key rows of 128 bytes per step; the
     // second 64-column half of d sits 16 KB further).
-    auto issue_pv = [&](uint32_t ocol, uint32_t scol, int vslot, bool started) {
+    auto issue_pv_half = [&](uint32_t ocol, uint32_t scol, int vslot, bool started, int k0) {
       const uint64_t dv = dv_ring + static_cast<uint64_t>(vslot) * SLOT16;
 #pragma unroll
-      for (int k = 0; k < TILE / 16; ++k)
+      for (int kk = 0; kk < TILE / 32; ++kk) {
+        const int k = k0 + kk;
         mma_ts_elect(tmem + ocol, tmem + scol + 8 * k, dv + ((k * 2048) >> 4), IDESC_O, (started || k > 0) ? 1u : 0u);
+      }
+    };
+    // P_w V.  With dropout (the softmax warps' share of the round is
+    // largest there) the first half (keys 0-63) is issued once the softmax
+    // warps have published that half of P and the rest once all of P is in;
+    // both barriers complete once per tile, so one phase bit serves both.
+    // Without dropout all of it waits for all of P (splitting measured
+    // neutral with a dense mask and slower with block masks).
+    auto pv = [&](int w, uint32_t& ph, int vslot, bool started) {
+      const uint32_t ocol = w ? L::O_COL1 : L::O_COL0, scol = w ? L::S_COL1 : L::S_COL0;
+      if constexpr (DROP) {
+        if (!mbar_wait_warp(bar(L::B_PH + w), ph, wc)) return false;
+        tc_fence_after();
+        issue_pv_half(ocol, scol, vslot, started, 0);
+      }
+      if (!mbar_wait_warp(bar(L::B_P + w), ph, wc)) return false;
+      tc_fence_after();
+      if constexpr (!DROP) issue_pv_half(ocol, scol, vslot, started, 0);
+      issue_pv_half(ocol, scol, vslot, started, TILE / 32);
+      ph ^= 1u;
+      return true;
     };
 
     if constexpr (!SPARSE) {
@@ -473,10 +497,7 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
       }
       // tile 0: PV(prev), then S(this)
       if (has_prev && pf0) {
-        if (!(ok = mbar_wait_warp(bar(L::B_P + 0), pph0, wc))) break;
-        pph0 ^= 1u;
-        tc_fence_after();
-        issue_pv(L::O_COL0, L::S_COL0, pvslot, done0 > 0);
+        if (!(ok = pv(0, pph0, pvslot, done0 > 0))) break;
         if (++done0 == nv0) mma_commit_elect(bar(L::B_O + 0));
       }
       if (f0) {
@@ -485,10 +506,7 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
       }
       // tile 1
       if (has_prev && pf1) {
-        if (!(ok = mbar_wait_warp(bar(L::B_P + 1), pph1, wc))) break;
-        pph1 ^= 1u;
-        tc_fence_after();
-        issue_pv(L::O_COL1, L::S_COL1, pvslot, done1 > 0);
+        if (!(ok = pv(1, pph1, pvslot, done1 > 0))) break;
         if (++done1 == nv1) mma_commit_elect(bar(L::B_O + 1));
       }
       if (f1) {
@@ -507,22 +525,12 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
     if (ok && has_prev) {
       ok = mbar_wait_warp(bar(L::B_FULL + pvslot), pvphase, wc);
       if (ok && pf0) {
-        ok = mbar_wait_warp(bar(L::B_P + 0), pph0, wc);
-        pph0 ^= 1u;                      // the phases continue into the next item
-        if (ok) {
-          tc_fence_after();
-          issue_pv(L::O_COL0, L::S_COL0, pvslot, done0 > 0);
-          mma_commit_elect(bar(L::B_O + 0));
-        }
+        ok = pv(0, pph0, pvslot, done0 > 0);   // (the phases continue into the next item)
+        if (ok) mma_commit_elect(bar(L::B_O + 0));
       }
       if (ok && pf1) {
-        ok = mbar_wait_warp(bar(L::B_P + 1), pph1, wc);
-        pph1 ^= 1u;
-        if (ok) {
-          tc_fence_after();
-          issue_pv(L::O_COL1, L::S_COL1, pvslot, done1 > 0);
-          mma_commit_elect(bar(L::B_O + 1));
-        }
+        ok = pv(1, pph1, pvslot, done1 > 0);
+        if (ok) mma_commit_elect(bar(L::B_O + 1));
       }
       if (ok) mma_commit_elect(bar(L::B_EMPTY + pvslot));
     }
@@ -557,10 +565,7 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
       // tile 0: PV of the previous round, then S of this round
       if (pa >= 0) {
         if (!(ok = ready(nva))) break;
-        if (!(ok = mbar_wait_warp(bar(L::B_P + 0), pph0, wc))) break;
-        pph0 ^= 1u;
-        tc_fence_after();
-        issue_pv(L::O_COL0, L::S_COL0, slot_of(nva), done0 > 0);
+        if (!(ok = pv(0, pph0, slot_of(nva), done0 > 0))) break;
         if (++done0 == nv0) mma_commit_elect(bar(L::B_O + 0));
         if (!vshared) mma_commit_elect(bar(L::B_EMPTY + slot_of(nva)));
       }
@@ -574,10 +579,7 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
       // tile 1
       if (pb >= 0) {
         if (!vshared && !(ok = ready(nvb))) break;
-        if (!(ok = mbar_wait_warp(bar(L::B_P + 1), pph1, wc))) break;
-        pph1 ^= 1u;
-        tc_fence_after();
-        issue_pv(L::O_COL1, L::S_COL1, slot_of(nvb), done1 > 0);
+        if (!(ok = pv(1, pph1, slot_of(nvb), done1 > 0))) break;
         if (++done1 == nv1) mma_commit_elect(bar(L::B_O + 1));
         mma_commit_elect(bar(L::B_EMPTY + slot_of(nvb)));
       }
@@ -688,6 +690,19 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
         // bf16-rounded values that P V multiplies, so O / lr weighs the V rows
         // with weights summing to exactly one.  Dropout zeroes the dropped
         // pairs of the P V operand only: l and lr are the softmax's own sums.
+        if (DROP && has_o && __any_sync(0xffffffffu, need)) {
+          // With dropout, O is rescaled before any of this tile's P is
+          // published (the P V halves accumulate onto it).  O may be read
+          // here: S(j) completing implies the previous P V is done.
+#pragma unroll 1
+          for (int c = 0; c < D; c += 16) {   // 16 columns at a time: S is live in registers here
+            uint32_t ov[16];
+            tmem_ld_x16(o_addr + c, ov);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
+            tmem_st_x16(o_addr + c, ov);
+          }
+        }
         const float2 sl2v = make_float2(sl2, sl2);
         const float2 negm = make_float2(-m, -m);
         float2 la = make_float2(0.f, 0.f), lb = la, ra = la, rb = la;
@@ -713,11 +728,19 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
               pk[e] = pku;
             }
           }
+          if (DROP && q == 2) {
+            // keys 0-63 of P are stored: publish that half (the stores of
+            // chunks 0 and 1 completed while chunk 2 was computed)
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(L::B_PH + w));
+          }
           tmem_st_x16_async(s_addr + 16 * q, pk);
         }
         l = l * alpha + ((la.x + la.y) + (lb.x + lb.y));
         lr = lr * alpha + ((ra.x + ra.y) + (rb.x + rb.y));
-        if (has_o && __any_sync(0xffffffffu, need)) {
+        if (!DROP && has_o && __any_sync(0xffffffffu, need)) {
           // O may be read here: S(j) completing implies the previous PV is done.
 #pragma unroll 1
           for (int c = 0; c < D; c += 32) {
