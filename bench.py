@@ -486,12 +486,14 @@ def run_cuda_decode(args, w):
     torch.cuda.synchronize()
     if ws > 1:
         dist.barrier()
+    step_ms = [e[0].elapsed_time(e[1]) for e in events]
+    eager_ms = max_over_ranks(sum(step_ms), dev) / args.steps
+    # the step (split kernel + chunk merge) as one CUDA-graph replay, unless --eager
+    ms_per_step = eager_ms if args.eager else _graph_ms_per_step(args, step, flush, ws, dev)
     clocks = sampler.stop() if sampler else None
     rc = fa.fa_get_device_error()
     if rc != 0:
         raise RuntimeError(f"device status after timing: {fa.status_string(rc)}")
-    step_ms = [e[0].elapsed_time(e[1]) for e in events]
-    ms_per_step = max_over_ranks(sum(step_ms), dev) / args.steps
     value = whole_job_tflops(ws, flops, ms_per_step)
 
     # end to end: the new query tokens in from pinned host memory, O and LSE back
@@ -520,7 +522,10 @@ def run_cuda_decode(args, w):
                 "note": "split kernel and chunk merge timed together (one step)"}
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": _decode_config(w),
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {**_decode_config(w), "launch": "eager calls" if args.eager else
+                       "cuda graph of the step, one replay per step"},
+            "eager_ms_per_step": eager_ms,
             "e2e": {"value": whole_job_tflops(ws, flops, e2e_ms), "unit": UNIT,
                     "h2d_bytes_per_step": hq.numel() * hq.element_size(),
                     "d2h_bytes_per_step": ho.numel() * ho.element_size() + hl.numel() * hl.element_size(),
@@ -578,10 +583,12 @@ def _run_cuda_fp8(args, w, t, f_fwd, fa, dev, ws, rank):
     torch.cuda.synchronize()
     if ws > 1:
         dist.barrier()
+    eager_ms = max_over_ranks(sum(e[0].elapsed_time(e[1]) for e in events), dev) / args.steps
+    # the step (V transpose + forward) as one CUDA-graph replay, unless --eager
+    ms_per_step = eager_ms if args.eager else _graph_ms_per_step(args, step, flush, ws, dev)
     clocks = sampler.stop() if sampler else None
     if fa.fa_get_device_error() != 0:
         raise RuntimeError("device status after timing")
-    ms_per_step = max_over_ranks(sum(e[0].elapsed_time(e[1]) for e in events), dev) / args.steps
     value = whole_job_tflops(ws, f_fwd, ms_per_step)
     host_in = {n: t[n].pin_memory() for n in d8}
     ho, hl = torch.empty(o.shape, dtype=o.dtype).pin_memory(), torch.empty(lse.shape).pin_memory()
@@ -609,7 +616,9 @@ def _run_cuda_fp8(args, w, t, f_fwd, fa, dev, ws, rank):
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "e4m3", "data": "synthetic", "config": {**_config(w, None), "inputs":
-            f"N(0,1) seed {w.seed}, e4m3 with per-(batch, head) descale amax/448"},
+            f"N(0,1) seed {w.seed}, e4m3 with per-(batch, head) descale amax/448",
+            "launch": "eager calls" if args.eager else "cuda graph of the step, one replay per step"},
+            "eager_ms_per_step": eager_ms,
             "e2e": {"value": whole_job_tflops(ws, f_fwd, e2e_ms), "unit": UNIT,
                     "h2d_bytes_per_step": sum(x.numel() * x.element_size() for x in host_in.values()),
                     "d2h_bytes_per_step": ho.numel() * ho.element_size() + hl.numel() * hl.element_size(),
