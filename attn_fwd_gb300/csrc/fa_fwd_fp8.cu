@@ -44,7 +44,8 @@ struct Fp8Layout {
   static constexpr int B_P = B_S + 2;            // 2
   static constexpr int B_O = B_P + 2;            // 2
   static constexpr int B_DONE = B_O + 2;         // 1
-  static constexpr int NBARS = B_DONE + 1;
+  static constexpr int B_QFREE = B_DONE + 1;     // 1: an item's S products done, Q may be reloaded
+  static constexpr int NBARS = B_QFREE + 1;
   static constexpr int SMEM_BYTES = BAR_OFF + NBARS * 8 + 16 + 1024;
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t S_COL0 = 0, S_COL1 = 128;
@@ -77,12 +78,31 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_fp8_kernel(const __grid_constan
 
   const uint32_t warp = warp_id();
   const uint32_t lane = lane_id();
-  const int bh = blockIdx.x % p.BH;
-  int pair = blockIdx.x / p.BH;
-  if (p.causal) pair = p.n_pairs - 1 - pair;               // longest rows first
-  const int qt0 = 2 * pair;
-  const int qt1 = 2 * pair + 1;
-  const int kt_end = p.causal ? min(qt1, p.n_qt - 1) + 1 : p.n_qt;
+  // Work items: query-tile pairs j of all (batch, head)s, head fastest,
+  // longest causal rows first; a persistent grid (at most one CTA per SM)
+  // where CTA c takes items c, 2G - 1 - c, 2G + c, ... (G CTAs), as in the
+  // bf16 forward.
+  const int n_items = p.n_pairs * p.BH;
+  auto item_index = [&](int k) {
+    const int G = static_cast<int>(gridDim.x), c = static_cast<int>(blockIdx.x);
+    const int j = k * G + ((k & 1) ? G - 1 - c : c);
+    return j < n_items ? j : -1;
+  };
+  struct Item {
+    int bh, qt0, qt1, kt_end, nv0, nv1;
+  };
+  auto item_info = [&](int j) {
+    Item it;
+    it.bh = j % p.BH;
+    int pair = j / p.BH;
+    if (p.causal) pair = p.n_pairs - 1 - pair;             // longest rows first
+    it.qt0 = 2 * pair;
+    it.qt1 = 2 * pair + 1;
+    it.kt_end = p.causal ? min(it.qt1, p.n_qt - 1) + 1 : p.n_qt;
+    it.nv0 = it.qt0 < p.n_qt ? (p.causal ? it.qt0 + 1 : p.n_qt) : 0;
+    it.nv1 = it.qt1 < p.n_qt ? (p.causal ? it.qt1 + 1 : p.n_qt) : 0;
+    return it;
+  };
 
   if (threadIdx.x == 0) {
     mbar_init(bar(L::B_Q + 0), 1);
@@ -97,6 +117,7 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_fp8_kernel(const __grid_constan
       mbar_init(bar(L::B_O + w), 1);
     }
     mbar_init(bar(L::B_DONE), 1);
+    mbar_init(bar(L::B_QFREE), 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -109,8 +130,6 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_fp8_kernel(const __grid_constan
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const WaitCtx wc{abort_flag, p.status, p.timeout_ns};
-  const int nv0 = qt0 < p.n_qt ? (p.causal ? qt0 + 1 : p.n_qt) : 0;
-  const int nv1 = qt1 < p.n_qt ? (p.causal ? qt1 + 1 : p.n_qt) : 0;
   auto visible = [&](int qt, int kt) { return qt < p.n_qt && (!p.causal || kt <= qt); };
 
   if (warp == 9) {
@@ -121,16 +140,26 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_fp8_kernel(const __grid_constan
       prefetch_tmap(&p.tm_vt);
       const uint64_t pol_q = l2_policy_evict_first();
       const uint64_t pol_kv = l2_policy_evict_last();
-      for (int w = 0; w < 2; ++w) {
-        const int qt = qt0 + w;
-        if (qt >= p.n_qt) continue;
-        mbar_arrive_expect_tx(bar(L::B_Q + w), L::TILE_BYTES);
-        tma_load_3d(sbase + L::Q_OFF + w * L::TILE_BYTES, &p.tm_q, bar(L::B_Q + w), 0, qt * TILE, bh, pol_q);
-      }
       int slot = 0;
       uint32_t phase = 0;
       uint32_t issued[L::STAGES] = {};
       bool ok = true;
+      for (int k = 0; ok; ++k) {
+      const int j = item_index(k);
+      if (j < 0) break;
+      const Item it = item_info(j);
+      const int bh = it.bh, qt0 = it.qt0, qt1 = it.qt1, kt_end = it.kt_end;
+      // the Q buffers are free once the previous item's S products are done
+      if (k > 0 && !(ok = mbar_wait(bar(L::B_QFREE), (k - 1) & 1, wc))) break;
+      for (int w = 0; w < 2; ++w) {
+        const int qt = qt0 + w;
+        if (qt >= p.n_qt) {              // no such tile: complete the phase empty
+          mbar_arrive(bar(L::B_Q + w));
+          continue;
+        }
+        mbar_arrive_expect_tx(bar(L::B_Q + w), L::TILE_BYTES);
+        tma_load_3d(sbase + L::Q_OFF + w * L::TILE_BYTES, &p.tm_q, bar(L::B_Q + w), 0, qt * TILE, bh, pol_q);
+      }
       for (int kt = 0; kt < kt_end && ok; ++kt) {
         if (!(visible(qt0, kt) || visible(qt1, kt))) continue;
         for (int which = 0; which < 2; ++which) {          // K_j, then V_j^T
@@ -146,6 +175,7 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_fp8_kernel(const __grid_constan
           if (++slot == L::STAGES) { slot = 0; phase ^= 1u; }
         }
       }
+      }
       if (!ok) {
         for (int s = 0; s < L::STAGES; ++s)
           if (issued[s]) fp8_drain(bar(L::B_FULL + s), (issued[s] - 1) & 1u, 100000000ull);
@@ -155,8 +185,6 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_fp8_kernel(const __grid_constan
     // ------------------------------------------------------------ MMA issuer
     constexpr uint32_t IDESC = idesc_e4m3(128, 128);
     bool ok = true;
-    if (nv0 > 0) ok = mbar_wait_warp(bar(L::B_Q + 0), 0, wc);
-    if (ok && nv1 > 0) ok = mbar_wait_warp(bar(L::B_Q + 1), 0, wc);
     const uint64_t dq0 = sdesc_sw128(sbase + L::Q_OFF, 16, 1024);
     const uint64_t dq1 = sdesc_sw128(sbase + L::Q_OFF + L::TILE_BYTES, 16, 1024);
     const uint64_t d_ring = sdesc_sw128(sbase + L::RING_OFF, 16, 1024);   // K and V^T slots, K-major
@@ -178,6 +206,15 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_fp8_kernel(const __grid_constan
     int slot = 0;
     uint32_t phase = 0;
     uint32_t pph0 = 0, pph1 = 0;
+    for (int k = 0; ok; ++k) {
+    const int j = item_index(k);
+    if (j < 0) break;
+    const Item it = item_info(j);
+    const int qt0 = it.qt0, qt1 = it.qt1, kt_end = it.kt_end, nv0 = it.nv0, nv1 = it.nv1;
+    // Q of both tiles (a missing tile's phase completes empty); see the bf16
+    // forward for why the next item's S and P V need no further barrier
+    if (!(ok = mbar_wait_warp(bar(L::B_Q + 0), k & 1, wc))) break;
+    if (!(ok = mbar_wait_warp(bar(L::B_Q + 1), k & 1, wc))) break;
     int done0 = 0, done1 = 0;
     bool has_prev = false, pf0 = false, pf1 = false;
     int pvslot = 0;
@@ -227,10 +264,12 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_fp8_kernel(const __grid_constan
       pvslot = vslot;
       pvphase = vphase;
     }
+    if (ok) mma_commit_elect(bar(L::B_QFREE));   // all S of this item issued: Q may be reloaded
     if (ok && has_prev) {
       ok = mbar_wait_warp(bar(L::B_FULL + pvslot), pvphase, wc);
       if (ok && pf0) {
         ok = mbar_wait_warp(bar(L::B_P + 0), pph0, wc);
+        pph0 ^= 1u;                      // the phases continue into the next item
         if (ok) {
           tc_fence_after();
           issue_pv(L::O_COL0, L::S_COL0, pvslot, done0 > 0);
@@ -239,6 +278,7 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_fp8_kernel(const __grid_constan
       }
       if (ok && pf1) {
         ok = mbar_wait_warp(bar(L::B_P + 1), pph1, wc);
+        pph1 ^= 1u;
         if (ok) {
           tc_fence_after();
           issue_pv(L::O_COL1, L::S_COL1, pvslot, done1 > 0);
@@ -247,6 +287,7 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_fp8_kernel(const __grid_constan
       }
       if (ok) mma_commit_elect(bar(L::B_EMPTY + pvslot));
     }
+    }
     mma_commit_elect(bar(L::B_DONE));
     if (lane == 0) fp8_drain(bar(L::B_DONE), 0, 1000000000ull);
     __syncwarp();
@@ -254,7 +295,15 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_fp8_kernel(const __grid_constan
     // ------------------------------------------------------------ softmax
     const int w = static_cast<int>(warp >> 2);
     const uint32_t quarter = warp & 3u;
-    const int qt = qt0 + w;
+    uint32_t sphase = 0;   // phase of this tile's S barrier, continued across items
+    int n_out = 0;         // items whose O this group has read (phase of its O barrier)
+    bool ok = true;
+    for (int k = 0; ok; ++k) {
+    const int j = item_index(k);
+    if (j < 0) break;
+    const Item it = item_info(j);
+    const int bh = it.bh, nv0 = it.nv0, nv1 = it.nv1;
+    const int qt = it.qt0 + w;
     if (qt < p.n_qt) {
       const int row = static_cast<int>(quarter * 32 + lane);
       const uint32_t s_addr = tmem_addr(tmem, quarter * 32, w ? L::S_COL1 : L::S_COL0);
@@ -264,8 +313,6 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_fp8_kernel(const __grid_constan
       float m = -INFINITY;   // running max of S * log2 e (exp2 units)
       float l = 0.f;         // sum of exp2(S - m + 8), fp32
       bool has_o = false;
-      bool ok = true;
-      uint32_t sphase = 0;
       const int n_vis = w ? nv1 : nv0;
       // only the last visited tile can need a per-element mask (causal
       // diagonal, keys past N)
@@ -346,7 +393,8 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_fp8_kernel(const __grid_constan
         const size_t grow = static_cast<size_t>(bh) * p.N + static_cast<size_t>(qt) * TILE + row;
         __nv_bfloat16* orow = p.o + grow * D;
         if (n_vis > 0) {
-          ok = mbar_wait_warp(bar(L::B_O + w), 0, wc);
+          ok = mbar_wait_warp(bar(L::B_O + w), n_out & 1, wc);
+          ++n_out;
           if (ok) {
             tc_fence_after();
             const float inv = (p.v_descale ? __ldg(p.v_descale + bh) : 1.f) / l;
@@ -375,6 +423,7 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_fp8_kernel(const __grid_constan
         }
       }
     }
+    }
   }
 
   tc_fence_before();
@@ -390,8 +439,12 @@ int launch_fwd_fp8(const Fp8Params& p, cudaStream_t stream) {
   static_assert(L::SMEM_BYTES <= 232448, "shared memory budget");
   static SmemAttrOnce attr;
   if (!attr.ensure(reinterpret_cast<const void*>(fa_fwd_fp8_kernel), L::SMEM_BYTES)) return -4;
-  const unsigned grid = static_cast<unsigned>(p.n_pairs) * static_cast<unsigned>(p.BH);
-  fa_fwd_fp8_kernel<<<grid, L::THREADS, L::SMEM_BYTES, stream>>>(p);
+  int dev = 0, sms = 1;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return -4;
+  const long long items = static_cast<long long>(p.n_pairs) * p.BH;
+  const long long grid = items < sms ? items : sms;      // persistent: at most one CTA per SM
+  fa_fwd_fp8_kernel<<<static_cast<unsigned>(grid), L::THREADS, L::SMEM_BYTES, stream>>>(p);
   return cudaGetLastError() == cudaSuccess ? 0 : -4;
 }
 

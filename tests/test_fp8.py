@@ -80,6 +80,19 @@ def test_fp8_forward_long_sampled_head(fa):
         _check(o[b:b + 1, h:h + 1], lse[b:b + 1, h:h + 1], th, True, scale, f"N=4096 head ({b}, {h})")
 
 
+def test_fp8_forward_persistent_odd_tiles(fa):
+    """B4 H16 N1100 causal: 320 query-tile pairs (more than SMs) whose last pair
+    per head has one tile; whole heads through the oracle, every head finite."""
+    B, H, N = 4, 16, 1100
+    t = make_fp8_inputs(B, H, N, 128, seed=1100)
+    scale = 1 / math.sqrt(128)
+    o, lse = _run(fa, t, True, scale)
+    assert np.isfinite(o).all() and np.isfinite(lse).all()
+    for b, h in ((0, 0), (2, 7), (3, 15)):
+        th = {n: t[n][b:b + 1, h:h + 1].contiguous() for n in t}
+        _check(o[b:b + 1, h:h + 1], lse[b:b + 1, h:h + 1], th, True, scale, f"N=1100 head ({b}, {h})")
+
+
 def test_fp8_outputs_stay_inside_their_rows(fa):
     B, H, N, d = 1, 2, 300, 128
     t = make_fp8_inputs(B, H, N, d, seed=3)
