@@ -42,7 +42,8 @@ struct Fp8Layout {
   static constexpr int B_EMPTY = 2 + STAGES;     // STAGES
   static constexpr int B_S = 2 + 2 * STAGES;     // 2
   static constexpr int B_P = B_S + 2;            // 2
-  static constexpr int B_O = B_P + 2;            // 2
+  static constexpr int B_PH = B_P + 2;           // 2: first half of P_w (keys 0-63) in tensor memory
+  static constexpr int B_O = B_PH + 2;           // 2
   static constexpr int B_DONE = B_O + 2;         // 1
   static constexpr int B_QFREE = B_DONE + 1;     // 1: an item's S products done, Q may be reloaded
   static constexpr int NBARS = B_QFREE + 1;
@@ -114,6 +115,7 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_fp8_kernel(const __grid_constan
     for (int w = 0; w < 2; ++w) {
       mbar_init(bar(L::B_S + w), 1);
       mbar_init(bar(L::B_P + w), 4);
+      mbar_init(bar(L::B_PH + w), 4);
       mbar_init(bar(L::B_O + w), 1);
     }
     mbar_init(bar(L::B_DONE), 1);
@@ -197,11 +199,27 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_fp8_kernel(const __grid_constan
     };
     // O_w += P_w V: 4 k-steps of 32 keys; P from tensor memory (8 columns of
     // 4 e4m3 per step), V^T K-major (32 bytes per step)
-    auto issue_pv = [&](uint32_t ocol, uint32_t scol, int vslot, bool started) {
+    auto issue_pv_half = [&](uint32_t ocol, uint32_t scol, int vslot, bool started, int k0) {
       const uint64_t dv = d_ring + static_cast<uint64_t>(vslot) * SLOT16;
 #pragma unroll
-      for (int k = 0; k < TILE / 32; ++k)
+      for (int kk = 0; kk < TILE / 64; ++kk) {
+        const int k = k0 + kk;
         mma_ts_f8_elect(tmem + ocol, tmem + scol + 8 * k, dv + 2 * k, IDESC, (started || k > 0) ? 1u : 0u);
+      }
+    };
+    // P_w V in two halves: keys 0-63 once the softmax warps have published
+    // that half of P, the rest once all of P is in (one phase bit: both
+    // barriers complete once per tile)
+    auto pv = [&](int w, uint32_t& ph, int vslot, bool started) {
+      const uint32_t ocol = w ? L::O_COL1 : L::O_COL0, scol = w ? L::S_COL1 : L::S_COL0;
+      if (!mbar_wait_warp(bar(L::B_PH + w), ph, wc)) return false;
+      tc_fence_after();
+      issue_pv_half(ocol, scol, vslot, started, 0);
+      if (!mbar_wait_warp(bar(L::B_P + w), ph, wc)) return false;
+      tc_fence_after();
+      issue_pv_half(ocol, scol, vslot, started, TILE / 64);
+      ph ^= 1u;
+      return true;
     };
     int slot = 0;
     uint32_t phase = 0;
@@ -235,10 +253,7 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_fp8_kernel(const __grid_constan
         if (!(ok = mbar_wait_warp(bar(L::B_FULL + pvslot), pvphase, wc))) break;
       }
       if (has_prev && pf0) {
-        if (!(ok = mbar_wait_warp(bar(L::B_P + 0), pph0, wc))) break;
-        pph0 ^= 1u;
-        tc_fence_after();
-        issue_pv(L::O_COL0, L::S_COL0, pvslot, done0 > 0);
+        if (!(ok = pv(0, pph0, pvslot, done0 > 0))) break;
         if (++done0 == nv0) mma_commit_elect(bar(L::B_O + 0));
       }
       if (f0) {
@@ -246,10 +261,7 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_fp8_kernel(const __grid_constan
         mma_commit_elect(bar(L::B_S + 0));
       }
       if (has_prev && pf1) {
-        if (!(ok = mbar_wait_warp(bar(L::B_P + 1), pph1, wc))) break;
-        pph1 ^= 1u;
-        tc_fence_after();
-        issue_pv(L::O_COL1, L::S_COL1, pvslot, done1 > 0);
+        if (!(ok = pv(1, pph1, pvslot, done1 > 0))) break;
         if (++done1 == nv1) mma_commit_elect(bar(L::B_O + 1));
       }
       if (f1) {
@@ -268,22 +280,12 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_fp8_kernel(const __grid_constan
     if (ok && has_prev) {
       ok = mbar_wait_warp(bar(L::B_FULL + pvslot), pvphase, wc);
       if (ok && pf0) {
-        ok = mbar_wait_warp(bar(L::B_P + 0), pph0, wc);
-        pph0 ^= 1u;                      // the phases continue into the next item
-        if (ok) {
-          tc_fence_after();
-          issue_pv(L::O_COL0, L::S_COL0, pvslot, done0 > 0);
-          mma_commit_elect(bar(L::B_O + 0));
-        }
+        ok = pv(0, pph0, pvslot, done0 > 0);   // (the phases continue into the next item)
+        if (ok) mma_commit_elect(bar(L::B_O + 0));
       }
       if (ok && pf1) {
-        ok = mbar_wait_warp(bar(L::B_P + 1), pph1, wc);
-        pph1 ^= 1u;
-        if (ok) {
-          tc_fence_after();
-          issue_pv(L::O_COL1, L::S_COL1, pvslot, done1 > 0);
-          mma_commit_elect(bar(L::B_O + 1));
-        }
+        ok = pv(1, pph1, pvslot, done1 > 0);
+        if (ok) mma_commit_elect(bar(L::B_O + 1));
       }
       if (ok) mma_commit_elect(bar(L::B_EMPTY + pvslot));
     }
@@ -348,6 +350,19 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_fp8_kernel(const __grid_constan
           alpha = ex2_approx(m - m_tile);                  // 0 when m = -inf
           m = m_tile;
         }
+        if (has_o && __any_sync(0xffffffffu, need)) {
+          // O rescaled before any of this tile's P is published (the P V
+          // halves accumulate onto it); O may be read here: S(j) completing
+          // implies the previous PV is done.  16 columns at a time: S is live.
+#pragma unroll 1
+          for (int c = 0; c < D; c += 16) {
+            uint32_t ov[16];
+            tmem_ld_x16(o_addr + c, ov);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
+            tmem_st_x16(o_addr + c, ov);
+          }
+        }
         // P = exp2(S sl2 - m + 8) in (0, 256]; four e4m3 per 32-bit column,
         // 32 columns in all, written over the first 32 columns of S
         const float2 sl2v = make_float2(sl2, sl2);
@@ -367,21 +382,17 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_fp8_kernel(const __grid_constan
             lb = fadd2(lb, p1);
             pk[e] = pack_e4m3x2(p0.x, p0.y) | (pack_e4m3x2(p1.x, p1.y) << 16);
           }
+          if (q == 1) {
+            // keys 0-63 of P are stored: publish that half (its store
+            // completed while keys 64-127 were computed)
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(L::B_PH + w));
+          }
           tmem_st_x16_async(s_addr + 16 * q, pk);
         }
         l = l * alpha + ((la.x + la.y) + (lb.x + lb.y));
-
-        if (has_o && __any_sync(0xffffffffu, need)) {
-          // O may be read here: S(j) completing implies the previous PV is done
-#pragma unroll 1
-          for (int c = 0; c < D; c += 32) {
-            uint32_t ov[32];
-            tmem_ld_x32(o_addr + c, ov);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
-            tmem_st_x32(o_addr + c, ov);
-          }
-        }
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
