@@ -233,6 +233,10 @@ __device__ __forceinline__ void mbar_drain(uint32_t bar, uint32_t parity, uint64
 template <int D, bool SPARSE, bool DROP>
 __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ FwdParams p) {
   using L = FwdLayout<D, SPARSE>;
+  // P V of a tile issued in two halves (the first once half of P is stored)
+  // where the softmax outweighs the products: with dropout, and at d = 64
+  // without a block mask
+  constexpr bool SPLIT_PV = DROP || (D == 64 && !SPARSE);
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
@@ -438,22 +442,23 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
         mma_ts_elect(tmem + ocol, tmem + scol + 8 * k, dv + ((k * 2048) >> 4), IDESC_O, (started || k > 0) ? 1u : 0u);
       }
     };
-    // P_w V.  With dropout (the softmax warps' share of the round is
-    // largest there) the first half (keys 0-63) is issued once the softmax
-    // warps have published that half of P and the rest once all of P is in;
-    // both barriers complete once per tile, so one phase bit serves both.
-    // Without dropout all of it waits for all of P (splitting measured
-    // neutral with a dense mask and slower with block masks).
+    // P_w V.  Where the softmax outweighs the products (SPLIT_PV: dropout,
+    // and d = 64 without a block mask) the first half (keys 0-63) is issued
+    // once the softmax warps have published that half of P and the rest once
+    // all of P is in; both barriers complete once per tile, so one phase bit
+    // serves both.  Otherwise all of it waits for all of P (splitting
+    // measured neutral with a dense mask at d = 128 and slower with block
+    // masks).
     auto pv = [&](int w, uint32_t& ph, int vslot, bool started) {
       const uint32_t ocol = w ? L::O_COL1 : L::O_COL0, scol = w ? L::S_COL1 : L::S_COL0;
-      if constexpr (DROP) {
+      if constexpr (SPLIT_PV) {
         if (!mbar_wait_warp(bar(L::B_PH + w), ph, wc)) return false;
         tc_fence_after();
         issue_pv_half(ocol, scol, vslot, started, 0);
       }
       if (!mbar_wait_warp(bar(L::B_P + w), ph, wc)) return false;
       tc_fence_after();
-      if constexpr (!DROP) issue_pv_half(ocol, scol, vslot, started, 0);
+      if constexpr (!SPLIT_PV) issue_pv_half(ocol, scol, vslot, started, 0);
       issue_pv_half(ocol, scol, vslot, started, TILE / 32);
       ph ^= 1u;
       return true;
@@ -690,7 +695,7 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
         // bf16-rounded values that P V multiplies, so O / lr weighs the V rows
         // with weights summing to exactly one.  Dropout zeroes the dropped
         // pairs of the P V operand only: l and lr are the softmax's own sums.
-        if (DROP && has_o && __any_sync(0xffffffffu, need)) {
+        if (SPLIT_PV && has_o && __any_sync(0xffffffffu, need)) {
           // With dropout, O is rescaled before any of this tile's P is
           // published (the P V halves accumulate onto it).  O may be read
           // here: S(j) completing implies the previous P V is done.
@@ -728,7 +733,7 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
               pk[e] = pku;
             }
           }
-          if (DROP && q == 2) {
+          if (SPLIT_PV && q == 2) {
             // keys 0-63 of P are stored: publish that half (the stores of
             // chunks 0 and 1 completed while chunk 2 was computed)
             tmem_wait_st();
@@ -740,7 +745,7 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
         }
         l = l * alpha + ((la.x + la.y) + (lb.x + lb.y));
         lr = lr * alpha + ((ra.x + ra.y) + (rb.x + rb.y));
-        if (!DROP && has_o && __any_sync(0xffffffffu, need)) {
+        if (!SPLIT_PV && has_o && __any_sync(0xffffffffu, need)) {
           // O may be read here: S(j) completing implies the previous PV is done.
 #pragma unroll 1
           for (int c = 0; c < D; c += 32) {
