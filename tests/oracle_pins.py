@@ -524,5 +524,38 @@ def pin_fp8(orc):
     assert 0.85 < ratio < 1.15, ratio
 
 
+def pin_visibility(orc):
+    """The visibility predicates against brute force on tiny shapes: key j is
+    visible to query row i when j <= i under the causal mask [P2 causal
+    masking] and when the block mask entry of (i // block, j // block) is set
+    [P2 "Block-sparse Flashattention"]; a decoding query i of nq against a
+    cache of L keys sits at position L - nq + i.  Covers row subsets, more keys
+    than rows, ragged last blocks and the reduction of decoding with nq = L to
+    the square causal mask."""
+    r = _rng(29)
+    for nq, nk, blk in ((1, 1, 4), (7, 7, 4), (9, 13, 4), (13, 9, 3), (16, 16, 8)):
+        bm = (r.random((-(-nq // blk), -(-nk // blk))) < 0.5).astype(np.uint8)
+        for causal in (False, True):
+            for use_bm in (False, True):
+                for rows in (None, np.array([nq - 1, 0, nq // 2])):
+                    got = orc.visible(nq, nk, causal, bm if use_bm else None, blk, rows)
+                    rr = range(nq) if rows is None else rows
+                    want = np.zeros((len(rr), nk), dtype=bool)
+                    for a, i in enumerate(rr):
+                        for j in range(nk):
+                            ok = (j <= i) if causal else True
+                            if use_bm:
+                                ok = ok and bool(bm[i // blk][j // blk])
+                            want[a, j] = ok
+                    np.testing.assert_array_equal(got, want)
+    for nq, L in ((1, 1), (1, 5), (4, 4), (4, 11), (8, 9)):
+        for causal in (False, True):
+            want = np.array([[(not causal) or j <= L - nq + i for j in range(L)] for i in range(nq)])
+            np.testing.assert_array_equal(orc.decode_visible(nq, L, causal), want)
+    for L in (1, 6, 17):
+        np.testing.assert_array_equal(orc.decode_visible(L, L, True), orc.visible(L, L, True))
+
+
 ALL_PINS = [pin_worked_example, pin_closed_forms, pin_invariants, pin_backward_fd,
-            pin_dvec, pin_backward_rows, pin_library, pin_block_masks, pin_decode, pin_philox, pin_dropout, pin_fp8]
+            pin_dvec, pin_backward_rows, pin_library, pin_block_masks, pin_decode, pin_philox, pin_dropout, pin_fp8,
+            pin_visibility]

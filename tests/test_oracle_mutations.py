@@ -53,6 +53,11 @@ def _m_block_transposed(nq, nk, causal=False, block_mask=None, block=128, rows=N
     return _real["visible"](nq, nk, causal, bm, block, rows)
 
 
+def _m_rows_ignored(nq, nk, causal=False, block_mask=None, block=128, rows=None):
+    vis = _real["visible"](nq, nk, causal, block_mask, block, None)
+    return vis if rows is None else vis[: len(rows)]
+
+
 def _m_fwd_kv_swapped(q, k, v, scale, **kw):
     if k.shape == v.shape:
         return _real["forward"](q, v, k, scale, **kw)
@@ -253,6 +258,7 @@ MUTANTS = {
     "dS_missing_D": ("_softmax_backward", _m_ds_no_d),
     "causal_off_by_one": ("visible", _m_causal_strict),
     "block_mask_transposed": ("visible", _m_block_transposed),
+    "visible_rows_ignored": ("visible", _m_rows_ignored),
     "forward_kv_swapped": ("forward", _m_fwd_kv_swapped),
     "dK_scale_dropped": ("backward", _m_bwd_dk_unscaled),
     "dQ_dS_transposed": ("backward", _m_bwd_dq_transposed),
