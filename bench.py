@@ -228,47 +228,135 @@ class ClockSampler:
 # --------------------------------------------------------------------------- #
 # the CPU oracle on a bounded sample
 # --------------------------------------------------------------------------- #
-def _oracle_sample(w, t, budget_s=15.0, max_heads=None):
+class Parity:
+    """Comparison of the timed step's outputs with the oracle's, on the whole
+    heads that the CPU-baseline leg runs anyway.  Bounds as in the parity
+    tests: O within 1e-2 + 2^-8 |O_ref| element-wise, LSE relative 1e-3
+    (against max(|LSE|, 1)), dQ, dK, dV relative L2 2e-2 per head and per
+    128-row tile, and (first two heads, no dropout) every gradient element
+    inside the oracle's error model, u |r| + (1 + u)(6 sigma + acc); the 8-bit
+    forward within the oracle's e4m3 error model plus O's bf16 rounding."""
+
+    def __init__(self):
+        self.o_excess = -float("inf")
+        self.o_max_abs = 0.0
+        self.lse_rel = 0.0
+        self.rel = {"dq": 0.0, "dk": 0.0, "dv": 0.0}
+        self.tile_rel = 0.0
+        self.grad_excess = None
+        self.heads = 0
+        self.element_heads = 0
+
+    @staticmethod
+    def _np(x):
+        return x.float().numpy()
+
+    def forward(self, o, lse, ro, rl, bound=None):
+        import numpy as np
+        o, lse = self._np(o), self._np(lse)
+        lim = (1e-2 + 2.0 ** -8 * np.abs(ro)) if bound is None else bound
+        err = np.abs(o - ro)
+        self.o_excess = max(self.o_excess, float(np.nanmax(np.where(np.isfinite(o), err - lim, np.inf))))
+        self.o_max_abs = max(self.o_max_abs, float(err.max()))
+        fin = np.isfinite(rl)
+        if not np.array_equal(np.isfinite(lse), fin):
+            self.lse_rel = float("inf")
+        elif fin.any():
+            self.lse_rel = max(self.lse_rel, float((np.abs(lse[fin] - rl[fin]) / np.maximum(np.abs(rl[fin]), 1.0)).max()))
+
+    def backward(self, g, ref, model=None):
+        import numpy as np
+        for i, (name, a, r) in enumerate(zip(("dq", "dk", "dv"), g, ref)):
+            a = self._np(a)
+            floor = 1e-3 * np.sqrt(r.size)
+            self.rel[name] = max(self.rel[name], float(np.linalg.norm(a - r) / max(np.linalg.norm(r), floor)))
+            n = r.shape[-2]
+            for t0 in range(0, n, 128):
+                x, y = a[..., t0:t0 + 128, :], r[..., t0:t0 + 128, :]
+                tr = np.linalg.norm(x - y) / max(np.linalg.norm(y), 1e-3 * np.sqrt(y.size))
+                self.tile_rel = max(self.tile_rel, float(tr))
+            if model is not None:
+                u = 2.0 ** -8
+                ex = float((np.abs(a - r) - (u * np.abs(r) + (1 + u) * (6 * model[0][i] + model[1][i]))).max())
+                self.grad_excess = ex if self.grad_excess is None else max(self.grad_excess, ex)
+
+    def report(self, backward):
+        ok = self.heads > 0 and self.o_excess <= 0 and self.lse_rel <= 1e-3
+        out = {"heads_checked": self.heads, "o_max_abs": self.o_max_abs, "o_excess": self.o_excess,
+               "lse_rel": self.lse_rel}
+        if backward:
+            out.update({f"{k}_rel_l2": v for k, v in self.rel.items()})
+            out["tile_rel_l2"] = self.tile_rel
+            ok = ok and max(self.rel.values()) <= 2e-2 and self.tile_rel <= 2e-2
+            if self.grad_excess is not None:
+                out["grad_element_excess"] = self.grad_excess
+                out["grad_element_heads"] = self.element_heads
+                ok = ok and self.grad_excess <= 0
+        out["ok"] = bool(ok)
+        out["source"] = "outputs of the last timed step vs the oracle on the cpu_baseline heads"
+        return out
+
+
+def _oracle_sample(w, t, budget_s=15.0, max_heads=None, gpu=None, parity=None):
     """Time the fp64 oracle (forward + backward) head by head until `budget_s`
-    has passed.  Returns (TFLOPS, seconds, heads)."""
+    of oracle time has passed.  Returns (TFLOPS, seconds, heads).  With `gpu`
+    (the timed step's outputs on the host) and a `parity` accumulator, each
+    head's oracle results are also compared with the GPU's, outside the
+    timed oracle calls."""
     import oracle
     import torch
     bm = t.get("block_mask")
     bmn = None if bm is None else bm.numpy()
     heads = 0
     flops = 0.0
-    t0 = time.perf_counter()
+    el = 0.0
     for hh in range(w.B * w.H):
         b, h = divmod(hh, w.H)
         sl = (slice(b, b + 1), slice(h, h + 1))
         if w.fp8:
             u8 = [t[n][sl].contiguous().view(torch.uint8).numpy() for n in ("q8", "k8", "v8")]
             qd, kd, vd = (t[n][sl].double().numpy() for n in ("qd", "kd", "vd"))
-            oracle.forward_fp8(*u8, qd, kd, vd, w.scale, causal=w.causal)
+            t0 = time.perf_counter()
+            ro, rl, probs, vv = oracle.forward_fp8(*u8, qd, kd, vd, w.scale, causal=w.causal)
+            el += time.perf_counter() - t0
             heads += 1
             ff, fb = _flops(type(w)(**{**w.__dict__, "B": 1, "H": 1}), None)
             flops += ff
-            if time.perf_counter() - t0 >= budget_s or (max_heads and heads >= max_heads):
+            if gpu is not None and parity is not None:
+                import numpy as np
+                bound, _ = oracle.fp8_error_model(ro, probs, vv)
+                parity.forward(gpu["o"][sl], gpu["lse"][sl], ro, rl, bound + 2.0 ** -8 * np.abs(ro) + 1e-3)
+                parity.heads += 1
+            if el >= budget_s or (max_heads and heads >= max_heads):
                 break
             continue
         q, k, v = (t[n][sl].double().numpy() for n in ("q", "k", "v"))
+        do = t["do"][sl].double().numpy() if w.backward else None
+        t0 = time.perf_counter()
         if w.dropout_p:
-            oracle.forward_dropout(q, k, v, w.scale, w.dropout_p, w.seed, causal=w.causal, block_mask=bmn, b0=b, h0=h)
-            if w.backward:
-                oracle.backward_dropout(q, k, v, t["do"][sl].double().numpy(), w.scale, w.dropout_p, w.seed,
-                                        causal=w.causal, block_mask=bmn, b0=b, h0=h)
+            ro, rl = oracle.forward_dropout(q, k, v, w.scale, w.dropout_p, w.seed, causal=w.causal, block_mask=bmn,
+                                            b0=b, h0=h)
+            ref = oracle.backward_dropout(q, k, v, do, w.scale, w.dropout_p, w.seed, causal=w.causal,
+                                          block_mask=bmn, b0=b, h0=h)[:3] if w.backward else None
         else:
-            oracle.forward(q, k, v, w.scale, causal=w.causal, block_mask=bmn,
-                           row_chunk=2048 if w.N > 8192 else None)
-            if w.backward:
-                oracle.backward(q, k, v, t["do"][sl].double().numpy(), w.scale, causal=w.causal, block_mask=bmn)
+            ro, rl = oracle.forward(q, k, v, w.scale, causal=w.causal, block_mask=bmn,
+                                    row_chunk=2048 if w.N > 8192 else None)
+            ref = oracle.backward(q, k, v, do, w.scale, causal=w.causal, block_mask=bmn)[:3] if w.backward else None
+        el += time.perf_counter() - t0
         heads += 1
         ff, fb = _flops(type(w)(**{**w.__dict__, "B": 1, "H": 1}), _density(t, w.causal))
         flops += ff + fb
-        el = time.perf_counter() - t0
+        if gpu is not None and parity is not None:
+            parity.forward(gpu["o"][sl], gpu["lse"][sl], ro, rl)
+            if w.backward:
+                model = None
+                if not w.dropout_p and parity.element_heads < 2:
+                    model = oracle.grad_error_model(q, k, v, do, w.scale, causal=w.causal, block_mask=bmn)
+                    parity.element_heads += 1
+                parity.backward([gpu[n][sl] for n in ("dq", "dk", "dv")], ref, model)
+            parity.heads += 1
         if el >= budget_s or (max_heads and heads >= max_heads):
             break
-    el = time.perf_counter() - t0
     return flops / el / 1e12, el, heads
 
 
@@ -367,23 +455,28 @@ def source_sha256(files):
     return hh.hexdigest()
 
 
-def _oracle_decode_sample(w, t, budget_s=15.0):
+def _oracle_decode_sample(w, t, budget_s=15.0, gpu=None, parity=None):
     """Time the fp64 oracle's decode (batch, head) by (batch, head) until
-    `budget_s` has passed.  Returns (TFLOPS, seconds, heads)."""
+    `budget_s` of oracle time has passed.  Returns (TFLOPS, seconds, heads);
+    with `gpu` and `parity`, each pair's result is also compared with the
+    timed step's, outside the timed calls."""
     import oracle
-    heads, flops = 0, 0.0
-    t0 = time.perf_counter()
+    heads, flops, el = 0, 0.0, 0.0
     for hh in range(w.B * w.H):
         b, h = divmod(hh, w.H)
         sl = (slice(b, b + 1), slice(h, h + 1))
         L = int(t["seqlens"][b])
         q, k, v = (t[n][sl].double().numpy() for n in ("q", "k", "v"))
-        oracle.decode(q, k, v, w.scale, seqlens=[L], causal=w.causal)
+        t0 = time.perf_counter()
+        ro, rl = oracle.decode(q, k, v, w.scale, seqlens=[L], causal=w.causal)
+        el += time.perf_counter() - t0
         flops += 4.0 * w.d * _decode_pairs(w.nq, L, w.causal)
         heads += 1
-        if time.perf_counter() - t0 >= budget_s:
+        if gpu is not None and parity is not None:
+            parity.forward(gpu["o"][sl], gpu["lse"][sl], ro, rl)
+            parity.heads += 1
+        if el >= budget_s:
             break
-    el = time.perf_counter() - t0
     return flops / el / 1e12, el, heads
 
 
@@ -495,6 +588,7 @@ def run_cuda_decode(args, w):
     if rc != 0:
         raise RuntimeError(f"device status after timing: {fa.status_string(rc)}")
     value = whole_job_tflops(ws, flops, ms_per_step)
+    timed_out = {"o": o.cpu(), "lse": lse.cpu()}
 
     # end to end: the new query tokens in from pinned host memory, O and LSE back
     hq = t["q"].pin_memory()
@@ -531,15 +625,19 @@ def run_cuda_decode(args, w):
                     "d2h_bytes_per_step": ho.numel() * ho.element_size() + hl.numel() * hl.element_size(),
                     "ms_per_step": e2e_ms},
             "gpu_launches": launches_per_step * args.steps, "roofline": roofline, "clocks": clocks}
+    rc_out = 0
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
-        tf, el, heads = _oracle_decode_sample(w, t, budget_s=args.cpu_budget)
+        par = Parity()
+        tf, el, heads = _oracle_decode_sample(w, t, budget_s=args.cpu_budget, gpu=timed_out, parity=par)
         line["cpu_baseline"] = {"value": tf, "unit": UNIT, "cores": _CORES, "kind": "oracle",
                                 "sample": f"{heads} of {w.B * w.H} (batch, head) pairs, decode, fp64, {el:.1f} s"}
+        line["parity"] = par.report(False)
+        rc_out = 0 if line["parity"]["ok"] else 1
     if rank == 0:
         print(json.dumps(line), flush=True)
     if ws > 1:
         dist.destroy_process_group()
-    return 0
+    return rc_out
 
 
 def _run_cuda_fp8(args, w, t, f_fwd, fa, dev, ws, rank):
@@ -590,6 +688,7 @@ def _run_cuda_fp8(args, w, t, f_fwd, fa, dev, ws, rank):
     if fa.fa_get_device_error() != 0:
         raise RuntimeError("device status after timing")
     value = whole_job_tflops(ws, f_fwd, ms_per_step)
+    timed_out = {"o": o.cpu(), "lse": lse.cpu()}
     host_in = {n: t[n].pin_memory() for n in d8}
     ho, hl = torch.empty(o.shape, dtype=o.dtype).pin_memory(), torch.empty(lse.shape).pin_memory()
     e2e_steps = max(3, min(args.steps, 20))
@@ -624,15 +723,19 @@ def _run_cuda_fp8(args, w, t, f_fwd, fa, dev, ws, rank):
                     "d2h_bytes_per_step": ho.numel() * ho.element_size() + hl.numel() * hl.element_size(),
                     "ms_per_step": e2e_ms},
             "gpu_launches": 2 * args.steps, "roofline": roofline, "clocks": clocks}
+    rc_out = 0
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
-        tf, el, heads = _oracle_sample(w, t, budget_s=args.cpu_budget)
+        par = Parity()
+        tf, el, heads = _oracle_sample(w, t, budget_s=args.cpu_budget, gpu=timed_out, parity=par)
         line["cpu_baseline"] = {"value": tf, "unit": UNIT, "cores": _CORES, "kind": "oracle",
                                 "sample": f"{heads} of {w.B * w.H} (batch, head) pairs, 8-bit forward, fp64, {el:.1f} s"}
+        line["parity"] = par.report(False)
+        rc_out = 0 if line["parity"]["ok"] else 1
     if rank == 0:
         print(json.dumps(line), flush=True)
     if ws > 1:
         dist.destroy_process_group()
-    return 0
+    return rc_out
 
 
 def _graph_ms_per_step(args, step, flush, ws, dev):
@@ -781,6 +884,10 @@ def run_cuda(args):
             raise RuntimeError(f"device status after the graph replays: {fa.status_string(rc)}")
     clocks = sampler.stop() if sampler else None
     value = whole_job_tflops(ws, f_fwd + f_bwd, ms_per_step)
+    # the outputs of the last timed step, for the parity check against the oracle
+    timed_out = {"o": o.cpu(), "lse": lse.cpu()}
+    if w.backward:
+        timed_out.update({"dq": dq.cpu(), "dk": dk.cpu(), "dv": dv.cpu()})
 
     # ---- end to end through the public binding, host buffers ------------- #
     host_in = {n: t[n].pin_memory() for n in (("q", "k", "v", "do") if w.backward else ("q", "k", "v"))}
@@ -834,6 +941,8 @@ def run_cuda(args):
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, dev)
     e2e_value = whole_job_tflops(ws, f_fwd + f_bwd, e2e_ms)
+    # what the end-to-end call returned against the timed device step's outputs
+    e2e_diff = {n: float((host_out[n].float() - timed_out[n].float()).abs().max()) for n in host_out}
 
     # ---- roofline of the dominant kernel -------------------------------- #
     peaks, peak_src = _peaks()
@@ -869,22 +978,27 @@ def run_cuda(args):
                     "ms_per_step": e2e_ms,
                     "call": ((("fa_fwd_bwd_host" if w.backward else "fa_fwd_host") +
                               ": chunks of heads, copies overlapped with the kernels") if streamed
-                             else "pinned copies in, device-resident step, copies out")},
+                             else "pinned copies in, device-resident step, copies out"),
+                    "max_abs_diff_vs_device_step": e2e_diff},
             "gpu_launches": launches_per_step * args.steps, "roofline": roofline, "kernels": kernels,
             "clocks": clocks}
     if not args.eager:
         line["eager_ms_per_step"] = eager_ms_per_step
 
+    rc_out = 0
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
-        tf, el, heads = _oracle_sample(w, t, budget_s=args.cpu_budget)
+        par = Parity()
+        tf, el, heads = _oracle_sample(w, t, budget_s=args.cpu_budget, gpu=timed_out, parity=par)
         line["cpu_baseline"] = {"value": tf, "unit": UNIT, "cores": _CORES, "kind": "oracle",
                                 "sample": f"{heads} of {w.B * w.H} (batch, head) pairs, forward"
                                           f"{' + backward' if w.backward else ''}, fp64, {el:.1f} s"}
+        line["parity"] = par.report(w.backward)
+        rc_out = 0 if line["parity"]["ok"] else 1
     if rank == 0:
         print(json.dumps(line), flush=True)
     if ws > 1:
         dist.destroy_process_group()
-    return 0
+    return rc_out
 
 
 def _apply_overrides(args, ap):

@@ -16,10 +16,10 @@ from .attention import (  # noqa: F401
     dropout_keep,
     dropout_threshold,
     e4m3_decode,
-    flops,
     forward_dropout,
     forward_fp8,
     fp8_error_model,
+    grad_error_model,
     forward,
     forward_rows,
     dilated_block_mask,

@@ -553,15 +553,90 @@ def merge_stats(m1, l1, m2, l2):
     return m, np.exp(m1 - m) * l1 + np.exp(m2 - m) * l2
 
 
-def flops(B, H, N, d, causal=False, backward=False, density=None) -> float:
-    """Algorithmic FLOP count: 4 B H N^2 d forward (two N x N x d products),
-    2.5x that backward (five products instead of two), halved when causal; a
-    block-sparse mask scales by the fraction of kept blocks."""
-    f = 4.0 * B * H * N * N * d
-    if backward:
-        f *= 2.5
-    if causal:
-        f *= 0.5
-    if density is not None:
-        f *= density
-    return f
+# --------------------------------------------------------------------------- #
+# error scale of gradients computed with bf16 operands and fp32 sums
+# --------------------------------------------------------------------------- #
+BF16_U = 2.0 ** -8      # unit roundoff of bf16 (8 significant bits, round to nearest even)
+FP32_STEP = 2.0 ** -23  # one fp32 rounding step, truncation included (24 significant bits)
+
+
+def grad_error_model(q, k, v, do, scale, causal=False, block_mask=None, block=128,
+                     row_chunk: int = 1024, u: float = BF16_U, f32: float = FP32_STEP):
+    """Per-element error scale of dQ, dK, dV computed from bf16 inputs with
+    bf16 outputs and fp32 accumulation.
+
+    Where such an implementation must round to bf16: the forward stores O
+    (and its P V product takes P as bf16); the backward's products take P
+    (dV = P^T dO) and dS (dK = s dS^T Q, dQ = s dS K) as bf16, and
+    D_i = dO_i . O_i uses the stored O ["FlashAttention" notes, "Backward Pass
+    of flashattention": D_i = do_i^T o_i].  Rounding x to bf16 moves it by at
+    most u |x|; taken as uniform, by a standard deviation of at most
+    u |x| / sqrt(3).  To first order, with independent rounding errors e:
+
+    * D_i: the forward's rounding of P moves O_i by sum_j P_ij e_ij (V_j - O_i)
+      (row sum of the rounded weights) or sum_j P_ij e_ij V_j (exact sum), so
+      D_i by sum_j P_ij e_ij (dP_ij - D_i) or sum_j P_ij e_ij dP_ij; O's own
+      rounding adds sum_c dO_ic O_ic e_ic:
+      Var D_i <= (u^2/3) [2 sum_j P_ij^2 (dP_ij^2 + D_i^2) + sum_c dO_ic^2 O_ic^2].
+    * dS_ij, apart from D_i: Var <= (u^2/3) dS_ij^2.
+    * dV_jc = sum_i P_ij dO_ic:  Var = (u^2/3) sum_i P_ij^2 dO_ic^2.
+    * dK_jc = s sum_i dS_ij Q_ic:  Var = s^2 [sum_i Var(dS_ij) Q_ic^2 + sum_i P_ij^2 Q_ic^2 Var D_i].
+    * dQ_ic = s sum_j dS_ij K_jc:  Var = s^2 [sum_j Var(dS_ij) K_jc^2 + (sum_j P_ij K_jc)^2 Var D_i]
+      (D_i's error is shared by the whole row, so it adds coherently over j).
+
+    fp32 effects, as worst cases added in quadrature: a product of length n
+    summed in steps of 16 is off by at most (n/16 + 2) f32 times the sum of
+    its absolute terms (f32 = 2^-23, one rounding or truncation step), which
+    bounds the scores' error, so P's relative error, at
+    (d/16 + 2) f32 s sum_c |Q_ic K_jc| + f32 (|LSE_i| + 8), dP's at
+    (d/16 + 2) f32 sum_c |dO_ic V_jc| and D_i's at (d/16 + 2) f32
+    sum_c |dO_ic O_ic|; each gradient's own sum over N terms is off by at
+    most acc = (N/16 + N/128 + 2) f32 times the sum of its absolute terms
+    (tensor-core steps of 16, then per-tile partial sums).
+
+    Returns (sigma, acc), each a tuple (dQ, dK, dV) of arrays [B, H, N, d].
+    A gradient g then satisfies |g - r| <= u |r| + (1 + u)(k sigma + acc) for
+    the exact r and a few k; u |r| is the output's own rounding.  Query rows
+    are taken in chunks of ``row_chunk`` full rows."""
+    q, k, v, do = (np.asarray(x, dtype=np.float64) for x in (q, k, v, do))
+    B, H, N, d = q.shape
+    r2 = u * u / 3.0
+    cd = (d / 16.0 + 2.0) * f32
+    n_acc = (N / 16.0 + N / 128.0 + 2.0) * f32
+    sig = [np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)]
+    acc = [np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)]
+    for b in range(B):
+        for h in range(H):
+            qh, kh, vh, doh = q[b, h], k[b, h], v[b, h], do[b, h]
+            aq, ak, av = np.abs(qh), np.abs(kh), np.abs(vh)
+            var_dk = np.zeros_like(kh)
+            var_dv = np.zeros_like(vh)
+            abs_dk = np.zeros_like(kh)
+            abs_dv = np.zeros_like(vh)
+            for r0 in range(0, N, row_chunk):
+                rows = np.arange(r0, min(N, r0 + row_chunk))
+                p, lse = head_probs(qh, kh, scale, causal, block_mask, block, rows)
+                o = p @ vh
+                dor = doh[rows]
+                adr = np.abs(dor)
+                dp = dor @ vh.T
+                d_row = (dor * o).sum(axis=1)
+                ds = _softmax_backward(p, dp, d_row)
+                p2 = p * p
+                lse_f = np.where(np.isfinite(lse), np.abs(lse), 0.0)
+                rho = cd * scale * (np.abs(qh[rows]) @ ak.T) + f32 * (lse_f[:, None] + 8.0)
+                var_d = (r2 * (2.0 * (p2 * (dp * dp + d_row[:, None] ** 2)).sum(axis=1) + ((dor * o) ** 2).sum(axis=1))
+                         + ((p * rho * np.abs(dp - d_row[:, None])).sum(axis=1)) ** 2
+                         + (cd * np.abs(dor * o).sum(axis=1)) ** 2)
+                var_ds = r2 * ds * ds + (rho * ds) ** 2 + (p * cd * (adr @ av.T)) ** 2
+                qr = qh[rows]
+                var_dq = scale ** 2 * (var_ds @ (kh * kh) + (p @ kh) ** 2 * var_d[:, None])
+                sig[0][b, h, rows] = np.sqrt(var_dq)
+                acc[0][b, h, rows] = n_acc * scale * (np.abs(ds) @ ak)
+                var_dk += scale ** 2 * (var_ds.T @ (qr * qr) + p2.T @ (qr * qr * var_d[:, None]))
+                abs_dk += n_acc * scale * (np.abs(ds).T @ np.abs(qr))
+                var_dv += r2 * (p2.T @ (dor * dor)) + ((p * rho) ** 2).T @ (dor * dor)
+                abs_dv += n_acc * (p.T @ adr)
+            sig[1][b, h], sig[2][b, h] = np.sqrt(var_dk), np.sqrt(var_dv)
+            acc[1][b, h], acc[2][b, h] = abs_dk, abs_dv
+    return tuple(sig), tuple(acc)

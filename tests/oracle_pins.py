@@ -556,6 +556,77 @@ def pin_visibility(orc):
         np.testing.assert_array_equal(orc.decode_visible(L, L, True), orc.visible(L, L, True))
 
 
+def _bf16(x):
+    """Round to bf16 (round to nearest even) and back, through PyTorch."""
+    return torch.from_numpy(np.ascontiguousarray(x)).to(torch.bfloat16).double().numpy()
+
+
+def pin_grad_error_model(orc):
+    """The gradient error model against the rounding it describes: (1) a bf16
+    pipeline simulated with real round-to-nearest-even bf16 values at every
+    rounding point (forward P for P V, stored O, backward P for dV, dS, the
+    outputs), with O normalised by the rounded or the exact row sum, stays
+    inside u |r| + (1 + u)(6 sigma + acc) everywhere; (2) uniform relative
+    perturbations of size u at those points spread with an RMS at most the
+    model's sigma and not far below it (the model is an upper bound, not a
+    vacuous one); (3) one wrong row of dQ or dK breaks the bound."""
+    u = orc.BF16_U
+    r = _rng(57)
+    cases = [(1, 2, 160, 32, False, 1.0, None), (1, 1, 200, 64, True, 3.0, None),
+             (1, 1, 256, 32, False, 1.0, np.array([[1, 0], [1, 1]], np.uint8))]
+    for B, H, N, d, causal, amp, bm in cases:
+        q, k, v, do = (_bf16(r.standard_normal((B, H, N, d)) * amp) for _ in range(4))
+        s = 1 / math.sqrt(d)
+        ref = orc.backward(q, k, v, do, s, causal=causal, block_mask=bm)[:3]
+        sig, acc = orc.grad_error_model(q, k, v, do, s, causal=causal, block_mask=bm, row_chunk=64)
+        vis = _dense_mask_torch(N, causal, bm).numpy()
+        for rounded_sum in (True, False):
+            sim = [np.zeros_like(q) for _ in range(3)]
+            for b in range(B):
+                for h in range(H):
+                    qh, kh, vh, doh = q[b, h], k[b, h], v[b, h], do[b, h]
+                    sc = np.where(vis, s * (qh @ kh.T), -np.inf)
+                    f = np.exp(sc - sc.max(axis=1)[:, None])
+                    fh = _bf16(f)
+                    o = _bf16((fh @ vh) / (fh if rounded_sum else f).sum(axis=1)[:, None])
+                    p = f / f.sum(axis=1)[:, None]
+                    ds = _bf16(p * (doh @ vh.T - (doh * o).sum(axis=1)[:, None]))
+                    sim[0][b, h] = _bf16(s * ds @ kh)
+                    sim[1][b, h] = _bf16(s * ds.T @ qh)
+                    sim[2][b, h] = _bf16(_bf16(p).T @ doh)
+            for g, rr, sg, ac in zip(sim, ref, sig, acc):
+                assert np.all(np.abs(g - rr) <= u * np.abs(rr) + (1 + u) * (6 * sg + ac))
+        # planted wrong rows are caught
+        for which in (0, 1):
+            bad = ref[which].copy()
+            bad[0, 0, [3, 4]] = bad[0, 0, [4, 3]]
+            assert np.any(np.abs(bad - ref[which]) > u * np.abs(ref[which]) + (1 + u) * (6 * sig[which] + acc[which]))
+        if amp == 1.0 and bm is None:
+            for g, sg, ac in zip(ref, sig, acc):
+                assert np.median((6 * sg + ac) / np.maximum(np.abs(g), 1e-30)) < 0.1
+    # uniform perturbations of size u: RMS spread against the model's sigma
+    B, H, N, d = 1, 1, 96, 16
+    q, k, v, do = (r.standard_normal((B, H, N, d)) for _ in range(4))
+    s = 0.25
+    ref = orc.backward(q, k, v, do, s, causal=True)[:3]
+    sig, _ = orc.grad_error_model(q, k, v, do, s, causal=True, f32=0.0)
+    p = np.where(_dense_mask_torch(N, True).numpy(), np.exp(s * (q[0, 0] @ k[0, 0].T)), 0.0)
+    p /= p.sum(axis=1)[:, None]
+    sq = [np.zeros((N, d)) for _ in range(3)]
+    S = 40
+    for _ in range(S):
+        w = p * (1 + r.uniform(-u, u, p.shape))
+        o = (w @ v[0, 0]) / w.sum(axis=1)[:, None] * (1 + r.uniform(-u, u, (N, d)))
+        dp = do[0, 0] @ v[0, 0].T
+        ds = p * (dp - (do[0, 0] * o).sum(axis=1)[:, None]) * (1 + r.uniform(-u, u, p.shape))
+        g = (s * ds @ k[0, 0], s * ds.T @ q[0, 0], (p * (1 + r.uniform(-u, u, p.shape))).T @ do[0, 0])
+        for i in range(3):
+            sq[i] += (g[i] - ref[i][0, 0]) ** 2
+    for i in range(3):
+        ratio = math.sqrt((sq[i] / S).mean()) / math.sqrt((sig[i] ** 2).mean())
+        assert 0.4 < ratio < 1.1, (i, ratio)
+
+
 ALL_PINS = [pin_worked_example, pin_closed_forms, pin_invariants, pin_backward_fd,
             pin_dvec, pin_backward_rows, pin_library, pin_block_masks, pin_decode, pin_philox, pin_dropout, pin_fp8,
-            pin_visibility]
+            pin_visibility, pin_grad_error_model]

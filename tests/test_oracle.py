@@ -48,10 +48,3 @@ def test_fully_masked_row_convention():
     dq, dk, dv, _ = orc.backward(q, k, v, do, 0.5, block_mask=bm, block=4)
     assert np.all(dq[0, 0, 4:] == 0)
     assert np.all(dk[0, 0, 4:] == 0) and np.all(dv[0, 0, 4:] == 0)
-
-
-def test_flop_convention():
-    assert orc.flops(1, 1, 128, 64) == 4 * 128 * 128 * 64
-    assert orc.flops(2, 16, 4096, 128, causal=True, backward=True) == \
-        4 * 2 * 16 * 4096 ** 2 * 128 * 2.5 / 2
-    assert math.isclose(orc.flops(1, 1, 256, 64, density=0.25), 4 * 256 * 256 * 64 / 4)

@@ -11,7 +11,8 @@ _real = {name: getattr(orc, name) for name in
          ("_scores", "_apply_mask", "_row_softmax", "_softmax_backward", "visible",
           "forward", "backward", "tiled_forward", "_lse", "window_block_mask", "dilated_block_mask",
           "decode_visible", "decode", "decode_split", "philox4x32_10", "dropout_bytes",
-          "forward_dropout", "backward_dropout", "e4m3_decode", "forward_fp8", "fp8_error_model")}
+          "forward_dropout", "backward_dropout", "e4m3_decode", "forward_fp8", "fp8_error_model",
+          "grad_error_model")}
 
 
 def _m_no_scale(q, k, scale):
@@ -249,6 +250,19 @@ def _m_fp8_sigma_halved(o, probs, v, rel=2.0 ** -4):
     return bound, sigma / 2
 
 
+def _m_grad_sigma_halved(*a, **kw):
+    sig, acc = _real["grad_error_model"](*a, **kw)
+    return tuple(x / 2 for x in sig), acc
+
+
+def _m_grad_ds_rounding_dropped(q, k, v, do, scale, causal=False, block_mask=None, block=128, row_chunk=1024,
+                                u=orc.BF16_U, f32=orc.FP32_STEP):
+    """The model without the bf16 rounding of dS and O (dQ and dK keep only fp32 terms)."""
+    sig, acc = _real["grad_error_model"](q, k, v, do, scale, causal, block_mask, block, row_chunk, u=0.0, f32=f32)
+    sig_v, _ = _real["grad_error_model"](q, k, v, do, scale, causal, block_mask, block, row_chunk, u=u, f32=f32)
+    return (sig[0], sig[1], sig_v[2]), acc
+
+
 MUTANTS = {
     "scale_dropped": ("_scores", _m_no_scale),
     "scores_transposed": ("_scores", _m_transposed_scores),
@@ -280,6 +294,8 @@ MUTANTS = {
     "e4m3_subnormals_as_normal": ("e4m3_decode", _m_e4m3_no_subnormal),
     "fp8_v_descale_dropped": ("forward_fp8", _m_fp8_v_descale_dropped),
     "fp8_sigma_halved": ("fp8_error_model", _m_fp8_sigma_halved),
+    "grad_sigma_halved": ("grad_error_model", _m_grad_sigma_halved),
+    "grad_ds_rounding_dropped": ("grad_error_model", _m_grad_ds_rounding_dropped),
 }
 
 

@@ -4,7 +4,9 @@ mask kind (none, causal, random block mask, block mask with the causal flag,
 sliding window) and dropout drawn from one fixed generator, so every run
 checks the same 24 cases.  Tolerances as in the other parity tests: O within
 1e-2 + 2^-8 |O|, LSE relative 1e-3 (against max(|LSE|, 1)), gradients
-relative L2 2e-2 (reference norm floored at an RMS of 1e-3).
+relative L2 2e-2 per tensor and per 128-row tile (reference norm floored at an
+RMS of 1e-3) and, without dropout, every element inside the oracle's gradient
+error model.
 """
 import math
 
@@ -14,6 +16,7 @@ import torch
 
 from attn_fwd_gb300.inputs import make_qkvdo
 import oracle
+from tests.parity_checks import check_bwd, oracle_bwd
 
 pytestmark = pytest.mark.gpu
 
@@ -55,11 +58,6 @@ def _mask(N, kind, seed):
     return None
 
 
-def _rel_l2(g, r):
-    g = g.float().cpu().numpy()
-    return np.linalg.norm(g - r) / max(np.linalg.norm(r), 1e-3 * np.sqrt(r.size))
-
-
 @pytest.mark.parametrize("i,B,H,N,d,mask,drop", _cases())
 def test_random_configuration(fa, i, B, H, N, d, mask, drop):
     what = f"case {i}: B{B} H{H} N{N} d{d} mask={mask} dropout={drop}"
@@ -77,6 +75,7 @@ def test_random_configuration(fa, i, B, H, N, d, mask, drop):
     assert fa.fa_get_device_error() == 0, what
     f64 = {n: t[n].double().numpy() for n in ("q", "k", "v", "do")}
     bmn = None if bm is None else bm.numpy()
+    model = None
     if drop:
         ro, rl = oracle.forward_dropout(f64["q"], f64["k"], f64["v"], scale, drop, seed, causal=causal,
                                         block_mask=bmn)
@@ -84,7 +83,7 @@ def test_random_configuration(fa, i, B, H, N, d, mask, drop):
                                       block_mask=bmn)[:3]
     else:
         ro, rl = oracle.forward(f64["q"], f64["k"], f64["v"], scale, causal=causal, block_mask=bmn)
-        ref = oracle.backward(f64["q"], f64["k"], f64["v"], f64["do"], scale, causal=causal, block_mask=bmn)[:3]
+        ref, model = oracle_bwd(f64, scale, causal, bmn)
     og, lg = o.float().cpu().numpy(), lse.cpu().numpy()
     assert np.isfinite(og).all(), what
     excess = (np.abs(og - ro) - (1e-2 + 2.0 ** -8 * np.abs(ro))).max()
@@ -94,7 +93,4 @@ def test_random_configuration(fa, i, B, H, N, d, mask, drop):
     if fin.any():
         lerr = (np.abs(lg[fin] - rl[fin]) / np.maximum(np.abs(rl[fin]), 1.0)).max()
         assert lerr <= 1e-3, f"{what}: LSE rel error {lerr}"
-    for name, g, r in zip(("dQ", "dK", "dV"), (dq, dk, dv), ref):
-        assert torch.isfinite(g).all(), f"{what}: {name} not finite"
-        rel = _rel_l2(g, r)
-        assert rel <= 2e-2, f"{what}: {name} rel-L2 {rel}"
+    check_bwd((dq, dk, dv), ref, what, model)
