@@ -679,53 +679,33 @@ int fa_debug_wait_timeout(uint64_t timeout_ns, fa_stream_t stream) {
 }  // extern "C"
 
 // --------------------------------------------------------------------------
-// fa_bwd_noalloc: the backward with its workspace in a static device array,
-// for callers that cannot allocate device memory on the compute path.
+// the steps of fa_bwd, for entry points in other translation units that
+// supply the workspace themselves (fa_noalloc.cu)
 // --------------------------------------------------------------------------
-namespace {
+namespace fa {
 
-// File-scope device array: its name in host code is only a stand-in, so the
-// device address comes from cudaGetSymbolAddress, once per device.
-static __device__ __align__(256) unsigned char g_noalloc_scratch[FA_NOALLOC_SCRATCH_BYTES];
+int api_check_shape(int B, int H, int N, int d) { return check_shape(B, H, N, d); }
 
-struct ScratchState {
-  std::once_flag once;
-  void* ptr = nullptr;
-  cudaError_t err = cudaSuccess;
-};
-ScratchState g_scratch[kMaxDevices];
-
-// Device address of the scratch array on the current device (looked up the
-// first time this device asks, with the device current).
-int scratch_ready(void** out) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FA_ERR_CUDA;
-  ScratchState& st = g_scratch[dev];
-  std::call_once(st.once, [&] { st.err = cudaGetSymbolAddress(&st.ptr, g_noalloc_scratch); });
-  if (st.err != cudaSuccess || st.ptr == nullptr) return FA_ERR_CUDA;
-  *out = st.ptr;
-  return FA_OK;
-}
-
-}  // namespace
-
-extern "C" int fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const void* dout,
-                              const float* lse, void* dq, void* dk, void* dv, int B, int H, int N, int d,
-                              float scale, int causal, fa_stream_t stream) {
+int api_check_bwd_args(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                       const float* lse, const void* dq, const void* dk, const void* dv, float scale) {
   int rc;
-  if ((rc = check_shape(B, H, N, d)) != FA_OK) return rc;
-  const size_t need = fa_bwd_workspace_bytes(B, H, N, d);
-  if (need == 0) return FA_ERR_INVALID;
-  if (need > FA_NOALLOC_SCRATCH_BYTES) return FA_ERR_SCRATCH;
   if ((rc = check_ptrs({q, k, v, o, dout, lse, dq, dk, dv})) != FA_OK) return rc;
-  if ((rc = check_scale(scale)) != FA_OK) return rc;
-  int* status = nullptr;
-  if ((rc = device_ready(&status)) != FA_OK) return rc;
-  void* ws = nullptr;
-  if ((rc = scratch_ready(&ws)) != FA_OK) return rc;
-  return bwd_impl(q, k, v, o, dout, lse, nullptr, dq, dk, dv, ws, B, H, N, d, scale,
-                  causal ? fa::MASK_CAUSAL : fa::MASK_NONE, 0.f, 0, stream);
+  return check_scale(scale);
 }
+
+int api_device_ready() {
+  int* status = nullptr;
+  return device_ready(&status);
+}
+
+int api_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
+            void* dq, void* dk, void* dv, void* workspace, int B, int H, int N, int d, float scale, int causal,
+            cudaStream_t stream) {
+  return bwd_impl(q, k, v, o, dout, lse, nullptr, dq, dk, dv, workspace, B, H, N, d, scale,
+                  causal ? MASK_CAUSAL : MASK_NONE, 0.f, 0, reinterpret_cast<fa_stream_t>(stream));
+}
+
+}  // namespace fa
 
 // --------------------------------------------------------------------------
 // fa_fwd_bwd_host: forward and backward of tensors in (pinned) host memory,

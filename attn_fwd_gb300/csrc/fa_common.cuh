@@ -159,4 +159,16 @@ int launch_bwd_dq_convert(const float* dq_acc, __nv_bfloat16* dq, long long n, f
                           cudaStream_t stream);
 int launch_wait_timeout_probe(int* status, uint64_t timeout_ns, cudaStream_t stream);
 
+// Steps of fa_bwd (fa_api.cu) for entry points that supply the workspace
+// themselves: the shape check, the pointer and scale checks, the device check
+// (compute capability 10.3), and the three backward stages on `workspace`.
+// Each returns FA_OK (0) or an fa_status code.
+int api_check_shape(int B, int H, int N, int d);
+int api_check_bwd_args(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                       const float* lse, const void* dq, const void* dk, const void* dv, float scale);
+int api_device_ready();
+int api_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
+            void* dq, void* dk, void* dv, void* workspace, int B, int H, int N, int d, float scale, int causal,
+            cudaStream_t stream);
+
 }  // namespace fa

@@ -9,6 +9,7 @@ missing or fails to load, every call raises: there is no fallback.
 from __future__ import annotations
 
 import ctypes
+import functools
 import os
 import threading
 
@@ -98,6 +99,26 @@ def _check(fn: str, rc: int):
         raise FAError(fn, rc)
 
 
+def _on_device(pick):
+    """Run the wrapped entry point with the device of its tensors current: the
+    library launches on the current device (its status word, its SM count,
+    the scratch array of fa_bwd_noalloc) and the default stream is that
+    device's current stream.  `pick` chooses the tensor from the arguments."""
+    def wrap(fn):
+        @functools.wraps(fn)
+        def run(*args, **kwargs):
+            t = pick(*args, **kwargs)
+            if isinstance(t, torch.Tensor) and t.is_cuda:
+                with torch.cuda.device(t.device):
+                    return fn(*args, **kwargs)
+            return fn(*args, **kwargs)
+        return run
+    return wrap
+
+
+_first = _on_device(lambda *a, **k: a[0] if a else None)
+
+
 def _stream(stream):
     if stream is None:
         stream = torch.cuda.current_stream()
@@ -135,6 +156,7 @@ def fa_version() -> int:
     return load().fa_version()
 
 
+@_first
 def fa_fwd(q, k, v, o, lse, scale, causal=False, stream=None):
     B, H, N, d = q.shape
     rc = load().fa_fwd(_bf16(q, "q"), _bf16(k, "k"), _bf16(v, "v"), _bf16(o, "o"), _f32(lse, "lse"),
@@ -142,6 +164,7 @@ def fa_fwd(q, k, v, o, lse, scale, causal=False, stream=None):
     _check("fa_fwd", rc)
 
 
+@_first
 def fa_fwd_blocksparse(q, k, v, o, lse, block_mask, scale, causal=False, stream=None):
     B, H, N, d = q.shape
     rc = load().fa_fwd_blocksparse(_bf16(q, "q"), _bf16(k, "k"), _bf16(v, "v"), _bf16(o, "o"),
@@ -154,6 +177,7 @@ def fa_bwd_workspace_bytes(B, H, N, d) -> int:
     return load().fa_bwd_workspace_bytes(B, H, N, d)
 
 
+@_first
 def fa_bwd(q, k, v, o, do, lse, dq, dk, dv, workspace, scale, causal=False, stream=None):
     B, H, N, d = q.shape
     rc = load().fa_bwd(_bf16(q, "q"), _bf16(k, "k"), _bf16(v, "v"), _bf16(o, "o"), _bf16(do, "do"),
@@ -163,6 +187,7 @@ def fa_bwd(q, k, v, o, do, lse, dq, dk, dv, workspace, scale, causal=False, stre
     _check("fa_bwd", rc)
 
 
+@_first
 def fa_bwd_blocksparse(q, k, v, o, do, lse, block_mask, dq, dk, dv, workspace, scale, causal=False, stream=None):
     B, H, N, d = q.shape
     rc = load().fa_bwd_blocksparse(_bf16(q, "q"), _bf16(k, "k"), _bf16(v, "v"), _bf16(o, "o"),
@@ -173,6 +198,7 @@ def fa_bwd_blocksparse(q, k, v, o, do, lse, block_mask, dq, dk, dv, workspace, s
     _check("fa_bwd_blocksparse", rc)
 
 
+@_first
 def fa_bwd_preprocess(o, do, lse, workspace, stream=None):
     B, H, N, d = o.shape
     rc = load().fa_bwd_preprocess(_bf16(o, "o"), _bf16(do, "do"), _f32(lse, "lse"),
@@ -180,6 +206,7 @@ def fa_bwd_preprocess(o, do, lse, workspace, stream=None):
     _check("fa_bwd_preprocess", rc)
 
 
+@_first
 def fa_bwd_main(q, k, v, do, block_mask, dk, dv, workspace, scale, mask_kind, dropout_p=0.0, seed=0,
                 stream=None):
     B, H, N, d = q.shape
@@ -190,6 +217,7 @@ def fa_bwd_main(q, k, v, do, block_mask, dk, dv, workspace, scale, mask_kind, dr
     _check("fa_bwd_main", rc)
 
 
+@_first
 def fa_fwd_dropout(q, k, v, o, lse, block_mask, scale, causal, dropout_p, seed, stream=None):
     B, H, N, d = q.shape
     rc = load().fa_fwd_dropout(_bf16(q, "q"), _bf16(k, "k"), _bf16(v, "v"), _bf16(o, "o"), _f32(lse, "lse"),
@@ -198,6 +226,7 @@ def fa_fwd_dropout(q, k, v, o, lse, block_mask, scale, causal, dropout_p, seed, 
     _check("fa_fwd_dropout", rc)
 
 
+@_first
 def fa_bwd_dropout(q, k, v, o, do, lse, block_mask, dq, dk, dv, workspace, scale, causal, dropout_p, seed,
                    stream=None):
     B, H, N, d = q.shape
@@ -208,6 +237,7 @@ def fa_bwd_dropout(q, k, v, o, do, lse, block_mask, dq, dk, dv, workspace, scale
     _check("fa_bwd_dropout", rc)
 
 
+@_first
 def fa_bwd_dq_convert(workspace, dq, scale, stream=None):
     B, H, N, d = dq.shape
     rc = load().fa_bwd_dq_convert(ctypes.c_void_p(workspace.data_ptr()), _bf16(dq, "dq"), B, H, N, d,
@@ -215,6 +245,7 @@ def fa_bwd_dq_convert(workspace, dq, scale, stream=None):
     _check("fa_bwd_dq_convert", rc)
 
 
+@_first
 def fa_bwd_noalloc(q, k, v, o, do, lse, dq, dk, dv, scale, causal=False, stream=None):
     """fa_bwd without a workspace argument: the library uses its own static
     device scratch (see include/fa.h), so this call allocates nothing."""
@@ -235,6 +266,7 @@ def fa_fwd_bwd_host_workspace_bytes(B, H, N, d) -> int:
     return load().fa_fwd_bwd_host_workspace_bytes(B, H, N, d)
 
 
+@_on_device(lambda *a, **k: k.get("workspace", a[10] if len(a) > 10 else None))
 def fa_fwd_bwd_host(q, k, v, do, o, lse, dq, dk, dv, block_mask, workspace, scale, causal=False, stream=None):
     """Forward and backward of host tensors (pinned for overlap), streamed
     through the device in chunks of heads; see include/fa.h."""
@@ -252,6 +284,7 @@ def fa_fwd_host_workspace_bytes(B, H, N, d) -> int:
     return load().fa_fwd_host_workspace_bytes(B, H, N, d)
 
 
+@_on_device(lambda *a, **k: k.get("workspace", a[6] if len(a) > 6 else None))
 def fa_fwd_host(q, k, v, o, lse, block_mask, workspace, scale, causal=False, stream=None):
     """The forward of host tensors (pinned for overlap), streamed through the
     device in chunks of heads; see include/fa.h."""
@@ -269,6 +302,7 @@ def fa_decode_workspace_bytes(B, H, Nq, Nk, d) -> int:
     return load().fa_decode_workspace_bytes(B, H, Nq, Nk, d)
 
 
+@_first
 def fa_decode(q, k, v, o, lse, seqlens_k, scale, causal=False, workspace=None, stream=None):
     """q, o [B,H,Nq,d]; k, v [B,H,Nk,d]; lse [B,H,Nq]; seqlens_k int32 [B] or None."""
     B, H, Nq, d = q.shape
@@ -305,6 +339,7 @@ def _descale(t, name, n):
     return ctypes.c_void_p(t.data_ptr())
 
 
+@_first
 def fa_fwd_fp8(q, k, v, o, lse, q_descale, k_descale, v_descale, scale, causal, workspace, stream=None):
     B, H, N, d = q.shape
     rc = load().fa_fwd_fp8(_fp8(q, "q"), _fp8(k, "k"), _fp8(v, "v"), _bf16(o, "o"), _f32(lse, "lse"),

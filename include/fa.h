@@ -281,13 +281,17 @@ FA_API int fa_decode(const void *q, const void *k, const void *v, void *o, float
  * up front, or a plugin inside a host framework that owns the allocator and
  * forbids side allocations.  They still pass every input and output buffer;
  * only the fp32 dQ accumulator and the D vector move into a file-scope
- * device array of FA_NOALLOC_SCRATCH_BYTES inside libfa.so, which every GPU
- * that loads the library holds until the process exits.
+ * device array of FA_NOALLOC_SCRATCH_BYTES inside libfa.so.  The array is a
+ * CUDA module of its own: under lazy module loading (the CUDA runtime's
+ * default) a device holds it from the first call of this entry point there
+ * until the process exits; with eager loading (CUDA_MODULE_LOADING=EAGER),
+ * every device that loads the library holds it.
  *
  * Behaviour:
  *   - Returns FA_ERR_SCRATCH, without enqueuing anything, when
  *     fa_bwd_workspace_bytes(B, H, N, d) exceeds FA_NOALLOC_SCRATCH_BYTES;
- *     the other argument checks are those of fa_bwd.
+ *     the other argument checks are those of fa_bwd, and q must live on
+ *     the current device (FA_ERR_INVALID otherwise).
  *   - The first call on each device looks up the device address of the
  *     array (cudaGetSymbolAddress, with that device current).  Make that
  *     first call before any stream capture on that device.
