@@ -4,6 +4,8 @@ Imported only by ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s
 CPU-baseline leg and reference arm.  It shares no code with the CUDA path.
 """
 from .attention import (  # noqa: F401
+    BF16_U,
+    FP32_STEP,
     NEG_INF,
     backward,
     backward_rows,
@@ -17,6 +19,7 @@ from .attention import (  # noqa: F401
     dropout_threshold,
     e4m3_decode,
     forward_dropout,
+    forward_error_bound,
     forward_fp8,
     fp8_error_model,
     grad_error_model,

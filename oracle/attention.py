@@ -560,6 +560,35 @@ BF16_U = 2.0 ** -8      # unit roundoff of bf16 (8 significant bits, round to ne
 FP32_STEP = 2.0 ** -23  # one fp32 rounding step, truncation included (24 significant bits)
 
 
+def forward_error_bound(q, k, v, scale, causal=False, block_mask=None, block=128, row_chunk=None,
+                        u: float = BF16_U, rows=None):
+    """Worst-case effect on O of feeding the probabilities to the P V product
+    as bf16, per element [B, H, N, dv].
+
+    O_i = sum_j w_ij V_j with weights w = P (1 + e), |e_ij| <= u (u = 2^-8),
+    divided by the sum of the rounded weights or by the exact one.  To first
+    order the first moves O_i by sum_j P_ij e_ij (V_j - O_i), the second by
+    sum_j P_ij e_ij V_j; both are at most u sum_j P_ij (|V_j| + |O_i|) =
+    u ((P |V|)_i + |O_i|).  With bf16 inputs this rounding is unavoidable, and
+    on peaked rows with large |V| (two keys of weight 1/2 whose V differ by
+    20 move O by up to 2^-8 x 10) it exceeds a fixed 1e-2 on its own.  Query
+    rows are taken in chunks of ``row_chunk`` full rows; with ``rows``, only
+    those query rows (the result is then [B, H, len(rows), dv])."""
+    q, k, v = (np.asarray(x, dtype=np.float64) for x in (q, k, v))
+    B, H, N, _ = q.shape
+    sel = np.arange(N) if rows is None else np.asarray(rows)
+    out = np.zeros((B, H, len(sel), v.shape[-1]))
+    step = len(sel) if row_chunk is None else row_chunk
+    for b in range(B):
+        for h in range(H):
+            av = np.abs(v[b, h])
+            for r0 in range(0, len(sel), step):
+                idx = np.arange(r0, min(len(sel), r0 + step))
+                p, _ = head_probs(q[b, h], k[b, h], scale, causal, block_mask, block, sel[idx])
+                out[b, h, idx] = u * (p @ av + np.abs(p @ v[b, h]))
+    return out
+
+
 def grad_error_model(q, k, v, do, scale, causal=False, block_mask=None, block=128,
                      row_chunk: int = 1024, u: float = BF16_U, f32: float = FP32_STEP):
     """Per-element error scale of dQ, dK, dV computed from bf16 inputs with

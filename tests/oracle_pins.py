@@ -627,6 +627,42 @@ def pin_grad_error_model(orc):
         assert 0.4 < ratio < 1.1, (i, ratio)
 
 
+def pin_forward_error_bound(orc):
+    """The forward's P-rounding bound against the rounding it describes: a
+    forward whose P V product takes round-to-nearest-even bf16 weights,
+    normalised by the rounded or by the exact row sum, stays inside
+    u ((P |V|) + |O|) everywhere, also on x3 inputs with peaked rows; on
+    those rows the rounding alone exceeds 1e-2; and moving 1 % of a row's
+    weight to another key breaks the bound."""
+    u = orc.BF16_U
+    r = _rng(61)
+    seen_big = False
+    for B, H, N, d, amp, causal in ((1, 2, 192, 64, 3.0, True), (1, 1, 256, 128, 1.0, False),
+                                    (1, 1, 300, 64, 3.0, False)):
+        q, k, v = (_bf16(r.standard_normal((B, H, N, d)) * amp) for _ in range(3))
+        s = 1 / math.sqrt(d)
+        o, _ = orc.forward(q, k, v, s, causal=causal)
+        bound = orc.forward_error_bound(q, k, v, s, causal=causal, row_chunk=100)
+        vis = _dense_mask_torch(N, causal).numpy()
+        for b in range(B):
+            for h in range(H):
+                sc = np.where(vis, s * (q[b, h] @ k[b, h].T), -np.inf)
+                f = np.exp(sc - sc.max(axis=1)[:, None])
+                fh = _bf16(f)
+                for den in (fh.sum(axis=1), f.sum(axis=1)):
+                    err = np.abs((fh @ v[b, h]) / den[:, None] - o[b, h])
+                    assert np.all(err <= bound[b, h] * (1 + 1e-6) + 1e-12)
+                    seen_big |= bool(err.max() > 1e-2)
+                # a wrong weight: 1 % of each row's mass moved to key 0
+                p = f / f.sum(axis=1)[:, None]
+                pw = 0.99 * p
+                pw[:, 0] += 0.01
+                err = np.abs(pw @ v[b, h] - o[b, h])
+                assert np.any(err > bound[b, h])
+    assert seen_big
+
+
 ALL_PINS = [pin_worked_example, pin_closed_forms, pin_invariants, pin_backward_fd,
             pin_dvec, pin_backward_rows, pin_library, pin_block_masks, pin_decode, pin_philox, pin_dropout, pin_fp8,
-            pin_visibility, pin_grad_error_model]
+            pin_visibility, pin_grad_error_model,
+            pin_forward_error_bound]

@@ -29,16 +29,20 @@ def np64(t):
     return t.double().numpy()
 
 
-def check_fwd(o_gpu, lse_gpu, o_ref, lse_ref, what=""):
+def check_fwd(o_gpu, lse_gpu, o_ref, lse_ref, what="", pbound=None):
+    """O within 1e-2 + 2^-8 |O_ref| (+ pbound: the oracle's bound on the
+    effect of bf16 probabilities in P V, used on inputs of amplitude > 1,
+    where that rounding alone can exceed 1e-2); LSE relative 1e-3."""
     o_gpu = o_gpu.float().cpu().numpy()
     lse_gpu = lse_gpu.float().cpu().numpy()
     assert np.isfinite(o_gpu).all(), what
     err_o = np.abs(o_gpu - o_ref).max()
-    excess = (np.abs(o_gpu - o_ref) - (O_ATOL + BF16_HALF_ULP_REL * np.abs(o_ref))).max()
+    limit = O_ATOL + BF16_HALF_ULP_REL * np.abs(o_ref) + (0.0 if pbound is None else pbound)
+    excess = (np.abs(o_gpu - o_ref) - limit).max()
     fin = np.isfinite(lse_ref)
     assert np.array_equal(np.isfinite(lse_gpu), fin), what
     err_l = (np.abs(lse_gpu[fin] - lse_ref[fin]) / np.maximum(np.abs(lse_ref[fin]), 1.0)).max() if fin.any() else 0.0
-    assert excess <= 0, f"{what}: O error {err_o} exceeds 1e-2 + 2^-8|O| by {excess}"
+    assert excess <= 0, f"{what}: O error {err_o} exceeds its bound by {excess}"
     assert err_l <= LSE_RTOL, f"{what}: LSE rel error {err_l}"
     return err_o, err_l
 

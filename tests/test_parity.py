@@ -206,16 +206,18 @@ def test_forward_workload_long_causal(fa):
     whole = _sampled_heads(w.H, 8, seed=3)
     for h in whole:
         sl = (slice(0, 1), slice(h, h + 1))
-        ro, rl = oracle.forward(np64(t["q"][sl]), np64(t["k"][sl]), np64(t["v"][sl]), w.scale, causal=True,
-                                row_chunk=2048)
-        check_fwd(o[sl], lse[sl], ro, rl, f"N=16384 whole head {h}")
+        q64, k64, v64 = np64(t["q"][sl]), np64(t["k"][sl]), np64(t["v"][sl])
+        ro, rl = oracle.forward(q64, k64, v64, w.scale, causal=True, row_chunk=2048)
+        pb = oracle.forward_error_bound(q64, k64, v64, w.scale, causal=True, row_chunk=2048)
+        check_fwd(o[sl], lse[sl], ro, rl, f"N=16384 whole head {h}", pb)
     r = np.random.default_rng(3)
     rows = sorted(set([0, 1, 127, 128, w.N - 1] + r.choice(w.N, 59, replace=False).tolist()))
     for h in [x for x in range(w.H) if x not in whole][:4]:
         sl = (slice(0, 1), slice(h, h + 1))
-        ro, rl = oracle.forward_rows(np64(t["q"][sl]), np64(t["k"][sl]), np64(t["v"][sl]), w.scale,
-                                     0, 0, rows, causal=True)
-        check_fwd(o[0, h, rows], lse[0, h, rows], ro, rl, f"N=16384 head {h}")
+        q64, k64, v64 = np64(t["q"][sl]), np64(t["k"][sl]), np64(t["v"][sl])
+        ro, rl = oracle.forward_rows(q64, k64, v64, w.scale, 0, 0, rows, causal=True)
+        pb = oracle.forward_error_bound(q64, k64, v64, w.scale, causal=True, rows=rows)[0, 0]
+        check_fwd(o[0, h, rows], lse[0, h, rows], ro, rl, f"N=16384 head {h}", pb)
 
 
 # --------------------------------------------------------------------------- #
