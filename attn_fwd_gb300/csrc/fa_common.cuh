@@ -52,8 +52,10 @@ struct FwdParams {
   int mask_kind;
   int H;                     // heads: (b, h) = divmod(bh, H) keys the dropout generator
   Dropout drop;
-  int max_ctas;              // persistent grid size for dense and causal masks (one CTA per SM)
+  int max_ctas;              // persistent grid size (one CTA per SM)
+  int band_heads;            // dense and causal masks: heads per band of the item order (BH: one band)
 };
+
 
 // Backward main-kernel parameters.  Q and dO use a {64, BQ, 1} box, K and V a
 // {64, 128, 1} box.

@@ -221,6 +221,41 @@ __device__ __forceinline__ bool dense_visible(const FwdParams& p, int qt, int kt
   return p.mask_kind != MASK_CAUSAL || kt <= qt;
 }
 
+// Banded item order (dense and causal masks whose heads' K and V outgrow
+// L2).  The items -- pairs of query tiles of one (batch, head) -- are cut
+// into bands of `band_heads` heads, so that the items of one band run
+// together and its heads' K and V stay in L2 while they do.  Within a band
+// the positions go pair-major (decreasing length when causal), heads
+// fastest.  CTA c of G takes band positions c, 2G-1-c, 2G+c, 4G-1-c, ...
+// (a zig-zag: long and short causal pairs even out), band after band;
+// successive bands mirror the CTA index and every second band rotates it, so
+// that a CTA drawing the heavier end of one band's partial last round draws
+// the lighter end of the next.  Item k of CTA c, encoded as
+// j = bh + BH * position, or -1 when c has fewer items.
+__device__ __forceinline__ int banded_item(const FwdParams& p, int c, int k) {
+  const int G = static_cast<int>(gridDim.x);
+  const int bhd = p.band_heads;
+  const int nb = (p.BH + bhd - 1) / bhd;
+  const int half = nb >= 2 ? nb / 2 : 1;
+  for (int b = 0; b < nb; ++b) {
+    const int heads = min(bhd, p.BH - b * bhd);
+    const int m = heads * p.n_pairs;
+    const int x = (c + (b >> 1) * (G / half)) % G;
+    const int cc = (b & 1) ? G - 1 - x : x;
+    // rounds 0 .. m / G - 1 give the CTA one position each; the partial
+    // round m / G gives one when the CTA's position falls inside the band
+    const int full = m / G;
+    const int jp = full * G + ((full & 1) ? G - 1 - cc : cc);
+    const int count = full + (jp < m ? 1 : 0);
+    if (k < count) {
+      const int jj = k * G + ((k & 1) ? G - 1 - cc : cc);
+      return b * bhd + jj % heads + p.BH * (jj / heads);
+    }
+    k -= count;
+  }
+  return -1;
+}
+
 // Bounded wait used only while tearing down after a failure: ignores the
 // abort flag, gives up after `ns`.
 __device__ __forceinline__ void mbar_drain(uint32_t bar, uint32_t parity, uint64_t ns) {
@@ -230,7 +265,7 @@ __device__ __forceinline__ void mbar_drain(uint32_t bar, uint32_t parity, uint64
   }
 }
 
-template <int D, bool SPARSE, bool DROP>
+template <int D, bool SPARSE, bool DROP, bool BANDED>
 __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ FwdParams p) {
   using L = FwdLayout<D, SPARSE>;
   // P V of a tile issued in two halves (the first once half of P is stored)
@@ -251,9 +286,11 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
   // head)s, head fastest, pairs in decreasing length when causal.  The grid
   // is persistent for dense and causal masks (at most one CTA per SM): CTA c
   // takes items c, 2G - 1 - c, 2G + c, ... (G CTAs), so the long and short
-  // causal pairs even out; one item per CTA with a block mask.
+  // causal pairs even out; one item per CTA with a block mask.  BANDED: the
+  // order of banded_item (the heads cut into bands that fit L2).
   const int n_items = p.n_pairs * p.BH;
   auto item_index = [&](int k) {
+    if constexpr (BANDED) return banded_item(p, static_cast<int>(blockIdx.x), k);
     const int G = static_cast<int>(gridDim.x), c = static_cast<int>(blockIdx.x);
     const int j = k * G + ((k & 1) ? G - 1 - c : c);
     return (SPARSE && k > 0) || j >= n_items ? -1 : j;
@@ -765,8 +802,12 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
       // ---------------------------------------------------------- epilogue
       if (ok) {
         // rows beyond N (ragged last query tile) are computed but not stored
-        const bool row_ok = qt * TILE + row < p.N;
-        const size_t grow = static_cast<size_t>(bh) * p.N + static_cast<size_t>(qt) * TILE + row;
+        // (banded order: the item recomputed here instead of kept in
+        // registers across the row loop)
+        const int qt_e = BANDED ? item_info(item_index(k)).qt0 + w : qt;
+        const int bh_e = BANDED ? item_index(k) % p.BH : bh;
+        const bool row_ok = qt_e * TILE + row < p.N;
+        const size_t grow = static_cast<size_t>(bh_e) * p.N + static_cast<size_t>(qt_e) * TILE + row;
         __nv_bfloat16* orow = p.o + grow * D;
         if (n_vis > 0) {
           ok = mbar_wait_warp(bar(L::B_O + w), n_out & 1, wc);
@@ -812,27 +853,32 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
   }
 }
 
-template <int D, bool SPARSE, bool DROP>
+template <int D, bool SPARSE, bool DROP, bool BANDED = false>
 static int launch_fwd_t(const FwdParams& p, cudaStream_t stream) {
   using L = FwdLayout<D, SPARSE>;
   static_assert(L::SMEM_BYTES <= 232448, "shared memory budget");
   static SmemAttrOnce attr;
-  if (!attr.ensure(reinterpret_cast<const void*>(fa_fwd_kernel<D, SPARSE, DROP>), L::SMEM_BYTES)) return -4;
+  if (!attr.ensure(reinterpret_cast<const void*>(fa_fwd_kernel<D, SPARSE, DROP, BANDED>), L::SMEM_BYTES)) return -4;
   const long long items = static_cast<long long>(p.n_pairs) * p.BH;
   const long long grid = SPARSE ? items : (items < p.max_ctas ? items : p.max_ctas);
-  fa_fwd_kernel<D, SPARSE, DROP><<<static_cast<unsigned>(grid), L::THREADS, L::SMEM_BYTES, stream>>>(p);
+  fa_fwd_kernel<D, SPARSE, DROP, BANDED><<<static_cast<unsigned>(grid), L::THREADS, L::SMEM_BYTES, stream>>>(p);
   return cudaGetLastError() == cudaSuccess ? 0 : -4;
 }
 
 int launch_fwd(const FwdParams& p, int d, cudaStream_t stream) {
   const bool sparse = (p.mask_kind & MASK_BLOCK) != 0;
   const bool drop = p.drop.t != 0;
+  // the banded order only where it was asked for (dense and causal masks
+  // without dropout whose heads' K and V outgrow L2)
+  const bool banded = !sparse && !drop && p.band_heads < p.BH;
   if (d == 128) {
     if (drop) return sparse ? launch_fwd_t<128, true, true>(p, stream) : launch_fwd_t<128, false, true>(p, stream);
+    if (banded) return launch_fwd_t<128, false, false, true>(p, stream);
     return sparse ? launch_fwd_t<128, true, false>(p, stream) : launch_fwd_t<128, false, false>(p, stream);
   }
   if (d == 64) {
     if (drop) return sparse ? launch_fwd_t<64, true, true>(p, stream) : launch_fwd_t<64, false, true>(p, stream);
+    if (banded) return launch_fwd_t<64, false, false, true>(p, stream);
     return sparse ? launch_fwd_t<64, true, false>(p, stream) : launch_fwd_t<64, false, false>(p, stream);
   }
   return -2;

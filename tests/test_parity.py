@@ -193,6 +193,38 @@ def test_forward_persistent_items(fa, B, H, N, d, causal):
         check_fwd(o[sl], lse[sl], ro, rl, f"B{B} H{H} N{N} d{d} head {hh}")
 
 
+BANDED = [
+    # B, H, N, d, causal: heads whose K and V outgrow the forward's L2 budget,
+    # so the persistent CTAs walk the items band by band (odd band counts,
+    # ragged N, d = 64)
+    (1, 12, 8192, 128, False),
+    (2, 24, 16384, 64, True),
+    (1, 24, 9000, 128, False),
+]
+
+
+@pytest.mark.parametrize("B,H,N,d,causal", BANDED)
+def test_forward_banded_item_order(fa, B, H, N, d, causal):
+    """Every item of a banded launch is computed exactly where it belongs:
+    outputs start as NaN and none is left; sampled whole heads against the
+    oracle."""
+    t = make_qkvdo(B, H, N, d, seed=90 + H, with_dout=False)
+    scale = 1 / math.sqrt(d)
+    q, k, v = (dev(t[n]) for n in ("q", "k", "v"))
+    o = torch.full_like(q, float("nan"))
+    lse = torch.full((B, H, N), float("nan"), dtype=torch.float32, device="cuda")
+    fa.fa_fwd(q, k, v, o, lse, scale, causal=causal)
+    check_device_status(fa)
+    assert torch.isfinite(o).all() and torch.isfinite(lse).all()
+    o, lse = o.cpu(), lse.cpu()
+    for hh in sorted(set([0, B * H - 1] + _sampled_heads(B * H, 2, seed=N))):
+        b, h = divmod(hh, H)
+        sl = (slice(b, b + 1), slice(h, h + 1))
+        ro, rl = oracle.forward(np64(t["q"][sl]), np64(t["k"][sl]), np64(t["v"][sl]), scale, causal=causal,
+                                row_chunk=2048)
+        check_fwd(o[sl], lse[sl], ro, rl, f"banded B{B} H{H} N{N} d{d} head {hh}")
+
+
 def test_forward_workload_long_causal(fa):
     """N=16384 causal with x3 inputs: S would be 16 GiB.  Eight whole heads
     through the oracle (rows in chunks of 2048 full rows), and sampled rows of
