@@ -557,6 +557,7 @@ const char* fa_status_string(int status) {
     case FA_ERR_TIMEOUT: return "FA_ERR_TIMEOUT: a kernel wait exceeded the wait timeout";
     case FA_ERR_CUDA: return "FA_ERR_CUDA: CUDA runtime error";
     case FA_ERR_SCRATCH: return "FA_ERR_SCRATCH: the backward workspace would exceed the static scratch of fa_bwd_noalloc";
+    case FA_ERR_BOUNDS: return "FA_ERR_BOUNDS: a device index check of the debug build failed (access skipped)";
     default: return "unknown fa_status";
   }
 }
@@ -603,6 +604,11 @@ int fa_bwd_main(const void* q, const void* k, const void* v, const void* dout, c
                 unsigned long long seed, fa_stream_t stream) {
   return bwd_main_impl(q, k, v, dout, block_mask, dk, dv, workspace, B, H, N, d, scale, mask_kind, dropout_p, seed,
                        stream);
+}
+
+float fa_dropout_effective_p(float dropout_p) {
+  if (check_dropout(dropout_p) != FA_OK) return -1.f;
+  return static_cast<float>(make_dropout(dropout_p, 0).t) / 256.f;
 }
 
 int fa_fwd_dropout(const void* q, const void* k, const void* v, void* o, float* lse, const uint8_t* block_mask, int B,

@@ -130,8 +130,9 @@ __device__ __forceinline__ int build_sparse_column(const BwdParams& p, int kt, u
   int n = 0;
   for (int base = 0; base < p.n_kt; base += 32) {
     const int qb = base + static_cast<int>(lane);
+    const size_t at = static_cast<size_t>(qb) * p.n_kt + kt;
     const bool v = qb < p.n_kt && (!(p.mask_kind & MASK_CAUSAL) || qb >= kt) &&
-                   __ldg(p.block_mask + static_cast<size_t>(qb) * p.n_kt + kt) != 0;
+                   dcheck(at < static_cast<size_t>(p.n_kt) * p.n_kt, p.status) && __ldg(p.block_mask + at) != 0;
     const uint32_t m = __ballot_sync(0xffffffffu, v);
     if (v) list[n + __popc(m & ((1u << lane) - 1u))] = static_cast<uint16_t>(qb);
     n += __popc(m);
@@ -285,17 +286,20 @@ __global__ void __launch_bounds__(448, 1) fa_bwd_kernel(const __grid_constant__ 
         if (!mbar_wait(bar(L::B_EMPTY + st), ((step / L::STAGES) & 1) ^ 1, wc)) { ok = false; break; }
         const uint32_t fb = bar(L::B_FULL + st);
         const uint32_t sb = sbase + L::RING_OFF + st * L::STAGE_BYTES;
-        mbar_arrive_expect_tx(fb, 2 * L::Q_BYTES + 2 * BQ * 4);
-        for (int c = 0; c < L::NCH; ++c) {
-          tma_load_3d(sb + L::ST_Q + c * L::Q_CHUNK, &p.tm_q, fb, c * 64, qi * BQ, bh, pol_last);
-          tma_load_3d(sb + L::ST_DO + c * L::Q_CHUNK, &p.tm_do, fb, c * 64, qi * BQ, bh, pol_last);
-        }
         // -LSE * log2 e and -D of the step's query rows (rows past N are zero;
         // each head's row is padded to a multiple of 128, so the copy stays in
         // bounds and 16-byte aligned)
         const size_t row0 = static_cast<size_t>(bh) * p.npad + static_cast<size_t>(qi) * BQ;
-        bulk_load(sb + L::ST_LSE, p.nlse + row0, BQ * 4, fb);
-        bulk_load(sb + L::ST_DV, p.nd + row0, BQ * 4, fb);
+        const bool vec_ok = dcheck(row0 + BQ <= static_cast<size_t>(p.BH) * p.npad, p.status);
+        mbar_arrive_expect_tx(fb, 2 * L::Q_BYTES + (vec_ok ? 2 * BQ * 4 : 0));
+        for (int c = 0; c < L::NCH; ++c) {
+          tma_load_3d(sb + L::ST_Q + c * L::Q_CHUNK, &p.tm_q, fb, c * 64, qi * BQ, bh, pol_last);
+          tma_load_3d(sb + L::ST_DO + c * L::Q_CHUNK, &p.tm_do, fb, c * 64, qi * BQ, bh, pol_last);
+        }
+        if (vec_ok) {
+          bulk_load(sb + L::ST_LSE, p.nlse + row0, BQ * 4, fb);
+          bulk_load(sb + L::ST_DV, p.nd + row0, BQ * 4, fb);
+        }
         ++issued[st];
       }
       if (!ok) {
@@ -491,7 +495,7 @@ __global__ void __launch_bounds__(448, 1) fa_bwd_kernel(const __grid_constant__ 
       if (lane == 0) mbar_arrive(bar(L::B_DS));
     }
     // ------------------------------------------------- epilogue: dV rows, half the columns each
-    const bool key_ok = key < p.N;                 // rows past N are not stored
+    const bool key_ok = key < p.N && dcheck(bh < p.BH, p.status);   // rows past N are not stored
     if (ok) {
       constexpr int DC = D / 2;
       __nv_bfloat16* out = p.dv + (static_cast<size_t>(bh) * p.N + static_cast<size_t>(kt) * TILE + r) * D + half * DC;
@@ -535,7 +539,8 @@ __global__ void __launch_bounds__(448, 1) fa_bwd_kernel(const __grid_constant__ 
       if constexpr (L::DQ_T) {
         // lane t holds head-dim column t of dQ for the BQ = 64 queries of the step
         float* dst = p.dq_acc + row0 * D + t;
-        const int c_lim = p.N - qi * BQ;          // query rows of the step inside N
+        int c_lim = p.N - qi * BQ;                // query rows of the step inside N
+        if (!dcheck(row0 + (c_lim < 64 ? c_lim : 64) <= static_cast<size_t>(p.BH) * p.N, p.status)) c_lim = 0;
         if (c_lim >= 64) {
 #pragma unroll
           for (int c = 0; c < 64; ++c) atomicAdd(dst + static_cast<size_t>(c) * D, __uint_as_float(v[c]));
@@ -547,7 +552,7 @@ __global__ void __launch_bounds__(448, 1) fa_bwd_kernel(const __grid_constant__ 
       } else {
         // lane t holds query row t of the step, 64 head-dim columns
         float4* dst = reinterpret_cast<float4*>(p.dq_acc + (row0 + t) * D);
-        if (qi * BQ + t < p.N)
+        if (qi * BQ + t < p.N && dcheck(row0 + t < static_cast<size_t>(p.BH) * p.N, p.status))
 #pragma unroll
         for (int c = 0; c < 16; ++c)
           atomicAdd(dst + c, make_float4(__uint_as_float(v[4 * c]), __uint_as_float(v[4 * c + 1]),
@@ -555,7 +560,7 @@ __global__ void __launch_bounds__(448, 1) fa_bwd_kernel(const __grid_constant__ 
       }
     }
     // dK rows (lane = key row), scaled by the chain-rule factor
-    const bool key_ok = kt * TILE + t < p.N;        // rows past N are not stored
+    const bool key_ok = kt * TILE + t < p.N && dcheck(bh < p.BH, p.status);   // rows past N are not stored
     if (ok) {
       __nv_bfloat16* out = p.dk + (static_cast<size_t>(bh) * p.N + static_cast<size_t>(kt) * TILE + t) * D;
       if (n_steps > 0 && mbar_wait_warp(bar(L::B_DONE), 0, wc)) {

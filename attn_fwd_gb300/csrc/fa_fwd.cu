@@ -87,8 +87,9 @@ __device__ __forceinline__ void build_sparse_bits(const FwdParams& p, int qt, ui
   const int nw = (p.n_qt + 31) / 32;
   for (int wd = 0; wd < nw; ++wd) {
     const int kt = wd * 32 + static_cast<int>(lane);
+    const size_t at = static_cast<size_t>(qt) * p.n_qt + kt;
     const bool v = qt < p.n_qt && kt < p.n_qt && (!(p.mask_kind & MASK_CAUSAL) || kt <= qt) &&
-                   __ldg(p.block_mask + static_cast<size_t>(qt) * p.n_qt + kt) != 0;
+                   dcheck(at < static_cast<size_t>(p.n_qt) * p.n_qt, p.status) && __ldg(p.block_mask + at) != 0;
     const uint32_t m = __ballot_sync(0xffffffffu, v);
     if (lane == 0) bits[wd] = m;
     n += __popc(m);
@@ -806,7 +807,8 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
         // registers across the row loop)
         const int qt_e = BANDED ? item_info(item_index(k)).qt0 + w : qt;
         const int bh_e = BANDED ? item_index(k) % p.BH : bh;
-        const bool row_ok = qt_e * TILE + row < p.N;
+        const bool row_ok = qt_e * TILE + row < p.N &&
+                            dcheck(bh_e < p.BH && qt_e * TILE + row >= 0, p.status);
         const size_t grow = static_cast<size_t>(bh_e) * p.N + static_cast<size_t>(qt_e) * TILE + row;
         __nv_bfloat16* orow = p.o + grow * D;
         if (n_vis > 0) {

@@ -151,6 +151,21 @@ struct WaitCtx {
 };
 
 constexpr int FA_DEV_TIMEOUT = -5;
+constexpr int FA_DEV_BOUNDS = -8;
+
+// Device index check of the debug build (compiled with FA_DEBUG): true when
+// `ok`; otherwise it records FA_ERR_BOUNDS in the device status word (the
+// first error wins) and returns false, and the caller skips the access --
+// no trap, the context stays usable.  Without FA_DEBUG: always true, no code.
+__device__ __forceinline__ bool dcheck(bool ok, int* status) {
+#ifdef FA_DEBUG
+  if (!ok) atomicCAS(status, 0, FA_DEV_BOUNDS);
+  return ok;
+#else
+  (void)status;
+  return true;
+#endif
+}
 
 __device__ __forceinline__ void wait_fail(const WaitCtx& w) {
   *w.abort = 1;

@@ -43,6 +43,7 @@ _SIGS = {
     "fa_bwd_preprocess": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp]),
     "fa_bwd_main": (_i, [_vp] * 8 + [_i, _i, _i, _i, _f, _i, _f, _u64, _vp]),
     "fa_fwd_dropout": (_i, [_vp] * 6 + [_i, _i, _i, _i, _f, _i, _f, _u64, _vp]),
+    "fa_dropout_effective_p": (_f, [_f]),
     "fa_bwd_dropout": (_i, [_vp] * 11 + [_i, _i, _i, _i, _f, _i, _f, _u64, _vp]),
     "fa_bwd_dq_convert": (_i, [_vp, _vp, _i, _i, _i, _i, _f, _vp]),
     "fa_bwd_noalloc": (_i, [_vp] * 9 + [_i, _i, _i, _i, _f, _i, _vp]),
@@ -215,6 +216,15 @@ def fa_bwd_main(q, k, v, do, block_mask, dk, dv, workspace, scale, mask_kind, dr
                             ctypes.c_void_p(workspace.data_ptr()), B, H, N, d, float(scale), int(mask_kind),
                             float(dropout_p), int(seed) & (2 ** 64 - 1), _stream(stream))
     _check("fa_bwd_main", rc)
+
+
+def fa_dropout_effective_p(dropout_p) -> float:
+    """The drop probability the dropout calls apply: dropout_p rounded to a
+    multiple of 1/256 (see include/fa.h)."""
+    v = load().fa_dropout_effective_p(float(dropout_p))
+    if v < 0:
+        raise ValueError("dropout_p must be in [0, 1)")
+    return v
 
 
 @_first

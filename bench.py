@@ -747,6 +747,59 @@ def _run_cuda_fp8(args, w, t, f_fwd, fa, dev, ws, rank):
     return rc_out
 
 
+def _read(path):
+    try:
+        with open(path) as f:
+            return f.read().strip()
+    except OSError:
+        return None
+
+
+def _host_link_info(dev):
+    """Where the host side of the end-to-end copies sits (read-only: sysfs and
+    the process status), and the pinned copy rates, each direction alone, on
+    256 MiB buffers timed with CUDA events (outside any timed step)."""
+    import torch
+    info = {}
+    try:
+        p = torch.cuda.get_device_properties(dev)
+        bus = "%04x:%02x:%02x.0" % (p.pci_domain_id, p.pci_bus_id, p.pci_device_id)
+        info["gpu_pci"] = bus
+        info["gpu_numa_node"] = _read(f"/sys/bus/pci/devices/{bus}/numa_node")
+        info["gpu_local_cpus"] = _read(f"/sys/bus/pci/devices/{bus}/local_cpulist")
+    except Exception:
+        pass
+    nodes = _read("/sys/devices/system/node/online")
+    info["numa_nodes_online"] = nodes
+    if hasattr(os, "sched_getaffinity"):
+        cpus = sorted(os.sched_getaffinity(0))
+        info["process_cpus"] = f"{cpus[0]}-{cpus[-1]}" if cpus == list(range(cpus[0], cpus[-1] + 1)) else cpus
+    status = _read("/proc/self/status") or ""
+    for line in status.splitlines():
+        if line.startswith("Mems_allowed_list"):
+            info["pinned_memory_nodes_allowed"] = line.split(":", 1)[1].strip()
+    try:
+        n = 256 << 20
+        h = torch.empty(n, dtype=torch.uint8).pin_memory()
+        d = torch.empty(n, dtype=torch.uint8, device=dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        for direction in ("h2d", "d2h"):
+            best = None
+            for _ in range(3):
+                torch.cuda.synchronize()
+                e0.record()
+                (d.copy_(h, non_blocking=True) if direction == "h2d" else h.copy_(d, non_blocking=True))
+                e1.record()
+                torch.cuda.synchronize()
+                ms = e0.elapsed_time(e1)
+                best = ms if best is None else min(best, ms)
+            info[f"{direction}_gbs"] = n / (best * 1e-3) / 1e9
+        del h, d
+    except Exception:
+        pass
+    return info
+
+
 def _graph_ms_per_step(args, step, flush, ws, dev):
     """Capture step() into a CUDA graph and time one replay per step (CUDA
     events around each replay, the L2 flushed before each, max over ranks)."""
@@ -988,7 +1041,8 @@ def run_cuda(args):
                     "call": ((("fa_fwd_bwd_host" if w.backward else "fa_fwd_host") +
                               ": chunks of heads, copies overlapped with the kernels") if streamed
                              else "pinned copies in, device-resident step, copies out"),
-                    "max_abs_diff_vs_device_step": e2e_diff},
+                    "max_abs_diff_vs_device_step": e2e_diff,
+                    "host_link": _host_link_info(dev)},
             "gpu_launches": launches_per_step * args.steps, "roofline": roofline, "kernels": kernels,
             "clocks": clocks}
     if not args.eager:

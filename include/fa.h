@@ -87,7 +87,9 @@ typedef enum fa_status {
   FA_ERR_LAUNCH = -4,      /* the CUDA runtime refused a launch or attribute call */
   FA_ERR_TIMEOUT = -5,     /* a kernel wait ran past the wait timeout (device status) */
   FA_ERR_CUDA = -6,        /* another CUDA runtime error (device query, descriptor) */
-  FA_ERR_SCRATCH = -7      /* fa_bwd_noalloc: the problem needs more than its static scratch */
+  FA_ERR_SCRATCH = -7,     /* fa_bwd_noalloc: the problem needs more than its static scratch */
+  FA_ERR_BOUNDS = -8       /* debug build (libfa_debug.so) only: a device index check failed;
+                              the access was skipped (reported by fa_get_device_error) */
 } fa_status;
 
 /* Library version, major * 10000 + minor * 100 + patch. */
@@ -185,6 +187,14 @@ FA_API int fa_bwd_dq_convert(const void *workspace, void *dq, int B, int H, int 
  * block_mask may be NULL (no block mask); causal as for fa_fwd.  dropout_p in
  * [0, 1), else FA_ERR_INVALID.  Everything else as for fa_fwd / fa_bwd.
  */
+/*
+ * The drop probability p' = round(256 dropout_p) / 256 (t at most 255) that
+ * fa_fwd_dropout and fa_bwd_dropout apply for a requested dropout_p: the
+ * requested value quantised to a multiple of 1/256 (0.1 runs as 26/256 =
+ * 0.1015625).  A host function (no device work); -1 when dropout_p is not in
+ * [0, 1).
+ */
+FA_API float fa_dropout_effective_p(float dropout_p);
 FA_API int fa_fwd_dropout(const void *q, const void *k, const void *v, void *o, float *lse,
                           const uint8_t *block_mask, int B, int H, int N, int d, float scale,
                           int causal, float dropout_p, unsigned long long seed, fa_stream_t stream);

@@ -241,6 +241,18 @@ def test_dropout_argument_checks(lib):
     assert lib.fa_fwd_dropout(NULL, P, P, P, P, NULL, 1, 1, 128, 64, 0.125, 0, 0.1, 1, NULL) == -1
 
 
+def test_dropout_effective_probability(lib):
+    """The applied drop probability is the requested one rounded to a multiple
+    of 1/256, as the oracle's dropout threshold defines it."""
+    import attn_fwd_gb300.fa as fa
+    import oracle
+    for p in (0.0, 0.1, 0.25, 0.3, 0.5, 0.999, 1e-4, 0.998):
+        assert fa.fa_dropout_effective_p(p) == oracle.dropout_threshold(p) / 256.0
+    assert fa.fa_dropout_effective_p(0.1) == 26 / 256
+    for bad in (-0.1, 1.0, float("nan")):
+        assert lib.fa_dropout_effective_p(bad) == -1.0
+
+
 def test_fp8_workspace_and_validation(lib):
     import attn_fwd_gb300.fa as fa
     assert fa.fa_fwd_fp8_workspace_bytes(2, 3, 300, 128) == 2 * 3 * 128 * 304 + (256 - (2 * 3 * 128 * 304) % 256) % 256
