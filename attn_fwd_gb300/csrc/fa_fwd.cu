@@ -661,7 +661,6 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
       const float sl2 = p.scale_log2;
       float m = -INFINITY;  // reference max, in exp2 units of scaled scores
       float l = 0.f;    // row sum of exp2(S - m), fp32
-      float lr = 0.f;   // the same sum over the bf16-rounded values used in P V
       bool has_o = false;
       const int n_vis = w ? nv1 : nv0;
       // Only the highest visible key tile can need a per-element mask: the
@@ -729,10 +728,11 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
         }
         // P = exp2(S * scale * log2e - m), two columns per packed FMA; the
         // bf16 pairs go to tensor memory 32 columns at a time while the next
-        // 32 are computed.  l sums the fp32 values (for LSE); lr sums the
-        // bf16-rounded values that P V multiplies, so O / lr weighs the V rows
-        // with weights summing to exactly one.  Dropout zeroes the dropped
-        // pairs of the P V operand only: l and lr are the softmax's own sums.
+        // 32 are computed.  l sums the fp32 values: it gives the LSE and
+        // normalises O (P V multiplies the bf16-rounded values, whose sum
+        // differs from l by the rounding only, within the bf16 error of O).
+        // Dropout zeroes the dropped pairs of the P V operand only: l is the
+        // softmax's own sum.
         if (SPLIT_PV && has_o && __any_sync(0xffffffffu, need)) {
           // With dropout, O is rescaled before any of this tile's P is
           // published (the P V halves accumulate onto it).  O may be read
@@ -748,7 +748,7 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
         }
         const float2 sl2v = make_float2(sl2, sl2);
         const float2 negm = make_float2(-m, -m);
-        float2 la = make_float2(0.f, 0.f), lb = la, ra = la, rb = la;
+        float2 la = make_float2(0.f, 0.f), lb = la;
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           uint32_t pk[16];
@@ -757,13 +757,10 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
             const float2 x = ffma2(make_float2(s[32 * q + 2 * e], s[32 * q + 2 * e + 1]), sl2v, negm);
             const float2 pv = make_float2(ex2_approx(x.x), ex2_approx(x.y));
             const uint32_t pku = pack_bf16x2(pv.x, pv.y);
-            if (e & 1) {
+            if (e & 1)
               lb = fadd2(lb, pv);
-              add_bf16x2_to_f32(rb, pku);
-            } else {
+            else
               la = fadd2(la, pv);
-              add_bf16x2_to_f32(ra, pku);
-            }
             if constexpr (DROP) {
               const uint32_t f = dbits[q] >> keep_bit(2 * e);   // columns 2e, 2e+1: adjacent bits
               pk[e] = pku & (((f & 1u) ? 0x0000FFFFu : 0u) | ((f & 2u) ? 0xFFFF0000u : 0u));
@@ -782,7 +779,6 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
           tmem_st_x16_async(s_addr + 16 * q, pk);
         }
         l = l * alpha + ((la.x + la.y) + (lb.x + lb.y));
-        lr = lr * alpha + ((ra.x + ra.y) + (rb.x + rb.y));
         if (!SPLIT_PV && has_o && __any_sync(0xffffffffu, need)) {
           // O may be read here: S(j) completing implies the previous PV is done.
 #pragma unroll 1
@@ -816,7 +812,7 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
           ++n_out;
           if (ok) {
             tc_fence_after();
-            const float inv_l = DROP ? p.drop.scale / lr : 1.f / lr;
+            const float inv_l = DROP ? p.drop.scale / l : 1.f / l;
 #pragma unroll 1
             for (int c = 0; c < D; c += 32) {
               uint32_t ov[32];
