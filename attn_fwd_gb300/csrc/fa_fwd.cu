@@ -67,7 +67,11 @@ struct FwdLayout {
   static constexpr int BITS_OFF = BAR_OFF + NBARS * 8 + 16;
   static constexpr int BITS_WORDS = MAX_SPARSE_TILES / 32;
   static constexpr int BITS_BYTES = SPARSE ? 2 * BITS_WORDS * 4 + 16 : 0;
-  static constexpr int SMEM_BYTES = BITS_OFF + BITS_BYTES + 1024;      // + 1 KB alignment slack
+  // block-sparse: one bit per round, set where both query tiles take the
+  // same key tile (written and read by the MMA warp only)
+  static constexpr int SHR_OFF = BITS_OFF + BITS_BYTES;
+  static constexpr int SHR_BYTES = SPARSE ? BITS_WORDS * 4 : 0;
+  static constexpr int SMEM_BYTES = SHR_OFF + SHR_BYTES + 1024;      // + 1 KB alignment slack
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t S_COL0 = 0, S_COL1 = 128;
   static constexpr uint32_t O_COL0 = 256, O_COL1 = 256 + D;
@@ -584,57 +588,101 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
     const int rounds = nv0 > nv1 ? nv0 : nv1;
     if (nv0 > 0) ok = mbar_wait_warp(bar(L::B_Q + 0), 0, wc);
     if (ok && nv1 > 0) ok = mbar_wait_warp(bar(L::B_Q + 1), 0, wc);
-    // Ring slots in load order (the producer's sequence): the n-th tile
-    // loaded sits in slot n % STAGES, and its fill barrier completes for the
-    // (n / STAGES)-th time.  Each slot is released right after the MMAs that
-    // read it.
-    auto slot_of = [](int n) { return n % L::STAGES; };
-    auto phase_of = [](int n) { return static_cast<uint32_t>((n / L::STAGES) & 1); };
-    auto ready = [&](int n) { return mbar_wait_warp(bar(L::B_FULL + slot_of(n)), phase_of(n), wc); };
-    int cnt = 0;                       // tiles taken so far, in load order
+    // The MMA warp needs, per round of SparseRounds' schedule, only which
+    // query tiles take a key tile and whether they take the same one (then
+    // one K and one V load serve both); not the tile indices themselves.
+    // Shared-first: rounds 0 .. split-1 give tile 0 a tile while r < na and
+    // tile 1 while r < nb, never the same; the nc rounds after split are all
+    // shared.  Otherwise round r takes the r-th visible tile of each, and it
+    // is the same tile exactly where a key tile t visible to both has equal
+    // rank (number of visible tiles before it) in both lists: one bit per
+    // round, set here with one lane per 32-tile word.
+    const SparsePlan pl = sparse_plan(bits0, bits1, p.n_qt);
+    const int split = pl.na > pl.nb ? pl.na : pl.nb;
+    uint32_t* shr = reinterpret_cast<uint32_t*>(smem + L::SHR_OFF);
+    if (!pl.shared_first) {
+      const int nw = (p.n_qt + 31) / 32;
+      const uint32_t x = lane < static_cast<uint32_t>(nw) ? bits0[lane] : 0u;
+      const uint32_t y = lane < static_cast<uint32_t>(nw) ? bits1[lane] : 0u;
+      int ex = __popc(x), ey = __popc(y);       // exclusive prefix counts over the words
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int tx = __shfl_up_sync(0xffffffffu, ex, o), ty = __shfl_up_sync(0xffffffffu, ey, o);
+        if (lane >= static_cast<uint32_t>(o)) { ex += tx; ey += ty; }
+      }
+      ex -= __popc(x);
+      ey -= __popc(y);
+      if (lane < static_cast<uint32_t>(nw)) shr[lane] = 0u;
+      __syncwarp();
+      for (uint32_t m = x & y; m != 0u; m &= m - 1u) {
+        const uint32_t below = (1u << (__ffs(m) - 1)) - 1u;
+        const int rx = ex + __popc(x & below), ry = ey + __popc(y & below);
+        if (rx == ry) atomicOr(shr + (rx >> 5), 1u << (rx & 31));
+      }
+      __syncwarp();
+    }
+    auto takes0 = [&](int r) { return r < rounds && (pl.shared_first ? (r < pl.na || r >= split) : r < nv0); };
+    auto takes1 = [&](int r) { return r < rounds && (pl.shared_first ? (r < pl.nb || r >= split) : r < nv1); };
+    auto same = [&](int r) { return pl.shared_first ? r >= split : ((shr[r >> 5] >> (r & 31)) & 1u) != 0u; };
+    // Ring slots in load order (the producer's sequence: per round V(a_{r-1}),
+    // K(a_r), V(b_{r-1}), K(b_r), a tile both use once): the running slot and
+    // phase of the next fill.  Each slot is released right after the MMAs
+    // that read it.
+    int cslot = 0;
+    uint32_t cphase = 0;
+    auto take = [&](int& sl, uint32_t& ph) {
+      sl = cslot;
+      ph = cphase;
+      if (++cslot == L::STAGES) { cslot = 0; cphase ^= 1u; }
+    };
     uint32_t pph0 = 0, pph1 = 0;       // phases of the P barriers
     int done0 = 0, done1 = 0;          // PV products issued per tile
-    SparseRounds sched(bits0, bits1, p.n_qt);
-    int pa = -1, pb = -1;              // previous round's key tiles
+    bool pa = false, pb = false, pshared = false;   // the previous round's takes
     for (int r = 0; r <= rounds && ok; ++r) {
-      int a = -1, b = -1;
-      if (r < rounds) sched.next(r, a, b);
-      const bool vshared = pb >= 0 && pb == pa;   // tile 1 reuses tile 0's V of the previous round
-      const bool kshared = b >= 0 && b == a;      // and its K of this round
-      const int nva = pa >= 0 ? cnt++ : -1;
-      const int nka = a >= 0 ? cnt++ : -1;
-      const int nvb = pb >= 0 ? (vshared ? nva : cnt++) : -1;
-      const int nkb = b >= 0 ? (kshared ? nka : cnt++) : -1;
-      // tile 0: PV of the previous round, then S of this round
-      if (pa >= 0) {
-        if (!(ok = ready(nva))) break;
-        if (!(ok = pv(0, pph0, slot_of(nva), done0 > 0))) break;
-        if (++done0 == nv0) mma_commit_elect(bar(L::B_O + 0));
-        if (!vshared) mma_commit_elect(bar(L::B_EMPTY + slot_of(nva)));
+      const bool a = takes0(r), b = takes1(r);
+      const bool kshared = a && b && same(r);     // tile 1 takes tile 0's K of this round
+      const bool vshared = pshared;               // and took its V of the previous round
+      int sva = 0, ska = 0, svb = 0, skb = 0;
+      uint32_t hva = 0, hka = 0, hvb = 0, hkb = 0;
+      if (pa) take(sva, hva);
+      if (a) take(ska, hka);
+      if (pb) {
+        if (vshared) { svb = sva; hvb = hva; } else { take(svb, hvb); }
       }
-      if (a >= 0) {
-        if (!(ok = ready(nka))) break;
+      if (b) {
+        if (kshared) { skb = ska; hkb = hka; } else { take(skb, hkb); }
+      }
+      // tile 0: PV of the previous round, then S of this round
+      if (pa) {
+        if (!(ok = mbar_wait_warp(bar(L::B_FULL + sva), hva, wc))) break;
+        if (!(ok = pv(0, pph0, sva, done0 > 0))) break;
+        if (++done0 == nv0) mma_commit_elect(bar(L::B_O + 0));
+        if (!vshared) mma_commit_elect(bar(L::B_EMPTY + sva));
+      }
+      if (a) {
+        if (!(ok = mbar_wait_warp(bar(L::B_FULL + ska), hka, wc))) break;
         tc_fence_after();
-        issue_s(dq0, L::S_COL0, slot_of(nka));
+        issue_s(dq0, L::S_COL0, ska);
         mma_commit_elect(bar(L::B_S + 0));
-        if (!kshared) mma_commit_elect(bar(L::B_EMPTY + slot_of(nka)));
+        if (!kshared) mma_commit_elect(bar(L::B_EMPTY + ska));
       }
       // tile 1
-      if (pb >= 0) {
-        if (!vshared && !(ok = ready(nvb))) break;
-        if (!(ok = pv(1, pph1, slot_of(nvb), done1 > 0))) break;
+      if (pb) {
+        if (!vshared && !(ok = mbar_wait_warp(bar(L::B_FULL + svb), hvb, wc))) break;
+        if (!(ok = pv(1, pph1, svb, done1 > 0))) break;
         if (++done1 == nv1) mma_commit_elect(bar(L::B_O + 1));
-        mma_commit_elect(bar(L::B_EMPTY + slot_of(nvb)));
+        mma_commit_elect(bar(L::B_EMPTY + svb));
       }
-      if (b >= 0) {
-        if (!kshared && !(ok = ready(nkb))) break;
+      if (b) {
+        if (!kshared && !(ok = mbar_wait_warp(bar(L::B_FULL + skb), hkb, wc))) break;
         tc_fence_after();
-        issue_s(dq1, L::S_COL1, slot_of(nkb));
+        issue_s(dq1, L::S_COL1, skb);
         mma_commit_elect(bar(L::B_S + 1));
-        mma_commit_elect(bar(L::B_EMPTY + slot_of(nkb)));
+        mma_commit_elect(bar(L::B_EMPTY + skb));
       }
       pa = a;
       pb = b;
+      pshared = kshared;
     }
     }
     // nothing may be in flight when tensor memory is released
