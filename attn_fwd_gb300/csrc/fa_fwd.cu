@@ -537,15 +537,23 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
       const uint32_t vphase = phase;
       if (++slot == L::STAGES) { slot = 0; phase ^= 1u; }
 
-      if (!(ok = mbar_wait_warp(bar(L::B_FULL + kslot), kphase, wc))) break;
-      tc_fence_after();
+      // tile 0: PV(prev), then S(this).  Unsplit P V: K(this) is waited for
+      // after PV(prev) is issued, so that check overlaps the product instead
+      // of delaying it (with the split P V, measured slower).
+      if constexpr (SPLIT_PV) {
+        if (!(ok = mbar_wait_warp(bar(L::B_FULL + kslot), kphase, wc))) break;
+        tc_fence_after();
+      }
       if (has_prev) {
         if (!(ok = mbar_wait_warp(bar(L::B_FULL + pvslot), pvphase, wc))) break;
       }
-      // tile 0: PV(prev), then S(this)
       if (has_prev && pf0) {
         if (!(ok = pv(0, pph0, pvslot, done0 > 0))) break;
         if (++done0 == nv0) mma_commit_elect(bar(L::B_O + 0));
+      }
+      if constexpr (!SPLIT_PV) {
+        if (!(ok = mbar_wait_warp(bar(L::B_FULL + kslot), kphase, wc))) break;
+        tc_fence_after();
       }
       if (f0) {
         issue_s(dq0, L::S_COL0, kslot);
