@@ -78,6 +78,45 @@ struct FwdLayout {
   static constexpr int THREADS = 320;
 };
 
+// Groups of MMAs into one accumulator under a single elect.sync: the k-steps
+// of one product.  The first accumulates onto D when `acc_first` is nonzero,
+// the rest always do.  Same operands as mma_ss_elect / mma_ts_elect.
+__device__ __forceinline__ void mma_ss_x8_elect(uint32_t d_tmem, const uint64_t (&a)[8], const uint64_t (&b)[8],
+                                                uint32_t idesc, uint32_t acc_first) {
+  asm volatile(
+      "{\n\t.reg .pred e, p, t;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %18, 0;\n\t"
+      "setp.eq.b32 t, %18, %18;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %9, %17, p;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %2, %10, %17, t;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %3, %11, %17, t;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %4, %12, %17, t;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %5, %13, %17, t;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %6, %14, %17, t;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %7, %15, %17, t;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %8, %16, %17, t;\n\t}" ::"r"(d_tmem),
+      "l"(a[0]), "l"(a[1]), "l"(a[2]), "l"(a[3]), "l"(a[4]), "l"(a[5]), "l"(a[6]), "l"(a[7]),
+      "l"(b[0]), "l"(b[1]), "l"(b[2]), "l"(b[3]), "l"(b[4]), "l"(b[5]), "l"(b[6]), "l"(b[7]),
+      "r"(idesc), "r"(acc_first)
+      : "memory");
+}
+__device__ __forceinline__ void mma_ts_x4_elect(uint32_t d_tmem, const uint32_t (&a)[4], const uint64_t (&b)[4],
+                                                uint32_t idesc, uint32_t acc_first) {
+  asm volatile(
+      "{\n\t.reg .pred e, p, t;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %10, 0;\n\t"
+      "setp.eq.b32 t, %10, %10;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %5, %9, p;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%2], %6, %9, t;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%3], %7, %9, t;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%4], %8, %9, t;\n\t}" ::"r"(d_tmem),
+      "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "l"(b[0]), "l"(b[1]), "l"(b[2]), "l"(b[3]),
+      "r"(idesc), "r"(acc_first)
+      : "memory");
+}
+
 // Reference-max threshold for lazy rescaling, in exp2 units (factor 256).
 constexpr float RESCALE_THRESHOLD = 8.0f;
 
@@ -467,10 +506,22 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
     // row; a new 16 KB chunk every 64 columns).
     auto issue_s = [&](uint64_t dq, uint32_t scol, int kslot) {
       const uint64_t dk = dk_ring + static_cast<uint64_t>(kslot) * SLOT16;
+      if constexpr (D == 128 && SPARSE) {   // the eight k-steps under one elect (measured:
+                                            // faster with block masks, slower without)
+        uint64_t da[8], db[8];
 #pragma unroll
-      for (int k = 0; k < D / 16; ++k) {
-        const uint32_t off = ((k >> 2) * L::CHUNK_BYTES + (k & 3) * 32) >> 4;
-        mma_ss_elect(tmem + scol, dq + off, dk + off, IDESC_S, k > 0 ? 1u : 0u);
+        for (int k = 0; k < 8; ++k) {
+          const uint32_t off = ((k >> 2) * L::CHUNK_BYTES + (k & 3) * 32) >> 4;
+          da[k] = dq + off;
+          db[k] = dk + off;
+        }
+        mma_ss_x8_elect(tmem + scol, da, db, IDESC_S, 0u);
+      } else {
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {
+          const uint32_t off = ((k >> 2) * L::CHUNK_BYTES + (k & 3) * 32) >> 4;
+          mma_ss_elect(tmem + scol, dq + off, dk + off, IDESC_S, k > 0 ? 1u : 0u);
+        }
       }
     };
     // O_w += P_w V: 128/16 k-steps; P from tensor memory (8 columns of bf16
@@ -478,10 +529,23 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
     // second 64-column half of d sits 16 KB further).
     auto issue_pv_half = [&](uint32_t ocol, uint32_t scol, int vslot, bool started, int k0) {
       const uint64_t dv = dv_ring + static_cast<uint64_t>(vslot) * SLOT16;
+      if constexpr (SPARSE) {          // four k-steps under one elect (as for S)
+        uint32_t ta[4];
+        uint64_t db[4];
 #pragma unroll
-      for (int kk = 0; kk < TILE / 32; ++kk) {
-        const int k = k0 + kk;
-        mma_ts_elect(tmem + ocol, tmem + scol + 8 * k, dv + ((k * 2048) >> 4), IDESC_O, (started || k > 0) ? 1u : 0u);
+        for (int kk = 0; kk < TILE / 32; ++kk) {
+          const int k = k0 + kk;
+          ta[kk] = tmem + scol + 8 * k;
+          db[kk] = dv + ((k * 2048) >> 4);
+        }
+        mma_ts_x4_elect(tmem + ocol, ta, db, IDESC_O, (started || k0 > 0) ? 1u : 0u);
+      } else {
+#pragma unroll
+        for (int kk = 0; kk < TILE / 32; ++kk) {
+          const int k = k0 + kk;
+          mma_ts_elect(tmem + ocol, tmem + scol + 8 * k, dv + ((k * 2048) >> 4), IDESC_O,
+                       (started || k > 0) ? 1u : 0u);
+        }
       }
     };
     // P_w V.  Where the softmax outweighs the products (SPLIT_PV: dropout,
