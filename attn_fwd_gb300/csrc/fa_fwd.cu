@@ -371,9 +371,34 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
                                     bit_counts + warp, lane);
   }
 
-  if (threadIdx.x == 0) {
+  // Q of the CTA's first item is requested by the producer warp before the
+  // rest of the set-up, so its copies land while the barriers, tensor memory
+  // and mask bits are prepared (it initialises the two Q barriers itself).
+  if (warp == 9 && lane == 0) {
     mbar_init(bar(L::B_Q + 0), 1);
     mbar_init(bar(L::B_Q + 1), 1);
+    fence_mbar_init();
+    const int j0 = item_index(0);
+    if (j0 >= 0) {
+      prefetch_tmap(&p.tm_q);
+      const uint64_t pol_q = l2_policy_evict_first();
+      const int bh0 = j0 % p.BH;
+      int pair = j0 / p.BH;
+      if (p.mask_kind & MASK_CAUSAL) pair = p.n_pairs - 1 - pair;   // as item_info
+      for (int w = 0; w < 2; ++w) {
+        const int qt = 2 * pair + w;
+        if (qt >= p.n_qt) {
+          mbar_arrive(bar(L::B_Q + w));
+          continue;
+        }
+        mbar_arrive_expect_tx(bar(L::B_Q + w), L::TILE_BYTES);
+        for (int c = 0; c < L::NCH; ++c)
+          tma_load_3d(sbase + L::Q_OFF + w * L::TILE_BYTES + c * L::CHUNK_BYTES, &p.tm_q, bar(L::B_Q + w), c * 64,
+                      qt * TILE, bh0, pol_q);
+      }
+    }
+  }
+  if (threadIdx.x == 0) {
     for (int s = 0; s < L::STAGES; ++s) {
       mbar_init(bar(L::B_FULL + s), 1);
       mbar_init(bar(L::B_EMPTY + s), 1);
@@ -425,8 +450,9 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
       const int bh = it.bh, qt0 = it.qt0, qt1 = it.qt1, kt_end = it.kt_end;
       const int rounds = it.nv0 > it.nv1 ? it.nv0 : it.nv1;
       // the Q buffers are free once the previous item's S products are done
+      // (the first item's Q was requested before the set-up)
       if (k > 0 && !(ok = mbar_wait(bar(L::B_QFREE), (k - 1) & 1, wc))) break;
-      for (int w = 0; w < 2; ++w) {
+      for (int w = 0; w < 2 && k > 0; ++w) {
         const int qt = qt0 + w;
         if (qt >= p.n_qt) {              // no such tile: complete the phase empty
           mbar_arrive(bar(L::B_Q + w));
