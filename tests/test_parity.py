@@ -457,6 +457,50 @@ def test_block_mask_odd_tile_counts(fa, B, H, N, d, causal, seed):
     check_bwd((dq, dk, dv), ref, f"N={N} d={d} odd tiles", model)
 
 
+def _schedule_mask(nb, seed):
+    """A block mask whose query-tile pairs (2t, 2t + 1) exercise the forward's
+    round schedules: shared tiles at equal ranks at the start (then the
+    tiles of one query tile alone), shared ranks with a gap, identical rows
+    (every round shared), disjoint rows, an empty row beside a full one, one
+    tile shared at different ranks; the remaining pairs random."""
+    rows = [set(range(0, 5)) | {10, 11, 12}, set(range(0, 5)) | set(range(14, 20)),
+            {1, 3, 5, 7, 9}, {0, 2, 4, 6, 8},
+            set(range(10)), set(range(10)),
+            set(), set(range(5, 10)),
+            set(range(nb)), {nb - 1},
+            {2, 5, 8, 11, 12, 13}, {2, 6, 8, 14, 15, 16}]
+    g = torch.Generator().manual_seed(seed)
+    bm = (torch.rand((nb, nb), generator=g) < 0.3).to(torch.uint8)
+    for qt, r in enumerate(rows):
+        bm[qt] = 0
+        for kt in r:
+            bm[qt, kt] = 1
+    return bm
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_block_mask_round_schedules(fa, causal):
+    """The block-mask forward runs each CTA's two query tiles in rounds whose
+    schedule depends on which key tiles they share (shared first, or the r-th
+    tile of each, with a shared load where those coincide); every schedule
+    above against the oracle, every element, forward and backward."""
+    B, H, N, d = 1, 2, 2560, 128
+    nb = N // 128
+    bm = _schedule_mask(nb, 123)
+    t = make_qkvdo(B, H, N, d, seed=91)
+    scale = 1 / math.sqrt(d)
+    q, k, v, do = (dev(t[n]) for n in ("q", "k", "v", "do"))
+    o, lse = fa.forward(q, k, v, causal=causal, scale=scale, block_mask=dev(bm))
+    dq, dk, dv = fa.backward(q, k, v, o, lse, do, causal=causal, scale=scale, block_mask=dev(bm))
+    check_device_status(fa)
+    f64 = {n: np64(t[n]) for n in ("q", "k", "v", "do")}
+    what = f"round schedules causal={causal}"
+    ro, rl = oracle.forward(f64["q"], f64["k"], f64["v"], scale, causal=causal, block_mask=bm.numpy())
+    check_fwd(o, lse, ro, rl, what)
+    ref, model = oracle_bwd(f64, scale, causal, bm.numpy())
+    check_bwd((dq, dk, dv), ref, what, model)
+
+
 def test_ragged_outputs_stay_inside_their_rows(fa):
     """With N not a multiple of 128, nothing is written past row N - 1."""
     B, H, N, d = 1, 2, 200, 128
