@@ -259,7 +259,7 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, c
   std::memset(&p, 0, sizeof(p));
   const int BH = B * H;
   if (make_map_bf16(&p.tm_q, q, BH, N, d, fa::TILE) != FA_OK || make_map_bf16(&p.tm_k, k, BH, N, d, fa::TILE) != FA_OK ||
-      make_map_bf16(&p.tm_v, v, BH, N, d, fa::TILE) != FA_OK)
+      make_map_bf16(&p.tm_v, v, BH, N, d, fa::TILE) != FA_OK || make_map_bf16(&p.tm_o, o, BH, N, d, 32) != FA_OK)
     return FA_ERR_CUDA;
   p.o = static_cast<__nv_bfloat16*>(o);
   p.lse = lse;

@@ -39,6 +39,7 @@ struct FwdParams {
   CUtensorMap tm_q;
   CUtensorMap tm_k;
   CUtensorMap tm_v;
+  CUtensorMap tm_o;          // O, {64, 32, 1} box: the epilogue's stores (dense and causal masks)
   __nv_bfloat16* o;          // [B*H][N][d]
   float* lse;                // [B*H][N]
   const uint8_t* block_mask; // [N/128][N/128] or null

@@ -40,7 +40,7 @@
 
 namespace fa {
 
-template <int D, bool SPARSE>
+template <int D, bool SPARSE, bool DROP = false>
 struct FwdLayout {
   static constexpr int NCH = D / 64;                      // 64-column (128-byte) chunks
   static constexpr int CHUNK_BYTES = TILE * 128;          // 128 rows x 128 bytes
@@ -71,7 +71,15 @@ struct FwdLayout {
   // same key tile (written and read by the MMA warp only)
   static constexpr int SHR_OFF = BITS_OFF + BITS_BYTES;
   static constexpr int SHR_BYTES = SPARSE ? BITS_WORDS * 4 : 0;
-  static constexpr int SMEM_BYTES = SHR_OFF + SHR_BYTES + 1024;      // + 1 KB alignment slack
+  // Dense and causal masks: the epilogue stages each softmax warp's 32 rows
+  // of O, one 64-column chunk (4 KB, 128-byte swizzle) at a time, for a TMA
+  // store.  Block masks keep per-thread stores (their 5-slot ring leaves no
+  // room), and so does dropout (measured slower: its softmax spills, and the
+  // staging tiles take shared memory from the L1 that holds the spills).
+  static constexpr bool TMA_EPI = !SPARSE && !DROP;
+  static constexpr int STG_OFF = (SHR_OFF + SHR_BYTES + 1023) / 1024 * 1024;
+  static constexpr int STG_BYTES = TMA_EPI ? 8 * 4096 : 0;
+  static constexpr int SMEM_BYTES = STG_OFF + STG_BYTES + 1024;      // + 1 KB alignment slack
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t S_COL0 = 0, S_COL1 = 128;
   static constexpr uint32_t O_COL0 = 256, O_COL1 = 256 + D;
@@ -116,6 +124,20 @@ __device__ __forceinline__ void mma_ts_x4_elect(uint32_t d_tmem, const uint32_t 
       "r"(idesc), "r"(acc_first)
       : "memory");
 }
+
+// TMA stores of shared memory to a tensor (bulk-group completion): the
+// epilogue's O.  x (c0) is 0 or 64 here, a multiple of 8 bf16 elements.
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* m, uint32_t src, int c0, int c1, int c2) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(m)),
+               "r"(src), "r"(c0), "r"(c1), "r"(c2)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// the staged source has been read (the buffer may be rewritten)
+__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// every store of the thread is complete
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 // Reference-max threshold for lazy rescaling, in exp2 units (factor 256).
 constexpr float RESCALE_THRESHOLD = 8.0f;
@@ -311,7 +333,7 @@ __device__ __forceinline__ void mbar_drain(uint32_t bar, uint32_t parity, uint64
 
 template <int D, bool SPARSE, bool DROP, bool BANDED>
 __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ FwdParams p) {
-  using L = FwdLayout<D, SPARSE>;
+  using L = FwdLayout<D, SPARSE, DROP>;
   // P V of a tile issued in two halves (the first once half of P is stored)
   // where the softmax outweighs the products: with dropout, and at d = 64
   // without a block mask
@@ -959,6 +981,43 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
           if (ok) {
             tc_fence_after();
             const float inv_l = DROP ? p.drop.scale / l : 1.f / l;
+            if constexpr (L::TMA_EPI) {
+              // this warp's 32 rows, a 64-column chunk at a time: bf16 into the
+              // warp's 4 KB staging tile (row = lane, 16-byte unit u of the
+              // 128-byte row at u ^ (row % 8)), then one TMA store, whose
+              // copies skip rows past N
+              uint8_t* stg = smem + L::STG_OFF + warp * 4096;
+#pragma unroll 1
+              for (int h = 0; h < D / 64; ++h) {
+                if (h > 0) {           // the previous chunk's store has read the tile
+                  if (lane == 0) bulk_wait_read_all();
+                  __syncwarp();
+                }
+#pragma unroll
+                for (int c2 = 0; c2 < 64; c2 += 32) {
+                  uint32_t ov[32];
+                  tmem_ld_x32(o_addr + h * 64 + c2, ov);
+                  uint4 pkd[4];
+                  uint32_t* pw = reinterpret_cast<uint32_t*>(pkd);
+#pragma unroll
+                  for (int i = 0; i < 16; ++i)
+                    pw[i] = pack_bf16x2(__uint_as_float(ov[2 * i]) * inv_l, __uint_as_float(ov[2 * i + 1]) * inv_l);
+#pragma unroll
+                  for (int e = 0; e < 4; ++e) {
+                    const uint32_t u = static_cast<uint32_t>(c2 / 8 + e) ^ (lane & 7u);
+                    *reinterpret_cast<uint4*>(stg + lane * 128 + u * 16) = pkd[e];
+                  }
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                  tma_store_3d(&p.tm_o, smem_u32(stg), h * 64, qt_e * TILE + static_cast<int>(quarter) * 32, bh_e);
+                  bulk_commit();
+                }
+              }
+              if (lane == 0) bulk_wait_read_all();   // the tile is free for the next item
+              __syncwarp();
+            } else {
 #pragma unroll 1
             for (int c = 0; c < D; c += 32) {
               uint32_t ov[32];
@@ -974,6 +1033,7 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
                 for (int i = 0; i < 4; ++i) dst[i] = pkd[i];
               }
             }
+            }
             if (row_ok) p.lse[grow] = (m + __log2f(l)) * 0.69314718055994530942f;
           }
         } else if (row_ok) {
@@ -987,6 +1047,10 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
     }
     if constexpr (SPARSE) break;         // one item per CTA
     }
+    if constexpr (L::TMA_EPI) {          // every O store of this warp complete
+      if (lane == 0) bulk_wait_all();
+      __syncwarp();
+    }
   }
 
   tc_fence_before();
@@ -999,7 +1063,7 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
 
 template <int D, bool SPARSE, bool DROP, bool BANDED = false>
 static int launch_fwd_t(const FwdParams& p, cudaStream_t stream) {
-  using L = FwdLayout<D, SPARSE>;
+  using L = FwdLayout<D, SPARSE, DROP>;
   static_assert(L::SMEM_BYTES <= 232448, "shared memory budget");
   static SmemAttrOnce attr;
   if (!attr.ensure(reinterpret_cast<const void*>(fa_fwd_kernel<D, SPARSE, DROP, BANDED>), L::SMEM_BYTES)) return -4;
